@@ -1,0 +1,264 @@
+"""Python binding of libpeagle, the GB300 (sm_103a) P-EAGLE drafting library.
+
+Argument marshalling only: every function below forwards to the C entry
+point of the same name declared in include/peagle.h. Tensors are passed as
+raw device pointers (torch tensors are accepted and must already live on the
+GPU); every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: importing this package fails if libpeagle.so has
+not been built (``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpeagle.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libpeagle.so is missing at {LIB_PATH}: build it first with "
+        "python -c 'import __graft_entry__ as g; g.build()'")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ------------------------------------------------------------------ constants
+PEAGLE_OK = 0
+PEAGLE_ERR_INVALID_ARG = 1
+PEAGLE_ERR_UNSUPPORTED = 2
+PEAGLE_ERR_CUDA = 3
+PEAGLE_ERR_WORKSPACE = 4
+PEAGLE_ERR_DEVICE = 5
+PEAGLE_DEV_BOUNDS = 0x1
+PEAGLE_DEV_TIMEOUT = 0x2
+PEAGLE_F32 = 0
+PEAGLE_BF16 = 1
+OPS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6,
+       "verify": 7, "cod": 8, "ce": 9}
+
+c_int32 = ctypes.c_int32
+c_int64 = ctypes.c_int64
+c_size_t = ctypes.c_size_t
+c_void_p = ctypes.c_void_p
+c_double = ctypes.c_double
+
+
+class peagle_config(ctypes.Structure):
+    _fields_ = [("hidden", c_int32), ("target_hidden", c_int32), ("num_aux", c_int32),
+                ("num_layers", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
+                ("head_dim", c_int32), ("intermediate", c_int32), ("target_vocab", c_int32),
+                ("draft_vocab", c_int32), ("ptd_token_id", c_int32),
+                ("norm_before_residual", c_int32), ("max_position", c_int32), ("dtype", c_int32),
+                ("rope_theta", c_double), ("rms_eps", c_double)]
+
+
+class peagle_layer_weights(ctypes.Structure):
+    _fields_ = [("in_norm_w", c_void_p), ("hidden_norm_w", c_void_p), ("qkv_w", c_void_p),
+                ("o_w", c_void_p), ("post_norm_w", c_void_p), ("gate_up_w", c_void_p),
+                ("down_w", c_void_p)]
+
+
+class peagle_weights(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("fc_w", c_void_p), ("fc_norm_w", c_void_p),
+                ("mask_hidden", c_void_p), ("final_norm_w", c_void_p), ("lm_head_w", c_void_p),
+                ("d2t", c_void_p), ("t2d", c_void_p),
+                ("layers", ctypes.POINTER(peagle_layer_weights))]
+
+
+def _sig(name, restype, *argtypes):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_sig("peagle_version", ctypes.c_char_p)
+_sig("peagle_status_string", ctypes.c_char_p, c_int32)
+_sig("peagle_last_error", ctypes.c_char_p)
+_sig("peagle_kernel_launches", ctypes.c_uint64)
+_sig("peagle_model_create", c_int32, ctypes.POINTER(peagle_config), ctypes.POINTER(peagle_weights),
+     c_void_p, ctypes.POINTER(c_void_p))
+_sig("peagle_model_destroy", c_int32, c_void_p)
+_sig("peagle_get_device_status", c_int32, c_void_p, c_void_p, ctypes.POINTER(c_int32))
+_sig("peagle_clear_device_status", c_int32, c_void_p, c_void_p)
+_sig("peagle_draft_step_workspace_size", c_int32, c_void_p, c_int32, c_int32, c_int32,
+     ctypes.POINTER(c_size_t))
+_sig("peagle_draft_step", c_int32, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+     ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_void_p, c_void_p, c_int64, c_int32,
+     c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
+_sig("peagle_verify_accept", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+     c_void_p)
+_sig("peagle_cod_counts", c_int32, c_int32, c_int32, c_double, c_double, ctypes.POINTER(c_int32))
+_sig("peagle_cod_select_workspace_size", c_int32, c_int32, c_int32, ctypes.POINTER(c_size_t))
+_sig("peagle_cod_select", c_int32, c_int32, c_int32, c_double, c_double, ctypes.c_uint64,
+     ctypes.POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
+_sig("peagle_parallel_forward_workspace_size", c_int32, c_void_p, c_int32, c_int32, c_double,
+     c_double, ctypes.POINTER(c_size_t))
+_sig("peagle_parallel_forward", c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+     c_int32, c_void_p, c_void_p, c_int32, c_double, c_double, ctypes.c_uint64, c_double,
+     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+     c_void_p)
+_sig("peagle_gemm_workspace_size", c_int32, c_int32, c_int32, c_int32, c_int32,
+     ctypes.POINTER(c_size_t))
+_sig("peagle_gemm", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+     c_void_p, c_size_t, c_void_p)
+_sig("peagle_op_name", ctypes.c_char_p, c_int32)
+_sig("peagle_probe_begin", c_int32, c_int32, c_int32)
+_sig("peagle_probe_end", c_int32, ctypes.POINTER(ctypes.c_float), c_int32, ctypes.POINTER(c_int32))
+
+
+class PeagleError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.peagle_last_error().decode()
+        super().__init__(f"{where}: {_lib.peagle_status_string(status).decode()} ({status}): {msg}")
+
+
+def _check(status, where):
+    if status != PEAGLE_OK:
+        raise PeagleError(status, where)
+
+
+def ptr(x):
+    """Device (or host) address of a tensor, an int, or None (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+# --------------------------------------------------------------- the ABI calls
+def peagle_version():
+    return _lib.peagle_version().decode()
+
+
+def peagle_last_error():
+    return _lib.peagle_last_error().decode()
+
+
+def peagle_kernel_launches():
+    return int(_lib.peagle_kernel_launches())
+
+
+def peagle_model_create(cfg: peagle_config, weights: peagle_weights, stream=None):
+    h = c_void_p()
+    _check(_lib.peagle_model_create(ctypes.byref(cfg), ctypes.byref(weights), _stream(stream),
+                                    ctypes.byref(h)), "peagle_model_create")
+    return h.value
+
+
+def peagle_model_destroy(model):
+    _check(_lib.peagle_model_destroy(model), "peagle_model_destroy")
+
+
+def peagle_get_device_status(model, stream=None):
+    v = c_int32()
+    _check(_lib.peagle_get_device_status(model, _stream(stream), ctypes.byref(v)),
+           "peagle_get_device_status")
+    return v.value
+
+
+def peagle_clear_device_status(model, stream=None):
+    _check(_lib.peagle_clear_device_status(model, _stream(stream)), "peagle_clear_device_status")
+
+
+def peagle_draft_step_workspace_size(model, B, K, max_kv_len):
+    n = c_size_t()
+    _check(_lib.peagle_draft_step_workspace_size(model, B, K, max_kv_len, ctypes.byref(n)),
+           "peagle_draft_step_workspace_size")
+    return n.value
+
+
+def peagle_draft_step(model, B, K, aux, anchor_tokens, anchor_pos, k_cache, v_cache, kv_offsets,
+                      kv_lens, kv_capacity, max_kv_len, append_anchor_kv, draft_tokens, logits,
+                      workspace, workspace_bytes, stream=None):
+    L = len(k_cache)
+    karr = (c_void_p * L)(*[ptr(t) for t in k_cache])
+    varr = (c_void_p * L)(*[ptr(t) for t in v_cache])
+    _check(_lib.peagle_draft_step(model, B, K, ptr(aux), ptr(anchor_tokens), ptr(anchor_pos), karr,
+                                  varr, ptr(kv_offsets), ptr(kv_lens), kv_capacity, max_kv_len,
+                                  int(append_anchor_kv), ptr(draft_tokens), ptr(logits),
+                                  ptr(workspace), workspace_bytes, _stream(stream)),
+           "peagle_draft_step")
+
+
+def peagle_verify_accept(B, K, draft_tokens, target_tokens, accept_len, next_token, stream=None):
+    _check(_lib.peagle_verify_accept(B, K, ptr(draft_tokens), ptr(target_tokens), ptr(accept_len),
+                                     ptr(next_token), _stream(stream)), "peagle_verify_accept")
+
+
+def peagle_cod_counts(n, K, r, r_min):
+    out = (c_int32 * K)()
+    _check(_lib.peagle_cod_counts(n, K, r, r_min, out), "peagle_cod_counts")
+    return list(out)
+
+
+def peagle_cod_select_workspace_size(n, K):
+    s = c_size_t()
+    _check(_lib.peagle_cod_select_workspace_size(n, K, ctypes.byref(s)),
+           "peagle_cod_select_workspace_size")
+    return s.value
+
+
+def peagle_cod_select(n, K, r, r_min, seed, indices, row_of=None, workspace=None,
+                      workspace_bytes=0, stream=None):
+    counts = (c_int32 * K)()
+    _check(_lib.peagle_cod_select(n, K, r, r_min, seed & ((1 << 64) - 1), counts, ptr(indices),
+                                  ptr(row_of), ptr(workspace), workspace_bytes, _stream(stream)),
+           "peagle_cod_select")
+    return list(counts)
+
+
+def peagle_parallel_forward_workspace_size(model, n, K, r, r_min):
+    s = c_size_t()
+    _check(_lib.peagle_parallel_forward_workspace_size(model, n, K, r, r_min, ctypes.byref(s)),
+           "peagle_parallel_forward_workspace_size")
+    return s.value
+
+
+def peagle_parallel_forward(model, n, aux, input_ids, position_ids, cu_seqlens, num_seqs, labels,
+                            loss_mask, K, r, r_min, seed, depth_decay, per_depth_loss,
+                            per_depth_acc, per_depth_valid, loss, row_argmax, row_ce, logits,
+                            workspace, workspace_bytes, stream=None):
+    _check(_lib.peagle_parallel_forward(
+        model, n, ptr(aux), ptr(input_ids), ptr(position_ids), ptr(cu_seqlens), num_seqs,
+        ptr(labels), ptr(loss_mask), K, r, r_min, seed & ((1 << 64) - 1), depth_decay,
+        ptr(per_depth_loss), ptr(per_depth_acc), ptr(per_depth_valid), ptr(loss), ptr(row_argmax),
+        ptr(row_ce), ptr(logits), ptr(workspace), workspace_bytes, _stream(stream)),
+        "peagle_parallel_forward")
+
+
+def peagle_gemm_workspace_size(dtype, M, N, K):
+    s = c_size_t()
+    _check(_lib.peagle_gemm_workspace_size(dtype, M, N, K, ctypes.byref(s)),
+           "peagle_gemm_workspace_size")
+    return s.value
+
+
+def peagle_gemm(dtype, M, N, K, X, W, D, workspace, workspace_bytes, stream=None):
+    _check(_lib.peagle_gemm(dtype, M, N, K, ptr(X), ptr(W), ptr(D), ptr(workspace),
+                            workspace_bytes, _stream(stream)), "peagle_gemm")
+
+
+def peagle_op_name(op):
+    return _lib.peagle_op_name(op).decode()
+
+
+def peagle_probe_begin(op, capacity):
+    _check(_lib.peagle_probe_begin(op, capacity), "peagle_probe_begin")
+
+
+def peagle_probe_end(capacity):
+    buf = (ctypes.c_float * max(1, capacity))()
+    n = c_int32()
+    _check(_lib.peagle_probe_end(buf, capacity, ctypes.byref(n)), "peagle_probe_end")
+    return [buf[i] for i in range(min(n.value, capacity))]
+
+
+from .model import Model, make_config  # noqa: E402  (convenience wrapper over the calls above)

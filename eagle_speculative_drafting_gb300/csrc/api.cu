@@ -1,0 +1,887 @@
+// C ABI of the P-EAGLE library: argument validation, the model handle,
+// workspace layout and the launch sequence of each entry point.
+// The arithmetic lives in gemm.cu, rows.cu and attn.cu.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "rows.cuh"
+
+using namespace pe;
+
+// ===================================================================== state
+static thread_local std::string g_err;
+static std::atomic<unsigned long long> g_launches{0};
+
+namespace pe {
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void set_error(const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+}
+int num_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    sms = v;
+  }
+  return sms;
+}
+
+// ---- timing probe: event pairs around the main kernel of one op class
+static std::mutex g_probe_mu;
+static int g_probe_op = -1, g_probe_cap = 0, g_probe_n = 0;
+static bool g_probe_armed = false;
+static std::vector<cudaEvent_t> g_ev0, g_ev1;
+
+void probe_start(int op, cudaStream_t s) {
+  if (op < 0 || op != g_probe_op || g_probe_n >= g_probe_cap) return;
+  cudaEventRecord(g_ev0[g_probe_n], s);
+  g_probe_armed = true;
+}
+void probe_stop(int op, cudaStream_t s) {
+  if (!g_probe_armed || op != g_probe_op) return;
+  cudaEventRecord(g_ev1[g_probe_n], s);
+  ++g_probe_n;
+  g_probe_armed = false;
+}
+}  // namespace pe
+
+struct peagle_model {
+  peagle_config cfg;
+  peagle_weights w;
+  std::vector<peagle_layer_weights> layers;
+  float* rcos = nullptr;
+  float* rsin = nullptr;
+  float* mask_qkv0 = nullptr;   // [QKV] pre-rotary q/k/v of a masked layer-0 row
+  float* mask_resid0 = nullptr; // [H] its layer-0 residual
+  int* status = nullptr;
+};
+
+#define FAIL(code, ...)      \
+  do {                       \
+    set_error(__VA_ARGS__);  \
+    return code;             \
+  } while (0)
+
+#define CUDA_TRY(expr)                                                                 \
+  do {                                                                                 \
+    cudaError_t e_ = (expr);                                                           \
+    if (e_ != cudaSuccess) FAIL(PEAGLE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Bump allocator over the caller's workspace; a dry run (base == NULL)
+// measures the size.
+struct Bump {
+  char* base;
+  size_t off = 0;
+  explicit Bump(void* b) : base(static_cast<char*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T) + 16;
+    return p;
+  }
+  void* take_bytes(size_t bytes) { return take<char>(bytes); }
+};
+
+static size_t esize(const peagle_config& c) { return c.dtype == PEAGLE_BF16 ? 2 : 4; }
+static int qkv_out(const peagle_config& c) { return (c.num_q_heads + 2 * c.num_kv_heads) * c.head_dim; }
+
+// ================================================================== library
+extern "C" {
+
+const char* peagle_version(void) { return "peagle-gb300 0.1 (sm_103a)"; }
+
+const char* peagle_status_string(peagle_status s) {
+  switch (s) {
+    case PEAGLE_OK: return "ok";
+    case PEAGLE_ERR_INVALID_ARG: return "invalid argument";
+    case PEAGLE_ERR_UNSUPPORTED: return "unsupported";
+    case PEAGLE_ERR_CUDA: return "CUDA error";
+    case PEAGLE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case PEAGLE_ERR_DEVICE: return "device status set";
+  }
+  return "unknown status";
+}
+
+const char* peagle_last_error(void) { return g_err.c_str(); }
+
+uint64_t peagle_kernel_launches(void) { return g_launches.load(); }
+
+const char* peagle_op_name(int32_t op) {
+  static const char* names[] = {"fc", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head",
+                                "verify", "cod", "ce"};
+  return (op >= 0 && op < PEAGLE_OP_COUNT) ? names[op] : "unknown";
+}
+
+peagle_status peagle_probe_begin(int32_t op, int32_t capacity) {
+  if (op < 0 || op >= PEAGLE_OP_COUNT || capacity <= 0 || capacity > (1 << 20))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "probe_begin: bad op %d or capacity %d", op, capacity);
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  for (auto e : g_ev0) cudaEventDestroy(e);
+  for (auto e : g_ev1) cudaEventDestroy(e);
+  g_ev0.assign(capacity, nullptr);
+  g_ev1.assign(capacity, nullptr);
+  for (int i = 0; i < capacity; ++i) {
+    CUDA_TRY(cudaEventCreate(&g_ev0[i]));
+    CUDA_TRY(cudaEventCreate(&g_ev1[i]));
+  }
+  g_probe_cap = capacity;
+  g_probe_n = 0;
+  g_probe_armed = false;
+  g_probe_op = op;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_probe_end(float* ms_out, int32_t capacity, int32_t* count) {
+  std::lock_guard<std::mutex> lk(g_probe_mu);
+  if (!count) FAIL(PEAGLE_ERR_INVALID_ARG, "probe_end: count is NULL");
+  const int n = g_probe_n;
+  for (int i = 0; i < n; ++i) {
+    CUDA_TRY(cudaEventSynchronize(g_ev1[i]));
+    float ms = 0.f;
+    CUDA_TRY(cudaEventElapsedTime(&ms, g_ev0[i], g_ev1[i]));
+    if (ms_out && i < capacity) ms_out[i] = ms;
+  }
+  *count = n;
+  for (auto e : g_ev0) cudaEventDestroy(e);
+  for (auto e : g_ev1) cudaEventDestroy(e);
+  g_ev0.clear();
+  g_ev1.clear();
+  g_probe_op = -1;
+  g_probe_cap = 0;
+  g_probe_n = 0;
+  return PEAGLE_OK;
+}
+
+// ==================================================================== model
+static peagle_status validate_config(const peagle_config* c) {
+  if (!c) FAIL(PEAGLE_ERR_INVALID_ARG, "config is NULL");
+  if (c->dtype != PEAGLE_F32 && c->dtype != PEAGLE_BF16) FAIL(PEAGLE_ERR_INVALID_ARG, "dtype %d", c->dtype);
+  if (c->hidden <= 0 || c->target_hidden <= 0 || c->num_aux <= 0 || c->num_layers <= 0 ||
+      c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->intermediate <= 0 || c->target_vocab <= 0 ||
+      c->draft_vocab <= 0 || c->max_position <= 0)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "config sizes must be positive");
+  if (c->num_q_heads % c->num_kv_heads) FAIL(PEAGLE_ERR_INVALID_ARG, "num_q_heads %% num_kv_heads != 0");
+  if (c->head_dim != 64 && c->head_dim != 128) FAIL(PEAGLE_ERR_UNSUPPORTED, "head_dim %d not in {64,128}", c->head_dim);
+  if (c->ptd_token_id < 0 || c->ptd_token_id >= c->target_vocab)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "ptd_token_id %d outside [0, %d)", c->ptd_token_id, c->target_vocab);
+  if (!(c->rms_eps > 0) || !(c->rope_theta > 0)) FAIL(PEAGLE_ERR_INVALID_ARG, "rms_eps and rope_theta must be > 0");
+  if (c->norm_before_residual != 0 && c->norm_before_residual != 1)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "norm_before_residual must be 0 or 1");
+  if (c->hidden > 12288) FAIL(PEAGLE_ERR_UNSUPPORTED, "hidden %d > 12288", c->hidden);
+  if (c->num_layers > 64) FAIL(PEAGLE_ERR_UNSUPPORTED, "num_layers %d > 64", c->num_layers);
+  if ((long long)c->max_position * c->head_dim > (1LL << 31)) FAIL(PEAGLE_ERR_UNSUPPORTED, "max_position too large");
+  if (c->dtype == PEAGLE_BF16) {
+    const long long ks[] = {(long long)c->num_aux * c->target_hidden, 2LL * c->hidden, c->hidden,
+                            (long long)c->num_q_heads * c->head_dim, c->intermediate};
+    for (long long k : ks)
+      if (k % 8) FAIL(PEAGLE_ERR_UNSUPPORTED, "bf16 contraction width %lld not a multiple of 8", k);
+  }
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights* w, void* stream,
+                                  peagle_model** out) {
+  if (!out) FAIL(PEAGLE_ERR_INVALID_ARG, "out is NULL");
+  peagle_status st = validate_config(cfg);
+  if (st) return st;
+  if (!w || !w->embed || !w->fc_w || !w->fc_norm_w || !w->mask_hidden || !w->final_norm_w || !w->lm_head_w ||
+      !w->layers)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "a required weight pointer is NULL");
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    const peagle_layer_weights& L = w->layers[l];
+    if (!L.in_norm_w || !L.qkv_w || !L.o_w || !L.post_norm_w || !L.gate_up_w || !L.down_w ||
+        (l == 0 && !L.hidden_norm_w))
+      FAIL(PEAGLE_ERR_INVALID_ARG, "layer %d: a required weight pointer is NULL", l);
+    if (cfg->dtype == PEAGLE_BF16 &&
+        !(aligned16(L.qkv_w) && aligned16(L.o_w) && aligned16(L.gate_up_w) && aligned16(L.down_w)))
+      FAIL(PEAGLE_ERR_INVALID_ARG, "layer %d: bf16 weights must be 16-byte aligned", l);
+  }
+  if (cfg->dtype == PEAGLE_BF16 && !(aligned16(w->fc_w) && aligned16(w->lm_head_w) && aligned16(w->mask_hidden)))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "bf16 weights must be 16-byte aligned");
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  peagle_model* m = new peagle_model();
+  m->cfg = *cfg;
+  m->w = *w;
+  m->layers.assign(w->layers, w->layers + cfg->num_layers);
+  m->w.layers = m->layers.data();
+  const peagle_config& c = m->cfg;
+  const int H = c.hidden, QKV = qkv_out(c), AHt = c.num_aux * c.target_hidden;
+  const size_t half = c.head_dim / 2;
+  void* tmp = nullptr;
+  auto cleanup = [&](peagle_status code) {
+    if (tmp) cudaFree(tmp);
+    if (code != PEAGLE_OK) {
+      cudaFree(m->rcos);
+      cudaFree(m->rsin);
+      cudaFree(m->mask_qkv0);
+      cudaFree(m->mask_resid0);
+      cudaFree(m->status);
+      delete m;
+    }
+    return code;
+  };
+#define CREATE_TRY(expr)                                                                    \
+  do {                                                                                      \
+    cudaError_t e_ = (expr);                                                                \
+    if (e_ != cudaSuccess) {                                                                \
+      set_error("model_create: %s: %s", #expr, cudaGetErrorString(e_));                     \
+      return cleanup(PEAGLE_ERR_CUDA);                                                      \
+    }                                                                                       \
+  } while (0)
+  CREATE_TRY(cudaMalloc(&m->rcos, (size_t)c.max_position * half * sizeof(float)));
+  CREATE_TRY(cudaMalloc(&m->rsin, (size_t)c.max_position * half * sizeof(float)));
+  CREATE_TRY(cudaMalloc(&m->mask_qkv0, (size_t)QKV * sizeof(float)));
+  CREATE_TRY(cudaMalloc(&m->mask_resid0, (size_t)H * sizeof(float)));
+  CREATE_TRY(cudaMalloc(&m->status, sizeof(int)));
+  CREATE_TRY(cudaMemsetAsync(m->status, 0, sizeof(int), s));
+  CREATE_TRY(launch_rope_table(m->rcos, m->rsin, c.max_position, c.head_dim, c.rope_theta, s));
+
+  // masked-row constants: fc_norm(fc(mask_hidden)), the ptd embedding, and
+  // the layer-0 pre-rotary q/k/v + residual every masked row shares
+  const size_t part_f = std::max(gemm_out_floats(c.dtype, 1, H, AHt), gemm_out_floats(c.dtype, 1, QKV, 2 * H));
+  const size_t x0_bytes = ((2 * (size_t)H * esize(c)) + 255) & ~size_t(255);
+  CREATE_TRY(cudaMalloc(&tmp, x0_bytes + part_f * sizeof(float)));
+  void* x0m = tmp;
+  float* part = reinterpret_cast<float*>(static_cast<char*>(tmp) + x0_bytes);
+  GemmOut go;
+  CREATE_TRY(gemm_launch(c.dtype, w->mask_hidden, AHt, w->fc_w, 1, H, AHt, part, &go, m->status, -1, s));
+  FcFinishArgs fa{};
+  fa.u = go;
+  fa.H = H;
+  fa.Vt = c.target_vocab;
+  fa.tok = nullptr;
+  fa.tok_const = c.ptd_token_id;
+  fa.embed = w->embed;
+  fa.g_fc = w->fc_norm_w;
+  fa.g_in = m->layers[0].in_norm_w;
+  fa.g_h = m->layers[0].hidden_norm_w;
+  fa.eps = (float)c.rms_eps;
+  fa.nbr = c.norm_before_residual;
+  fa.x0 = x0m;
+  fa.resid = m->mask_resid0;
+  fa.status = m->status;
+  CREATE_TRY(launch_fc_finish(c.dtype, 1, fa, s));
+  CREATE_TRY(gemm_launch(c.dtype, x0m, 2 * H, m->layers[0].qkv_w, 1, QKV, 2 * H, part, &go, m->status, -1, s));
+  CREATE_TRY(launch_sum_splits(go, 1, QKV, m->mask_qkv0, s));
+  CREATE_TRY(cudaStreamSynchronize(s));
+  int hs = 0;
+  CREATE_TRY(cudaMemcpy(&hs, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (hs) {
+    set_error("model_create: device status 0x%x while precomputing masked-row constants", hs);
+    return cleanup(PEAGLE_ERR_DEVICE);
+  }
+  cleanup(PEAGLE_OK);
+  *out = m;
+#undef CREATE_TRY
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_model_destroy(peagle_model* m) {
+  if (!m) return PEAGLE_OK;
+  cudaDeviceSynchronize();
+  cudaFree(m->rcos);
+  cudaFree(m->rsin);
+  cudaFree(m->mask_qkv0);
+  cudaFree(m->mask_resid0);
+  cudaFree(m->status);
+  delete m;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_get_device_status(const peagle_model* m, void* stream, int32_t* host_status) {
+  if (!m || !host_status) FAIL(PEAGLE_ERR_INVALID_ARG, "get_device_status: NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaStreamSynchronize(s));
+  int v = 0;
+  CUDA_TRY(cudaMemcpy(&v, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+  *host_status = v;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_clear_device_status(const peagle_model* m, void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "clear_device_status: NULL model");
+  CUDA_TRY(cudaMemsetAsync(m->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)));
+  return PEAGLE_OK;
+}
+
+// =============================================================== draft step
+struct DraftWs {
+  void *x0, *xin, *act, *q, *kc, *vc, *ao;
+  float *h, *resid0, *part, *attn_o, *attn_ml, *am_val;
+  int* am_idx;
+  int chunk, nsplit;
+};
+
+static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, Bump& bp, DraftWs& ws) {
+  const size_t es = esize(c);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K;
+  const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
+  ws.x0 = bp.take_bytes((size_t)B * 2 * H * es);
+  ws.xin = bp.take_bytes((size_t)rows * H * es);
+  ws.act = bp.take_bytes((size_t)rows * I * es);
+  ws.q = bp.take_bytes((size_t)rows * nq * hd * es);
+  ws.kc = bp.take_bytes((size_t)rows * nkv * hd * es);
+  ws.vc = bp.take_bytes((size_t)rows * nkv * hd * es);
+  ws.ao = bp.take_bytes((size_t)rows * nq * hd * es);
+  ws.h = bp.take<float>((size_t)rows * H);
+  ws.resid0 = bp.take<float>((size_t)B * H);
+  size_t pf = gemm_out_floats(c.dtype, B, H, AHt);
+  pf = std::max(pf, gemm_out_floats(c.dtype, B, QKV, 2 * H));
+  pf = std::max(pf, gemm_out_floats(c.dtype, rows, QKV, H));
+  pf = std::max(pf, gemm_out_floats(c.dtype, rows, H, nq * hd));
+  pf = std::max(pf, gemm_out_floats(c.dtype, rows, 2 * I, H));
+  pf = std::max(pf, gemm_out_floats(c.dtype, rows, H, I));
+  pf = std::max(pf, gemm_out_floats(c.dtype, rows, c.draft_vocab, H));
+  ws.part = bp.take<float>(pf);
+  decode_attn_plan(B, nkv, max_kv_len, &ws.chunk, &ws.nsplit);
+  const size_t prow = (size_t)B * nkv * ws.nsplit * K * (nq / nkv);
+  ws.attn_o = bp.take<float>(prow * hd);
+  ws.attn_ml = bp.take<float>(prow * 2);
+  const size_t nch = lm_argmax_chunks(c.draft_vocab);
+  ws.am_val = bp.take<float>((size_t)rows * nch);
+  ws.am_idx = bp.take<int>((size_t)rows * nch);
+}
+
+peagle_status peagle_draft_step_workspace_size(const peagle_model* m, int32_t B, int32_t K, int32_t max_kv_len,
+                                               size_t* bytes) {
+  if (!m || !bytes) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_workspace_size: NULL argument");
+  if (B < 0 || K < 1 || K > 16 || max_kv_len < 0)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_workspace_size: B=%d K=%d max_kv_len=%d", B, K, max_kv_len);
+  Bump bp(nullptr);
+  DraftWs ws;
+  draft_layout(m->cfg, B, K, max_kv_len, bp, ws);
+  *bytes = bp.off;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, const void* aux,
+                                const int32_t* anchor_tokens, const int32_t* anchor_pos, void* const* k_cache,
+                                void* const* v_cache, const int64_t* kv_offsets, const int32_t* kv_lens,
+                                int64_t kv_capacity, int32_t max_kv_len, int32_t append_anchor_kv,
+                                int32_t* draft_tokens, float* logits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: model is NULL");
+  const peagle_config& c = m->cfg;
+  if (B < 0 || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: B=%d K=%d (K in [1,16])", B, K);
+  if (max_kv_len < 0 || kv_capacity < 0) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: negative KV bound");
+  if (append_anchor_kv != 0 && append_anchor_kv != 1) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: append_anchor_kv");
+  if (B == 0) return PEAGLE_OK;
+  if (!aux || !anchor_tokens || !anchor_pos || !k_cache || !v_cache || !kv_offsets || !kv_lens || !draft_tokens)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: a required pointer is NULL");
+  for (int l = 0; l < c.num_layers; ++l)
+    if (!k_cache[l] || !v_cache[l]) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is NULL", l);
+  if (c.dtype == PEAGLE_BF16 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: aux not 16-byte aligned");
+  size_t need = 0;
+  peagle_draft_step_workspace_size(m, B, K, max_kv_len, &need);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "draft_step: workspace %zu bytes at %p, need %zu (256-byte aligned)",
+         workspace_bytes, workspace, need);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Bump bp(workspace);
+  DraftWs ws;
+  draft_layout(c, B, K, max_kv_len, bp, ws);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K, L = c.num_layers;
+  const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
+  const int dt = c.dtype;
+  const float eps = (float)c.rms_eps;
+  GemmOut go;
+
+  // fc + fc_norm over the anchors' aux states, then the layer-0 input rows
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->status, PEAGLE_OP_FC, s));
+  FcFinishArgs fa{};
+  fa.u = go;
+  fa.H = H;
+  fa.Vt = c.target_vocab;
+  fa.tok = anchor_tokens;
+  fa.embed = m->w.embed;
+  fa.g_fc = m->w.fc_norm_w;
+  fa.g_in = m->layers[0].in_norm_w;
+  fa.g_h = m->layers[0].hidden_norm_w;
+  fa.eps = eps;
+  fa.nbr = c.norm_before_residual;
+  fa.x0 = ws.x0;
+  fa.resid = ws.resid0;
+  fa.status = m->status;
+  CUDA_TRY(launch_fc_finish(dt, B, fa, s));
+
+  for (int l = 0; l < L; ++l) {
+    const peagle_layer_weights& W = m->layers[l];
+    QkvArgs qa{};
+    if (l == 0) {
+      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->status, PEAGLE_OP_QKV, s));
+      qa.mode = 1;
+      qa.resid0 = ws.resid0;
+      qa.mask_resid = m->mask_resid0;
+      qa.h = ws.h;
+    } else {
+      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, m->status, PEAGLE_OP_QKV, s));
+      qa.mode = 0;
+    }
+    qa.in = go;
+    qa.nq = nq;
+    qa.nkv = nkv;
+    qa.hd = hd;
+    qa.H = H;
+    qa.K = K;
+    qa.mask_qkv = m->mask_qkv0;
+    qa.rcos = m->rcos;
+    qa.rsin = m->rsin;
+    qa.max_pos = c.max_position;
+    qa.anchor_pos = anchor_pos;
+    qa.Q = ws.q;
+    qa.Kout = ws.kc;
+    qa.Vout = ws.vc;
+    if (append_anchor_kv) {
+      qa.kcache = k_cache[l];
+      qa.vcache = v_cache[l];
+    }
+    qa.kv_off = kv_offsets;
+    qa.kv_len = kv_lens;
+    qa.kv_cap = kv_capacity;
+    qa.status = m->status;
+    // mode 1 reads the GEMM row of the anchor; mode 0 row r
+    CUDA_TRY(launch_qkv_finish(dt, rows, qa, s));
+
+    DecodeAttnArgs da{};
+    da.B = B;
+    da.K = K;
+    da.nq = nq;
+    da.nkv = nkv;
+    da.hd = hd;
+    da.Q = ws.q;
+    da.Kc = ws.kc;
+    da.Vc = ws.vc;
+    da.kcache = k_cache[l];
+    da.vcache = v_cache[l];
+    da.kv_off = kv_offsets;
+    da.kv_len = kv_lens;
+    da.kv_cap = kv_capacity;
+    da.max_kv_len = max_kv_len;
+    da.chunk = ws.chunk;
+    da.nsplit = ws.nsplit;
+    da.part_o = ws.attn_o;
+    da.part_ml = ws.attn_ml;
+    da.O = ws.ao;
+    da.scale = 1.0f / sqrtf((float)hd);
+    da.status = m->status;
+    CUDA_TRY(launch_decode_attn(dt, da, PEAGLE_OP_ATTN, s));
+
+    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, m->status, PEAGLE_OP_O, s));
+    ResidNormArgs ra{};
+    ra.in = go;
+    ra.H = H;
+    ra.row0 = 0;
+    ra.h = ws.h;
+    ra.gain = W.post_norm_w;
+    ra.eps = eps;
+    ra.y = ws.xin;
+    CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
+
+    CUDA_TRY(gemm_launch(dt, ws.xin, H, W.gate_up_w, rows, 2 * I, H, ws.part, &go, m->status, PEAGLE_OP_GATE_UP, s));
+    CUDA_TRY(launch_swiglu(dt, go, rows, I, ws.act, s));
+    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->status, PEAGLE_OP_DOWN, s));
+    ra.in = go;
+    ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
+    CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
+  }
+  // draft-vocab head and argmax per depth
+  CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->status,
+                       PEAGLE_OP_LM_HEAD, s));
+  CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
+  return PEAGLE_OK;
+}
+
+// ==================================================================== verify
+peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_tokens, const int32_t* target_tokens,
+                                   int32_t* accept_len, int32_t* next_token, void* stream) {
+  if (B < 0 || K < 1 || K > 64) FAIL(PEAGLE_ERR_INVALID_ARG, "verify_accept: B=%d K=%d (K in [1,64])", B, K);
+  if (B == 0) return PEAGLE_OK;
+  if (!draft_tokens || !target_tokens || !accept_len || !next_token)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "verify_accept: a pointer is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  probe_start(PEAGLE_OP_VERIFY, s);
+  CUDA_TRY(launch_verify(B, K, draft_tokens, target_tokens, accept_len, next_token, s));
+  probe_stop(PEAGLE_OP_VERIFY, s);
+  return PEAGLE_OK;
+}
+
+// ======================================================================= COD
+peagle_status peagle_cod_counts(int32_t n, int32_t K, double r, double r_min, int32_t* counts) {
+  if (n < 0 || n > (1 << 24) || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "cod_counts: n=%d K=%d", n, K);
+  if (!(r_min > 0.0) || !(r_min <= r) || !(r <= 1.0))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "cod_counts: need 0 < r_min <= r <= 1 (r=%g r_min=%g)", r, r_min);
+  if (!counts) FAIL(PEAGLE_ERR_INVALID_ARG, "cod_counts: counts is NULL");
+  counts[0] = n;
+  double rd = 1.0;
+  const long long fmin = (long long)floor((double)n * r_min);
+  for (int d = 1; d < K; ++d) {
+    rd = rd * r;
+    long long c = (long long)floor((double)n * rd);
+    if (c < fmin) c = fmin;
+    if (c > counts[d - 1]) c = counts[d - 1];
+    counts[d] = (int32_t)c;
+  }
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_cod_select_workspace_size(int32_t n, int32_t K, size_t* bytes) {
+  if (!bytes || n < 0 || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "cod_select_workspace_size: bad argument");
+  *bytes = 0;  // keys are regenerated from the counter, nothing is staged
+  return PEAGLE_OK;
+}
+
+static peagle_status cod_enqueue(int n, int K, uint64_t seed, const int32_t* counts, int32_t* indices,
+                                 int32_t* row_of, cudaStream_t s) {
+  CodArgs ca{};
+  ca.n = n;
+  ca.K = K;
+  ca.seed = seed;
+  ca.off[0] = 0;
+  for (int d = 0; d < K; ++d) {
+    ca.counts[d] = counts[d];
+    ca.off[d + 1] = ca.off[d] + counts[d];
+  }
+  ca.indices = indices;
+  ca.row_of = row_of;
+  probe_start(PEAGLE_OP_COD, s);
+  CUDA_TRY(launch_cod_select(ca, s));
+  probe_stop(PEAGLE_OP_COD, s);
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_cod_select(int32_t n, int32_t K, double r, double r_min, uint64_t seed, int32_t* counts_host,
+                                int32_t* indices, int32_t* row_of, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  int32_t counts[16];
+  peagle_status st = peagle_cod_counts(n, K, r, r_min, counts);
+  if (st) return st;
+  if (counts_host) memcpy(counts_host, counts, sizeof(int32_t) * K);
+  if (n == 0) return PEAGLE_OK;
+  if (!indices) FAIL(PEAGLE_ERR_INVALID_ARG, "cod_select: indices is NULL");
+  return cod_enqueue(n, K, seed, counts, indices, row_of, static_cast<cudaStream_t>(stream));
+}
+
+// ============================================================= dense GEMM
+peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, int32_t K, size_t* bytes) {
+  if (!bytes || M < 0 || N < 0 || K < 1 || (dtype != PEAGLE_F32 && dtype != PEAGLE_BF16))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "gemm_workspace_size: bad argument");
+  *bytes = dtype == PEAGLE_BF16 ? gemm_out_floats(dtype, M, N, K) * sizeof(float) : 0;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X, const void* W, float* D,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 1 || (dtype != PEAGLE_F32 && dtype != PEAGLE_BF16))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "gemm: M=%d N=%d K=%d dtype=%d", M, N, K, dtype);
+  if (M == 0 || N == 0) return PEAGLE_OK;
+  if (!X || !W || !D) FAIL(PEAGLE_ERR_INVALID_ARG, "gemm: NULL operand");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == PEAGLE_F32) {
+    CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, D, nullptr, nullptr, -1, s));
+    return PEAGLE_OK;
+  }
+  if (K % 8 || !aligned16(X) || !aligned16(W)) FAIL(PEAGLE_ERR_INVALID_ARG, "gemm: bf16 needs K %% 8 == 0 and 16-byte aligned operands");
+  size_t need = gemm_out_floats(dtype, M, N, K) * sizeof(float);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "gemm: workspace %zu bytes, need %zu", workspace_bytes, need);
+  GemmOut go;
+  CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, static_cast<float*>(workspace), &go, nullptr, -1, s));
+  CUDA_TRY(launch_sum_splits(go, M, N, D, s));
+  return PEAGLE_OK;
+}
+
+}  // extern "C"
+
+
+// ========================================================= parallel forward
+struct TrainWs {
+  int *indices, *row_of, *anchor, *depth, *pos, *start, *label;
+  void *x0, *xin, *act, *q, *kr, *vr, *ao;
+  float *resid0, *h, *part, *row_ce;
+  int* row_am;
+  int rc;  // rows per GEMM chunk
+};
+
+static const int kTrainChunk = 16384;
+
+static size_t chunk_part_floats(int dt, int total, int rc, int N, int K) {
+  if (total <= 0) return 0;
+  size_t f = gemm_out_floats(dt, std::min(total, rc), N, K);
+  const int last = total % rc;
+  if (last) f = std::max(f, gemm_out_floats(dt, last, N, K));
+  return f;
+}
+
+static void train_layout(const peagle_config& c, int n, int K, int R, Bump& bp, TrainWs& ws) {
+  const size_t es = esize(c);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), AHt = c.num_aux * c.target_hidden;
+  const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, dt = c.dtype;
+  const int rc = std::max(1, std::min(R, kTrainChunk));
+  ws.rc = rc;
+  ws.indices = bp.take<int>(R);
+  ws.row_of = bp.take<int>((size_t)K * n);
+  ws.anchor = bp.take<int>(R);
+  ws.depth = bp.take<int>(R);
+  ws.pos = bp.take<int>(R);
+  ws.start = bp.take<int>(R);
+  ws.label = bp.take<int>(R);
+  ws.x0 = bp.take_bytes((size_t)n * 2 * H * es);
+  ws.resid0 = bp.take<float>((size_t)n * H);
+  ws.h = bp.take<float>((size_t)R * H);
+  ws.xin = bp.take_bytes((size_t)R * H * es);
+  ws.act = bp.take_bytes((size_t)rc * I * es);
+  ws.q = bp.take_bytes((size_t)R * nq * hd * es);
+  ws.kr = bp.take_bytes((size_t)R * nkv * hd * es);
+  ws.vr = bp.take_bytes((size_t)R * nkv * hd * es);
+  ws.ao = bp.take_bytes((size_t)R * nq * hd * es);
+  size_t pf = chunk_part_floats(dt, n, rc, H, AHt);
+  pf = std::max(pf, chunk_part_floats(dt, n, rc, QKV, 2 * H));
+  pf = std::max(pf, chunk_part_floats(dt, R, rc, QKV, H));
+  pf = std::max(pf, chunk_part_floats(dt, R, rc, H, nq * hd));
+  pf = std::max(pf, chunk_part_floats(dt, R, rc, 2 * I, H));
+  pf = std::max(pf, chunk_part_floats(dt, R, rc, H, I));
+  pf = std::max(pf, chunk_part_floats(dt, R, rc, c.draft_vocab, H));
+  ws.part = bp.take<float>(pf);
+  ws.row_ce = bp.take<float>(R);
+  ws.row_am = bp.take<int>(R);
+}
+
+extern "C" {
+
+peagle_status peagle_parallel_forward_workspace_size(const peagle_model* m, int32_t n, int32_t K, double r,
+                                                     double r_min, size_t* bytes) {
+  if (!m || !bytes) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward_workspace_size: NULL argument");
+  int32_t counts[16];
+  peagle_status st = peagle_cod_counts(n, K, r, r_min, counts);
+  if (st) return st;
+  int R = 0;
+  for (int d = 0; d < K; ++d) R += counts[d];
+  Bump bp(nullptr);
+  TrainWs ws;
+  train_layout(m->cfg, n, K, R, bp, ws);
+  *bytes = bp.off;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const void* aux, const int32_t* input_ids,
+                                      const int32_t* position_ids, const int32_t* cu_seqlens, int32_t num_seqs,
+                                      const int32_t* labels, const uint8_t* loss_mask, int32_t K, double r,
+                                      double r_min, uint64_t seed, double depth_decay, float* per_depth_loss,
+                                      float* per_depth_acc, int32_t* per_depth_valid, float* loss,
+                                      int32_t* row_argmax, float* row_ce, float* logits, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: model is NULL");
+  const peagle_config& c = m->cfg;
+  int32_t counts[16];
+  peagle_status st = peagle_cod_counts(n, K, r, r_min, counts);
+  if (st) return st;
+  if (!isfinite(depth_decay)) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: depth_decay not finite");
+  if (!per_depth_loss || !per_depth_acc || !per_depth_valid || !loss)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: a required output is NULL");
+  if (n > 0 && (!aux || !input_ids || !position_ids || !cu_seqlens || !labels || num_seqs < 1 || num_seqs > n))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: a required input is NULL or num_seqs=%d out of [1, n]", num_seqs);
+  if (c.dtype == PEAGLE_BF16 && n > 0 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: aux not 16-byte aligned");
+  int off[17];
+  off[0] = 0;
+  for (int d = 0; d < K; ++d) off[d + 1] = off[d] + counts[d];
+  const int R = off[K];
+  size_t need = 0;
+  peagle_parallel_forward_workspace_size(m, n, K, r, r_min, &need);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "parallel_forward: workspace %zu bytes at %p, need %zu (256-byte aligned)",
+         workspace_bytes, workspace, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Bump bp(workspace);
+  TrainWs ws;
+  train_layout(c, n, K, R, bp, ws);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), L = c.num_layers, V = c.draft_vocab;
+  const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
+  const int dt = c.dtype, rc = ws.rc;
+  const size_t es = esize(c);
+  const float eps = (float)c.rms_eps;
+  float* rce = row_ce ? row_ce : ws.row_ce;
+  int* ram = row_argmax ? row_argmax : ws.row_am;
+  auto at = [es](void* base, size_t elems) { return static_cast<char*>(base) + elems * es; };
+  auto atc = [es](const void* base, size_t elems) { return static_cast<const char*>(base) + elems * es; };
+  GemmOut go;
+
+  if (n > 0) {
+    // COD rows and per-row metadata
+    st = cod_enqueue(n, K, seed, counts, ws.indices, ws.row_of, s);
+    if (st) return st;
+    TrainMetaArgs ta{};
+    ta.n = n;
+    ta.R = R;
+    ta.K = K;
+    ta.S = num_seqs;
+    ta.Vt = c.target_vocab;
+    ta.Vd = V;
+    ta.max_pos = c.max_position;
+    memcpy(ta.off, off, sizeof off);
+    ta.indices = ws.indices;
+    ta.position_ids = position_ids;
+    ta.cu = cu_seqlens;
+    ta.labels = labels;
+    ta.loss_mask = loss_mask;
+    ta.t2d = m->w.t2d;
+    ta.row_anchor = ws.anchor;
+    ta.row_depth = ws.depth;
+    ta.row_pos = ws.pos;
+    ta.row_start = ws.start;
+    ta.row_label = ws.label;
+    ta.status = m->status;
+    CUDA_TRY(launch_train_meta(ta, s));
+
+    // fc + fc_norm + layer-0 inputs of the n depth-0 rows
+    for (int c0 = 0; c0 < n; c0 += rc) {
+      const int mr = std::min(rc, n - c0);
+      CUDA_TRY(gemm_launch(dt, atc(aux, (size_t)c0 * AHt), AHt, m->w.fc_w, mr, H, AHt, ws.part, &go, m->status,
+                           PEAGLE_OP_FC, s));
+      FcFinishArgs fa{};
+      fa.u = go;
+      fa.H = H;
+      fa.Vt = c.target_vocab;
+      fa.tok = input_ids + c0;
+      fa.embed = m->w.embed;
+      fa.g_fc = m->w.fc_norm_w;
+      fa.g_in = m->layers[0].in_norm_w;
+      fa.g_h = m->layers[0].hidden_norm_w;
+      fa.eps = eps;
+      fa.nbr = c.norm_before_residual;
+      fa.x0 = at(ws.x0, (size_t)c0 * 2 * H);
+      fa.resid = ws.resid0 + (size_t)c0 * H;
+      fa.status = m->status;
+      CUDA_TRY(launch_fc_finish(dt, mr, fa, s));
+    }
+
+    for (int l = 0; l < L; ++l) {
+      const peagle_layer_weights& W = m->layers[l];
+      QkvArgs qa{};
+      qa.nq = nq;
+      qa.nkv = nkv;
+      qa.hd = hd;
+      qa.H = H;
+      qa.K = K;
+      qa.mask_qkv = m->mask_qkv0;
+      qa.mask_resid = m->mask_resid0;
+      qa.rcos = m->rcos;
+      qa.rsin = m->rsin;
+      qa.max_pos = c.max_position;
+      qa.row_pos = ws.pos;
+      qa.Q = ws.q;
+      qa.Kout = ws.kr;
+      qa.Vout = ws.vr;
+      qa.status = m->status;
+      const int src_rows = (l == 0) ? n : R;
+      for (int c0 = 0; c0 < src_rows; c0 += rc) {
+        const int mr = std::min(rc, src_rows - c0);
+        if (l == 0)
+          CUDA_TRY(gemm_launch(dt, atc(ws.x0, (size_t)c0 * 2 * H), 2 * H, W.qkv_w, mr, QKV, 2 * H, ws.part, &go,
+                               m->status, PEAGLE_OP_QKV, s));
+        else
+          CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.qkv_w, mr, QKV, H, ws.part, &go, m->status,
+                               PEAGLE_OP_QKV, s));
+        qa.in = go;
+        qa.mode = 0;
+        qa.row0 = c0;
+        qa.src0 = c0;
+        qa.resid0 = (l == 0) ? ws.resid0 + (size_t)c0 * H : nullptr;
+        qa.h = (l == 0) ? ws.h : nullptr;
+        CUDA_TRY(launch_qkv_finish(dt, mr, qa, s));
+      }
+      if (l == 0 && R > n) {  // every masked row of layer 0 shares one pre-rotary q/k/v
+        qa.mode = 2;
+        qa.row0 = n;
+        qa.src0 = n;
+        qa.resid0 = nullptr;
+        qa.h = ws.h;
+        CUDA_TRY(launch_qkv_finish(dt, R - n, qa, s));
+      }
+      TrainAttnArgs aa{};
+      aa.R = R;
+      aa.n = n;
+      aa.nq = nq;
+      aa.nkv = nkv;
+      aa.hd = hd;
+      aa.Q = ws.q;
+      aa.Kr = ws.kr;
+      aa.Vr = ws.vr;
+      aa.row_anchor = ws.anchor;
+      aa.row_depth = ws.depth;
+      aa.row_start = ws.start;
+      aa.row_of = ws.row_of;
+      aa.O = ws.ao;
+      aa.scale = 1.0f / sqrtf((float)hd);
+      CUDA_TRY(launch_train_attn(dt, aa, PEAGLE_OP_ATTN, s));
+
+      for (int c0 = 0; c0 < R; c0 += rc) {
+        const int mr = std::min(rc, R - c0);
+        CUDA_TRY(gemm_launch(dt, atc(ws.ao, (size_t)c0 * nq * hd), nq * hd, W.o_w, mr, H, nq * hd, ws.part, &go,
+                             m->status, PEAGLE_OP_O, s));
+        ResidNormArgs ra{};
+        ra.in = go;
+        ra.H = H;
+        ra.row0 = c0;
+        ra.h = ws.h;
+        ra.gain = W.post_norm_w;
+        ra.eps = eps;
+        ra.y = ws.xin;
+        CUDA_TRY(launch_resid_norm(dt, mr, ra, s));
+        CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.gate_up_w, mr, 2 * I, H, ws.part, &go, m->status,
+                             PEAGLE_OP_GATE_UP, s));
+        CUDA_TRY(launch_swiglu(dt, go, mr, I, ws.act, s));
+        CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, mr, H, I, ws.part, &go, m->status, PEAGLE_OP_DOWN, s));
+        ra.in = go;
+        ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
+        CUDA_TRY(launch_resid_norm(dt, mr, ra, s));
+      }
+    }
+    // draft-vocab head + per-row CE, chunked so the logits never all exist
+    for (int c0 = 0; c0 < R; c0 += rc) {
+      const int mr = std::min(rc, R - c0);
+      CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, m->status,
+                           PEAGLE_OP_LM_HEAD, s));
+      probe_start(PEAGLE_OP_CE, s);
+      CUDA_TRY(launch_ce_rows(go, mr, V, c0, ws.label, logits, rce, ram, s));
+      probe_stop(PEAGLE_OP_CE, s);
+    }
+  }
+  CeReduceArgs cr{};
+  cr.row_ce = rce;
+  cr.row_am = ram;
+  cr.row_label = ws.label;
+  memcpy(cr.off, off, sizeof off);
+  cr.K = K;
+  cr.decay = depth_decay;
+  cr.loss_d = per_depth_loss;
+  cr.acc_d = per_depth_acc;
+  cr.valid_d = per_depth_valid;
+  cr.loss = loss;
+  CUDA_TRY(launch_ce_reduce(cr, s));
+  return PEAGLE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Shared internals of the P-EAGLE GB300 library: element types, reductions,
+// the device status word, launch bookkeeping and the launchers each .cu file
+// exports to the host API (api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/peagle.h"
+
+namespace pe {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- elements
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// Block-wide sum; every thread gets the result. `red` holds >= 33 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = (lane < nw) ? red[lane] : 0.f;
+  t = warp_sum(t);
+  return t;
+}
+
+// Argmax pair order: larger value wins, NaN above every number, then the
+// lower index wins among equal values (and among NaNs).
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  const bool vn = v != v, bn = bv != bv;
+  if (vn != bn) return vn;
+  if (!vn && v != bv) return v > bv;
+  return i < bi;
+}
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void set_status(int* st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- host side
+void note_launch();                       // counts one kernel launch
+void set_error(const char* fmt, ...);     // records peagle_last_error()
+void probe_start(int op, cudaStream_t s); // timing probe around main kernels
+void probe_stop(int op, cudaStream_t s);
+int num_sms();
+
+// ---------------------------------------------------------------- GEMM
+// Partial-sum output of a contraction D = X W^T: `splits` slabs of
+// [M][ldo] floats, `split_stride` floats apart; the consumer sums them.
+struct GemmOut {
+  float* out;
+  int ldo;
+  int splits;
+  size_t split_stride;
+};
+// Choose the split count for an M x N x K contraction (bf16 tensor-core path).
+int gemm_splits(int M, int N, int K);
+// Workspace floats the partial output of gemm_launch needs.
+size_t gemm_out_floats(int dtype, int M, int N, int K);
+// Runs D = X W^T into out (planning the split itself; fills *o).
+// X [M, K] with row stride ldx elements, W [N, K] contiguous.
+cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
+                        float* out, GemmOut* o, int* dev_status, int probe_op, cudaStream_t s);
+
+}  // namespace pe

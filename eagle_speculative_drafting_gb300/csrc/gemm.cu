@@ -1,0 +1,544 @@
+// Dense contractions D = X W^T of the draft model (fc, QKV, O, gate/up, down,
+// lm_head; "P-EAGLE" user guide, Architecture: the projected hidden states
+// pass through Llama-style decoder layers and a draft-vocab head).
+//
+// bf16: a persistent, warp-specialized tcgen05 kernel for sm_103a.
+//   warp 0  one thread issues TMA tile loads (128B-swizzled, K-major) into a
+//           STAGES-deep shared-memory ring, completing on mbarriers;
+//   warp 1  one thread issues tcgen05.mma (kind::f16, fp32 accumulate) into
+//           one of two TMEM accumulators and commits to mbarriers;
+//   warps 2-5 drain a finished accumulator with tcgen05.ld and store fp32
+//           partial sums while the next work item accumulates in the other.
+// The 128-row operand ("A role") is the activation tile, or -- for a few
+// activation rows (M <= 256) -- the weight tile ("swap": weights stream
+// through the 128-lane side, activations sit in the narrow N side). Work
+// items are (output tile, K slice); the K slices of a tile land in separate
+// partial slabs that the consumer kernel sums, so no item waits on another.
+// Every mbarrier wait is bounded (1 s); on expiry the kernel sets
+// PEAGLE_DEV_TIMEOUT, stops issuing, frees its TMEM and returns.
+//
+// fp32: a tiled CUDA-core kernel (FFMA), exact fp32 accumulation.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pe {
+
+// =========================================================================
+// tcgen05 / TMA / mbarrier primitives (inline PTX, sm_100 family)
+// =========================================================================
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `parity` to complete; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Shared-memory matrix descriptor: K-major tile of 128-byte rows written by a
+// 128B-swizzled TMA box; 8-row core groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4
+  d |= static_cast<uint64_t>(1) << 16;                   // leading offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride offset: 1024 B
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 32 lanes x 16 columns of 32-bit accumulator; thread i gets lane (base+i).
+// The wait is folded in and takes the registers as operands so no use of
+// them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
+}
+
+}  // namespace tc
+
+// =========================================================================
+// The tcgen05 kernel
+// =========================================================================
+struct TcArgs {
+  int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
+  int splits;              // K slices per output tile
+  float* out;              // fp32 partial slabs
+  int ldo;                 // row stride of a slab (elements)
+  size_t split_stride;     // elements between slabs
+  int M, N;                // D is M x N
+  int* status;
+};
+
+constexpr int TC_THREADS = 192;
+constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
+
+template <int BN>
+struct TcCfg {
+  static constexpr int A_BYTES = 128 * 128;             // 128 rows x 64 bf16
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = std::min(12, (kSmemLimit - 1024 - 256) / STAGE);
+  static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+};
+
+template <int BN, bool SWAP>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   TcArgs g) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 4);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_map(&tmA);
+    tc::prefetch_map(&tmB);
+  }
+  if (warp == 1) tc::tmem_alloc(tslot, C::TMEM_COLS);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+
+  const int tilesA = (g.rowsA + 127) / 128;
+  const int tilesB = (g.rowsB + BN - 1) / BN;
+  const int items = tilesA * tilesB * g.splits;
+  const int ktiles = (g.K + 63) / 64;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int w = blockIdx.x; w < items && !*abort_flag; w += gridDim.x) {
+        const int tile = w / g.splits, sp = w % g.splits;
+        const int ta = tile % tilesA, tb = tile / tilesA;
+        const int kb = (int)((long long)sp * ktiles / g.splits);
+        const int ke = (int)((long long)(sp + 1) * ktiles / g.splits);
+        for (int k = kb; k < ke; ++k, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+            *abort_flag = 1;
+            set_status(g.status, PEAGLE_DEV_TIMEOUT);
+            break;
+          }
+          tc::mbar_expect_tx(&full[s], C::STAGE);
+          tc::tma_load_2d(sA + s * C::A_BYTES, &tmA, k * 64, ta * 128, &full[s]);
+          tc::tma_load_2d(sB + s * C::B_BYTES, &tmB, k * 64, tb * BN, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16(128, BN);
+      int it = 0, j = 0;
+      for (int w = blockIdx.x; w < items && !*abort_flag; w += gridDim.x, ++j) {
+        const int sp = w % g.splits;
+        const int kb = (int)((long long)sp * ktiles / g.splits);
+        const int ke = (int)((long long)(sp + 1) * ktiles / g.splits);
+        const int buf = j & 1;
+        const uint32_t use = j >> 1;
+        if (!tc::mbar_wait(&tempty[buf], (use & 1) ^ 1)) {
+          *abort_flag = 1;
+          set_status(g.status, PEAGLE_DEV_TIMEOUT);
+          break;
+        }
+        tc::fence_after();
+        const uint32_t dcol = tbase + buf * BN;
+        bool ok = true;
+        for (int k = kb; k < ke; ++k, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1;
+          if (!tc::mbar_wait(&full[s], ph)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after();
+          const uint32_t a0 = tc::smem_u32(sA + s * C::A_BYTES);
+          const uint32_t b0 = tc::smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            tc::mma_bf16(dcol, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
+                         (k > kb || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&empty[s]);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          set_status(g.status, PEAGLE_DEV_TIMEOUT);
+          break;
+        }
+        tc::mma_commit(&tfull[buf]);
+      }
+    }
+  } else {
+    // epilogue: warps 2..5 cover TMEM lane quadrants (warp % 4)
+    const int quad = warp & 3;
+    int j = 0;
+    for (int w = blockIdx.x; w < items; w += gridDim.x, ++j) {
+      const int tile = w / g.splits, sp = w % g.splits;
+      const int ta = tile % tilesA, tb = tile / tilesA;
+      const int buf = j & 1;
+      const uint32_t use = j >> 1;
+      if (*abort_flag) break;
+      // the wait result must be warp-uniform before the .sync.aligned loads
+      const bool ready = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[buf], use & 1));
+      if (!ready) {
+        *abort_flag = 1;
+        set_status(g.status, PEAGLE_DEV_TIMEOUT);
+        break;
+      }
+      tc::fence_after();
+      float* slab = g.out + (size_t)sp * g.split_stride;
+      const int arow = ta * 128 + quad * 32 + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
+        const int brow0 = tb * BN + c0;
+        if (SWAP) {
+          // lane = weight row n, column = activation row m
+          const int n = arow;
+          if (n < g.N) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int m = brow0 + c;
+              if (m < g.M) slab[(size_t)m * g.ldo + n] = __uint_as_float(r[c]);
+            }
+          }
+        } else {
+          const int m = arow;
+          if (m < g.M) {
+            float* dst = slab + (size_t)m * g.ldo + brow0;
+            if (brow0 + 16 <= g.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+#pragma unroll
+              for (int c = 0; c < 16; c += 4)
+                *reinterpret_cast<float4*>(dst + c) =
+                    make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < 16; ++c)
+                if (brow0 + c < g.N) dst[c] = __uint_as_float(r[c]);
+            }
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// =========================================================================
+// fp32 CUDA-core kernel: 64x64 output tile, 256 threads x (4x4) outputs
+// =========================================================================
+template <typename T>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X, int ldx,
+                                                        const T* __restrict__ W, int M, int N, int K,
+                                                        float* __restrict__ out, int ldo) {
+  __shared__ float sx[16][64 + 4];
+  __shared__ float sw[16][64 + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+      const int r = e / 16, c = e % 16;
+      const int m = m0 + r, n = n0 + r, k = k0 + c;
+      sx[c][r] = (m < M && k < K) ? to_f(X[(size_t)m * ldx + k]) : 0.f;
+      sw[c][r] = (n < N && k < K) ? to_f(W[(size_t)n * K + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = sx[c][ty * 4 + i];
+        b[i] = sw[c][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(a[i], b[jj], acc[i][jj]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + jj;
+      if (m < M && n < N) out[(size_t)m * ldo + n] = acc[i][jj];
+    }
+}
+
+// =========================================================================
+// Host side: tensor maps, planning, launch
+// =========================================================================
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 map over a [rows, K] matrix (row stride ld elements); box = 64 x box_rows.
+static bool make_map(CUtensorMap* map, const void* base, int rows, int K, int ld, int box_rows) {
+  if (!get_encoder()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int swap_bn(int M) {
+  int bn = 16;
+  while (bn < M) bn *= 2;
+  return bn;
+}
+
+struct Plan {
+  bool swap;
+  int bn;
+  int splits;
+  int tiles;
+};
+
+// Work items are (tile, K slice); pick the slice count that best fills
+// whole rounds of `sms` persistent CTAs, preferring fewer slices on ties.
+static Plan plan_gemm(int M, int N, int K) {
+  Plan p;
+  p.swap = M <= 256;
+  p.bn = p.swap ? swap_bn(M) : 256;
+  if (!p.swap && N <= 128 * 6) p.bn = 128;
+  const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
+  const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
+  p.tiles = tilesA * tilesB;
+  const int ktiles = (K + 63) / 64;
+  const int sms = num_sms();
+  const int smax = std::max(1, std::min(p.swap ? 19 : 4, ktiles / 2));
+  double best = -1.0;
+  p.splits = 1;
+  for (int s = 1; s <= smax; ++s) {
+    const long long items = (long long)p.tiles * s;
+    const long long rounds = (items + sms - 1) / sms;
+    const double eff = (double)items / (double)(rounds * sms);
+    if (eff > best + 0.02) {
+      best = eff;
+      p.splits = s;
+    }
+  }
+  return p;
+}
+
+int gemm_splits(int M, int N, int K) { return plan_gemm(M, N, K).splits; }
+
+size_t gemm_out_floats(int dtype, int M, int N, int K) {
+  if (dtype != PEAGLE_BF16) return (size_t)M * N;
+  return (size_t)plan_gemm(M, N, K).splits * M * N;
+}
+
+template <int BN, bool SWAP>
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int items,
+                             cudaStream_t s) {
+  using C = TcCfg<BN>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int grid = std::min(items, num_sms());
+  gemm_tc_kernel<BN, SWAP><<<grid, TC_THREADS, C::SMEM, s>>>(a, b, args);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
+                        GemmOut* o, int* dev_status, int probe_op, cudaStream_t s) {
+  if (M <= 0 || N <= 0) {
+    if (o) *o = GemmOut{out, N, 1, 0};
+    return cudaSuccess;
+  }
+  if (dtype != PEAGLE_BF16) {
+    if (o) *o = GemmOut{out, N, 1, 0};
+    dim3 grid((N + 63) / 64, (M + 63) / 64);
+    probe_start(probe_op, s);
+    gemm_simt_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(X), ldx,
+                                                  static_cast<const float*>(W), M, N, K, out, N);
+    note_launch();
+    probe_stop(probe_op, s);
+    return cudaGetLastError();
+  }
+  const Plan p = plan_gemm(M, N, K);
+  TcArgs args;
+  args.K = K;
+  args.splits = p.splits;
+  args.out = out;
+  args.ldo = N;
+  args.split_stride = (size_t)M * N;
+  args.M = M;
+  args.N = N;
+  args.status = dev_status;
+  CUtensorMap ma, mb;
+  bool ok;
+  if (p.swap) {
+    args.rowsA = N;
+    args.rowsB = M;
+    ok = make_map(&ma, W, N, K, K, 128) && make_map(&mb, X, M, K, ldx, p.bn);
+  } else {
+    args.rowsA = M;
+    args.rowsB = N;
+    ok = make_map(&ma, X, M, K, ldx, 128) && make_map(&mb, W, N, K, K, p.bn);
+  }
+  if (!ok) {
+    set_error("cuTensorMapEncodeTiled failed (M=%d N=%d K=%d)", M, N, K);
+    return cudaErrorInvalidValue;
+  }
+  if (o) *o = GemmOut{out, N, p.splits, args.split_stride};
+  const int items = p.tiles * p.splits;
+  cudaError_t e;
+  probe_start(probe_op, s);
+  if (p.swap) {
+    switch (p.bn) {
+      case 16: e = launch_tc<16, true>(ma, mb, args, items, s); break;
+      case 32: e = launch_tc<32, true>(ma, mb, args, items, s); break;
+      case 64: e = launch_tc<64, true>(ma, mb, args, items, s); break;
+      case 128: e = launch_tc<128, true>(ma, mb, args, items, s); break;
+      default: e = launch_tc<256, true>(ma, mb, args, items, s); break;
+    }
+  } else {
+    e = (p.bn == 128) ? launch_tc<128, false>(ma, mb, args, items, s)
+                      : launch_tc<256, false>(ma, mb, args, items, s);
+  }
+  probe_stop(probe_op, s);
+  return e;
+}
+
+}  // namespace pe

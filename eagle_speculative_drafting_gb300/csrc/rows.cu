@@ -1,0 +1,689 @@
+// Row-wise kernels of the P-EAGLE step: everything between the dense
+// contractions. Each consumer first sums the K-slice partial slabs the
+// tensor-core GEMM wrote, then applies the row operation in fp32.
+#include <math.h>
+
+#include "rows.cuh"
+
+namespace pe {
+
+__device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
+  float v = 0.f;
+  for (int s = 0; s < g.splits; ++s) v += g.out[(size_t)s * g.split_stride + idx];
+  return v;
+}
+
+// -------------------------------------------------------------------------
+// Rotary table: cos/sin of p * theta^(-2j/hd) for every position p <
+// max_position ("feat(speculative) ... #2376", RoPE fix commit: the cache is
+// sized to the highest position and gathered by position value). Angles in
+// double, so large positions keep their phase.
+// -------------------------------------------------------------------------
+__global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int half, int hd, double theta) {
+  const long long total = (long long)max_pos * half;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(e / half), j = (int)(e % half);
+    const double a = (double)p * pow(theta, -2.0 * j / hd);
+    double s, c;
+    sincos(a, &s, &c);
+    cosb[e] = (float)c;
+    sinb[e] = (float)s;
+  }
+}
+
+// -------------------------------------------------------------------------
+// fc_norm and the layer-0 input rows ("P-EAGLE" user guide, Architecture;
+// #2376 Changelog: mask_hidden is projected through the same fc/fc_norm).
+// Row r: u = sum of partials; h = RMSNorm_fc(u);
+//   x0[r] = [RMSNorm_in(E[tok]) , RMSNorm_hidden(h)]   (2H wide)
+//   resid[r] = RMSNorm_hidden(h) if norm_before_residual else h.
+// -------------------------------------------------------------------------
+template <typename T>
+__global__ void fc_finish_kernel(FcFinishArgs a) {
+  extern __shared__ float sh[];
+  __shared__ float red[33];
+  const int r = blockIdx.x, H = a.H;
+  const T* g_fc = static_cast<const T*>(a.g_fc);
+  const T* g_in = static_cast<const T*>(a.g_in);
+  const T* g_h = static_cast<const T*>(a.g_h);
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const float v = sum_parts(a.u, (size_t)r * a.u.ldo + j);
+    sh[j] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / H + a.eps);
+  float ss2 = 0.f;
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const float h = sh[j] * inv * to_f(g_fc[j]);
+    sh[j] = h;
+    ss2 += h * h;
+  }
+  ss2 = block_sum(ss2, red);
+  const float inv2 = rsqrtf(ss2 / H + a.eps);
+  int t = a.tok ? a.tok[r] : a.tok_const;
+  if (t < 0 || t >= a.Vt) {
+    if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+    t = 0;
+  }
+  const T* e = static_cast<const T*>(a.embed) + (size_t)t * H;
+  float ss3 = 0.f;
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const float v = to_f(e[j]);
+    ss3 += v * v;
+  }
+  ss3 = block_sum(ss3, red);
+  const float inv3 = rsqrtf(ss3 / H + a.eps);
+  T* x0 = static_cast<T*>(a.x0) + (size_t)r * 2 * H;
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const float hn = sh[j] * inv2 * to_f(g_h[j]);
+    x0[j] = from_f<T>(to_f(e[j]) * inv3 * to_f(g_in[j]));
+    x0[H + j] = from_f<T>(hn);
+    if (a.resid) a.resid[(size_t)r * H + j] = a.nbr ? hn : sh[j];
+  }
+}
+
+// -------------------------------------------------------------------------
+// q/k/v rows with rotary phases gathered by position value (#2376, RoPE fix
+// commit). Source of row r:
+//   mode 0  the GEMM row r (layers >= 1);
+//   mode 1  decode layer 0: row r = (b, d) takes GEMM row b if d == 0,
+//           otherwise the precomputed masked q/k/v (every masked row of layer
+//           0 has the same input: ptd embedding + projected mask_hidden);
+//   mode 2  all rows masked (training layer 0, depths >= 1).
+// Position: decode pos = anchor_pos[b] + d; training pos = row_pos[r].
+// Layer 0 also seeds the residual stream h with the row's layer-0 residual.
+// Decode can append the anchor row's K/V to its cache.
+// -------------------------------------------------------------------------
+template <typename T>
+__global__ void qkv_finish_kernel(QkvArgs a) {
+  const int r = blockIdx.x + a.row0;
+  const int half = a.hd / 2;
+  int src;
+  if (a.mode == 0) src = r - a.src0;
+  else if (a.mode == 1) src = (r % a.K == 0) ? r / a.K : -1;
+  else src = -1;
+  int pos;
+  if (a.row_pos) pos = a.row_pos[r];
+  else pos = a.anchor_pos[r / a.K] + r % a.K;
+  if (pos < 0 || pos >= a.max_pos) {
+    if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+    pos = pos < 0 ? 0 : a.max_pos - 1;
+  }
+  const int QKV = (a.nq + 2 * a.nkv) * a.hd;
+  T* Q = static_cast<T*>(a.Q) + (size_t)r * a.nq * a.hd;
+  T* Ko = static_cast<T*>(a.Kout) + (size_t)r * a.nkv * a.hd;
+  T* Vo = static_cast<T*>(a.Vout) + (size_t)r * a.nkv * a.hd;
+  const float* cs = a.rcos + (size_t)pos * half;
+  const float* sn = a.rsin + (size_t)pos * half;
+
+  bool append = false;
+  size_t cache_row = 0;
+  if (a.kcache && a.mode == 1 && (r % a.K) == 0) {
+    const int b = r / a.K;
+    const long long row = a.kv_off[b] + (long long)a.kv_len[b];
+    if (a.kv_len[b] >= 0 && row < a.kv_off[b + 1] && row < a.kv_cap && a.kv_off[b] >= 0) {
+      append = true;
+      cache_row = (size_t)row;
+    } else if (threadIdx.x == 0) {
+      set_status(a.status, PEAGLE_DEV_BOUNDS);
+    }
+  }
+  const int pairs = (a.nq + a.nkv) * half;
+  for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
+    const int head = p / half, j = p % half;
+    const int lo = head * a.hd + j, hi = lo + half;
+    float xl, xh;
+    if (src >= 0) {
+      xl = sum_parts(a.in, (size_t)src * a.in.ldo + lo);
+      xh = sum_parts(a.in, (size_t)src * a.in.ldo + hi);
+    } else {
+      xl = a.mask_qkv[lo];
+      xh = a.mask_qkv[hi];
+    }
+    const float c = cs[j], s = sn[j];
+    const float ol = xl * c - xh * s, oh = xh * c + xl * s;
+    if (head < a.nq) {
+      Q[head * a.hd + j] = from_f<T>(ol);
+      Q[head * a.hd + j + half] = from_f<T>(oh);
+    } else {
+      const int kh = head - a.nq;
+      Ko[kh * a.hd + j] = from_f<T>(ol);
+      Ko[kh * a.hd + j + half] = from_f<T>(oh);
+      if (append) {
+        T* kc = static_cast<T*>(a.kcache) + cache_row * a.nkv * a.hd;
+        kc[kh * a.hd + j] = from_f<T>(ol);
+        kc[kh * a.hd + j + half] = from_f<T>(oh);
+      }
+    }
+  }
+  const int v0 = (a.nq + a.nkv) * a.hd;
+  for (int e = threadIdx.x; e < a.nkv * a.hd; e += blockDim.x) {
+    const float v = (src >= 0) ? sum_parts(a.in, (size_t)src * a.in.ldo + v0 + e) : a.mask_qkv[v0 + e];
+    Vo[e] = from_f<T>(v);
+    if (append) static_cast<T*>(a.vcache)[cache_row * a.nkv * a.hd + e] = from_f<T>(v);
+  }
+  (void)QKV;
+  if (a.h) {
+    float* h = a.h + (size_t)r * a.H;
+    if (src >= 0) {
+      const float* r0 = a.resid0 + (size_t)src * a.H;
+      for (int j = threadIdx.x; j < a.H; j += blockDim.x) h[j] = r0[j];
+    } else {
+      for (int j = threadIdx.x; j < a.H; j += blockDim.x) h[j] = a.mask_resid[j];
+    }
+  }
+}
+
+// -------------------------------------------------------------------------
+// Residual add + RMSNorm: h[r] += sum of partials; y[r] = RMSNorm_gain(h[r]).
+// (Llama layer: after O-proj with the post-attention gain; after the MLP
+// down-proj with the next layer's input gain or the final gain.)
+// -------------------------------------------------------------------------
+template <typename T>
+__global__ void resid_norm_kernel(ResidNormArgs a) {
+  extern __shared__ float sh[];
+  __shared__ float red[33];
+  const int rl = blockIdx.x;           // row within the chunk
+  const int r = a.row0 + rl;           // global row
+  float* h = a.h + (size_t)r * a.H;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
+    const float v = h[j] + sum_parts(a.in, (size_t)rl * a.in.ldo + j);
+    h[j] = v;
+    sh[j] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / a.H + a.eps);
+  const T* g = static_cast<const T*>(a.gain);
+  T* y = static_cast<T*>(a.y) + (size_t)r * a.H;
+  for (int j = threadIdx.x; j < a.H; j += blockDim.x) y[j] = from_f<T>(sh[j] * inv * to_f(g[j]));
+}
+
+// -------------------------------------------------------------------------
+// SwiGLU: act[r, j] = silu(gate) * up, gate/up = columns j and I + j.
+// -------------------------------------------------------------------------
+template <typename T>
+__global__ void swiglu_kernel(GemmOut in, int rows, int I, void* act_) {
+  T* act = static_cast<T*>(act_);
+  const long long total = (long long)rows * I;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(e / I), j = (int)(e % I);
+    const float gt = sum_parts(in, (size_t)r * in.ldo + j);
+    const float up = sum_parts(in, (size_t)r * in.ldo + I + j);
+    act[e] = from_f<T>(gt / (1.f + expf(-gt)) * up);
+  }
+}
+
+// -------------------------------------------------------------------------
+// Draft-vocab argmax, two stages: per (row, vocab chunk) best pair, then per
+// row over chunks, mapped through d2t. Lowest index wins ties.
+// -------------------------------------------------------------------------
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (am_better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+__global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* logits, float* pval,
+                                         int* pidx) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int r = blockIdx.y, c = blockIdx.x, nchunks = gridDim.x;
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    const float x = sum_parts(in, (size_t)r * in.ldo + v);
+    if (logits) logits[(size_t)r * V + v] = x;
+    if (am_better(x, v, bv, bi)) {
+      bv = x;
+      bi = v;
+    }
+  }
+  warp_argmax(bv, bi);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) {
+    sv[w] = bv;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    bv = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      pval[(size_t)r * nchunks + c] = bv;
+      pidx[(size_t)r * nchunks + c] = bi;
+    }
+  }
+}
+
+__global__ void lm_argmax_final_kernel(int rows, int nchunks, const float* pval, const int* pidx,
+                                       const int* d2t, int* tokens) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = lane; c < nchunks; c += 32) {
+    const float v = pval[(size_t)r * nchunks + c];
+    const int i = pidx[(size_t)r * nchunks + c];
+    if (am_better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+  warp_argmax(bv, bi);
+  if (lane == 0) tokens[r] = d2t ? d2t[bi] : bi;
+}
+
+// -------------------------------------------------------------------------
+// Per-row cross-entropy over the draft vocab (#2376: CE per depth, shared
+// with EAGLE-3), one pass with an online max / sum of exponentials.
+// row_ce = logsumexp - logit[label], NaN for rows without a label.
+// -------------------------------------------------------------------------
+__global__ void ce_rows_kernel(GemmOut in, int V, int row0, const int* row_label, float* logits_out,
+                               float* row_ce, int* row_am) {
+  __shared__ float sm[32], ss[32], sv[32];
+  __shared__ int si[32];
+  const int rl = blockIdx.x, r = row0 + rl;
+  float m = -INFINITY, s = 0.f, bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    const float x = sum_parts(in, (size_t)rl * in.ldo + v);
+    if (logits_out) logits_out[(size_t)r * V + v] = x;
+    if (am_better(x, v, bv, bi)) {
+      bv = x;
+      bi = v;
+    }
+    if (x > m) {
+      s = s * expf(m - x) + 1.f;
+      m = x;
+    } else {
+      s += expf(x - m);
+    }
+  }
+  // combine (m, s) across the warp
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float nm = fmaxf(m, om);
+    s = (m == -INFINITY ? 0.f : s * expf(m - nm)) + (om == -INFINITY ? 0.f : os * expf(om - nm));
+    m = nm;
+  }
+  warp_argmax(bv, bi);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    sm[w] = m;
+    ss[w] = s;
+    sv[w] = bv;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    m = lane < nw ? sm[lane] : -INFINITY;
+    s = lane < nw ? ss[lane] : 0.f;
+    bv = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, o);
+      const float os = __shfl_xor_sync(0xffffffffu, s, o);
+      const float nm = fmaxf(m, om);
+      s = (m == -INFINITY ? 0.f : s * expf(m - nm)) + (om == -INFINITY ? 0.f : os * expf(om - nm));
+      m = nm;
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      const int lab = row_label[r];
+      float ce = __int_as_float(0x7fc00000);
+      if (lab >= 0) ce = (m + logf(s)) - sum_parts(in, (size_t)rl * in.ldo + lab);
+      row_ce[r] = ce;
+      row_am[r] = bi;
+    }
+  }
+}
+
+// Per-depth means and the decay-weighted total (#2376, Changelog: 0.8**d
+// weighted-mean schedule). One block; fixed summation order.
+__global__ void ce_reduce_kernel(CeReduceArgs a) {
+  __shared__ double red_d[32];
+  __shared__ int red_i[32], red_j[32];
+  __shared__ double loss_acc;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) loss_acc = 0.0;
+  for (int d = 0; d < a.K; ++d) {
+    double sum = 0.0;
+    int cnt = 0, cor = 0;
+    for (int r = a.off[d] + threadIdx.x; r < a.off[d + 1]; r += blockDim.x) {
+      const int lab = a.row_label[r];
+      if (lab >= 0) {
+        sum += (double)a.row_ce[r];
+        cnt += 1;
+        cor += (a.row_am[r] == lab) ? 1 : 0;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      cor += __shfl_xor_sync(0xffffffffu, cor, o);
+    }
+    __syncthreads();
+    if (lane == 0) {
+      red_d[w] = sum;
+      red_i[w] = cnt;
+      red_j[w] = cor;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double S = 0.0;
+      int C = 0, R = 0;
+      for (int i = 0; i < nw; ++i) {
+        S += red_d[i];
+        C += red_i[i];
+        R += red_j[i];
+      }
+      const double ld = C ? S / C : 0.0;
+      a.loss_d[d] = (float)ld;
+      a.acc_d[d] = C ? (float)((double)R / C) : 0.f;
+      a.valid_d[d] = C;
+      loss_acc += pow(a.decay, (double)d) * ld;
+    }
+  }
+  if (threadIdx.x == 0) a.loss[0] = (float)loss_acc;
+}
+
+// -------------------------------------------------------------------------
+// Training rows: depth, anchor, rotary position, conversation start and
+// label of every row (#2376, PR description; "P_Eagle" README: cu_seqlens
+// isolation). Row r of depth d has anchor i = indices[r]; its label is
+// labels[i + d] when i + d is inside i's conversation, unmasked and mapped
+// into the draft vocab, else -1.
+// -------------------------------------------------------------------------
+__global__ void train_meta_kernel(TrainMetaArgs a) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bool ok = a.cu[0] == 0 && a.cu[a.S] == a.n;
+    for (int c = 0; c < a.S; ++c) ok = ok && a.cu[c] <= a.cu[c + 1];
+    if (!ok) set_status(a.status, PEAGLE_DEV_BOUNDS);
+  }
+  if (r >= a.R) return;
+  int d = 0;
+  while (d + 1 < a.K && r >= a.off[d + 1]) ++d;
+  int i = a.indices[r];
+  if (i < 0 || i >= a.n) {
+    set_status(a.status, PEAGLE_DEV_BOUNDS);
+    i = 0;
+  }
+  int lo = 0, hi = a.S - 1;  // conversation c with cu[c] <= i < cu[c+1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (a.cu[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  const int s = a.cu[lo], e = a.cu[lo + 1];
+  int pos = a.position_ids[i] + d;
+  if (pos < 0 || pos >= a.max_pos) {
+    set_status(a.status, PEAGLE_DEV_BOUNDS);
+    pos = pos < 0 ? 0 : a.max_pos - 1;
+  }
+  int lab = -1;
+  const int p = i + d;
+  if (p < e && (!a.loss_mask || a.loss_mask[p])) {
+    const int t = a.labels[p];
+    if (t < 0 || t >= a.Vt) {
+      set_status(a.status, PEAGLE_DEV_BOUNDS);
+    } else {
+      const int dl = a.t2d ? a.t2d[t] : t;
+      if (dl >= a.Vd) set_status(a.status, PEAGLE_DEV_BOUNDS);
+      else lab = dl;
+    }
+  }
+  a.row_anchor[r] = i;
+  a.row_depth[r] = d;
+  a.row_pos[r] = pos;
+  a.row_start[r] = s;
+  a.row_label[r] = lab;
+}
+
+// -------------------------------------------------------------------------
+// Greedy verification ("P-EAGLE" user guide, Inference Process): accept the
+// longest prefix of drafts equal to the target's tokens; next = target at
+// the first mismatch (or the bonus column).
+// -------------------------------------------------------------------------
+__global__ void verify_kernel(int B, int K, const int* draft, const int* target, int* acc, int* next) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int* d = draft + (size_t)b * K;
+  const int* t = target + (size_t)b * (K + 1);
+  int a = 0;
+  while (a < K && d[a] == t[a]) ++a;
+  acc[b] = a;
+  next[b] = t[a];
+}
+
+// -------------------------------------------------------------------------
+// COD selection ("P-EAGLE" user guide, COD Sampling). Keys are SplitMix64
+// outputs (Steele, Lea, Flood, OOPSLA 2014), distinct for distinct i.
+// S_d = positions whose key is at most the counts[d]-th smallest key. One
+// block: an 8-pass radix select finds every depth's threshold key at once,
+// then a block scan writes each S_d in ascending order.
+// -------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t splitmix64_out(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__global__ void __launch_bounds__(1024) cod_select_kernel(CodArgs a) {
+  __shared__ unsigned hist[16][256];
+  __shared__ uint64_t prefix[16], maskv[16], thr[16];
+  __shared__ int rank_left[16], wsum[32], base[16];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int n = a.n, K = a.K;
+  if (tid < 16) {
+    prefix[tid] = 0;
+    maskv[tid] = 0;
+    rank_left[tid] = (tid < K) ? a.counts[tid] : 0;
+    base[tid] = 0;
+  }
+  __syncthreads();
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int e = tid; e < 16 * 256; e += blockDim.x) hist[e >> 8][e & 255] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+      const uint64_t key = splitmix64_out(a.seed, (uint64_t)i);
+      const unsigned dig = (unsigned)(key >> shift) & 255u;
+      for (int d = 1; d < K; ++d)
+        if (rank_left[d] > 0 && a.counts[d] < n && (key & maskv[d]) == prefix[d]) atomicAdd(&hist[d][dig], 1u);
+    }
+    __syncthreads();
+    if (tid >= 1 && tid < K && rank_left[tid] > 0 && a.counts[tid] < n) {
+      int left = rank_left[tid];
+      unsigned bsel = 255;
+      for (unsigned b = 0; b < 256; ++b) {
+        const int c = (int)hist[tid][b];
+        if (left <= c) {
+          bsel = b;
+          break;
+        }
+        left -= c;
+      }
+      rank_left[tid] = left;
+      prefix[tid] |= (uint64_t)bsel << shift;
+      maskv[tid] |= (uint64_t)255 << shift;
+    }
+    __syncthreads();
+  }
+  if (tid < 16) {
+    if (tid == 0 || (tid < K && a.counts[tid] >= n)) thr[tid] = ~0ull;   // keep everything
+    else if (tid < K && a.counts[tid] > 0) thr[tid] = prefix[tid];
+    else thr[tid] = 0;                                                    // keep nothing
+  }
+  __syncthreads();
+  // ascending compaction, tile by tile
+  for (int t0 = 0; t0 < n; t0 += blockDim.x) {
+    const int i = t0 + tid;
+    const bool live = i < n;
+    uint64_t key = live ? splitmix64_out(a.seed, (uint64_t)i) : 0;
+    if (live) {
+      a.indices[i] = i;
+      if (a.row_of) a.row_of[i] = i;
+    }
+    for (int d = 1; d < K; ++d) {
+      const bool keep = live && a.counts[d] > 0 && key <= thr[d];
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) wsum[w] = __popc(bal);
+      __syncthreads();
+      if (w == 0) {
+        const int nw = blockDim.x >> 5;
+        int v = lane < nw ? wsum[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane < nw) wsum[lane] = incl - v;   // exclusive warp offsets
+        if (lane == 31) rank_left[0] = incl;    // tile total (scratch slot)
+      }
+      __syncthreads();
+      const int pos = base[d] + wsum[w] + __popc(bal & ((1u << lane) - 1u));
+      const bool fits = keep && pos < a.counts[d];   // always true for distinct keys
+      if (fits) a.indices[a.off[d] + pos] = i;
+      if (live && a.row_of) a.row_of[(size_t)d * n + i] = fits ? a.off[d] + pos : -1;
+      __syncthreads();
+      if (tid == 0) base[d] += rank_left[0];
+      __syncthreads();
+    }
+  }
+}
+
+// D = sum of the partial slabs (the plain GEMM entry point).
+__global__ void sum_splits_kernel(GemmOut in, int M, int N, float* D) {
+  const long long total = (long long)M * N;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int m = (int)(e / N), n = (int)(e % N);
+    D[e] = sum_parts(in, (size_t)m * in.ldo + n);
+  }
+}
+
+// =========================================================================
+// launchers
+// =========================================================================
+static int grid_for(long long total, int threads) {
+  long long g = (total + threads - 1) / threads;
+  const long long cap = (long long)num_sms() * 8;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+#define PE_LAUNCH_END() \
+  do {                  \
+    note_launch();      \
+    return cudaGetLastError(); \
+  } while (0)
+
+cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double theta, cudaStream_t st) {
+  const long long total = (long long)max_pos * (hd / 2);
+  rope_table_kernel<<<grid_for(total, 256), 256, 0, st>>>(c, s, max_pos, hd / 2, hd, theta);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const size_t sm = (size_t)a.H * sizeof(float);
+  if (dtype == PEAGLE_BF16) fc_finish_kernel<bf16><<<rows, 256, sm, st>>>(a);
+  else fc_finish_kernel<float><<<rows, 256, sm, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (dtype == PEAGLE_BF16) qkv_finish_kernel<bf16><<<rows, 256, 0, st>>>(a);
+  else qkv_finish_kernel<float><<<rows, 256, 0, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const size_t sm = (size_t)a.H * sizeof(float);
+  if (dtype == PEAGLE_BF16) resid_norm_kernel<bf16><<<rows, 256, sm, st>>>(a);
+  else resid_norm_kernel<float><<<rows, 256, sm, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_swiglu(int dtype, const GemmOut& in, int rows, int I, void* act, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const long long total = (long long)rows * I;
+  if (dtype == PEAGLE_BF16) swiglu_kernel<bf16><<<grid_for(total, 256), 256, 0, st>>>(in, rows, I, act);
+  else swiglu_kernel<float><<<grid_for(total, 256), 256, 0, st>>>(in, rows, I, act);
+  PE_LAUNCH_END();
+}
+
+int lm_argmax_chunks(int V) { return (V + 2047) / 2048; }
+
+cudaError_t launch_lm_argmax(const GemmOut& in, int rows, int V, float* logits, float* pval, int* pidx,
+                             const int* d2t, int* tokens, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int nch = lm_argmax_chunks(V);
+  lm_argmax_partial_kernel<<<dim3(nch, rows), 256, 0, st>>>(in, V, 2048, logits, pval, pidx);
+  note_launch();
+  lm_argmax_final_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, nch, pval, pidx, d2t, tokens);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const int* row_label,
+                           float* logits_out, float* row_ce, int* row_am, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  ce_rows_kernel<<<rows, 256, 0, st>>>(in, V, row0, row_label, logits_out, row_ce, row_am);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st) {
+  ce_reduce_kernel<<<1, 1024, 0, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_train_meta(const TrainMetaArgs& a, cudaStream_t st) {
+  if (a.R <= 0) return cudaSuccess;
+  train_meta_kernel<<<(a.R + 255) / 256, 256, 0, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, int* next, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  verify_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, K, d, t, acc, next);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st) {
+  if (a.n <= 0) return cudaSuccess;
+  cod_select_kernel<<<1, 1024, 0, st>>>(a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStream_t st) {
+  const long long total = (long long)M * N;
+  if (total <= 0) return cudaSuccess;
+  sum_splits_kernel<<<grid_for(total, 256), 256, 0, st>>>(in, M, N, D);
+  PE_LAUNCH_END();
+}
+
+}  // namespace pe

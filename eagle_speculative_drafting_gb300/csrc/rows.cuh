@@ -1,0 +1,132 @@
+// Argument blocks and launchers of the row-wise and attention kernels.
+#pragma once
+#include "common.cuh"
+
+namespace pe {
+
+struct FcFinishArgs {
+  GemmOut u;              // fc partials, row r at u.out + r * ldo
+  int H, Vt;
+  const int* tok;         // token per row, or NULL -> tok_const
+  int tok_const;
+  const void* embed;      // [Vt, H]
+  const void *g_fc, *g_in, *g_h;
+  float eps;
+  int nbr;                // norm_before_residual
+  void* x0;               // out [rows, 2H]
+  float* resid;           // out [rows, H] or NULL
+  int* status;
+};
+
+struct QkvArgs {
+  GemmOut in;             // QKV partials (rows = GEMM rows)
+  int nq, nkv, hd, H;
+  int mode;               // 0 GEMM row r - src0; 1 decode layer 0; 2 all masked
+  int K;                  // decode depths (mode 1 and decode positions)
+  int row0, src0;         // first output row of this launch; GEMM row of output row src0
+  const float* mask_qkv;  // [QKV] pre-rotary q/k/v of a masked layer-0 row
+  const float* resid0;    // layer-0 residual rows of GEMM rows (mode 1) or NULL
+  const float* mask_resid;// layer-0 residual of a masked row
+  float* h;               // residual stream to seed (layer 0) or NULL
+  const float *rcos, *rsin;
+  int max_pos;
+  const int* anchor_pos;  // decode positions (used when row_pos == NULL)
+  const int* row_pos;     // training positions per row
+  void *Q, *Kout, *Vout;  // [rows, nq*hd], [rows, nkv*hd] x2
+  void *kcache, *vcache;  // decode append target (layer's cache) or NULL
+  const int64_t* kv_off;
+  const int* kv_len;
+  long long kv_cap;
+  int* status;
+};
+
+struct ResidNormArgs {
+  GemmOut in;             // partials, chunk-local rows
+  int H;
+  int row0;               // global row of chunk row 0
+  float* h;               // residual stream [rows, H] (global rows)
+  const void* gain;
+  float eps;
+  void* y;                // out normalised rows (global rows)
+};
+
+struct CeReduceArgs {
+  const float* row_ce;
+  const int* row_am;
+  const int* row_label;
+  int off[17];            // depth d rows: [off[d], off[d+1])
+  int K;
+  double decay;
+  float *loss_d, *acc_d, *loss;
+  int* valid_d;
+};
+
+struct TrainMetaArgs {
+  int n, R, K, S, Vt, Vd, max_pos;
+  int off[17];
+  const int* indices;
+  const int* position_ids;
+  const int* cu;
+  const int* labels;
+  const uint8_t* loss_mask;
+  const int* t2d;
+  int *row_anchor, *row_depth, *row_pos, *row_start, *row_label;
+  int* status;
+};
+
+struct CodArgs {
+  int n, K;
+  uint64_t seed;
+  int counts[16];
+  int off[17];
+  int* indices;
+  int* row_of;
+};
+
+// Depth-masked decode attention (split over the context) + combine.
+struct DecodeAttnArgs {
+  int B, K, nq, nkv, hd;
+  const void* Q;          // [B*K, nq, hd]
+  const void *Kc, *Vc;    // chain rows [B*K, nkv, hd]
+  const void *kcache, *vcache;  // [cap, nkv, hd]
+  const int64_t* kv_off;
+  const int* kv_len;
+  long long kv_cap;
+  int max_kv_len;
+  int chunk, nsplit;      // context keys per split, splits per (b, kv head)
+  float* part_o;          // [B, nkv, nsplit, K*G, hd]
+  float* part_ml;         // [B, nkv, nsplit, K*G, 2]
+  void* O;                // out [B*K, nq, hd]
+  float scale;
+  int* status;
+};
+
+struct TrainAttnArgs {
+  int R, n, nq, nkv, hd;
+  const void *Q, *Kr, *Vr;   // [R, nq|nkv, hd]
+  const int *row_anchor, *row_depth, *row_start, *row_of;  // row_of [K, n]
+  void* O;
+  float scale;
+};
+
+cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double theta, cudaStream_t st);
+cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStream_t st);
+cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_t st);
+cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaStream_t st);
+cudaError_t launch_swiglu(int dtype, const GemmOut& in, int rows, int I, void* act, cudaStream_t st);
+int lm_argmax_chunks(int V);
+cudaError_t launch_lm_argmax(const GemmOut& in, int rows, int V, float* logits, float* pval, int* pidx,
+                             const int* d2t, int* tokens, cudaStream_t st);
+cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const int* row_label,
+                           float* logits_out, float* row_ce, int* row_am, cudaStream_t st);
+cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st);
+cudaError_t launch_train_meta(const TrainMetaArgs& a, cudaStream_t st);
+cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, int* next, cudaStream_t st);
+cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st);
+cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStream_t st);
+
+void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit);
+cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op, cudaStream_t st);
+cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, int probe_op, cudaStream_t st);
+
+}  // namespace pe

@@ -1,0 +1,286 @@
+/*
+ * peagle.h -- C ABI of the P-EAGLE parallel-drafting library for GB300
+ * (sm_103a). One process, one GPU.
+ *
+ * P-EAGLE drafts all K future tokens of an anchor in one forward pass of an
+ * EAGLE-3 style draft model ("P-EAGLE" user guide, How It Works /
+ * Architecture; "feat(speculative): add P-EAGLE parallel-drafting training
+ * for EAGLE-3 drafts - #2376", PR description and Changelog):
+ *   - the target's aux hidden states from the selected layers are
+ *     concatenated and projected through fc and fc_norm;
+ *   - every masked depth d >= 1 takes the learnable mask_hidden row, projected
+ *     the same way, and the embedding of the reserved ptd_token_id;
+ *   - rotary phases are looked up at the actual position values (anchor + d),
+ *     not the sequence index (#2376, RoPE fix commit);
+ *   - Llama-style decoder layers attend over the context plus each anchor's
+ *     own depth chain (the diagonal-extension mask, #2376 "Equivalence to
+ *     vLLM inference"); packed conversations never attend across their
+ *     cu_seqlens boundaries ("P_Eagle" README, variable-length attention);
+ *   - a draft-vocab lm_head and argmax run per depth.
+ * Greedy verification accepts the longest prefix of drafts that matches the
+ * target's argmax tokens (user guide, Inference Process). The training-shaped
+ * pass keeps all n positions at depth 0 and about n*r^d (floored by
+ * n*r_min) at depth d (user guide, COD Sampling) and weights the per-depth
+ * cross-entropy by 0.8^d (#2376, Changelog).
+ *
+ * Conventions for every entry point:
+ *   - The return value is a peagle_status. Nothing throws or aborts across
+ *     the ABI. peagle_last_error() returns a one-line description of the last
+ *     failure on the calling thread.
+ *   - Arguments are validated on the host before any launch. A failed
+ *     validation returns PEAGLE_ERR_INVALID_ARG (or _UNSUPPORTED) and leaves
+ *     every output untouched.
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     "host" pointers are ordinary host memory. Every array is contiguous and
+ *     row-major. Floating-point tensors use the model's dtype (fp32 or bf16)
+ *     unless the signature says float.
+ *   - `stream` is a cudaStream_t (passed as void*). Work is enqueued
+ *     asynchronously on it; calls return before the GPU finishes unless the
+ *     comment says the call synchronizes.
+ *   - Hot calls never allocate device memory: the caller passes a workspace
+ *     of at least the size the matching *_workspace_size call reports, 256-byte
+ *     aligned. Workspaces must not be shared by calls that may overlap on the GPU.
+ *   - Faults the device detects (an index out of range, a bounded wait that
+ *     ran out) set bits of the model's sticky device status word instead of
+ *     trapping; read it with peagle_get_device_status.
+ */
+#ifndef PEAGLE_H_
+#define PEAGLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum peagle_status {
+  PEAGLE_OK = 0,
+  PEAGLE_ERR_INVALID_ARG = 1,    /* a size, pointer, id or option is invalid */
+  PEAGLE_ERR_UNSUPPORTED = 2,    /* valid, but outside what this build handles */
+  PEAGLE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  PEAGLE_ERR_WORKSPACE = 4,      /* workspace NULL, misaligned or too small */
+  PEAGLE_ERR_DEVICE = 5          /* the device status word is non-zero */
+} peagle_status;
+
+/* Bits of the sticky device status word. */
+#define PEAGLE_DEV_BOUNDS  0x1   /* token id, position or KV range out of range */
+#define PEAGLE_DEV_TIMEOUT 0x2   /* a bounded wait inside a kernel gave up */
+
+typedef enum peagle_dtype { PEAGLE_F32 = 0, PEAGLE_BF16 = 1 } peagle_dtype;
+
+/* Draft model configuration; mirrors the draft's config.json (#2376,
+ * Checkpoint contract: ptd_token_id rides in config.json). */
+typedef struct peagle_config {
+  int32_t hidden;               /* H, draft hidden size */
+  int32_t target_hidden;        /* Ht, width of one aux hidden state */
+  int32_t num_aux;              /* A, aux states concatenated (3 in EAGLE-3) */
+  int32_t num_layers;           /* draft decoder layers (>= 1) */
+  int32_t num_q_heads;          /* nq */
+  int32_t num_kv_heads;         /* nkv, nq % nkv == 0 */
+  int32_t head_dim;             /* hd in {64, 128} */
+  int32_t intermediate;         /* I, SwiGLU width */
+  int32_t target_vocab;         /* Vt, rows of the embedding */
+  int32_t draft_vocab;          /* Vd, rows of lm_head */
+  int32_t ptd_token_id;         /* required, 0 <= id < Vt (#2376: no silent default) */
+  int32_t norm_before_residual; /* 1 (default): layer-0 residual = normed hidden */
+  int32_t max_position;         /* rows of the rotary table; positions must be < it */
+  int32_t dtype;                /* peagle_dtype of weights, activations, KV cache */
+  double rope_theta;            /* rotary base */
+  double rms_eps;               /* RMSNorm epsilon */
+} peagle_config;
+
+/* Weights of one decoder layer, nn.Linear layout [out, in], device. */
+typedef struct peagle_layer_weights {
+  const void* in_norm_w;        /* [H] gain of the input RMSNorm */
+  const void* hidden_norm_w;    /* [H] gain of the hidden RMSNorm; layer 0 only, else NULL */
+  const void* qkv_w;            /* [(nq+2nkv)*hd, 2H] for layer 0, [(nq+2nkv)*hd, H] after;
+                                   rows: q heads, then k heads, then v heads */
+  const void* o_w;              /* [H, nq*hd] */
+  const void* post_norm_w;      /* [H] gain of the post-attention RMSNorm */
+  const void* gate_up_w;        /* [2I, H]: rows 0..I-1 gate, rows I..2I-1 up */
+  const void* down_w;           /* [H, I] */
+} peagle_layer_weights;
+
+/* Model weights, device pointers borrowed by the model: they must stay valid
+ * and unchanged until peagle_model_destroy. */
+typedef struct peagle_weights {
+  const void* embed;            /* [Vt, H] */
+  const void* fc_w;             /* [H, A*Ht] */
+  const void* fc_norm_w;        /* [H] */
+  const void* mask_hidden;      /* [1, A*Ht] learnable placeholder (#2376, Changelog) */
+  const void* final_norm_w;     /* [H] */
+  const void* lm_head_w;        /* [Vd, H] draft-vocab head */
+  const int32_t* d2t;           /* [Vd] draft id -> target id, or NULL = identity */
+  const int32_t* t2d;           /* [Vt] target id -> draft id, -1 = not in the draft
+                                   vocab (label ignored), or NULL = identity */
+  const peagle_layer_weights* layers; /* HOST array of num_layers entries */
+} peagle_weights;
+
+typedef struct peagle_model peagle_model;
+
+/* ---- library ------------------------------------------------------------ */
+const char* peagle_version(void);
+const char* peagle_status_string(peagle_status s);
+/* One-line description of the last failure on this thread ("" if none). */
+const char* peagle_last_error(void);
+/* Number of kernels this library has launched in this process. */
+uint64_t peagle_kernel_launches(void);
+
+/* ---- model -------------------------------------------------------------- */
+/* Validates the config, borrows the weights, allocates the model's own small
+ * device state (rotary table, status word, constants) and precomputes what
+ * every masked row shares: fc_norm(fc(mask_hidden)), the ptd embedding, the
+ * layer-0 pre-rotary q/k/v and residual of a masked row (#2376, Changelog:
+ * masked_projected_hidden). Synchronizes `stream` before returning. */
+peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights* w,
+                                  void* stream, peagle_model** out);
+/* Frees what create allocated (synchronizes the device first). NULL is a no-op. */
+peagle_status peagle_model_destroy(peagle_model* model);
+/* Synchronizes `stream`, then copies the sticky device status word
+ * (PEAGLE_DEV_* bits) to *host_status. */
+peagle_status peagle_get_device_status(const peagle_model* model, void* stream,
+                                       int32_t* host_status);
+/* Clears the device status word (enqueued on `stream`). */
+peagle_status peagle_clear_device_status(const peagle_model* model, void* stream);
+
+/* ---- draft step (decode) ------------------------------------------------ */
+peagle_status peagle_draft_step_workspace_size(const peagle_model* model, int32_t B,
+                                               int32_t K, int32_t max_kv_len, size_t* bytes);
+/* One parallel draft step for B independent requests: all K depths of every
+ * request in one pass (user guide, Inference Process step 1).
+ * Row (b, d), d in [0, K), is depth d of request b (user guide: depth d
+ * predicts position anchor + d):
+ *   depth 0 takes anchor_tokens[b] and fc_norm(fc(aux[b])); depths >= 1 take
+ *   ptd_token_id and fc_norm(fc(mask_hidden)); rotary position anchor_pos[b]+d.
+ * Attention of row (b, d) at every layer reads the request's context rows
+ * k_cache[l][kv_offsets[b] + t], t < kv_lens[b] (post-rotary, written by
+ * earlier steps), then the chain rows (b, 0..d) of this pass.
+ *   aux            device [B, A*Ht]
+ *   anchor_tokens  device int32 [B], target ids < Vt
+ *   anchor_pos     device int32 [B], anchor_pos[b] + K - 1 < max_position
+ *   k_cache/v_cache HOST arrays of num_layers device pointers, each
+ *                  [kv_capacity, nkv, hd]; rows kv_offsets[b].. belong to b
+ *   kv_offsets     device int64 [B+1], kv_lens device int32 [B],
+ *                  kv_lens[b] <= max_kv_len (host bound used to size the grid),
+ *                  kv_offsets[b] + kv_lens[b] + append_anchor_kv <= kv_offsets[b+1]
+ *                  <= kv_capacity
+ *   append_anchor_kv  if 1, the anchor row's post-rotary K/V of every layer is
+ *                  written to row kv_offsets[b] + kv_lens[b] (kv_lens unchanged)
+ *   draft_tokens   device int32 [B, K] out: d2t(argmax over the draft vocab),
+ *                  lowest index among equal maxima
+ *   logits         device float [B, K, Vd] out, or NULL
+ * K in [1, 16]. Violations of the device-side ranges set PEAGLE_DEV_BOUNDS
+ * and the offending row is skipped. */
+peagle_status peagle_draft_step(const peagle_model* model, int32_t B, int32_t K,
+                                const void* aux, const int32_t* anchor_tokens,
+                                const int32_t* anchor_pos, void* const* k_cache,
+                                void* const* v_cache, const int64_t* kv_offsets,
+                                const int32_t* kv_lens, int64_t kv_capacity,
+                                int32_t max_kv_len, int32_t append_anchor_kv,
+                                int32_t* draft_tokens, float* logits, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* ---- greedy verification ------------------------------------------------ */
+/* accept_len[b] = the largest a <= K with draft_tokens[b, i] ==
+ * target_tokens[b, i] for all i < a; next_token[b] = target_tokens[b, a]
+ * (the target's correction, or its bonus token when all K match). The next
+ * round starts from that token (user guide, Inference Process steps 3-4).
+ *   draft_tokens device int32 [B, K]; target_tokens device int32 [B, K+1];
+ *   accept_len, next_token device int32 [B]. B >= 0, K in [1, 64]. */
+peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_tokens,
+                                   const int32_t* target_tokens, int32_t* accept_len,
+                                   int32_t* next_token, void* stream);
+
+/* ---- COD selection ------------------------------------------------------ */
+/* Host only: counts[0] = n, counts[d] = min(counts[d-1], max(floor(n*r^d),
+ * floor(n*r_min))) with r^d formed by repeated multiplication in double
+ * (user guide, COD Sampling and Key Parameters). 0 < r_min <= r <= 1. */
+peagle_status peagle_cod_counts(int32_t n, int32_t K, double r, double r_min,
+                                int32_t* counts_host);
+peagle_status peagle_cod_select_workspace_size(int32_t n, int32_t K, size_t* bytes);
+/* Position i gets key_i = output i of SplitMix64 seeded with `seed` (Steele,
+ * Lea, Flood, OOPSLA 2014: mix(seed + (i+1) * 0x9E3779B97F4A7C15)); keys are
+ * distinct. S_d = the counts[d] positions with the smallest keys, so S_d is
+ * a subset of S_{d-1}, and over random seeds each S_d is a uniform subset.
+ *   counts_host  HOST int32 [K] out (as peagle_cod_counts)
+ *   indices      device int32 [sum counts] out: S_0 = 0..n-1, then S_1, ...,
+ *                each ascending (depth-major)
+ *   row_of       device int32 [K, n] out or NULL: row_of[d*n + i] = index of
+ *                position i within `indices` at depth d, or -1
+ * n in [0, 2^24], K in [1, 16]. */
+peagle_status peagle_cod_select(int32_t n, int32_t K, double r, double r_min,
+                                uint64_t seed, int32_t* counts_host, int32_t* indices,
+                                int32_t* row_of, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* ---- training-shaped parallel forward ----------------------------------- */
+peagle_status peagle_parallel_forward_workspace_size(const peagle_model* model, int32_t n,
+                                                     int32_t K, double r, double r_min,
+                                                     size_t* bytes);
+/* Forward of one packed sequence of n tokens split into num_seqs
+ * conversations by cu_seqlens (#2376, PR description: depth 0 consumes the
+ * real token and projected aux states, depths >= 1 the ptd token and
+ * mask_hidden, no recurrence). Rows are depth-major: depth 0 anchors
+ * 0..n-1, then the COD-kept anchors of each depth, ascending (the order of
+ * peagle_cod_select's indices with the same n, K, r, r_min, seed).
+ * Row (i, d) has rotary position position_ids[i] + d and attends to the
+ * depth-0 rows s(i)..i of its conversation and to its own chain rows
+ * (i, 1..d). Its label is labels[i+d] when i+d is inside the conversation,
+ * loss_mask[i+d] != 0 (if given) and t2d maps it into the draft vocab;
+ * otherwise the row has no label.
+ *   aux          device [n, A*Ht]; input_ids, position_ids, labels device int32 [n]
+ *   cu_seqlens   device int32 [num_seqs+1], 0 = cu[0] <= ... <= cu[num_seqs] = n
+ *   loss_mask    device uint8 [n] or NULL
+ * Outputs (device, float unless noted):
+ *   per_depth_loss [K] mean CE over labelled rows of depth d (0 if none)
+ *   per_depth_acc  [K] fraction of labelled rows whose argmax is the label
+ *   per_depth_valid int32 [K] labelled rows per depth
+ *   loss [1]       sum_d depth_decay^d * per_depth_loss[d]
+ *   row_argmax     int32 [R] or NULL (draft-vocab argmax, lowest index on ties)
+ *   row_ce         [R] or NULL (CE of the row, NaN if it has no label)
+ *   logits         [R, Vd] or NULL
+ * R = sum of the COD counts. */
+peagle_status peagle_parallel_forward(const peagle_model* model, int32_t n, const void* aux,
+                                      const int32_t* input_ids, const int32_t* position_ids,
+                                      const int32_t* cu_seqlens, int32_t num_seqs,
+                                      const int32_t* labels, const uint8_t* loss_mask,
+                                      int32_t K, double r, double r_min, uint64_t seed,
+                                      double depth_decay, float* per_depth_loss,
+                                      float* per_depth_acc, int32_t* per_depth_valid,
+                                      float* loss, int32_t* row_argmax, float* row_ce,
+                                      float* logits, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/* ---- dense contraction --------------------------------------------------- */
+peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, int32_t K,
+                                         size_t* bytes);
+/* D = X W^T accumulated and stored in float: the contraction behind every
+ * projection of the draft (fc, QKV, O, gate/up, down, lm_head; user guide,
+ * Architecture). X device [M, K] and W device [N, K] of `dtype` (nn.Linear
+ * layout), D device float [M, N]. bf16 runs on the tcgen05 tensor cores
+ * (K % 8 == 0, 16-byte aligned X and W), fp32 on the CUDA cores. */
+peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
+                          const void* W, float* D, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* ---- per-kernel timing probe -------------------------------------------- */
+/* Operation classes the probe can time (one class at a time). */
+typedef enum peagle_op {
+  PEAGLE_OP_FC = 0, PEAGLE_OP_QKV = 1, PEAGLE_OP_ATTN = 2, PEAGLE_OP_O = 3,
+  PEAGLE_OP_GATE_UP = 4, PEAGLE_OP_DOWN = 5, PEAGLE_OP_LM_HEAD = 6,
+  PEAGLE_OP_VERIFY = 7, PEAGLE_OP_COD = 8, PEAGLE_OP_CE = 9, PEAGLE_OP_COUNT = 10
+} peagle_op;
+const char* peagle_op_name(int32_t op);
+/* Starts recording a CUDA event pair around every launch of the main kernel
+ * of operation `op` (the GEMM of a projection, the attention kernel, ...) on
+ * the stream it runs on, for up to `capacity` launches. Process-wide. */
+peagle_status peagle_probe_begin(int32_t op, int32_t capacity);
+/* Synchronizes the recorded events and writes up to `capacity` per-launch
+ * durations (ms) to HOST ms_out; *count = launches recorded. Ends recording. */
+peagle_status peagle_probe_end(float* ms_out, int32_t capacity, int32_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PEAGLE_H_ */

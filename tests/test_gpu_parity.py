@@ -1,0 +1,275 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle on
+the same seeded inputs.
+
+Bars: integers bit-exact (COD indices, verify, argmax tokens given clear
+margins); floats within max|gpu - ref| / max|ref| <= 1e-4 (fp32 models) or
+2e-2 (bf16 models). A bf16 draft token may differ from the oracle's only at a
+near-tie: where the oracle's own top-1 / top-2 margin is below 2e-2 of the
+largest |logit|; and every GPU token must equal the argmax of the GPU's own
+exported logits exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import peagle_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+BF16_TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def H():
+    from tests import harness
+    return harness
+
+
+def pe():
+    import eagle_speculative_drafting_gb300 as m
+    return m
+
+
+# ------------------------------------------------------------------ GEMM
+GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17, 1000, 256),
+               (64, 4096, 4096), (100, 1000, 2048), (256, 512, 256), (257, 640, 512),
+               (512, 4096, 1024), (1000, 300, 200), (333, 32000, 128)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_bf16_tensor_core(M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    X = synth.bf16_round(rng.standard_normal((M, K), dtype=np.float32))
+    W = synth.bf16_round(rng.standard_normal((N, K), dtype=np.float32))
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    m = pe()
+    Xd = torch.from_numpy(X).to(torch.bfloat16).cuda()
+    Wd = torch.from_numpy(W).to(torch.bfloat16).cuda()
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nb = m.peagle_gemm_workspace_size(m.PEAGLE_BF16, M, N, K)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    m.peagle_gemm(m.PEAGLE_BF16, M, N, K, Xd, Wd, D, ws, ws.numel())
+    torch.cuda.synchronize()
+    err = H().max_abs_rel(D.cpu().numpy(), ref)
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 70, 33), (5, 64, 64), (65, 130, 100)])
+def test_gemm_f32_cuda_core(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    X = rng.standard_normal((M, K), dtype=np.float32)
+    W = rng.standard_normal((N, K), dtype=np.float32)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    m = pe()
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    m.peagle_gemm(m.PEAGLE_F32, M, N, K, torch.from_numpy(X).cuda(), torch.from_numpy(W).cuda(), D,
+                  None, 0)
+    torch.cuda.synchronize()
+    assert H().max_abs_rel(D.cpu().numpy(), ref) < 1e-6
+
+
+# ---------------------------------------------------------------- verify
+def test_verify_accept_exhaustive_and_random():
+    import itertools
+    V, K = 3, 3
+    d, t = [], []
+    for dd in itertools.product(range(V), repeat=K):
+        for tt in itertools.product(range(V), repeat=K + 1):
+            d.append(dd)
+            t.append(tt)
+    d = np.array(d, dtype=np.int32)
+    t = np.array(t, dtype=np.int32)
+    a, n = H().run_verify(d, t)
+    ra, rn = O.verify_accept(d, t)
+    assert np.array_equal(a, ra) and np.array_equal(n, rn)
+    rng = np.random.default_rng(1)
+    for B, K in ((1, 1), (64, 8), (1000, 16), (7, 64)):
+        d = rng.integers(0, 4, (B, K)).astype(np.int32)
+        t = rng.integers(0, 4, (B, K + 1)).astype(np.int32)
+        match = rng.random((B, K)) < 0.6
+        tk = t[:, :K]
+        tk[match] = d[match]
+        a, n = H().run_verify(d, t)
+        ra, rn = O.verify_accept(d, t)
+        assert np.array_equal(a, ra) and np.array_equal(n, rn)
+
+
+# ------------------------------------------------------------------- COD
+@pytest.mark.parametrize("n,K,r,rmin,seed", [(1, 3, 0.7, 0.2, 5), (7, 4, 0.7, 0.2, 1),
+                                             (1000, 8, 0.7, 0.2, 42), (4096, 4, 0.7, 0.2, 7),
+                                             (32768, 8, 0.7, 0.2, 0x5EED04D7), (5000, 16, 0.9, 0.05, 3),
+                                             (2048, 3, 1.0, 1.0, 9), (100003, 5, 0.6, 0.3, 2**63 + 5)])
+def test_cod_select_bit_exact(n, K, r, rmin, seed):
+    m = pe()
+    counts = m.peagle_cod_counts(n, K, r, rmin)
+    R = sum(counts)
+    idx = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    row_of = torch.full((K * n,), -7, dtype=torch.int32, device="cuda")
+    got_counts = m.peagle_cod_select(n, K, r, rmin, seed, idx, row_of)
+    torch.cuda.synchronize()
+    rc, sets = O.cod_select(n, K, r, rmin, seed)
+    assert got_counts == rc
+    want = np.concatenate(sets).astype(np.int32)
+    assert np.array_equal(idx.cpu().numpy(), want)
+    ro = row_of.cpu().numpy().reshape(K, n)
+    off = np.concatenate([[0], np.cumsum(rc)])
+    for d in range(K):
+        w = np.full(n, -1, dtype=np.int64)
+        w[sets[d]] = off[d] + np.arange(len(sets[d]))
+        assert np.array_equal(ro[d], w)
+
+
+# ---------------------------------------------------------------- decode
+def small_bf16_decode(**kw):
+    wl = synth.WORKLOADS["decode_b64_ragged_k8"].scaled(
+        hidden=256, target_hidden=128, num_aux=3, num_layers=2, num_q_heads=4, num_kv_heads=2,
+        head_dim=64, intermediate=512, vocab=1000, K=4, batch=5, kv_len_range=(0, 300),
+        max_position=2048, seed=501)
+    return wl.scaled(**kw) if kw else wl
+
+
+def check_decode(wl, got, ref, tol):
+    err = H().max_abs_rel(got["logits"], ref["logits"])
+    assert err <= tol, f"logits max-abs-rel {err:.3e} > {tol}"
+    # every GPU token is the argmax of the GPU's own logits
+    assert np.array_equal(got["draft_tokens"], np.argmax(got["logits"], axis=-1))
+    if tol <= F32_TOL:
+        assert np.array_equal(got["draft_tokens"], ref["draft_tokens"])
+    else:
+        bad = H().token_mismatches_explained(got["draft_tokens"], ref["logits"])
+        assert not bad, bad
+    return err
+
+
+def test_decode_tiny_f32():
+    wl = synth.WORKLOADS["tiny_f32_decode"]
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    got = H().run_decode(wl, model, inp, want_logits=True)
+    ref = H().oracle_decode(wl, W, inp)
+    check_decode(wl, got, ref, F32_TOL)
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(batch=80, K=3), dict(num_layers=1, K=1),
+                                dict(kv_len_range=(0, 0)), dict(batch=1, K=16, kv_len_range=(700, 700))])
+def test_decode_bf16_small(kw):
+    wl = small_bf16_decode(**kw)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    got = H().run_decode(wl, model, inp, want_logits=True)
+    ref = H().oracle_decode(wl, W, inp)
+    check_decode(wl, got, ref, BF16_TOL)
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
+def test_decode_f32_multilayer_gqa_append():
+    wl = small_bf16_decode(dtype="f32", batch=3, kv_len_range=(1, 40))
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    got = H().run_decode(wl, model, inp, want_logits=True, append=True)
+    ref = H().oracle_decode(wl, W, inp, append=True)
+    check_decode(wl, got, ref, F32_TOL)
+    d = got["dev"]
+    for l in range(wl.num_layers):
+        kc = d["k_cache"][l].cpu().numpy()
+        vc = d["v_cache"][l].cpu().numpy()
+        for b in range(wl.batch):
+            row = int(inp["kv_offsets"][b] + inp["kv_lens"][b])
+            rk, rv = ref["appended"][l][b]
+            assert H().max_abs_rel(kc[row], rk) <= F32_TOL
+            assert H().max_abs_rel(vc[row], rv) <= F32_TOL
+
+
+def test_decode_prefix_consistency_on_gpu():
+    wl = small_bf16_decode(dtype="f32", batch=2)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    full = H().run_decode(wl, model, inp, want_logits=True, K=4)
+    part = H().run_decode(wl, model, inp, want_logits=True, K=2)
+    assert H().max_abs_rel(part["logits"], full["logits"][:, :2]) < 1e-5
+
+
+def test_decode_flags_out_of_range_token():
+    wl = synth.WORKLOADS["tiny_f32_decode"]
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    inp["anchor_tokens"] = np.array([wl.vocab + 5], dtype=np.int32)
+    model = H().make_model(wl, W)
+    H().run_decode(wl, model, inp)
+    assert pe().peagle_get_device_status(model.handle) & pe().PEAGLE_DEV_BOUNDS
+    pe().peagle_clear_device_status(model.handle)
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
+# -------------------------------------------------------------- training
+def small_train(dtype="f32", n=64, lens=(20, 1, 30, 13), K=4, **kw):
+    wl = small_bf16_decode(dtype=dtype, kind="train", n_tokens=n, K=K, **kw)
+    rng = np.random.default_rng(n + K)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    assert cu[-1] == n
+    pos = np.concatenate([np.arange(l) for l in lens]).astype(np.int32)
+    aux = rng.standard_normal((n, wl.num_aux * wl.target_hidden)).astype(np.float32)
+    if dtype == "bf16":
+        aux = synth.bf16_round(aux)
+    inp = dict(aux=aux, input_ids=rng.integers(0, wl.vocab, n), position_ids=pos, cu_seqlens=cu,
+               labels=rng.integers(0, wl.vocab, n), loss_mask=None)
+    return wl, inp
+
+
+def check_train(wl, inp, K, r, rmin, seed, tol, got=None):
+    W = synth.make_weights(wl)
+    model = H().make_model(wl, W)
+    got = H().run_train(wl, model, inp, K, r, rmin, seed, want_logits=True)
+    ref = O.parallel_forward(H().oracle_model(wl, W), **inp, K=K, r=r, r_min=rmin, seed=seed)
+    assert got["counts"] == ref["counts"]
+    assert H().max_abs_rel(got["logits"], ref["logits"]) <= tol
+    assert np.array_equal(got["per_depth_valid"], ref["per_depth_valid"])
+    assert H().max_abs_rel(got["per_depth_loss"], ref["per_depth_loss"]) <= tol
+    assert abs(float(got["loss"][0]) - ref["loss"]) <= tol * max(1.0, abs(ref["loss"]))
+    lab = ref["row_label"] >= 0
+    assert np.all(np.isnan(got["row_ce"][~lab]))
+    assert H().max_abs_rel(got["row_ce"][lab], ref["row_ce"][lab]) <= tol
+    assert np.array_equal(got["row_argmax"], np.argmax(got["logits"], -1))
+    if tol <= F32_TOL:
+        assert np.array_equal(got["row_argmax"], ref["row_argmax"])
+        assert np.allclose(got["per_depth_acc"], ref["per_depth_acc"], atol=1e-6)
+    else:
+        assert not H().token_mismatches_explained(got["row_argmax"], ref["logits"])
+    assert pe().peagle_get_device_status(model.handle) == 0
+    return got, ref
+
+
+def test_train_tiny_f32():
+    wl, inp = small_train()
+    check_train(wl, inp, 4, 0.7, 0.2, 11, F32_TOL)
+
+
+def test_train_f32_all_rows_and_loss_mask():
+    wl, inp = small_train(n=50, lens=(50,), K=3)
+    inp["loss_mask"] = (np.arange(50) % 3 != 0).astype(np.uint8)
+    check_train(wl, inp, 3, 1.0, 1.0, 2, F32_TOL)
+
+
+def test_train_bf16_small():
+    wl, inp = small_train(dtype="bf16", n=300, lens=(120, 7, 100, 73), K=5)
+    check_train(wl, inp, 5, 0.7, 0.2, 99, BF16_TOL)
+
+
+def test_train_bf16_multi_chunk_rows():
+    # more than 256 rows per GEMM so the wide (non-swapped) tensor-core tiles run
+    wl, inp = small_train(dtype="bf16", n=700, lens=(300, 400), K=2)
+    check_train(wl, inp, 2, 0.7, 0.2, 5, BF16_TOL)
