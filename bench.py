@@ -1,0 +1,407 @@
+#!/usr/bin/env python3
+"""Throughput of the P-EAGLE parallel draft step on GB300.
+
+One step = one pass of the decode hot path over one synthetic batch: the
+parallel draft step (fc/fc_norm, masked-depth inputs, rotary-by-position,
+depth-masked attention over context + chain, MLP, draft-vocab head and
+argmax) followed by greedy verify/accept, all through the C ABI.
+
+Workload (default): bf16 decode, batch 1, KV context 2048, K = 4 depths,
+target hidden 4096 with 3 aux layers, one Llama-3-8B-sized draft layer
+(32 q / 8 kv heads x 128, SwiGLU 14336), draft vocab 32000. Weights and
+inputs are seeded synthetic data; the 849 MB of weights streamed every step
+exceed the 129 MB L2, so no L2 flush is needed between steps.
+
+Metric: drafted tokens/s = B * K / step time (whole job over all ranks).
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "drafted tokens/s per P-EAGLE draft step"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "decode_b1_ctx2048_k4"
+FALLBACK_HBM_GBS = 6800.0
+OP_IDS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="bound on the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's value (the job is as slow as its slowest
+    rank); identity without a process group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, B, K, ms_step):
+    """Drafted tokens/s of the whole job: every rank drafts B*K per step."""
+    return world * B * K / (ms_step / 1000.0)
+
+
+def algorithmic_bytes(wl, B, kv_lens):
+    """Bytes each operation must move at minimum, per launch: weights once,
+    activations in, fp32 results out; attention reads the context K/V once."""
+    es = 2 if wl.dtype == "bf16" else 4
+    K, H, I, V = wl.K, wl.hidden, wl.intermediate, wl.vocab
+    AHt = wl.num_aux * wl.target_hidden
+    QKV, nqhd = wl.qkv_out, wl.num_q_heads * wl.head_dim
+    rows = B * K
+    kv = int(np.sum(kv_lens)) * wl.num_kv_heads * wl.head_dim * 2 * es
+    return {
+        "fc": es * (H * AHt + B * AHt) + 4 * B * H,
+        "qkv": es * (QKV * 2 * H + B * 2 * H) + 4 * B * QKV,   # layer 0 (one-layer draft)
+        "attn": kv + 2 * rows * nqhd * es + rows * 2 * wl.num_kv_heads * wl.head_dim * es,
+        "o_proj": es * (H * nqhd + rows * nqhd) + 4 * rows * H,
+        "gate_up": es * (2 * I * H + rows * H) + 4 * rows * 2 * I,
+        "down": es * (H * I + rows * I) + 4 * rows * H,
+        "lm_head": es * (V * H + rows * H) + 4 * rows * V,
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "eagle_speculative_drafting_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{workload}:{op}")
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_leg(wl, W, inp, seconds, warm=1, max_steps=None):
+    """Times whole oracle draft steps (all requests, all depths) on the host
+    until `seconds` have passed; returns (tokens/s, steps, elapsed, cores)."""
+    from oracle import peagle_oracle as O
+    model = O.DraftModel(O.model_config(wl), W)
+    args = (inp["aux"], inp["anchor_tokens"], inp["anchor_pos"], inp["k_cache"], inp["v_cache"],
+            inp["kv_offsets"], inp["kv_lens"], wl.K)
+    for _ in range(warm):
+        O.draft_step(model, *args)
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        O.draft_step(model, *args)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and steps >= max_steps):
+            break
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    return wl.batch * wl.K * steps / el, steps, el, cores
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    # every step is one whole oracle draft step; the number of steps is bounded
+    # so the run stays within a few minutes whatever --steps asks for
+    budget = min(180.0, 3.0 + 0.5 * args.steps)
+    v, steps, el, cores = oracle_leg(wl, W, inp, seconds=min(budget, 60.0), warm=min(args.warmup, 1),
+                                     max_steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": 1000.0 * el / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{steps} whole float64 oracle draft steps ({wl.batch} request x "
+                                   f"{wl.K} depths each) in {el:.1f} s"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "batch": wl.batch, "K": wl.K,
+            "kv_context": wl.kv_len or list(wl.kv_len_range), "hidden": wl.hidden,
+            "target_hidden": wl.target_hidden, "num_aux": wl.num_aux, "layers": wl.num_layers,
+            "heads": f"{wl.num_q_heads}q/{wl.num_kv_heads}kv x {wl.head_dim}",
+            "intermediate": wl.intermediate, "draft_vocab": wl.vocab,
+            "l2": "weights larger than L2 (streamed every step), no flush",
+            "parallelism": "replicas (independent requests per GPU)"}
+
+
+# ------------------------------------------------------------------- ours
+def main():
+    args = parse_args()
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
+    import eagle_speculative_drafting_gb300 as pe
+    from tests import harness
+
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = harness.make_model(wl, W)
+    d = harness.upload_decode(wl, inp)
+    B, K = wl.batch, wl.K
+    kv_cap = int(inp["kv_capacity"])
+    max_kv = int(np.max(inp["kv_lens"]))
+    drafts = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws_bytes = pe.peagle_draft_step_workspace_size(model.handle, B, K, max_kv)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(dd, targets):
+        pe.peagle_draft_step(model.handle, B, K, dd["aux"], dd["anchor_tokens"], dd["anchor_pos"],
+                             dd["k_cache"], dd["v_cache"], dd["kv_offsets"], dd["kv_lens"], kv_cap,
+                             max_kv, 0, drafts, None, ws, ws_bytes, stream)
+        pe.peagle_verify_accept(B, K, drafts, targets, acc, nxt, stream)
+
+    # targets whose agreement with the drafts has geometric(0.7) length
+    step(d, torch.zeros((B, K + 1), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    accept = synth.draw_accept_lengths(wl, B, K)
+    tgt_np = synth.make_targets_with_accept(wl, drafts.cpu().numpy(), accept)
+    targets = torch.from_numpy(tgt_np).cuda()
+
+    for _ in range(max(args.warmup, 3)):
+        step(d, targets)
+    torch.cuda.synchronize()
+
+    # which kernel dominates: probe each projection / attention class briefly
+    abytes = algorithmic_bytes(wl, B, inp["kv_lens"])
+    shares = {}
+    for name, op in OP_IDS.items():
+        pe.peagle_probe_begin(op, 64)
+        for _ in range(8):
+            step(d, targets)
+        ms = pe.peagle_probe_end(64)
+        shares[name] = float(np.sum(ms)) / 8.0 if ms else 0.0
+    dom = max(shares, key=shares.get)
+
+    # ---- timed region: K steps, device events, barrier + sync both sides
+    launches0 = pe.peagle_kernel_launches()
+    pe.peagle_probe_begin(OP_IDS[dom], args.steps * wl.num_layers + 8)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(d, targets)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    launches = pe.peagle_kernel_launches() - launches0
+    dom_ms = pe.peagle_probe_end(args.steps * wl.num_layers + 8)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
+    ms_step = ms_total / args.steps
+    value = job_throughput(world, B, K, ms_step)
+
+    # ---- end to end through the public API with host buffers
+    h_in = {"aux": torch.from_numpy(inp["aux"]).to(harness.tdtype(wl)).pin_memory(),
+            "anchor_tokens": torch.from_numpy(inp["anchor_tokens"].astype(np.int32)).pin_memory(),
+            "anchor_pos": torch.from_numpy(inp["anchor_pos"].astype(np.int32)).pin_memory(),
+            "kv_offsets": torch.from_numpy(inp["kv_offsets"].astype(np.int64)).pin_memory(),
+            "kv_lens": torch.from_numpy(inp["kv_lens"].astype(np.int32)).pin_memory(),
+            "targets": torch.from_numpy(tgt_np).pin_memory()}
+    h_out = {"drafts": torch.empty((B, K), dtype=torch.int32).pin_memory(),
+             "accept": torch.empty(B, dtype=torch.int32).pin_memory(),
+             "next": torch.empty(B, dtype=torch.int32).pin_memory()}
+    dd = dict(d)
+    dev_tgt = torch.empty_like(targets)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e_steps = max(1, min(args.steps, 2000))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(e_steps):
+        for k in ("aux", "anchor_tokens", "anchor_pos", "kv_offsets", "kv_lens"):
+            dd[k].copy_(h_in[k], non_blocking=True)
+        dev_tgt.copy_(h_in["targets"], non_blocking=True)
+        step(dd, dev_tgt)
+        h_out["drafts"].copy_(drafts, non_blocking=True)
+        h_out["accept"].copy_(acc, non_blocking=True)
+        h_out["next"].copy_(nxt, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / e_steps, dist, "cuda")
+    e2e_value = job_throughput(world, B, K, e2e_ms)
+    status = pe.peagle_get_device_status(model.handle)
+
+    if rank != 0:
+        model.close()
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = measured_peaks()
+    dom_avg_ms = float(np.mean(dom_ms)) if dom_ms else None
+    achieved = abytes[dom] / (dom_avg_ms / 1000.0) / 1e9 if dom_avg_ms else None
+    traffic = recorded_traffic(dom, wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl),
+        "gpu_launches": int(launches),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s",
+                     "frac": (achieved / peak) if achieved else None,
+                     "traffic": traffic, "algorithmic_bytes": abytes[dom],
+                     "avg_launch_ms": dom_avg_ms},
+        "step_shares_ms": {k: round(v, 5) for k, v in shares.items()},
+        "device_status": status,
+    }
+    line["clocks"] = clk.summary()
+    if world == 1 and not args.no_cpu_baseline:
+        v, steps, el, cores = oracle_leg(wl, W, inp, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{steps} whole float64 oracle draft steps "
+                                          f"({B} request x {K} depths) in {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+    model.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -388,8 +388,11 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   if (B == 0) return PEAGLE_OK;
   if (!aux || !anchor_tokens || !anchor_pos || !k_cache || !v_cache || !kv_offsets || !kv_lens || !draft_tokens)
     FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: a required pointer is NULL");
-  for (int l = 0; l < c.num_layers; ++l)
+  for (int l = 0; l < c.num_layers; ++l) {
     if (!k_cache[l] || !v_cache[l]) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is NULL", l);
+    if (!aligned16(k_cache[l]) || !aligned16(v_cache[l]))
+      FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is not 16-byte aligned", l);
+  }
   if (c.dtype == PEAGLE_BF16 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: aux not 16-byte aligned");
   size_t need = 0;
   peagle_draft_step_workspace_size(m, B, K, max_kv_len, &need);
@@ -835,7 +838,12 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
       aa.row_of = ws.row_of;
       aa.O = ws.ao;
       aa.scale = 1.0f / sqrtf((float)hd);
-      CUDA_TRY(launch_train_attn(dt, aa, PEAGLE_OP_ATTN, s));
+      TrainTileArgs tt{};
+      tt.K = K;
+      for (int d = 0; d <= K; ++d) tt.row_off[d] = off[d];
+      tt.tile_off[0] = 0;
+      for (int d = 0; d < K; ++d) tt.tile_off[d + 1] = tt.tile_off[d] + (counts[d] + 63) / 64;
+      CUDA_TRY(launch_train_attn(dt, aa, tt, PEAGLE_OP_ATTN, s));
 
       for (int c0 = 0; c0 < R; c0 += rc) {
         const int mr = std::min(rc, R - c0);

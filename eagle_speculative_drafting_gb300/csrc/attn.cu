@@ -135,6 +135,265 @@ __global__ void decode_combine(DecodeAttnArgs a) {
   }
 }
 
+// ------------------------------------------------- decode, bf16 tensor cores
+// Same split as above, but the chunk's K/V stream through shared memory in
+// 64-key tiles (cp.async, double-buffered) and both products run on the
+// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+//   S = Q K^T   warp w scores keys 16w..16w+15 of the tile for all rows;
+//   softmax     row maxima/sums meet in shared memory, P goes to smem (bf16);
+//   O += P V    warp w owns head dims [w*hd/4, (w+1)*hd/4).
+// Rows are the K*G queries reading this KV head, padded to 16*MT.
+namespace mm {
+__device__ __forceinline__ uint32_t sa(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+      " {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void cp16(uint32_t dst, const void* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+}  // namespace mm
+
+template <int MT, int HD>
+struct MmaAttnCfg {
+  static constexpr int QR = 16 * MT, TK = 64, LDS = HD + 8, LDP = TK + 8;
+  static constexpr int SMEM = (QR * LDS + 4 * TK * LDS + QR * LDP) * 2 + 2 * 4 * QR * 4;
+};
+
+template <int MT, int HD>
+__global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
+  using C = MmaAttnCfg<MT, HD>;
+  constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP;
+  constexpr int DW = HD / 4;          // head dims per warp in the PV product
+  constexpr int NTO = DW / 8;         // n-tiles of 8 dims per warp
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
+  bf16* sK = sQ + QR * LDS;           // [2][TK][LDS]
+  bf16* sV = sK + 2 * TK * LDS;       // [2][TK][LDS]
+  bf16* sP = sV + 2 * TK * LDS;       // [QR][LDP]
+  float* sMax = reinterpret_cast<float*>(sP + QR * LDP);  // [4][QR]
+  float* sSum = sMax + 4 * QR;                             // [4][QR]
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int G = a.nq / a.nkv, KG = a.K * G;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const long long off = a.kv_off[b];
+  int L = a.kv_len[b];
+  const bool ok = L >= 0 && L <= a.max_kv_len && off >= 0 && off + L <= a.kv_off[b + 1] && off + L <= a.kv_cap;
+  if (!ok) {
+    if (tid == 0 && split == 0 && g == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+    L = 0;
+  }
+  const int k0 = split * a.chunk, k1 = min(L, k0 + a.chunk);
+  const int ntiles = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
+  const bf16* kc = static_cast<const bf16*>(a.kcache);
+  const bf16* vc = static_cast<const bf16*>(a.vcache);
+  const bf16* Q = static_cast<const bf16*>(a.Q);
+
+  // queries of this KV head: row qi = d*G + (h % G)
+  for (int e = tid; e < QR * (HD / 8); e += 128) {
+    const int qi = e / (HD / 8), c8 = e % (HD / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (qi < KG) {
+      const int r = b * a.K + qi / G, h = g * G + qi % G;
+      v = *reinterpret_cast<const uint4*>(Q + ((size_t)r * a.nq + h) * HD + c8 * 8);
+    }
+    *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
+  }
+  auto load_tile = [&](int t, int buf) {
+    const int base = k0 + t * TK;
+    for (int e = tid; e < TK * (HD / 8); e += 128) {
+      const int kr = e / (HD / 8), c8 = e % (HD / 8);
+      const int key = base + kr;
+      const bool in = key < k1;
+      const size_t src = ((size_t)(off + (in ? key : k0)) * a.nkv + g) * HD + c8 * 8;
+      mm::cp16(mm::sa(sK + (buf * TK + kr) * LDS + c8 * 8), kc + src, in ? 16 : 0);
+      mm::cp16(mm::sa(sV + (buf * TK + kr) * LDS + c8 * 8), vc + src, in ? 16 : 0);
+    }
+  };
+  if (ntiles > 0) load_tile(0, 0);
+  mm::cp_commit();
+
+  const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
+  float m_run[MT][2], l_run[MT][2];
+  float O[MT][NTO][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    m_run[mt][0] = m_run[mt][1] = -INFINITY;
+    l_run[mt][0] = l_run[mt][1] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
+  }
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(t + 1, buf ^ 1);
+      mm::cp_commit();
+      mm::cp_wait<1>();
+    } else {
+      mm::cp_wait<0>();
+    }
+    __syncthreads();
+    const bf16* tK = sK + buf * TK * LDS;
+    const bf16* tV = sV + buf * TK * LDS;
+    // ---- S = Q K^T for keys 16w..16w+15
+    float S[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      uint32_t bk[4];
+      mm::ldsm4(bk, mm::sa(tK + (16 * w + (lane >> 4) * 8 + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t aq[4];
+        mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+        mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
+        mm::mma16816(S[mt][1], aq, bk[2], bk[3]);
+      }
+    }
+    // ---- scale, mask the tail, per-row maxima of this warp's 16 keys
+    const int kbase = k0 + t * TK + 16 * w + (lane & 3) * 2;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int key = kbase + nt * 8 + c;
+            float v = S[mt][nt][hf * 2 + c] * sl2;
+            v = key < k1 ? v : -INFINITY;
+            S[mt][nt][hf * 2 + c] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if ((lane & 3) == 0) sMax[w * QR + mt * 16 + hf * 8 + (lane >> 2)] = mx;
+      }
+    }
+    __syncthreads();
+    // ---- new running max, probabilities to smem, row sums
+    float corr[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int row = mt * 16 + hf * 8 + (lane >> 2);
+        const float tmax = fmaxf(fmaxf(sMax[row], sMax[QR + row]), fmaxf(sMax[2 * QR + row], sMax[3 * QR + row]));
+        const float mn = fmaxf(m_run[mt][hf], tmax);
+        corr[mt][hf] = (mn == -INFINITY) ? 1.f : exp2f(m_run[mt][hf] - mn);
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          float p0 = (mn == -INFINITY) ? 0.f : exp2f(S[mt][nt][hf * 2] - mn);
+          float p1 = (mn == -INFINITY) ? 0.f : exp2f(S[mt][nt][hf * 2 + 1] - mn);
+          const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+          *reinterpret_cast<__nv_bfloat162*>(sP + row * LDP + 16 * w + nt * 8 + (lane & 3) * 2) = pp;
+          sum += __low2float(pp) + __high2float(pp);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if ((lane & 3) == 0) sSum[w * QR + row] = sum;
+        m_run[mt][hf] = mn;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int row = mt * 16 + hf * 8 + (lane >> 2);
+        l_run[mt][hf] = l_run[mt][hf] * corr[mt][hf] + (sSum[row] + sSum[QR + row] + sSum[2 * QR + row] + sSum[3 * QR + row]);
+#pragma unroll
+        for (int nt = 0; nt < NTO; ++nt) {
+          O[mt][nt][hf * 2] *= corr[mt][hf];
+          O[mt][nt][hf * 2 + 1] *= corr[mt][hf];
+        }
+      }
+    // ---- O += P V over this warp's head dims
+#pragma unroll
+    for (int ks = 0; ks < TK / 16; ++ks) {
+      uint32_t ap[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        mm::ldsm4(ap[mt], mm::sa(sP + (mt * 16 + (lane & 15)) * LDP + ks * 16 + (lane >> 4) * 8));
+#pragma unroll
+      for (int np = 0; np < NTO / 2; ++np) {
+        uint32_t bv[4];
+        mm::ldsm4t(bv, mm::sa(tV + (ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + w * DW + np * 16 +
+                                  (lane >> 4) * 8));
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mm::mma16816(O[mt][2 * np], ap[mt], bv[0], bv[1]);
+          mm::mma16816(O[mt][2 * np + 1], ap[mt], bv[2], bv[3]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // ---- partial (unnormalised O, m in natural-log units, l)
+  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KG;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int row = mt * 16 + hf * 8 + (lane >> 2);
+      if (row >= KG) continue;
+      float* po = a.part_o + (prow + row) * HD + w * DW + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < NTO; ++nt)
+        *reinterpret_cast<float2*>(po + nt * 8) = make_float2(O[mt][nt][hf * 2], O[mt][nt][hf * 2 + 1]);
+      if (w == 0 && (lane & 3) == 0) {
+        a.part_ml[(prow + row) * 2 + 0] = m_run[mt][hf] * 0.6931471805599453f;
+        a.part_ml[(prow + row) * 2 + 1] = l_run[mt][hf];
+      }
+    }
+}
+
+template <int MT, int HD>
+static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
+  using C = MmaAttnCfg<MT, HD>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_mma<MT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  decode_split_mma<MT, HD><<<dim3(a.nsplit, a.nkv, a.B), 128, C::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int HD>
+static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
+  const int KG = a.K * (a.nq / a.nkv);
+  if (KG <= 16) return launch_split_mma<1, HD>(a, st);
+  if (KG <= 32) return launch_split_mma<2, HD>(a, st);
+  if (KG <= 64) return launch_split_mma<4, HD>(a, st);
+  return launch_split_mma<8, HD>(a, st);
+}
+
 void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit) {
   const long long work = (long long)B * nkv * (max_kv_len > 0 ? max_kv_len : 1);
   long long c = work / (2LL * num_sms());
@@ -148,7 +407,12 @@ template <typename T, int E>
 static cudaError_t decode_attn_t(const DecodeAttnArgs& a, int probe_op, cudaStream_t st) {
   dim3 grid(a.nsplit, a.nkv, a.B);
   probe_start(probe_op, st);
-  decode_split_simt<T, E><<<grid, 256, 0, st>>>(a);
+  if (sizeof(T) == 2 && a.K * (a.nq / a.nkv) <= 128) {
+    cudaError_t e = (E == 4) ? split_mma_hd<128>(a, st) : split_mma_hd<64>(a, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    decode_split_simt<T, E><<<grid, 256, 0, st>>>(a);
+  }
   note_launch();
   probe_stop(probe_op, st);
   const int threads = 32 * (a.nq < 32 ? a.nq : 32);
@@ -205,6 +469,222 @@ __global__ void __launch_bounds__(128) train_attn_simt(TrainAttnArgs a) {
   }
 }
 
+// ---------------------------------------------- training, bf16 tensor cores
+// One CTA = 64 consecutive rows of one depth (anchors ascending) x one query
+// head; warp w owns rows 16w..16w+15. Keys stream through shared memory in
+// 64-row tiles (cp.async double buffer):
+//   depth-0 tiles  rows j in [min start, max anchor]; row (i, d) keeps key j
+//                  when start(i) <= j <= i (its own conversation, causal);
+//   chain tiles    for c = 1..d the tile holds rows (a_t, c) of this tile's
+//                  anchors a_t, gathered through row_of; row t keeps only
+//                  key t (its own chain).
+// S = Q K^T and O += P V run on mma.sync m16n8k16; P stays in registers
+// (the accumulator layout of two 8-key tiles is the A layout of a 16-key
+// step). Online softmax in exp2 units.
+template <int HD>
+struct TrainMmaCfg {
+  static constexpr int TQ = 64, TK = 64, LDS = HD + 8;
+  static constexpr int SMEM = (TQ * LDS + 4 * TK * LDS) * 2 + 2 * TK * 4;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTileArgs tt) {
+  using C = TrainMmaCfg<HD>;
+  constexpr int TQ = C::TQ, TK = C::TK, LDS = C::LDS, NTO = HD / 8;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
+  bf16* sK = sQ + TQ * LDS;             // [2][TK][LDS]
+  bf16* sV = sK + 2 * TK * LDS;         // [2][TK][LDS]
+  int* sKey = reinterpret_cast<int*>(sV + 2 * TK * LDS);  // [2][TK] key row ids (-1 = none)
+
+  const int tile = blockIdx.x, h = blockIdx.y;
+  int d = 0;
+  while (d + 1 < tt.K && tile >= tt.tile_off[d + 1]) ++d;
+  const int row0 = tt.row_off[d] + (tile - tt.tile_off[d]) * TQ;
+  const int nrows = min(TQ, tt.row_off[d + 1] - row0);
+  const int G = a.nq / a.nkv, g = h / G;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const bf16* Q = static_cast<const bf16*>(a.Q);
+  const bf16* Kr = static_cast<const bf16*>(a.Kr);
+  const bf16* Vr = static_cast<const bf16*>(a.Vr);
+
+  for (int e = tid; e < TQ * (HD / 8); e += 128) {
+    const int q = e / (HD / 8), c8 = e % (HD / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (q < nrows) v = *reinterpret_cast<const uint4*>(Q + ((size_t)(row0 + q) * a.nq + h) * HD + c8 * 8);
+    *reinterpret_cast<uint4*>(sQ + q * LDS + c8 * 8) = v;
+  }
+  // this thread's two rows (r, r + 8 within the warp's 16)
+  int anc[2], st[2];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int q = 16 * w + hf * 8 + (lane >> 2);
+    const bool live = q < nrows;
+    anc[hf] = live ? a.row_anchor[row0 + q] : -1;
+    st[hf] = live ? a.row_start[row0 + q] : 0x7fffffff;
+  }
+  // key range of the depth-0 part
+  const int last = row0 + nrows - 1;
+  const int kend = a.row_anchor[last];
+  int kbeg = a.row_start[row0];
+  // conversation starts are non-decreasing in the anchor, so row0's start is the minimum
+  const int n0 = (kend - kbeg + 1 + TK - 1) / TK;    // depth-0 key tiles
+  const int ntiles = n0 + d;                         // + one chain tile per depth 1..d
+
+  auto load_tile = [&](int t, int buf) {
+    for (int e = tid; e < TK; e += 128) {
+      int kr;
+      if (t < n0) {
+        const int j = kbeg + t * TK + e;
+        kr = j <= kend ? j : -1;
+      } else {
+        const int c = t - n0 + 1;
+        kr = e < nrows ? a.row_of[(size_t)c * a.n + a.row_anchor[row0 + e]] : -1;
+        if (kr >= a.R) kr = -1;
+      }
+      sKey[buf * TK + e] = kr;
+    }
+    __syncthreads();
+    for (int e = tid; e < TK * (HD / 8); e += 128) {
+      const int kk = e / (HD / 8), c8 = e % (HD / 8);
+      const int kr = sKey[buf * TK + kk];
+      const size_t src = ((size_t)(kr >= 0 ? kr : 0) * a.nkv + g) * HD + c8 * 8;
+      mm::cp16(mm::sa(sK + (buf * TK + kk) * LDS + c8 * 8), Kr + src, kr >= 0 ? 16 : 0);
+      mm::cp16(mm::sa(sV + (buf * TK + kk) * LDS + c8 * 8), Vr + src, kr >= 0 ? 16 : 0);
+    }
+  };
+
+  const float sl2 = a.scale * 1.4426950408889634f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float O[NTO][4];
+#pragma unroll
+  for (int nt = 0; nt < NTO; ++nt) O[nt][0] = O[nt][1] = O[nt][2] = O[nt][3] = 0.f;
+
+  if (ntiles > 0) load_tile(0, 0);
+  mm::cp_commit();
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) {
+      load_tile(t + 1, buf ^ 1);
+      mm::cp_commit();
+      mm::cp_wait<1>();
+    } else {
+      mm::cp_wait<0>();
+    }
+    __syncthreads();
+    const bf16* tK = sK + buf * TK * LDS;
+    const bf16* tV = sV + buf * TK * LDS;
+    const int* keys = sKey + buf * TK;
+    const bool chain = t >= n0;
+    // S = Q_w K^T : 16 rows x 64 keys
+    float S[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      uint32_t aq[4];
+      mm::ldsm4(aq, mm::sa(sQ + (16 * w + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t bk[4];
+        mm::ldsm4(bk, mm::sa(tK + (np * 16 + (lane >> 4) * 8 + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8));
+        mm::mma16816(S[2 * np], aq, bk[0], bk[1]);
+        mm::mma16816(S[2 * np + 1], aq, bk[2], bk[3]);
+      }
+    }
+    // mask + online softmax (rows owned by this quad)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int qrow = 16 * w + hf * 8 + (lane >> 2);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int kk = nt * 8 + (lane & 3) * 2 + c;
+          const int kr = keys[kk];
+          bool ok;
+          if (!chain) ok = kr >= 0 && kr >= st[hf] && kr <= anc[hf];
+          else ok = kr >= 0 && kk == qrow;
+          const float v = ok ? S[nt][hf * 2 + c] * sl2 : -INFINITY;
+          S[nt][hf * 2 + c] = v;
+          mx = fmaxf(mx, v);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m_run[hf], mx);
+      const float corr = (mn == -INFINITY) ? 1.f : exp2f(m_run[hf] - mn);
+      float sum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float p = (mn == -INFINITY) ? 0.f : exp2f(S[nt][hf * 2 + c] - mn);
+          S[nt][hf * 2 + c] = p;
+          sum += p;
+        }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      l_run[hf] = l_run[hf] * corr + sum;
+      m_run[hf] = mn;
+#pragma unroll
+      for (int nt = 0; nt < NTO; ++nt) {
+        O[nt][hf * 2] *= corr;
+        O[nt][hf * 2 + 1] *= corr;
+      }
+    }
+    // O += P V, P from registers
+#pragma unroll
+    for (int kc = 0; kc < 4; ++kc) {
+      uint32_t ap[4];
+      ap[0] = pack_bf16(S[2 * kc][0], S[2 * kc][1]);
+      ap[1] = pack_bf16(S[2 * kc][2], S[2 * kc][3]);
+      ap[2] = pack_bf16(S[2 * kc + 1][0], S[2 * kc + 1][1]);
+      ap[3] = pack_bf16(S[2 * kc + 1][2], S[2 * kc + 1][3]);
+#pragma unroll
+      for (int np = 0; np < NTO / 2; ++np) {
+        uint32_t bv[4];
+        mm::ldsm4t(bv, mm::sa(tV + (kc * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + np * 16 + (lane >> 4) * 8));
+        mm::mma16816(O[2 * np], ap, bv[0], bv[1]);
+        mm::mma16816(O[2 * np + 1], ap, bv[2], bv[3]);
+      }
+    }
+    __syncthreads();
+  }
+  bf16* Og = static_cast<bf16*>(a.O);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int q = 16 * w + hf * 8 + (lane >> 2);
+    if (q >= nrows) continue;
+    const float inv = l_run[hf] > 0.f ? 1.f / l_run[hf] : 0.f;
+    bf16* dst = Og + ((size_t)(row0 + q) * a.nq + h) * HD + (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt)
+      *reinterpret_cast<__nv_bfloat162*>(dst + nt * 8) = __floats2bfloat162_rn(O[nt][hf * 2] * inv, O[nt][hf * 2 + 1] * inv);
+  }
+}
+
+template <int HD>
+static cudaError_t launch_train_mma(const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op, cudaStream_t st) {
+  using C = TrainMmaCfg<HD>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(train_attn_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  probe_start(probe_op, st);
+  train_attn_mma<HD><<<dim3(tt.tile_off[tt.K], a.nq), 128, C::SMEM, st>>>(a, tt);
+  note_launch();
+  probe_stop(probe_op, st);
+  return cudaGetLastError();
+}
+
 template <typename T, int E>
 static cudaError_t train_attn_t(const TrainAttnArgs& a, int probe_op, cudaStream_t st) {
   dim3 grid(a.R, (a.nq + 3) / 4);
@@ -215,10 +695,11 @@ static cudaError_t train_attn_t(const TrainAttnArgs& a, int probe_op, cudaStream
   return cudaGetLastError();
 }
 
-cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, int probe_op, cudaStream_t st) {
+cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op,
+                              cudaStream_t st) {
   if (a.R <= 0) return cudaSuccess;
   if (dtype == PEAGLE_BF16)
-    return a.hd == 128 ? train_attn_t<bf16, 4>(a, probe_op, st) : train_attn_t<bf16, 2>(a, probe_op, st);
+    return a.hd == 128 ? launch_train_mma<128>(a, tt, probe_op, st) : launch_train_mma<64>(a, tt, probe_op, st);
   return a.hd == 128 ? train_attn_t<float, 4>(a, probe_op, st) : train_attn_t<float, 2>(a, probe_op, st);
 }
 

@@ -121,7 +121,7 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
 
   bool append = false;
   size_t cache_row = 0;
-  if (a.kcache && a.mode == 1 && (r % a.K) == 0) {
+  if (a.kcache && !a.row_pos && (r % a.K) == 0) {   // decode anchor row, every layer
     const int b = r / a.K;
     const long long row = a.kv_off[b] + (long long)a.kv_len[b];
     if (a.kv_len[b] >= 0 && row < a.kv_off[b + 1] && row < a.kv_cap && a.kv_off[b] >= 0) {

@@ -127,6 +127,13 @@ cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStr
 
 void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit);
 cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op, cudaStream_t st);
-cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, int probe_op, cudaStream_t st);
+// Query tiles of the tensor-core training attention: 64 rows of one depth.
+struct TrainTileArgs {
+  int K;
+  int row_off[17];   // depth d rows [row_off[d], row_off[d+1])
+  int tile_off[17];  // depth d tiles [tile_off[d], tile_off[d+1])
+};
+cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op,
+                              cudaStream_t st);
 
 }  // namespace pe

@@ -465,6 +465,27 @@ def train_attention_structured(q, k, v, a, d):
     return out
 
 
+def row_labels(n, K, r, r_min, seed, cu_seqlens, labels, loss_mask=None, t2d=None):
+    """Draft-vocab label of every training row (depth-major order), -1 where
+    the row has none: labels[i+d] if i+d is inside anchor i's conversation,
+    not masked out, and mapped into the draft vocab."""
+    counts, sets = cod_select(n, K, r, r_min, seed)
+    anchor, depth = train_rows(n, counts, sets)
+    _, _, end = conversation_bounds(cu_seqlens, n)
+    labels = np.asarray(labels, dtype=np.int64)
+    out = np.full(len(anchor), -1, dtype=np.int64)
+    for t in range(len(anchor)):
+        p = int(anchor[t] + depth[t])
+        if p >= end[anchor[t]]:
+            continue
+        if loss_mask is not None and not loss_mask[p]:
+            continue
+        lab = int(labels[p]) if t2d is None else int(t2d[int(labels[p])])
+        if lab >= 0:
+            out[t] = lab
+    return out, counts
+
+
 def parallel_forward(model: DraftModel, aux, input_ids, position_ids, cu_seqlens, labels,
                      loss_mask, K, r, r_min, seed, depth_decay=0.8,
                      conversations=None, keep_logits=True, keep_kv=False, dense_rows=False):

@@ -529,3 +529,11 @@ def test_masked_row_is_an_anchor_row_fed_mask_hidden_and_ptd():
     out2 = O.draft_step(model, inp["aux"], inp["anchor_tokens"], np.array([5]),
                         inp["k_cache"], inp["v_cache"], inp["kv_offsets"], inp["kv_lens"], 2)
     assert not np.allclose(out2["logits"][0, 0], out2["logits"][0, 1])
+
+
+def test_row_labels_agree_with_forward():
+    wl, model, W, inp = tiny_train()
+    res = O.parallel_forward(model, **inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    lab, counts = O.row_labels(wl.n_tokens, wl.K, 0.7, 0.2, 9, inp["cu_seqlens"], inp["labels"])
+    assert counts == res["counts"]
+    assert np.array_equal(lab, res["row_label"])
