@@ -260,11 +260,14 @@ peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights
   // the layer-0 pre-rotary q/k/v + residual every masked row shares
   const size_t part_f = std::max(gemm_out_floats(c.dtype, 1, H, AHt), gemm_out_floats(c.dtype, 1, QKV, 2 * H));
   const size_t x0_bytes = ((2 * (size_t)H * esize(c)) + 255) & ~size_t(255);
-  CREATE_TRY(cudaMalloc(&tmp, x0_bytes + part_f * sizeof(float)));
+  const size_t part_bytes = ((part_f * sizeof(float)) + 255) & ~size_t(255);
+  CREATE_TRY(cudaMalloc(&tmp, x0_bytes + part_bytes + kGemmSemCount * sizeof(int)));
   void* x0m = tmp;
   float* part = reinterpret_cast<float*>(static_cast<char*>(tmp) + x0_bytes);
+  int* sem = reinterpret_cast<int*>(static_cast<char*>(tmp) + x0_bytes + part_bytes);
+  CREATE_TRY(cudaMemsetAsync(sem, 0, kGemmSemCount * sizeof(int), s));
   GemmOut go;
-  CREATE_TRY(gemm_launch(c.dtype, w->mask_hidden, AHt, w->fc_w, 1, H, AHt, part, &go, m->status, -1, s));
+  CREATE_TRY(gemm_launch(c.dtype, w->mask_hidden, AHt, w->fc_w, 1, H, AHt, part, &go, sem, m->status, -1, s));
   FcFinishArgs fa{};
   fa.u = go;
   fa.H = H;
@@ -281,7 +284,7 @@ peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights
   fa.resid = m->mask_resid0;
   fa.status = m->status;
   CREATE_TRY(launch_fc_finish(c.dtype, 1, fa, s));
-  CREATE_TRY(gemm_launch(c.dtype, x0m, 2 * H, m->layers[0].qkv_w, 1, QKV, 2 * H, part, &go, m->status, -1, s));
+  CREATE_TRY(gemm_launch(c.dtype, x0m, 2 * H, m->layers[0].qkv_w, 1, QKV, 2 * H, part, &go, sem, m->status, -1, s));
   CREATE_TRY(launch_sum_splits(go, 1, QKV, m->mask_qkv0, s));
   CREATE_TRY(cudaStreamSynchronize(s));
   int hs = 0;
@@ -326,6 +329,7 @@ peagle_status peagle_clear_device_status(const peagle_model* m, void* stream) {
 
 // =============================================================== draft step
 struct DraftWs {
+  int* sem;
   void *x0, *xin, *act, *q, *kc, *vc, *ao;
   float *h, *resid0, *part, *attn_o, *attn_ml, *am_val;
   int* am_idx;
@@ -336,6 +340,7 @@ static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, B
   const size_t es = esize(c);
   const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K;
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
+  ws.sem = bp.take<int>(kGemmSemCount);
   ws.x0 = bp.take_bytes((size_t)B * 2 * H * es);
   ws.xin = bp.take_bytes((size_t)rows * H * es);
   ws.act = bp.take_bytes((size_t)rows * I * es);
@@ -409,9 +414,10 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   const int dt = c.dtype;
   const float eps = (float)c.rms_eps;
   GemmOut go;
+  CUDA_TRY(cudaMemsetAsync(ws.sem, 0, kGemmSemCount * sizeof(int), s));
 
   // fc + fc_norm over the anchors' aux states, then the layer-0 input rows
-  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->status, PEAGLE_OP_FC, s));
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, ws.sem, m->status, PEAGLE_OP_FC, s));
   FcFinishArgs fa{};
   fa.u = go;
   fa.H = H;
@@ -432,13 +438,13 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     const peagle_layer_weights& W = m->layers[l];
     QkvArgs qa{};
     if (l == 0) {
-      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->status, PEAGLE_OP_QKV, s));
+      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV, s));
       qa.mode = 1;
       qa.resid0 = ws.resid0;
       qa.mask_resid = m->mask_resid0;
       qa.h = ws.h;
     } else {
-      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, m->status, PEAGLE_OP_QKV, s));
+      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV, s));
       qa.mode = 0;
     }
     qa.in = go;
@@ -490,7 +496,7 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     da.status = m->status;
     CUDA_TRY(launch_decode_attn(dt, da, PEAGLE_OP_ATTN, s));
 
-    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, m->status, PEAGLE_OP_O, s));
+    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, ws.sem, m->status, PEAGLE_OP_O, s));
     ResidNormArgs ra{};
     ra.in = go;
     ra.H = H;
@@ -501,15 +507,15 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ra.y = ws.xin;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
 
-    CUDA_TRY(gemm_launch(dt, ws.xin, H, W.gate_up_w, rows, 2 * I, H, ws.part, &go, m->status, PEAGLE_OP_GATE_UP, s));
+    CUDA_TRY(gemm_launch(dt, ws.xin, H, W.gate_up_w, rows, 2 * I, H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_GATE_UP, s));
     CUDA_TRY(launch_swiglu(dt, go, rows, I, ws.act, s));
-    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->status, PEAGLE_OP_DOWN, s));
+    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, ws.sem, m->status, PEAGLE_OP_DOWN, s));
     ra.in = go;
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
   }
   // draft-vocab head and argmax per depth
-  CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->status,
+  CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem, m->status,
                        PEAGLE_OP_LM_HEAD, s));
   CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
   return PEAGLE_OK;
@@ -588,10 +594,17 @@ peagle_status peagle_cod_select(int32_t n, int32_t K, double r, double r_min, ui
 }
 
 // ============================================================= dense GEMM
+static size_t gemm_slab_bytes(int M, int N, int K) {
+  return ((gemm_out_floats(PEAGLE_BF16, M, N, K) * sizeof(float)) + 255) & ~size_t(255);
+}
+static size_t gemm_ws_bytes(int M, int N, int K) {
+  return gemm_slab_bytes(M, N, K) + kGemmSemCount * sizeof(int);
+}
+
 peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, int32_t K, size_t* bytes) {
   if (!bytes || M < 0 || N < 0 || K < 1 || (dtype != PEAGLE_F32 && dtype != PEAGLE_BF16))
     FAIL(PEAGLE_ERR_INVALID_ARG, "gemm_workspace_size: bad argument");
-  *bytes = dtype == PEAGLE_BF16 ? gemm_out_floats(dtype, M, N, K) * sizeof(float) : 0;
+  *bytes = dtype == PEAGLE_BF16 ? gemm_ws_bytes(M, N, K) : 0;
   return PEAGLE_OK;
 }
 
@@ -603,15 +616,17 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
   if (!X || !W || !D) FAIL(PEAGLE_ERR_INVALID_ARG, "gemm: NULL operand");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == PEAGLE_F32) {
-    CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, D, nullptr, nullptr, -1, s));
+    CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, D, nullptr, nullptr, nullptr, -1, s));
     return PEAGLE_OK;
   }
   if (K % 8 || !aligned16(X) || !aligned16(W)) FAIL(PEAGLE_ERR_INVALID_ARG, "gemm: bf16 needs K %% 8 == 0 and 16-byte aligned operands");
-  size_t need = gemm_out_floats(dtype, M, N, K) * sizeof(float);
+  size_t need = gemm_ws_bytes(M, N, K);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     FAIL(PEAGLE_ERR_WORKSPACE, "gemm: workspace %zu bytes, need %zu", workspace_bytes, need);
   GemmOut go;
-  CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, static_cast<float*>(workspace), &go, nullptr, -1, s));
+  int* sem = reinterpret_cast<int*>(static_cast<char*>(workspace) + gemm_slab_bytes(M, N, K));
+  CUDA_TRY(cudaMemsetAsync(sem, 0, kGemmSemCount * sizeof(int), s));
+  CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, static_cast<float*>(workspace), &go, sem, nullptr, -1, s));
   CUDA_TRY(launch_sum_splits(go, M, N, D, s));
   return PEAGLE_OK;
 }
@@ -621,6 +636,7 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
 
 // ========================================================= parallel forward
 struct TrainWs {
+  int* sem;
   int *indices, *row_of, *anchor, *depth, *pos, *start, *label;
   void *x0, *xin, *act, *q, *kr, *vr, *ao;
   float *resid0, *h, *part, *row_ce;
@@ -644,6 +660,7 @@ static void train_layout(const peagle_config& c, int n, int K, int R, Bump& bp, 
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, dt = c.dtype;
   const int rc = std::max(1, std::min(R, kTrainChunk));
   ws.rc = rc;
+  ws.sem = bp.take<int>(kGemmSemCount);
   ws.indices = bp.take<int>(R);
   ws.row_of = bp.take<int>((size_t)K * n);
   ws.anchor = bp.take<int>(R);
@@ -732,6 +749,7 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
   GemmOut go;
 
   if (n > 0) {
+    CUDA_TRY(cudaMemsetAsync(ws.sem, 0, kGemmSemCount * sizeof(int), s));
     // COD rows and per-row metadata
     st = cod_enqueue(n, K, seed, counts, ws.indices, ws.row_of, s);
     if (st) return st;
@@ -761,7 +779,7 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
     // fc + fc_norm + layer-0 inputs of the n depth-0 rows
     for (int c0 = 0; c0 < n; c0 += rc) {
       const int mr = std::min(rc, n - c0);
-      CUDA_TRY(gemm_launch(dt, atc(aux, (size_t)c0 * AHt), AHt, m->w.fc_w, mr, H, AHt, ws.part, &go, m->status,
+      CUDA_TRY(gemm_launch(dt, atc(aux, (size_t)c0 * AHt), AHt, m->w.fc_w, mr, H, AHt, ws.part, &go, ws.sem, m->status,
                            PEAGLE_OP_FC, s));
       FcFinishArgs fa{};
       fa.u = go;
@@ -803,9 +821,9 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
         const int mr = std::min(rc, src_rows - c0);
         if (l == 0)
           CUDA_TRY(gemm_launch(dt, atc(ws.x0, (size_t)c0 * 2 * H), 2 * H, W.qkv_w, mr, QKV, 2 * H, ws.part, &go,
-                               m->status, PEAGLE_OP_QKV, s));
+                               ws.sem, m->status, PEAGLE_OP_QKV, s));
         else
-          CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.qkv_w, mr, QKV, H, ws.part, &go, m->status,
+          CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.qkv_w, mr, QKV, H, ws.part, &go, ws.sem, m->status,
                                PEAGLE_OP_QKV, s));
         qa.in = go;
         qa.mode = 0;
@@ -848,7 +866,7 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
       for (int c0 = 0; c0 < R; c0 += rc) {
         const int mr = std::min(rc, R - c0);
         CUDA_TRY(gemm_launch(dt, atc(ws.ao, (size_t)c0 * nq * hd), nq * hd, W.o_w, mr, H, nq * hd, ws.part, &go,
-                             m->status, PEAGLE_OP_O, s));
+                             ws.sem, m->status, PEAGLE_OP_O, s));
         ResidNormArgs ra{};
         ra.in = go;
         ra.H = H;
@@ -858,10 +876,10 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
         ra.eps = eps;
         ra.y = ws.xin;
         CUDA_TRY(launch_resid_norm(dt, mr, ra, s));
-        CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.gate_up_w, mr, 2 * I, H, ws.part, &go, m->status,
+        CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.gate_up_w, mr, 2 * I, H, ws.part, &go, ws.sem, m->status,
                              PEAGLE_OP_GATE_UP, s));
         CUDA_TRY(launch_swiglu(dt, go, mr, I, ws.act, s));
-        CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, mr, H, I, ws.part, &go, m->status, PEAGLE_OP_DOWN, s));
+        CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, mr, H, I, ws.part, &go, ws.sem, m->status, PEAGLE_OP_DOWN, s));
         ra.in = go;
         ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
         CUDA_TRY(launch_resid_norm(dt, mr, ra, s));
@@ -870,7 +888,7 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
     // draft-vocab head + per-row CE, chunked so the logits never all exist
     for (int c0 = 0; c0 < R; c0 += rc) {
       const int mr = std::min(rc, R - c0);
-      CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, m->status,
+      CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, ws.sem, m->status,
                            PEAGLE_OP_LM_HEAD, s));
       probe_start(PEAGLE_OP_CE, s);
       CUDA_TRY(launch_ce_rows(go, mr, V, c0, ws.label, logits, rce, ram, s));

@@ -40,6 +40,7 @@ __device__ __forceinline__ void online_add(float s, const float (&v)[E], float& 
 // ---------------------------------------------------------------- decode
 template <typename T, int E>
 __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
+  pdl_trigger();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
 
 template <typename T, int E>
 __global__ void decode_combine(DecodeAttnArgs a) {
+  pdl_trigger();
   const int r = blockIdx.x;
   const int b = r / a.K, d = r % a.K;
   const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
@@ -94,15 +96,17 @@ __global__ void decode_combine(DecodeAttnArgs a) {
   const T* Kc = static_cast<const T*>(a.Kc);
   const T* Vc = static_cast<const T*>(a.Vc);
   T* O = static_cast<T*>(a.O);
-  for (int h = w; h < a.nq; h += nw) {
+  for (int h = blockIdx.y * nw + w; h < a.nq; h += gridDim.y * nw) {
     const int g = h / G, qi = d * G + h % G;
     float M = -INFINITY;
     const size_t prow = (size_t)(b * a.nkv + g) * a.nsplit * KG;
+#pragma unroll 8
     for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.part_ml[(prow + (size_t)s * KG + qi) * 2]);
     float o[E], l = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.f;
     if (M != -INFINITY) {
+#pragma unroll 4
       for (int s = 0; s < a.nsplit; ++s) {
         const size_t pr = prow + (size_t)s * KG + qi;
         const float ms = a.part_ml[pr * 2], ls = a.part_ml[pr * 2 + 1];
@@ -178,6 +182,7 @@ struct MmaAttnCfg {
 
 template <int MT, int HD>
 __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
+  pdl_trigger();
   using C = MmaAttnCfg<MT, HD>;
   constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP;
   constexpr int DW = HD / 4;          // head dims per warp in the PV product
@@ -415,8 +420,7 @@ static cudaError_t decode_attn_t(const DecodeAttnArgs& a, int probe_op, cudaStre
   }
   note_launch();
   probe_stop(probe_op, st);
-  const int threads = 32 * (a.nq < 32 ? a.nq : 32);
-  decode_combine<T, E><<<a.B * a.K, threads, 0, st>>>(a);
+  decode_combine<T, E><<<dim3(a.B * a.K, (a.nq + 3) / 4), 128, 0, st>>>(a);
   note_launch();
   return cudaGetLastError();
 }
@@ -432,6 +436,7 @@ cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op,
 // ---------------------------------------------------------------- training
 template <typename T, int E>
 __global__ void __launch_bounds__(128) train_attn_simt(TrainAttnArgs a) {
+  pdl_trigger();
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int G = a.nq / a.nkv, hd = a.hd;
@@ -494,6 +499,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 template <int HD>
 __global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTileArgs tt) {
+  pdl_trigger();
   using C = TrainMmaCfg<HD>;
   constexpr int TQ = C::TQ, TK = C::TK, LDS = C::LDS, NTO = HD / 8;
   extern __shared__ __align__(16) uint8_t smem_raw[];

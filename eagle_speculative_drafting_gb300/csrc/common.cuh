@@ -64,6 +64,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor finishes; it must wait
+// before touching anything the predecessor writes or reads. Every kernel of
+// the library lets its dependents launch as soon as it starts.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- host side
 void note_launch();                       // counts one kernel launch
 void set_error(const char* fmt, ...);     // records peagle_last_error()
@@ -84,9 +91,14 @@ struct GemmOut {
 int gemm_splits(int M, int N, int K);
 // Workspace floats the partial output of gemm_launch needs.
 size_t gemm_out_floats(int dtype, int M, int N, int K);
-// Runs D = X W^T into out (planning the split itself; fills *o).
+// Per-tile arrival counters a contraction needs when it splits K (ints).
+// They must be zero before the first launch that uses them; every launch
+// leaves them zero again.
+constexpr int kGemmSemCount = 4096;
+// Runs D = X W^T into out (planning the split itself; fills *o). The K
+// slices are summed inside the kernel, so *o always describes one slab.
 // X [M, K] with row stride ldx elements, W [N, K] contiguous.
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
-                        float* out, GemmOut* o, int* dev_status, int probe_op, cudaStream_t s);
+                        float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s);
 
 }  // namespace pe

@@ -152,6 +152,7 @@ struct TcArgs {
   int ldo;                 // row stride of a slab (elements)
   size_t split_stride;     // elements between slabs
   int M, N;                // D is M x N
+  int* sem;                // per-tile arrival counters (zero between launches)
   int* status;
 };
 
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* s_last = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -212,15 +214,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int it = 0;
+      int it = 0, pre = 0;
+      bool waited = false;
       for (int w = blockIdx.x; w < items && !*abort_flag; w += gridDim.x) {
         const int tile = w / g.splits, sp = w % g.splits;
         const int ta = tile % tilesA, tb = tile / tilesA;
         const int kb = (int)((long long)sp * ktiles / g.splits);
         const int ke = (int)((long long)(sp + 1) * ktiles / g.splits);
+        if (!waited) {
+          // the weight tiles of the first stages depend on no earlier kernel:
+          // start streaming them before waiting for the activations
+          pre = min(ke - kb, C::STAGES);
+          for (int q = 0; q < pre; ++q) {
+            tc::mbar_expect_tx(&full[q], C::STAGE);
+            if (SWAP) tc::tma_load_2d(sA + q * C::A_BYTES, &tmA, (kb + q) * 64, ta * 128, &full[q]);
+            else tc::tma_load_2d(sB + q * C::B_BYTES, &tmB, (kb + q) * 64, tb * BN, &full[q]);
+          }
+          pdl_wait();
+          waited = true;
+        }
         for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
+          if (it < pre) {   // weight half already in flight
+            if (SWAP) tc::tma_load_2d(sB + s * C::B_BYTES, &tmB, k * 64, tb * BN, &full[s]);
+            else tc::tma_load_2d(sA + s * C::A_BYTES, &tmA, k * 64, ta * 128, &full[s]);
+            continue;
+          }
           if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
             *abort_flag = 1;
             set_status(g.status, PEAGLE_DEV_TIMEOUT);
@@ -231,6 +251,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc::tma_load_2d(sB + s * C::B_BYTES, &tmB, k * 64, tb * BN, &full[s]);
         }
       }
+      if (!waited) pdl_wait();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -276,7 +297,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    // epilogue: warps 2..5 cover TMEM lane quadrants (warp % 4)
+    // epilogue: warps 2..5 cover TMEM lane quadrants (warp % 4); the output
+    // slabs may still be read by the previous kernel until it completes
+    pdl_wait();
     const int quad = warp & 3;
     int j = 0;
     for (int w = blockIdx.x; w < items; w += gridDim.x, ++j) {
@@ -331,6 +354,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+      if (g.splits > 1) {
+        // the CTA that stores a tile's last K slice sums every slab of the
+        // tile into slab 0, in slab order (deterministic), and re-arms the
+        // tile's counter for the next launch
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) *s_last = (atomicAdd(&g.sem[tile], 1) == g.splits - 1) ? 1 : 0;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*s_last) {
+          __threadfence();
+          if (SWAP) {
+            const int n = arow;
+            if (n < g.N) {
+              for (int c = 0; c < BN; ++c) {
+                const int m = tb * BN + c;
+                if (m >= g.M) break;
+                const size_t idx = (size_t)m * g.ldo + n;
+                float v = 0.f;
+                for (int q = 0; q < g.splits; ++q) v += __ldcg(g.out + (size_t)q * g.split_stride + idx);
+                g.out[idx] = v;
+              }
+            }
+          } else {
+            const int m = arow;
+            if (m < g.M) {
+              for (int c = 0; c < BN; ++c) {
+                const int n = tb * BN + c;
+                if (n >= g.N) break;
+                const size_t idx = (size_t)m * g.ldo + n;
+                float v = 0.f;
+                for (int q = 0; q < g.splits; ++q) v += __ldcg(g.out + (size_t)q * g.split_stride + idx);
+                g.out[idx] = v;
+              }
+            }
+          }
+          if (warp == 2 && lane == 0) g.sem[tile] = 0;
+        }
+      }
     }
   }
   tc::fence_before();
@@ -444,7 +505,7 @@ static Plan plan_gemm(int M, int N, int K) {
   const int smax = std::max(1, std::min(p.swap ? 19 : 4, ktiles / 2));
   double best = -1.0;
   p.splits = 1;
-  for (int s = 1; s <= smax; ++s) {
+  for (int s = 1; s <= smax && (s == 1 || p.tiles <= kGemmSemCount); ++s) {
     const long long items = (long long)p.tiles * s;
     const long long rounds = (items + sms - 1) / sms;
     const double eff = (double)items / (double)(rounds * sms);
@@ -474,14 +535,23 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const T
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const int grid = std::min(items, num_sms());
-  gemm_tc_kernel<BN, SWAP><<<grid, TC_THREADS, C::SMEM, s>>>(a, b, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(items, num_sms()));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP>, a, b, args);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
-                        GemmOut* o, int* dev_status, int probe_op, cudaStream_t s) {
+                        GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s) {
   if (M <= 0 || N <= 0) {
     if (o) *o = GemmOut{out, N, 1, 0};
     return cudaSuccess;
@@ -505,6 +575,7 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
   args.split_stride = (size_t)M * N;
   args.M = M;
   args.N = N;
+  args.sem = sem;
   args.status = dev_status;
   CUtensorMap ma, mb;
   bool ok;
@@ -521,7 +592,8 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
     set_error("cuTensorMapEncodeTiled failed (M=%d N=%d K=%d)", M, N, K);
     return cudaErrorInvalidValue;
   }
-  if (o) *o = GemmOut{out, N, p.splits, args.split_stride};
+  // the kernel folds the K slices into slab 0
+  if (o) *o = GemmOut{out, N, 1, 0};
   const int items = p.tiles * p.splits;
   cudaError_t e;
   probe_start(probe_op, s);

@@ -7,6 +7,8 @@
 
 namespace pe {
 
+constexpr int kQkvChunk = 1024;   // per-row elements one qkv_finish block handles
+
 __device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
   float v = 0.f;
   for (int s = 0; s < g.splits; ++s) v += g.out[(size_t)s * g.split_stride + idx];
@@ -20,6 +22,7 @@ __device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
 // double, so large positions keep their phase.
 // -------------------------------------------------------------------------
 __global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int half, int hd, double theta) {
+  pdl_trigger();
   const long long total = (long long)max_pos * half;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -41,6 +44,7 @@ __global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int hal
 // -------------------------------------------------------------------------
 template <typename T>
 __global__ void fc_finish_kernel(FcFinishArgs a) {
+  pdl_trigger();
   extern __shared__ float sh[];
   __shared__ float red[33];
   const int r = blockIdx.x, H = a.H;
@@ -99,6 +103,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
 // -------------------------------------------------------------------------
 template <typename T>
 __global__ void qkv_finish_kernel(QkvArgs a) {
+  pdl_trigger();
   const int r = blockIdx.x + a.row0;
   const int half = a.hd / 2;
   int src;
@@ -112,7 +117,6 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
     if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
     pos = pos < 0 ? 0 : a.max_pos - 1;
   }
-  const int QKV = (a.nq + 2 * a.nkv) * a.hd;
   T* Q = static_cast<T*>(a.Q) + (size_t)r * a.nq * a.hd;
   T* Ko = static_cast<T*>(a.Kout) + (size_t)r * a.nkv * a.hd;
   T* Vo = static_cast<T*>(a.Vout) + (size_t)r * a.nkv * a.hd;
@@ -127,52 +131,52 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
     if (a.kv_len[b] >= 0 && row < a.kv_off[b + 1] && row < a.kv_cap && a.kv_off[b] >= 0) {
       append = true;
       cache_row = (size_t)row;
-    } else if (threadIdx.x == 0) {
+    } else if (threadIdx.x == 0 && blockIdx.y == 0) {
       set_status(a.status, PEAGLE_DEV_BOUNDS);
     }
   }
+  // this block's slice of the row's work: rotary pairs of q/k heads, then v
+  // elements, then (layer 0) the residual seed
   const int pairs = (a.nq + a.nkv) * half;
-  for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-    const int head = p / half, j = p % half;
-    const int lo = head * a.hd + j, hi = lo + half;
-    float xl, xh;
-    if (src >= 0) {
-      xl = sum_parts(a.in, (size_t)src * a.in.ldo + lo);
-      xh = sum_parts(a.in, (size_t)src * a.in.ldo + hi);
-    } else {
-      xl = a.mask_qkv[lo];
-      xh = a.mask_qkv[hi];
-    }
-    const float c = cs[j], s = sn[j];
-    const float ol = xl * c - xh * s, oh = xh * c + xl * s;
-    if (head < a.nq) {
-      Q[head * a.hd + j] = from_f<T>(ol);
-      Q[head * a.hd + j + half] = from_f<T>(oh);
-    } else {
-      const int kh = head - a.nq;
-      Ko[kh * a.hd + j] = from_f<T>(ol);
-      Ko[kh * a.hd + j + half] = from_f<T>(oh);
-      if (append) {
-        T* kc = static_cast<T*>(a.kcache) + cache_row * a.nkv * a.hd;
-        kc[kh * a.hd + j] = from_f<T>(ol);
-        kc[kh * a.hd + j + half] = from_f<T>(oh);
-      }
-    }
-  }
+  const int vcount = a.nkv * a.hd;
+  const int total = pairs + vcount + (a.h ? a.H : 0);
+  const int e0 = blockIdx.y * kQkvChunk, e1 = min(total, e0 + kQkvChunk);
   const int v0 = (a.nq + a.nkv) * a.hd;
-  for (int e = threadIdx.x; e < a.nkv * a.hd; e += blockDim.x) {
-    const float v = (src >= 0) ? sum_parts(a.in, (size_t)src * a.in.ldo + v0 + e) : a.mask_qkv[v0 + e];
-    Vo[e] = from_f<T>(v);
-    if (append) static_cast<T*>(a.vcache)[cache_row * a.nkv * a.hd + e] = from_f<T>(v);
-  }
-  (void)QKV;
-  if (a.h) {
-    float* h = a.h + (size_t)r * a.H;
-    if (src >= 0) {
-      const float* r0 = a.resid0 + (size_t)src * a.H;
-      for (int j = threadIdx.x; j < a.H; j += blockDim.x) h[j] = r0[j];
+  for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    if (e < pairs) {
+      const int head = e / half, j = e % half;
+      const int lo = head * a.hd + j, hi = lo + half;
+      float xl, xh;
+      if (src >= 0) {
+        xl = sum_parts(a.in, (size_t)src * a.in.ldo + lo);
+        xh = sum_parts(a.in, (size_t)src * a.in.ldo + hi);
+      } else {
+        xl = a.mask_qkv[lo];
+        xh = a.mask_qkv[hi];
+      }
+      const float c = cs[j], sv = sn[j];
+      const float ol = xl * c - xh * sv, oh = xh * c + xl * sv;
+      if (head < a.nq) {
+        Q[head * a.hd + j] = from_f<T>(ol);
+        Q[head * a.hd + j + half] = from_f<T>(oh);
+      } else {
+        const int kh = head - a.nq;
+        Ko[kh * a.hd + j] = from_f<T>(ol);
+        Ko[kh * a.hd + j + half] = from_f<T>(oh);
+        if (append) {
+          T* kc = static_cast<T*>(a.kcache) + cache_row * a.nkv * a.hd;
+          kc[kh * a.hd + j] = from_f<T>(ol);
+          kc[kh * a.hd + j + half] = from_f<T>(oh);
+        }
+      }
+    } else if (e < pairs + vcount) {
+      const int ev = e - pairs;
+      const float v = (src >= 0) ? sum_parts(a.in, (size_t)src * a.in.ldo + v0 + ev) : a.mask_qkv[v0 + ev];
+      Vo[ev] = from_f<T>(v);
+      if (append) static_cast<T*>(a.vcache)[cache_row * a.nkv * a.hd + ev] = from_f<T>(v);
     } else {
-      for (int j = threadIdx.x; j < a.H; j += blockDim.x) h[j] = a.mask_resid[j];
+      const int j = e - pairs - vcount;
+      a.h[(size_t)r * a.H + j] = (src >= 0) ? a.resid0[(size_t)src * a.H + j] : a.mask_resid[j];
     }
   }
 }
@@ -184,6 +188,7 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
 // -------------------------------------------------------------------------
 template <typename T>
 __global__ void resid_norm_kernel(ResidNormArgs a) {
+  pdl_trigger();
   extern __shared__ float sh[];
   __shared__ float red[33];
   const int rl = blockIdx.x;           // row within the chunk
@@ -208,6 +213,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
 // -------------------------------------------------------------------------
 template <typename T>
 __global__ void swiglu_kernel(GemmOut in, int rows, int I, void* act_) {
+  pdl_trigger();
   T* act = static_cast<T*>(act_);
   const long long total = (long long)rows * I;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -237,6 +243,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 
 __global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* logits, float* pval,
                                          int* pidx) {
+  pdl_trigger();
   __shared__ float sv[32];
   __shared__ int si[32];
   const int r = blockIdx.y, c = blockIdx.x, nchunks = gridDim.x;
@@ -272,6 +279,7 @@ __global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* lo
 
 __global__ void lm_argmax_final_kernel(int rows, int nchunks, const float* pval, const int* pidx,
                                        const int* d2t, int* tokens) {
+  pdl_trigger();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -296,6 +304,7 @@ __global__ void lm_argmax_final_kernel(int rows, int nchunks, const float* pval,
 // -------------------------------------------------------------------------
 __global__ void ce_rows_kernel(GemmOut in, int V, int row0, const int* row_label, float* logits_out,
                                float* row_ce, int* row_am) {
+  pdl_trigger();
   __shared__ float sm[32], ss[32], sv[32];
   __shared__ int si[32];
   const int rl = blockIdx.x, r = row0 + rl;
@@ -360,6 +369,7 @@ __global__ void ce_rows_kernel(GemmOut in, int V, int row0, const int* row_label
 // Per-depth means and the decay-weighted total (#2376, Changelog: 0.8**d
 // weighted-mean schedule). One block; fixed summation order.
 __global__ void ce_reduce_kernel(CeReduceArgs a) {
+  pdl_trigger();
   __shared__ double red_d[32];
   __shared__ int red_i[32], red_j[32];
   __shared__ double loss_acc;
@@ -415,6 +425,7 @@ __global__ void ce_reduce_kernel(CeReduceArgs a) {
 // into the draft vocab, else -1.
 // -------------------------------------------------------------------------
 __global__ void train_meta_kernel(TrainMetaArgs a) {
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     bool ok = a.cu[0] == 0 && a.cu[a.S] == a.n;
@@ -466,6 +477,7 @@ __global__ void train_meta_kernel(TrainMetaArgs a) {
 // the first mismatch (or the bonus column).
 // -------------------------------------------------------------------------
 __global__ void verify_kernel(int B, int K, const int* draft, const int* target, int* acc, int* next) {
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int* d = draft + (size_t)b * K;
@@ -491,6 +503,7 @@ __device__ __forceinline__ uint64_t splitmix64_out(uint64_t seed, uint64_t i) {
 }
 
 __global__ void __launch_bounds__(1024) cod_select_kernel(CodArgs a) {
+  pdl_trigger();
   __shared__ unsigned hist[16][256];
   __shared__ uint64_t prefix[16], maskv[16], thr[16];
   __shared__ int rank_left[16], wsum[32], base[16];
@@ -576,6 +589,7 @@ __global__ void __launch_bounds__(1024) cod_select_kernel(CodArgs a) {
 
 // D = sum of the partial slabs (the plain GEMM entry point).
 __global__ void sum_splits_kernel(GemmOut in, int M, int N, float* D) {
+  pdl_trigger();
   const long long total = (long long)M * N;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -616,8 +630,10 @@ cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStr
 
 cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  if (dtype == PEAGLE_BF16) qkv_finish_kernel<bf16><<<rows, 256, 0, st>>>(a);
-  else qkv_finish_kernel<float><<<rows, 256, 0, st>>>(a);
+  const int total = (a.nq + a.nkv) * (a.hd / 2) + a.nkv * a.hd + (a.h ? a.H : 0);
+  const dim3 grid(rows, (total + kQkvChunk - 1) / kQkvChunk);
+  if (dtype == PEAGLE_BF16) qkv_finish_kernel<bf16><<<grid, 256, 0, st>>>(a);
+  else qkv_finish_kernel<float><<<grid, 256, 0, st>>>(a);
   PE_LAUNCH_END();
 }
 
