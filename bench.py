@@ -207,10 +207,52 @@ def oracle_leg(wl, W, inp, seconds, warm=1, max_steps=None):
     return wl.batch * wl.K * steps / el, steps, el, cores
 
 
+def run_reference_train(args, wl):
+    """Oracle timing of the training-shaped forward on whole sampled
+    conversations (exact on their own: conversations never attend to one
+    another), reported as rows of those conversations per second."""
+    import synth
+    from oracle import peagle_oracle as O
+    W = synth.make_weights(wl)
+    inp = synth.make_train_inputs(wl)
+    model = O.DraftModel(O.model_config(wl), W)
+    cu = inp["cu_seqlens"]
+    conv = int(np.argmin(np.diff(cu)))
+    fwd = {k: inp[k] for k in ("aux", "input_ids", "position_ids", "cu_seqlens", "labels", "loss_mask")}
+    kw = dict(K=inp["K"], r=inp["r"], r_min=inp["r_min"], seed=inp["seed"], conversations=[conv],
+              keep_logits=False)
+    res = O.parallel_forward(model, **fwd, **kw)
+    rows = int(np.sum(res["row_argmax"] >= 0))
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        O.parallel_forward(model, **fwd, **kw)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= min(60.0, args.cpu_seconds * 2) or steps >= args.steps:
+            break
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count()
+    v = rows * steps / el
+    sample = (f"{steps} oracle forwards of conversation {conv} ({int(cu[conv + 1] - cu[conv])} tokens, "
+              f"{rows} rows) in {el:.1f} s")
+    line = {"impl": "reference", "metric": TRAIN_METRIC, "value": v, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": 1, "ms_per_step": 1000.0 * el / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name},
+            "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    if wl.kind == "train":
+        return run_reference_train(args, wl)
     import synth
     W = synth.make_weights(wl)
     inp = synth.make_decode_inputs(wl)
@@ -242,6 +284,157 @@ def workload_config(wl):
             "parallelism": "replicas (independent requests per GPU)"}
 
 
+# ------------------------------------------------------ training-shaped pass
+TRAIN_METRIC = "drafted depth-rows/s per P-EAGLE parallel forward"
+TRAIN_OPS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6, "ce": 9}
+
+
+def train_flops(wl, n, R, pairs):
+    """Algorithmic flops per forward of each operation (dense products only
+    over the rows that exist; attention over allowed key pairs)."""
+    H, I, V = wl.hidden, wl.intermediate, wl.vocab
+    AHt, QKV, nqhd, L = wl.num_aux * wl.target_hidden, wl.qkv_out, wl.num_q_heads * wl.head_dim, wl.num_layers
+    return {
+        "fc": 2.0 * n * H * AHt,
+        "qkv": 2.0 * n * QKV * 2 * H + 2.0 * (L - 1) * R * QKV * H,
+        "attn": 4.0 * wl.head_dim * wl.num_q_heads * pairs * L,
+        "o_proj": 2.0 * L * R * H * nqhd,
+        "gate_up": 2.0 * L * R * 2 * I * H,
+        "down": 2.0 * L * R * H * I,
+        "lm_head": 2.0 * R * V * H,
+        "ce": 0.0,
+    }
+
+
+def allowed_pairs(indices, counts, cu):
+    """Key pairs the depth-masked attention scores: row (i, d) reads the
+    depth-0 rows start(i)..i and its d chain rows."""
+    cu = np.asarray(cu, dtype=np.int64)
+    n = int(cu[-1])
+    start = np.zeros(n, dtype=np.int64)
+    for c in range(len(cu) - 1):
+        start[cu[c]:cu[c + 1]] = cu[c]
+    depth = np.repeat(np.arange(len(counts)), counts)
+    idx = np.asarray(indices, dtype=np.int64)
+    return int(np.sum(idx - start[idx] + 1 + depth))
+
+
+def run_train(args, wl):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import eagle_speculative_drafting_gb300 as pe
+    import synth
+    from tests import harness
+
+    W = synth.make_weights(wl)
+    inp = synth.make_train_inputs(wl)
+    model = harness.make_model(wl, W)
+    d = harness.upload_train(wl, inp)
+    n, K, r, rmin, seed = wl.n_tokens, inp["K"], inp["r"], inp["r_min"], inp["seed"]
+    counts = pe.peagle_cod_counts(n, K, r, rmin)
+    R = sum(counts)
+    idx = torch.empty(R, dtype=torch.int32, device="cuda")
+    pe.peagle_cod_select(n, K, r, rmin, seed, idx)
+    pairs = allowed_pairs(idx.cpu().numpy(), counts, inp["cu_seqlens"])
+    flops = train_flops(wl, n, R, pairs)
+    dev = dict(device="cuda")
+    outs = [torch.empty(K, dtype=torch.float32, **dev), torch.empty(K, dtype=torch.float32, **dev),
+            torch.empty(K, dtype=torch.int32, **dev), torch.empty(1, dtype=torch.float32, **dev)]
+    nbytes = pe.peagle_parallel_forward_workspace_size(model.handle, n, K, r, rmin)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    S = len(inp["cu_seqlens"]) - 1
+
+    def step(dd):
+        pe.peagle_parallel_forward(model.handle, n, dd["aux"], dd["input_ids"], dd["position_ids"],
+                                   dd["cu_seqlens"], S, dd["labels"], None, K, r, rmin, seed,
+                                   inp["depth_decay"], *outs, None, None, None, ws, nbytes, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step(d)
+    torch.cuda.synchronize()
+    shares = {}
+    for name, op in TRAIN_OPS.items():
+        pe.peagle_probe_begin(op, 4096)
+        for _ in range(2):
+            step(d)
+        ms = pe.peagle_probe_end(4096)
+        shares[name] = float(np.sum(ms)) / 2.0 if ms else 0.0
+    dom = max(shares, key=shares.get)
+    launches0 = pe.peagle_kernel_launches()
+    pe.peagle_probe_begin(TRAIN_OPS[dom], 1 << 18)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step(d)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    launches = pe.peagle_kernel_launches() - launches0
+    dom_ms = pe.peagle_probe_end(1 << 18)
+    ms_step = e0.elapsed_time(e1) / args.steps
+    # end to end: the step's inputs from pinned host memory, the loss back
+    keys = ("aux", "input_ids", "position_ids", "cu_seqlens", "labels")
+    h_in = {k: d[k].cpu().pin_memory() for k in keys}
+    h_out = torch.empty(3 * K + 1, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e_steps = max(1, min(args.steps, 50))
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(e_steps):
+        for k in keys:
+            d[k].copy_(h_in[k], non_blocking=True)
+        step(d)
+        h_out[:K].copy_(outs[0], non_blocking=True)
+        h_out[K:2 * K].copy_(outs[1], non_blocking=True)
+        h_out[2 * K:3 * K].copy_(outs[2].float(), non_blocking=True)
+        h_out[3 * K:].copy_(outs[3], non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2.elapsed_time(e3) / e_steps
+    peak = 1728.9
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "fallback"
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peak = float(json.load(f)["bf16_tflops_sustained"])
+        src = "measured (sustained)"
+    total_dom_ms = float(np.sum(dom_ms)) / args.steps if dom_ms else None
+    achieved = flops[dom] / (total_dom_ms / 1000.0) / 1e12 if total_dom_ms else None
+    line = {
+        "metric": TRAIN_METRIC, "value": R / (ms_step / 1000.0), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic",
+        "config": {"workload": wl.name, "n_tokens": n, "conversations": S, "K": K, "rows": R,
+                   "cod_counts": counts, "layers": wl.num_layers, "hidden": wl.hidden,
+                   "heads": f"{wl.num_q_heads}q/{wl.num_kv_heads}kv x {wl.head_dim}",
+                   "intermediate": wl.intermediate, "draft_vocab": wl.vocab,
+                   "l2": "activations and weights far larger than L2, no flush"},
+        "gpu_launches": int(launches),
+        "e2e": {"value": R / (e2e_ms / 1000.0), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_source": src, "unit": "TFLOP/s",
+                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "algorithmic_flops_per_step": flops[dom], "ms_per_step": total_dom_ms},
+        "step_shares_ms": {k: round(v, 4) for k, v in shares.items()},
+        "flops_per_step": {k: v for k, v in flops.items()},
+        "device_status": pe.peagle_get_device_status(model.handle),
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 # ------------------------------------------------------------------- ours
 def main():
     args = parse_args()
@@ -249,6 +442,8 @@ def main():
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
+    if wl.kind == "train":
+        return run_train(args, wl)
 
     import torch
     rank, world, local = dist_env()

@@ -98,21 +98,27 @@ __global__ void decode_combine(DecodeAttnArgs a) {
   T* O = static_cast<T*>(a.O);
   for (int h = blockIdx.y * nw + w; h < a.nq; h += gridDim.y * nw) {
     const int g = h / G, qi = d * G + h % G;
-    float M = -INFINITY;
     const size_t prow = (size_t)(b * a.nkv + g) * a.nsplit * KG;
-#pragma unroll 8
-    for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.part_ml[(prow + (size_t)s * KG + qi) * 2]);
-    float o[E], l = 0.f;
+    // the chunks' (m, l): lanes over chunks, then warp reductions
+    float M = -INFINITY;
+    for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, a.part_ml[(prow + (size_t)s * KG + qi) * 2]);
+    M = warp_max(M);
+    float l = 0.f;
+    for (int s = lane; s < a.nsplit; s += 32) {
+      const size_t pr = prow + (size_t)s * KG + qi;
+      const float ms = a.part_ml[pr * 2];
+      if (ms != -INFINITY) l += a.part_ml[pr * 2 + 1] * __expf(ms - M);
+    }
+    l = warp_sum(l);
+    float o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.f;
     if (M != -INFINITY) {
-#pragma unroll 4
+#pragma unroll 8
       for (int s = 0; s < a.nsplit; ++s) {
         const size_t pr = prow + (size_t)s * KG + qi;
-        const float ms = a.part_ml[pr * 2], ls = a.part_ml[pr * 2 + 1];
-        if (ms == -INFINITY) continue;
-        const float c = __expf(ms - M);
-        l += ls * c;
+        const float ms = a.part_ml[pr * 2];
+        const float c = (ms == -INFINITY) ? 0.f : __expf(ms - M);
         const float* po = a.part_o + pr * hd + lane * E;
 #pragma unroll
         for (int e = 0; e < E; ++e) o[e] += po[e] * c;
@@ -400,10 +406,12 @@ static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
 }
 
 void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit) {
+  // about one chunk per SM: each chunk streams its keys once, and fewer
+  // chunks keep the combine short
   const long long work = (long long)B * nkv * (max_kv_len > 0 ? max_kv_len : 1);
-  long long c = work / (2LL * num_sms());
-  int ch = 32;
-  while (ch < c && ch < 512) ch *= 2;
+  long long c = work / num_sms();
+  int ch = 64;
+  while (ch < c && ch < 1024) ch *= 2;
   *chunk = ch;
   *nsplit = max_kv_len > 0 ? (max_kv_len + ch - 1) / ch : 1;
 }

@@ -161,9 +161,15 @@ constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
 template <int BN>
 struct TcCfg {
-  static constexpr int A_BYTES = 128 * 128;             // 128 rows x 64 bf16
-  static constexpr int B_BYTES = BN * 128;
+  // Narrow (swapped) tiles read several 64-wide boxes per stage, so each
+  // weight row is fetched in 256-512 byte runs rather than 128-byte pieces.
+  static constexpr int SUB = (BN == 16) ? 4 : (BN <= 64 ? 2 : 1);
+  static constexpr int A_SUB = 128 * 128;               // 128 rows x 64 bf16
+  static constexpr int B_SUB = BN * 128;                // BN rows x 64 bf16
+  static constexpr int A_BYTES = SUB * A_SUB;
+  static constexpr int B_BYTES = SUB * B_SUB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int KT = 64 * SUB;                   // K elements per stage
   static constexpr int STAGES = std::min(12, (kSmemLimit - 1024 - 256) / STAGE);
   static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
@@ -210,7 +216,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int tilesA = (g.rowsA + 127) / 128;
   const int tilesB = (g.rowsB + BN - 1) / BN;
   const int items = tilesA * tilesB * g.splits;
-  const int ktiles = (g.K + 63) / 64;
+  const int ktiles = (g.K + C::KT - 1) / C::KT;
+  // boxes of 64 K-columns that exist in k-tile k (the last one may be short)
+  auto nsub = [&](int k) { return min(C::SUB, (g.K - k * C::KT + 63) / 64); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -226,9 +234,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           // start streaming them before waiting for the activations
           pre = min(ke - kb, C::STAGES);
           for (int q = 0; q < pre; ++q) {
-            tc::mbar_expect_tx(&full[q], C::STAGE);
-            if (SWAP) tc::tma_load_2d(sA + q * C::A_BYTES, &tmA, (kb + q) * 64, ta * 128, &full[q]);
-            else tc::tma_load_2d(sB + q * C::B_BYTES, &tmB, (kb + q) * 64, tb * BN, &full[q]);
+            const int k = kb + q, nv = nsub(k);
+            tc::mbar_expect_tx(&full[q], nv * (C::A_SUB + C::B_SUB));
+            for (int i = 0; i < nv; ++i) {
+              if (SWAP) tc::tma_load_2d(sA + q * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[q]);
+              else tc::tma_load_2d(sB + q * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[q]);
+            }
           }
           pdl_wait();
           waited = true;
@@ -236,9 +247,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
+          const int nv = nsub(k);
           if (it < pre) {   // weight half already in flight
-            if (SWAP) tc::tma_load_2d(sB + s * C::B_BYTES, &tmB, k * 64, tb * BN, &full[s]);
-            else tc::tma_load_2d(sA + s * C::A_BYTES, &tmA, k * 64, ta * 128, &full[s]);
+            for (int i = 0; i < nv; ++i) {
+              if (SWAP) tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
+              else tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
+            }
             continue;
           }
           if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
@@ -246,9 +260,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             set_status(g.status, PEAGLE_DEV_TIMEOUT);
             break;
           }
-          tc::mbar_expect_tx(&full[s], C::STAGE);
-          tc::tma_load_2d(sA + s * C::A_BYTES, &tmA, k * 64, ta * 128, &full[s]);
-          tc::tma_load_2d(sB + s * C::B_BYTES, &tmB, k * 64, tb * BN, &full[s]);
+          tc::mbar_expect_tx(&full[s], nv * (C::A_SUB + C::B_SUB));
+          for (int i = 0; i < nv; ++i) {
+            tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
+            tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
+          }
         }
       }
       if (!waited) pdl_wait();
@@ -279,12 +295,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             break;
           }
           tc::fence_after();
-          const uint32_t a0 = tc::smem_u32(sA + s * C::A_BYTES);
-          const uint32_t b0 = tc::smem_u32(sB + s * C::B_BYTES);
+          const int nv = nsub(k);
+          for (int i = 0; i < nv; ++i) {
+            const uint32_t a0 = tc::smem_u32(sA + s * C::A_BYTES + i * C::A_SUB);
+            const uint32_t b0 = tc::smem_u32(sB + s * C::B_BYTES + i * C::B_SUB);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc::mma_bf16(dcol, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
-                         (k > kb || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              tc::mma_bf16(dcol, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
+                           (k > kb || i > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc::mma_commit(&empty[s]);
         }
@@ -365,27 +384,41 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (*s_last) {
           __threadfence();
           if (SWAP) {
-            const int n = arow;
+            const int n = arow, m0 = tb * BN, mc = min(BN, g.M - m0);
             if (n < g.N) {
-              for (int c = 0; c < BN; ++c) {
-                const int m = tb * BN + c;
-                if (m >= g.M) break;
-                const size_t idx = (size_t)m * g.ldo + n;
-                float v = 0.f;
-                for (int q = 0; q < g.splits; ++q) v += __ldcg(g.out + (size_t)q * g.split_stride + idx);
-                g.out[idx] = v;
+              for (int c0 = 0; c0 < mc; c0 += 8) {
+                float acc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+                const float* src = g.out + (size_t)(m0 + c0) * g.ldo + n;
+#pragma unroll 4
+                for (int q = 0; q < g.splits; ++q) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    if (c0 + c < mc) acc[c] += __ldcg(src + (size_t)q * g.split_stride + (size_t)c * g.ldo);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  if (c0 + c < mc) g.out[(size_t)(m0 + c0 + c) * g.ldo + n] = acc[c];
               }
             }
           } else {
-            const int m = arow;
+            const int m = arow, n0 = tb * BN, nc = min(BN, g.N - n0);
             if (m < g.M) {
-              for (int c = 0; c < BN; ++c) {
-                const int n = tb * BN + c;
-                if (n >= g.N) break;
-                const size_t idx = (size_t)m * g.ldo + n;
-                float v = 0.f;
-                for (int q = 0; q < g.splits; ++q) v += __ldcg(g.out + (size_t)q * g.split_stride + idx);
-                g.out[idx] = v;
+              for (int c0 = 0; c0 < nc; c0 += 8) {
+                float acc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+                const float* src = g.out + (size_t)m * g.ldo + n0 + c0;
+#pragma unroll 4
+                for (int q = 0; q < g.splits; ++q) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c)
+                    if (c0 + c < nc) acc[c] += __ldcg(src + (size_t)q * g.split_stride + c);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                  if (c0 + c < nc) g.out[(size_t)m * g.ldo + n0 + c0 + c] = acc[c];
               }
             }
           }
@@ -500,9 +533,10 @@ static Plan plan_gemm(int M, int N, int K) {
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
-  const int ktiles = (K + 63) / 64;
+  const int kt_elems = p.swap ? 64 * (p.bn == 16 ? 4 : (p.bn <= 64 ? 2 : 1)) : 64;
+  const int ktiles = (K + kt_elems - 1) / kt_elems;
   const int sms = num_sms();
-  const int smax = std::max(1, std::min(p.swap ? 19 : 4, ktiles / 2));
+  const int smax = std::max(1, p.swap ? std::min(19, ktiles) : std::min(4, ktiles / 2));
   double best = -1.0;
   p.splits = 1;
   for (int s = 1; s <= smax && (s == 1 || p.tiles <= kGemmSemCount); ++s) {

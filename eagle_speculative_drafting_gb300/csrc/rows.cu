@@ -52,6 +52,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
   const T* g_in = static_cast<const T*>(a.g_in);
   const T* g_h = static_cast<const T*>(a.g_h);
   float ss = 0.f;
+#pragma unroll 4
   for (int j = threadIdx.x; j < H; j += blockDim.x) {
     const float v = sum_parts(a.u, (size_t)r * a.u.ldo + j);
     sh[j] = v;
@@ -60,6 +61,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / H + a.eps);
   float ss2 = 0.f;
+#pragma unroll 4
   for (int j = threadIdx.x; j < H; j += blockDim.x) {
     const float h = sh[j] * inv * to_f(g_fc[j]);
     sh[j] = h;
@@ -74,6 +76,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
   }
   const T* e = static_cast<const T*>(a.embed) + (size_t)t * H;
   float ss3 = 0.f;
+#pragma unroll 4
   for (int j = threadIdx.x; j < H; j += blockDim.x) {
     const float v = to_f(e[j]);
     ss3 += v * v;
@@ -81,6 +84,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
   ss3 = block_sum(ss3, red);
   const float inv3 = rsqrtf(ss3 / H + a.eps);
   T* x0 = static_cast<T*>(a.x0) + (size_t)r * 2 * H;
+#pragma unroll 4
   for (int j = threadIdx.x; j < H; j += blockDim.x) {
     const float hn = sh[j] * inv2 * to_f(g_h[j]);
     x0[j] = from_f<T>(to_f(e[j]) * inv3 * to_f(g_in[j]));
@@ -195,6 +199,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
   const int r = a.row0 + rl;           // global row
   float* h = a.h + (size_t)r * a.H;
   float ss = 0.f;
+#pragma unroll 4
   for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
     const float v = h[j] + sum_parts(a.in, (size_t)rl * a.in.ldo + j);
     h[j] = v;
@@ -205,6 +210,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
   const float inv = rsqrtf(ss / a.H + a.eps);
   const T* g = static_cast<const T*>(a.gain);
   T* y = static_cast<T*>(a.y) + (size_t)r * a.H;
+#pragma unroll 4
   for (int j = threadIdx.x; j < a.H; j += blockDim.x) y[j] = from_f<T>(sh[j] * inv * to_f(g[j]));
 }
 
@@ -250,6 +256,7 @@ __global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* lo
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   float bv = -INFINITY;
   int bi = 0x7fffffff;
+#pragma unroll 8
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     const float x = sum_parts(in, (size_t)r * in.ldo + v);
     if (logits) logits[(size_t)r * V + v] = x;
@@ -608,6 +615,15 @@ static int grid_for(long long total, int threads) {
   return (int)(g < 1 ? 1 : g);
 }
 
+// Threads per row of a row-reduction kernel: few rows get wide blocks so the
+// row's loads are all in flight at once; many rows keep blocks small.
+static int row_threads(int rows, int H) {
+  if (rows >= 2 * num_sms()) return 256;
+  int t = 256;
+  while (t < 1024 && t * 4 < H) t *= 2;
+  return t;
+}
+
 #define PE_LAUNCH_END() \
   do {                  \
     note_launch();      \
@@ -623,8 +639,9 @@ cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double th
 cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const size_t sm = (size_t)a.H * sizeof(float);
-  if (dtype == PEAGLE_BF16) fc_finish_kernel<bf16><<<rows, 256, sm, st>>>(a);
-  else fc_finish_kernel<float><<<rows, 256, sm, st>>>(a);
+  const int threads = row_threads(rows, a.H);
+  if (dtype == PEAGLE_BF16) fc_finish_kernel<bf16><<<rows, threads, sm, st>>>(a);
+  else fc_finish_kernel<float><<<rows, threads, sm, st>>>(a);
   PE_LAUNCH_END();
 }
 
@@ -640,8 +657,9 @@ cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_
 cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const size_t sm = (size_t)a.H * sizeof(float);
-  if (dtype == PEAGLE_BF16) resid_norm_kernel<bf16><<<rows, 256, sm, st>>>(a);
-  else resid_norm_kernel<float><<<rows, 256, sm, st>>>(a);
+  const int threads = row_threads(rows, a.H);
+  if (dtype == PEAGLE_BF16) resid_norm_kernel<bf16><<<rows, threads, sm, st>>>(a);
+  else resid_norm_kernel<float><<<rows, threads, sm, st>>>(a);
   PE_LAUNCH_END();
 }
 
