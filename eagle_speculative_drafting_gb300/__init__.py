@@ -100,6 +100,8 @@ _sig("peagle_gemm_workspace_size", c_int32, c_int32, c_int32, c_int32, c_int32,
      ctypes.POINTER(c_size_t))
 _sig("peagle_gemm", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
      c_void_p, c_size_t, c_void_p)
+_sig("peagle_gemm_noalloc", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+     c_void_p, c_void_p)
 _sig("peagle_op_name", ctypes.c_char_p, c_int32)
 _sig("peagle_probe_begin", c_int32, c_int32, c_int32)
 _sig("peagle_probe_end", c_int32, ctypes.POINTER(ctypes.c_float), c_int32, ctypes.POINTER(c_int32))
@@ -244,6 +246,11 @@ def peagle_gemm_workspace_size(dtype, M, N, K):
 def peagle_gemm(dtype, M, N, K, X, W, D, workspace, workspace_bytes, stream=None):
     _check(_lib.peagle_gemm(dtype, M, N, K, ptr(X), ptr(W), ptr(D), ptr(workspace),
                             workspace_bytes, _stream(stream)), "peagle_gemm")
+
+
+def peagle_gemm_noalloc(dtype, M, N, K, X, W, D, stream=None):
+    _check(_lib.peagle_gemm_noalloc(dtype, M, N, K, ptr(X), ptr(W), ptr(D), _stream(stream)),
+           "peagle_gemm_noalloc")
 
 
 def peagle_op_name(op):

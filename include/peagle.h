@@ -264,6 +264,29 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
                           const void* W, float* D, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* ---- dense contraction without allocation -------------------------------- */
+/* peagle_gemm for callers that cannot allocate device memory. Examples:
+ * serving engines whose allocator already owns the device heap; plugins
+ * whose host framework forbids allocation; latency-critical loops that
+ * cannot take cudaMalloc's implicit synchronisation. The pages have no
+ * counterpart for this entry point.
+ * Same operands and result as peagle_gemm, but the split-K partial sums and
+ * tile counters live in a fixed device array inside the library: 8 MiB of
+ * partial sums plus 16 KiB of counters, held on every GPU that loads the
+ * library until the process exits. No workspace is taken and nothing is
+ * allocated.
+ *   - Contractions whose partial sums exceed the array (more than 2^21
+ *     floats, e.g. a few hundred rows of a 32000-wide head) return
+ *     PEAGLE_ERR_UNSUPPORTED.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current. Make that first call
+ *     before any stream capture.
+ *   - Every call clears the counters before use. Calls share the array, so
+ *     calls that may overlap on the GPU race: serialise them, e.g. on one
+ *     stream. */
+peagle_status peagle_gemm_noalloc(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
+                                  const void* W, float* D, void* stream);
+
 /* ---- per-kernel timing probe -------------------------------------------- */
 /* Operation classes the probe can time (one class at a time). */
 typedef enum peagle_op {
