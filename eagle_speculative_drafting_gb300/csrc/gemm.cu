@@ -147,13 +147,72 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 // =========================================================================
 struct TcArgs {
   int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
-  int splits;              // K slices per output tile
+  int splits;              // K slices per output tile (split mode)
+  int streamk;             // 1: stream-K schedule (see Sched)
   float* out;              // fp32 partial slabs
   int ldo;                 // row stride of a slab (elements)
   size_t split_stride;     // elements between slabs
   int M, N;                // D is M x N
   int* sem;                // per-tile arrival counters (zero between launches)
   int* status;
+};
+
+// Work of one persistent CTA, as segments (tile, k-tiles [kb, ke)).
+//   stream-K: the tiles x ktiles (tile, k-tile) units are cut into gridDim
+//     equal contiguous ranges, so every CTA streams the same number of
+//     k-tiles (+-1). The CTAs sharing a tile each write one partial slab:
+//     slab = CTA - first CTA of the tile.
+//   split: items (tile, slice) are dealt round-robin; slice s writes slab s.
+struct Seg {
+  int tile, kb, ke, slab, nslab;
+};
+
+struct Sched {
+  long long U, u, ue;
+  int tiles, ktiles, splits, streamk, grid, cta, w;
+
+  __host__ __device__ static long long begin(long long U, int G, long long c) { return c * U / G; }
+  __host__ __device__ static int owner(long long u, long long U, int G) {
+    long long c = u * G / U;
+    while (c + 1 < G && begin(U, G, c + 1) <= u) ++c;
+    while (c > 0 && begin(U, G, c) > u) --c;
+    return (int)c;
+  }
+  __host__ __device__ void init(int tiles_, int ktiles_, int splits_, int streamk_, int grid_, int cta_) {
+    tiles = tiles_;
+    ktiles = ktiles_;
+    splits = splits_;
+    streamk = streamk_;
+    grid = grid_;
+    cta = cta_;
+    U = (long long)tiles * ktiles;
+    u = begin(U, grid, cta);
+    ue = begin(U, grid, cta + 1);
+    w = cta;
+  }
+  __host__ __device__ bool next(Seg& s) {
+    if (streamk) {
+      if (u >= ue) return false;
+      s.tile = (int)(u / ktiles);
+      s.kb = (int)(u % ktiles);
+      s.ke = (int)((long long)s.kb + (ue - u) < ktiles ? s.kb + (ue - u) : ktiles);
+      const int first = owner((long long)s.tile * ktiles, U, grid);
+      const int last = owner((long long)s.tile * ktiles + ktiles - 1, U, grid);
+      s.slab = cta - first;
+      s.nslab = last - first + 1;
+      u += s.ke - s.kb;
+      return true;
+    }
+    if (w >= tiles * splits) return false;
+    s.tile = w / splits;
+    const int sp = w % splits;
+    s.kb = (int)((long long)sp * ktiles / splits);
+    s.ke = (int)((long long)(sp + 1) * ktiles / splits);
+    s.slab = sp;
+    s.nslab = splits;
+    w += grid;
+    return true;
+  }
 };
 
 constexpr int TC_THREADS = 192;
@@ -215,8 +274,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   const int tilesA = (g.rowsA + 127) / 128;
   const int tilesB = (g.rowsB + BN - 1) / BN;
-  const int items = tilesA * tilesB * g.splits;
   const int ktiles = (g.K + C::KT - 1) / C::KT;
+  Sched sc;
+  sc.init(tilesA * tilesB, ktiles, g.splits, g.streamk, gridDim.x, blockIdx.x);
+  Seg sg;
   // boxes of 64 K-columns that exist in k-tile k (the last one may be short)
   auto nsub = [&](int k) { return min(C::SUB, (g.K - k * C::KT + 63) / 64); };
 
@@ -224,11 +285,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       int it = 0, pre = 0;
       bool waited = false;
-      for (int w = blockIdx.x; w < items && !*abort_flag; w += gridDim.x) {
-        const int tile = w / g.splits, sp = w % g.splits;
-        const int ta = tile % tilesA, tb = tile / tilesA;
-        const int kb = (int)((long long)sp * ktiles / g.splits);
-        const int ke = (int)((long long)(sp + 1) * ktiles / g.splits);
+      while (!*abort_flag && sc.next(sg)) {
+        const int ta = sg.tile % tilesA, tb = sg.tile / tilesA;
+        const int kb = sg.kb, ke = sg.ke;
         if (!waited) {
           // the weight tiles of the first stages depend on no earlier kernel:
           // start streaming them before waiting for the activations
@@ -273,10 +332,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16(128, BN);
       int it = 0, j = 0;
-      for (int w = blockIdx.x; w < items && !*abort_flag; w += gridDim.x, ++j) {
-        const int sp = w % g.splits;
-        const int kb = (int)((long long)sp * ktiles / g.splits);
-        const int ke = (int)((long long)(sp + 1) * ktiles / g.splits);
+      for (; !*abort_flag && sc.next(sg); ++j) {
+        const int kb = sg.kb, ke = sg.ke;
         const int buf = j & 1;
         const uint32_t use = j >> 1;
         if (!tc::mbar_wait(&tempty[buf], (use & 1) ^ 1)) {
@@ -321,8 +378,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     pdl_wait();
     const int quad = warp & 3;
     int j = 0;
-    for (int w = blockIdx.x; w < items; w += gridDim.x, ++j) {
-      const int tile = w / g.splits, sp = w % g.splits;
+    for (; sc.next(sg); ++j) {
+      const int tile = sg.tile, sp = sg.slab;
       const int ta = tile % tilesA, tb = tile / tilesA;
       const int buf = j & 1;
       const uint32_t use = j >> 1;
@@ -373,13 +430,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-      if (g.splits > 1) {
+      if (sg.nslab > 1) {
         // the CTA that stores a tile's last K slice sums every slab of the
         // tile into slab 0, in slab order (deterministic), and re-arms the
         // tile's counter for the next launch
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 2 && lane == 0) *s_last = (atomicAdd(&g.sem[tile], 1) == g.splits - 1) ? 1 : 0;
+        if (warp == 2 && lane == 0) *s_last = (atomicAdd(&g.sem[tile], 1) == sg.nslab - 1) ? 1 : 0;
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*s_last) {
           __threadfence();
@@ -392,7 +449,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int c = 0; c < 8; ++c) acc[c] = 0.f;
                 const float* src = g.out + (size_t)(m0 + c0) * g.ldo + n;
 #pragma unroll 4
-                for (int q = 0; q < g.splits; ++q) {
+                for (int q = 0; q < sg.nslab; ++q) {
 #pragma unroll
                   for (int c = 0; c < 8; ++c)
                     if (c0 + c < mc) acc[c] += __ldcg(src + (size_t)q * g.split_stride + (size_t)c * g.ldo);
@@ -411,7 +468,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int c = 0; c < 8; ++c) acc[c] = 0.f;
                 const float* src = g.out + (size_t)m * g.ldo + n0 + c0;
 #pragma unroll 4
-                for (int q = 0; q < g.splits; ++q) {
+                for (int q = 0; q < sg.nslab; ++q) {
 #pragma unroll
                   for (int c = 0; c < 8; ++c)
                     if (c0 + c < nc) acc[c] += __ldcg(src + (size_t)q * g.split_stride + c);
@@ -519,12 +576,18 @@ static int swap_bn(int M) {
 struct Plan {
   bool swap;
   int bn;
-  int splits;
+  int splits;   // partial slabs per tile (the most any tile needs)
   int tiles;
+  int ktiles;
+  int streamk;
+  int grid;
 };
 
-// Work items are (tile, K slice); pick the slice count that best fills
-// whole rounds of `sms` persistent CTAs, preferring fewer slices on ties.
+static int sub_boxes(int bn) { return bn == 16 ? 4 : (bn <= 64 ? 2 : 1); }
+
+// Few activation rows (swap): stream-K over all (tile, k-tile) units, one
+// persistent CTA per SM. Wide tiles: items (tile, K slice), choosing the
+// slice count that best fills whole rounds of CTAs (fewer on ties).
 static Plan plan_gemm(int M, int N, int K) {
   Plan p;
   p.swap = M <= 256;
@@ -533,10 +596,24 @@ static Plan plan_gemm(int M, int N, int K) {
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
-  const int kt_elems = p.swap ? 64 * (p.bn == 16 ? 4 : (p.bn <= 64 ? 2 : 1)) : 64;
-  const int ktiles = (K + kt_elems - 1) / kt_elems;
+  const int kt_elems = 64 * (p.swap ? sub_boxes(p.bn) : 1);
+  p.ktiles = (K + kt_elems - 1) / kt_elems;
   const int sms = num_sms();
-  const int smax = std::max(1, p.swap ? std::min(19, ktiles) : std::min(4, ktiles / 2));
+  if (p.swap && p.tiles <= kGemmSemCount) {
+    p.streamk = 1;
+    const long long U = (long long)p.tiles * p.ktiles;
+    p.grid = (int)std::min<long long>(U, sms);
+    int most = 1;
+    for (int t = 0; t < p.tiles; ++t) {
+      const int first = Sched::owner((long long)t * p.ktiles, U, p.grid);
+      const int last = Sched::owner((long long)t * p.ktiles + p.ktiles - 1, U, p.grid);
+      most = std::max(most, last - first + 1);
+    }
+    p.splits = most;
+    return p;
+  }
+  p.streamk = 0;
+  const int smax = std::max(1, std::min(4, p.ktiles / 2));
   double best = -1.0;
   p.splits = 1;
   for (int s = 1; s <= smax && (s == 1 || p.tiles <= kGemmSemCount); ++s) {
@@ -548,6 +625,7 @@ static Plan plan_gemm(int M, int N, int K) {
       p.splits = s;
     }
   }
+  p.grid = (int)std::min<long long>((long long)p.tiles * p.splits, sms);
   return p;
 }
 
@@ -559,7 +637,7 @@ size_t gemm_out_floats(int dtype, int M, int N, int K) {
 }
 
 template <int BN, bool SWAP>
-static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int items,
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
                              cudaStream_t s) {
   using C = TcCfg<BN>;
   static bool attr_done = false;
@@ -570,7 +648,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const T
     attr_done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(std::min(items, num_sms()));
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
@@ -604,6 +682,7 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
   TcArgs args;
   args.K = K;
   args.splits = p.splits;
+  args.streamk = p.streamk;
   args.out = out;
   args.ldo = N;
   args.split_stride = (size_t)M * N;
@@ -628,7 +707,7 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
   }
   // the kernel folds the K slices into slab 0
   if (o) *o = GemmOut{out, N, 1, 0};
-  const int items = p.tiles * p.splits;
+  const int items = p.grid;
   cudaError_t e;
   probe_start(probe_op, s);
   if (p.swap) {
