@@ -218,19 +218,23 @@ struct Sched {
 constexpr int TC_THREADS = 192;
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
-template <int BN>
+template <int BN, bool SWAP>
 struct TcCfg {
   // Narrow (swapped) tiles read several 64-wide boxes per stage, so each
   // weight row is fetched in 256-512 byte runs rather than 128-byte pieces.
-  static constexpr int SUB = (BN == 16) ? 4 : (BN <= 64 ? 2 : 1);
+  static constexpr int SUB = (SWAP && BN == 16) ? 4 : ((SWAP && BN <= 64) ? 2 : 1);
   static constexpr int A_SUB = 128 * 128;               // 128 rows x 64 bf16
   static constexpr int B_SUB = BN * 128;                // BN rows x 64 bf16
   static constexpr int A_BYTES = SUB * A_SUB;
   static constexpr int B_BYTES = SUB * B_SUB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int KT = 64 * SUB;                   // K elements per stage
-  static constexpr int STAGES = std::min(12, (kSmemLimit - 1024 - 256) / STAGE);
-  static constexpr int SMEM = 1024 + STAGES * STAGE + 256;
+  // wide tiles stage each epilogue warp's 32 x 32 fp32 block in shared
+  // memory so the stores leave as whole 128-byte lines
+  static constexpr int STG_LD = 33;
+  static constexpr int STAGING = SWAP ? 0 : 4 * 32 * STG_LD * 4;
+  static constexpr int STAGES = std::min(12, (kSmemLimit - 1024 - 256 - STAGING) / STAGE);
+  static constexpr int SMEM = 1024 + STAGES * STAGE + 256 + STAGING;
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
 };
 
@@ -238,7 +242,7 @@ template <int BN, bool SWAP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcArgs g) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -250,6 +254,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* s_last = abort_flag + 1;
+  float* staging = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -394,37 +399,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::fence_after();
       float* slab = g.out + (size_t)sp * g.split_stride;
       const int arow = ta * 128 + quad * 32 + lane;
+      if (SWAP) {
+        // lane = weight row n, column = activation row m: each store of the
+        // warp covers 32 consecutive n
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
-        const int brow0 = tb * BN + c0;
-        if (SWAP) {
-          // lane = weight row n, column = activation row m
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
           const int n = arow;
           if (n < g.N) {
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const int m = brow0 + c;
+              const int m = tb * BN + c0 + c;
               if (m < g.M) slab[(size_t)m * g.ldo + n] = __uint_as_float(r[c]);
             }
           }
-        } else {
-          const int m = arow;
-          if (m < g.M) {
-            float* dst = slab + (size_t)m * g.ldo + brow0;
-            if (brow0 + 16 <= g.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+        }
+      } else {
+        // lane = row m: transpose 32 x 32 blocks through shared memory, then
+        // each warp store writes 4 rows x 128 contiguous bytes
+        float* stg = staging + (warp - 2) * 32 * C::STG_LD;
+        const int m0 = ta * 128 + quad * 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[16];
+          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
 #pragma unroll
-              for (int c = 0; c < 16; c += 4)
-                *reinterpret_cast<float4*>(dst + c) =
-                    make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
-                                __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
-            } else {
+          for (int c = 0; c < 16; ++c) stg[lane * C::STG_LD + c] = __uint_as_float(r[c]);
+          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + 16, r);
 #pragma unroll
-              for (int c = 0; c < 16; ++c)
-                if (brow0 + c < g.N) dst[c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 16; ++c) stg[lane * C::STG_LD + 16 + c] = __uint_as_float(r[c]);
+          __syncwarp();
+          const int cc = (lane & 7) * 4;
+          const int n = tb * BN + c0 + cc;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);
+            const int m = m0 + rr;
+            if (m < g.M) {
+              const float* srow = stg + rr * C::STG_LD + cc;
+              float* dst = slab + (size_t)m * g.ldo + n;
+              if (n + 4 <= g.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+                *reinterpret_cast<float4*>(dst) = make_float4(srow[0], srow[1], srow[2], srow[3]);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                  if (n + c < g.N) dst[c] = srow[c];
+              }
             }
           }
+          __syncwarp();
         }
       }
       tc::fence_before();
@@ -460,22 +484,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               }
             }
           } else {
-            const int m = arow, n0 = tb * BN, nc = min(BN, g.N - n0);
-            if (m < g.M) {
-              for (int c0 = 0; c0 < nc; c0 += 8) {
-                float acc[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-                const float* src = g.out + (size_t)m * g.ldo + n0 + c0;
+            // warp sums its 32 rows; lanes walk 32 consecutive columns
+            const int n0 = tb * BN;
+            for (int rr = 0; rr < 32; ++rr) {
+              const int m = ta * 128 + quad * 32 + rr;
+              if (m >= g.M) break;
+#pragma unroll 2
+              for (int c0 = 0; c0 < BN; c0 += 32) {
+                const int n = n0 + c0 + lane;
+                if (n < g.N) {
+                  const size_t idx = (size_t)m * g.ldo + n;
+                  float acc = 0.f;
 #pragma unroll 4
-                for (int q = 0; q < sg.nslab; ++q) {
-#pragma unroll
-                  for (int c = 0; c < 8; ++c)
-                    if (c0 + c < nc) acc[c] += __ldcg(src + (size_t)q * g.split_stride + c);
+                  for (int q = 0; q < sg.nslab; ++q) acc += __ldcg(g.out + (size_t)q * g.split_stride + idx);
+                  g.out[idx] = acc;
                 }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                  if (c0 + c < nc) g.out[(size_t)m * g.ldo + n0 + c0 + c] = acc[c];
               }
             }
           }
@@ -613,7 +636,7 @@ static Plan plan_gemm(int M, int N, int K) {
     return p;
   }
   p.streamk = 0;
-  const int smax = std::max(1, std::min(4, p.ktiles / 2));
+  const int smax = (2 * p.tiles >= sms) ? 1 : std::max(1, std::min(4, p.ktiles / 2));
   double best = -1.0;
   p.splits = 1;
   for (int s = 1; s <= smax && (s == 1 || p.tiles <= kGemmSemCount); ++s) {
@@ -639,7 +662,7 @@ size_t gemm_out_floats(int dtype, int M, int N, int K) {
 template <int BN, bool SWAP>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
                              cudaStream_t s) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, SWAP>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP>,
