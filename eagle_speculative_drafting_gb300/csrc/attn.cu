@@ -176,10 +176,6 @@ __device__ __forceinline__ void cp16(uint32_t dst, const void* src, int bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Pulls `bytes` (multiple of 16, 16-byte aligned) into L2 only.
-__device__ __forceinline__ void l2_prefetch(const void* p, int bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 }  // namespace mm
@@ -233,14 +229,6 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
   }
   auto load_tile = [&](int t, int buf) {
     const int base = k0 + t * TK;
-    // rows of the tile three ahead go to L2 now (one K and one V row per thread)
-    {
-      const int key = base + 3 * TK + (tid & (TK - 1));
-      if (key < k1) {
-        const size_t src = ((size_t)(off + key) * a.nkv + g) * HD;
-        mm::l2_prefetch((tid < TK ? kc : vc) + src, HD * 2);
-      }
-    }
     for (int e = tid; e < TK * (HD / 8); e += 128) {
       const int kr = e / (HD / 8), c8 = e % (HD / 8);
       const int key = base + kr;

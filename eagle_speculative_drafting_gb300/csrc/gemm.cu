@@ -77,13 +77,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// Pulls a box into L2 only (no shared memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -295,29 +288,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // Weight tiles are also pulled into L2 about 512 KB ahead of the
-      // shared-memory ring: HBM latency under full load is several
-      // microseconds, more than the ring alone can cover.
-      constexpr int W_KT = SWAP ? C::A_BYTES : C::B_BYTES;
-      constexpr int PF = (512 * 1024 / W_KT) > 2 ? (512 * 1024 / W_KT) : 2;
-      auto prefetch = [&](int tile, int k) {
-        const int pa = tile % tilesA, pb = tile / tilesA, nv = nsub(k);
-        for (int i = 0; i < nv; ++i) {
-          if (SWAP) tc::tma_prefetch_2d(&tmA, k * C::KT + i * 64, pa * 128);
-          else tc::tma_prefetch_2d(&tmB, k * C::KT + i * 64, pb * BN);
-        }
-      };
-      const long long ub = sc.u, uend = sc.ue;   // this CTA's stream-K units
-      if (g.streamk)
-        for (long long u = ub + C::STAGES; u < uend && u < ub + PF; ++u)
-          prefetch((int)(u / ktiles), (int)(u % ktiles));
       int it = 0, pre = 0;
       bool waited = false;
       while (!*abort_flag && sc.next(sg)) {
         const int ta = sg.tile % tilesA, tb = sg.tile / tilesA;
         const int kb = sg.kb, ke = sg.ke;
-        if (!g.streamk)
-          for (int k = kb + C::STAGES; k < ke && k < kb + PF; ++k) prefetch(sg.tile, k);
         if (!waited) {
           // the weight tiles of the first stages depend on no earlier kernel:
           // start streaming them before waiting for the activations
@@ -337,12 +312,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           const int nv = nsub(k);
-          if (g.streamk) {
-            const long long u = (long long)sg.tile * ktiles + k + PF;
-            if (u < uend) prefetch((int)(u / ktiles), (int)(u % ktiles));
-          } else if (k + PF < ke) {
-            prefetch(sg.tile, k + PF);
-          }
           if (it < pre) {   // weight half already in flight
             for (int i = 0; i < nv; ++i) {
               if (SWAP) tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
