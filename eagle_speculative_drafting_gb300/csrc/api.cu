@@ -362,7 +362,7 @@ static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, B
   const size_t prow = (size_t)B * nkv * ws.nsplit * K * (nq / nkv);
   ws.attn_o = bp.take<float>(prow * hd);
   ws.attn_ml = bp.take<float>(prow * 2);
-  const size_t nch = lm_argmax_chunks(c.draft_vocab);
+  const size_t nch = std::max<size_t>(lm_argmax_chunks(c.draft_vocab), (c.draft_vocab + 127) / 128);
   ws.am_val = bp.take<float>((size_t)rows * nch);
   ws.am_idx = bp.take<int>((size_t)rows * nch);
 }
@@ -514,10 +514,24 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
   }
-  // draft-vocab head and argmax per depth
-  CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem, m->status,
-                       PEAGLE_OP_LM_HEAD, s));
-  CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
+  // draft-vocab head and argmax per depth: bf16 reduces each output tile
+  // inside the GEMM (warp argmax); fp32 stores the logits and reduces them
+  if (dt == PEAGLE_BF16) {
+    GemmEpi ep{};
+    ep.op = GEMM_EPI_ARGMAX;
+    ep.logits = logits;
+    ep.logits_ld = c.draft_vocab;
+    ep.p_max = ws.am_val;
+    ep.p_idx = ws.am_idx;
+    CUDA_TRY(gemm_launch_epi(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem,
+                             m->status, PEAGLE_OP_LM_HEAD, &ep, s));
+    CUDA_TRY(launch_lm_argmax_final(rows, gemm_col_tiles(rows, c.draft_vocab, H), ws.am_val, ws.am_idx, m->w.d2t,
+                                    draft_tokens, s));
+  } else {
+    CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem, m->status,
+                         PEAGLE_OP_LM_HEAD, s));
+    CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
+  }
   return PEAGLE_OK;
 }
 
@@ -641,6 +655,8 @@ struct TrainWs {
   void *x0, *xin, *act, *q, *kr, *vr, *ao;
   float *resid0, *h, *part, *row_ce;
   int* row_am;
+  float *p_max, *p_sum, *p_lab;   // fused head partials of one chunk
+  int* p_idx;
   int rc;  // rows per GEMM chunk
 };
 
@@ -687,6 +703,11 @@ static void train_layout(const peagle_config& c, int n, int K, int R, Bump& bp, 
   ws.part = bp.take<float>(pf);
   ws.row_ce = bp.take<float>(R);
   ws.row_am = bp.take<int>(R);
+  const size_t parts = (size_t)rc * ((c.draft_vocab + 127) / 128);
+  ws.p_max = bp.take<float>(parts);
+  ws.p_sum = bp.take<float>(parts);
+  ws.p_lab = bp.take<float>(parts);
+  ws.p_idx = bp.take<int>(parts);
 }
 
 extern "C" {
@@ -888,11 +909,29 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
     // draft-vocab head + per-row CE, chunked so the logits never all exist
     for (int c0 = 0; c0 < R; c0 += rc) {
       const int mr = std::min(rc, R - c0);
-      CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, ws.sem, m->status,
-                           PEAGLE_OP_LM_HEAD, s));
-      probe_start(PEAGLE_OP_CE, s);
-      CUDA_TRY(launch_ce_rows(go, mr, V, c0, ws.label, logits, rce, ram, s));
-      probe_stop(PEAGLE_OP_CE, s);
+      if (dt == PEAGLE_BF16) {  // cross-entropy partials reduced inside the GEMM
+        GemmEpi ep{};
+        ep.op = GEMM_EPI_CE;
+        ep.logits = logits ? logits + (size_t)c0 * V : nullptr;
+        ep.logits_ld = V;
+        ep.p_max = ws.p_max;
+        ep.p_sum = ws.p_sum;
+        ep.p_lab = ws.p_lab;
+        ep.p_idx = ws.p_idx;
+        ep.labels = ws.label + c0;
+        CUDA_TRY(gemm_launch_epi(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, ws.sem,
+                                 m->status, PEAGLE_OP_LM_HEAD, &ep, s));
+        probe_start(PEAGLE_OP_CE, s);
+        CUDA_TRY(launch_ce_merge(mr, gemm_col_tiles(mr, V, H), c0, ws.p_max, ws.p_sum, ws.p_lab, ws.p_idx, ws.label,
+                                 rce, ram, s));
+        probe_stop(PEAGLE_OP_CE, s);
+      } else {
+        CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, m->w.lm_head_w, mr, V, H, ws.part, &go, ws.sem,
+                             m->status, PEAGLE_OP_LM_HEAD, s));
+        probe_start(PEAGLE_OP_CE, s);
+        CUDA_TRY(launch_ce_rows(go, mr, V, c0, ws.label, logits, rce, ram, s));
+        probe_stop(PEAGLE_OP_CE, s);
+      }
     }
   }
   CeReduceArgs cr{};

@@ -101,4 +101,23 @@ constexpr int kGemmSemCount = 4096;
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
                         float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s);
 
+// Fused head epilogue of a bf16 contraction: instead of (or besides) the
+// fp32 result, per (row, column tile) partials of the row's argmax (value,
+// lowest index) and, for cross-entropy, the max, the sum of exp(x - max) and
+// the label's logit (-inf when the label is in another tile).
+enum { GEMM_EPI_ARGMAX = 1, GEMM_EPI_CE = 2 };
+struct GemmEpi {
+  int op;
+  float* logits;        // optional fp32 copy of D [M, logits_ld]
+  int logits_ld;
+  float *p_max, *p_sum, *p_lab;   // [M, gemm_col_tiles]
+  int* p_idx;
+  const int* labels;    // GEMM_EPI_CE: label per row, -1 = none
+};
+// Column tiles (partials per row) of the fused head epilogue.
+int gemm_col_tiles(int M, int N, int K);
+cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
+                            float* out, GemmOut* o, int* sem, int* dev_status, int probe_op,
+                            const GemmEpi* epi, cudaStream_t s);
+
 }  // namespace pe

@@ -145,6 +145,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 // =========================================================================
 // The tcgen05 kernel
 // =========================================================================
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_CE = 2 };
+
 struct TcArgs {
   int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
   int splits;              // K slices per output tile (split mode)
@@ -155,7 +157,95 @@ struct TcArgs {
   int M, N;                // D is M x N
   int* sem;                // per-tile arrival counters (zero between launches)
   int* status;
+  // fused head epilogue (op != EPI_STORE): one partial per (row, column tile)
+  int op;
+  int part_ld;             // column tiles per row
+  float* logits;           // optional fp32 copy of D, row stride logits_ld
+  int logits_ld;
+  float *p_max, *p_sum, *p_lab;
+  int* p_idx;
+  const int* labels;       // EPI_CE: draft-vocab label per GEMM row, -1 = none
 };
+
+// Running head statistics of one row over some columns: argmax (lowest
+// index on ties), and for cross-entropy the online max / sum of exp and the
+// logit of the label.
+struct HeadAcc {
+  float bv, mx, se, ll;
+  int bi;
+  __device__ __forceinline__ void init() {
+    bv = -INFINITY;
+    bi = 0x7fffffff;
+    mx = -INFINITY;
+    se = 0.f;
+    ll = -INFINITY;
+  }
+  __device__ __forceinline__ void add(float v, int n, int lab, bool ce) {
+    if (am_better(v, n, bv, bi)) {
+      bv = v;
+      bi = n;
+    }
+    if (ce) {
+      if (v > mx) {
+        se = se * __expf(mx - v) + 1.f;
+        mx = v;
+      } else {
+        se += __expf(v - mx);
+      }
+      if (n == lab) ll = v;
+    }
+  }
+  __device__ __forceinline__ void warp_merge(bool ce) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (am_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+      if (ce) {
+        const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+        const float os = __shfl_xor_sync(0xffffffffu, se, o);
+        const float nm = fmaxf(mx, om);
+        se = (mx == -INFINITY ? 0.f : se * __expf(mx - nm)) + (om == -INFINITY ? 0.f : os * __expf(om - nm));
+        mx = nm;
+        ll = fmaxf(ll, __shfl_xor_sync(0xffffffffu, ll, o));
+      }
+    }
+  }
+  __device__ __forceinline__ void write(const struct TcArgs& g, int m, int ct) const;
+};
+
+__device__ __forceinline__ void HeadAcc::write(const TcArgs& g, int m, int ct) const {
+  const size_t idx = (size_t)m * g.part_ld + ct;
+  g.p_idx[idx] = bi;
+  g.p_max[idx] = bv;
+  if (g.op == EPI_CE) {
+    g.p_sum[idx] = se;
+    g.p_lab[idx] = ll;
+  }
+}
+
+// Head statistics of finished rows read back from slab 0: a warp per row,
+// lanes across the tile's columns.
+__device__ void head_finish_rows(const TcArgs& g, int m_begin, int m_end, int m_step, int n0, int ncols,
+                                 int ct, int lane) {
+  const bool ce = g.op == EPI_CE;
+  for (int m = m_begin; m < m_end; m += m_step) {
+    const int lab = (ce && g.labels) ? g.labels[m] : -1;
+    HeadAcc a;
+    a.init();
+    for (int c = lane; c < ncols; c += 32) {
+      const int n = n0 + c;
+      const float v = __ldcg(g.out + (size_t)m * g.ldo + n);
+      if (g.logits) g.logits[(size_t)m * g.logits_ld + n] = v;
+      a.add(v, n, lab, ce);
+    }
+    a.warp_merge(ce);
+    if (lane == 0) a.write(g, m, ct);
+  }
+}
 
 // Work of one persistent CTA, as segments (tile, k-tiles [kb, ke)).
 //   stream-K: the tiles x ktiles (tile, k-tile) units are cut into gridDim
@@ -417,39 +507,59 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       } else {
         // lane = row m: transpose 32 x 32 blocks through shared memory, then
-        // each warp store writes 4 rows x 128 contiguous bytes
+        // each warp store writes 4 rows x 128 contiguous bytes. A fused head
+        // epilogue on an unsplit tile reduces the row straight from TMEM and
+        // stores fp32 only if the caller asked for logits.
         float* stg = staging + (warp - 2) * 32 * C::STG_LD;
         const int m0 = ta * 128 + quad * 32;
+        const bool fuse = g.op != EPI_STORE && sg.nslab == 1;
+        float* tgt = fuse ? g.logits : slab;
+        const int ldt = fuse ? g.logits_ld : g.ldo;
+        const bool ce = g.op == EPI_CE;
+        const int my_m = m0 + lane;
+        const int lab = (fuse && ce && g.labels && my_m < g.M) ? g.labels[my_m] : -1;
+        HeadAcc acc;
+        acc.init();
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r[16];
           tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) stg[lane * C::STG_LD + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 16; ++c) {
+            stg[lane * C::STG_LD + c] = __uint_as_float(r[c]);
+            if (fuse && tb * BN + c0 + c < g.N) acc.add(__uint_as_float(r[c]), tb * BN + c0 + c, lab, ce);
+          }
           tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + 16, r);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) stg[lane * C::STG_LD + 16 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 16; ++c) {
+            stg[lane * C::STG_LD + 16 + c] = __uint_as_float(r[c]);
+            if (fuse && tb * BN + c0 + 16 + c < g.N)
+              acc.add(__uint_as_float(r[c]), tb * BN + c0 + 16 + c, lab, ce);
+          }
           __syncwarp();
-          const int cc = (lane & 7) * 4;
-          const int n = tb * BN + c0 + cc;
+          if (tgt) {
+            const int cc = (lane & 7) * 4;
+            const int n = tb * BN + c0 + cc;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + (lane >> 3);
-            const int m = m0 + rr;
-            if (m < g.M) {
-              const float* srow = stg + rr * C::STG_LD + cc;
-              float* dst = slab + (size_t)m * g.ldo + n;
-              if (n + 4 <= g.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
-                *reinterpret_cast<float4*>(dst) = make_float4(srow[0], srow[1], srow[2], srow[3]);
-              } else {
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + (lane >> 3);
+              const int m = m0 + rr;
+              if (m < g.M) {
+                const float* srow = stg + rr * C::STG_LD + cc;
+                float* dst = tgt + (size_t)m * ldt + n;
+                if (n + 4 <= g.N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+                  *reinterpret_cast<float4*>(dst) = make_float4(srow[0], srow[1], srow[2], srow[3]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  if (n + c < g.N) dst[c] = srow[c];
+                  for (int c = 0; c < 4; ++c)
+                    if (n + c < g.N) dst[c] = srow[c];
+                }
               }
             }
           }
           __syncwarp();
         }
+        if (fuse && my_m < g.M) acc.write(g, my_m, tb);
       }
       tc::fence_before();
       __syncwarp();
@@ -503,6 +613,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
           }
           if (warp == 2 && lane == 0) g.sem[tile] = 0;
+        }
+      }
+      if (g.op != EPI_STORE && (SWAP || sg.nslab > 1)) {
+        // head statistics of a finished tile, from slab 0: by the only CTA
+        // of an unsplit tile, or by the CTA that summed the slabs
+        const bool fin = (sg.nslab == 1) || *s_last;
+        if (fin) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (SWAP)
+            head_finish_rows(g, warp - 2, g.M, 4, ta * 128, min(128, g.N - ta * 128), ta, lane);
+          else
+            head_finish_rows(g, ta * 128 + quad * 32, min(g.M, ta * 128 + quad * 32 + 32), 1, tb * BN,
+                             min(BN, g.N - tb * BN), tb, lane);
         }
       }
     }
@@ -685,8 +808,19 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const T
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+int gemm_col_tiles(int M, int N, int K) {
+  const Plan p = plan_gemm(M, N, K);
+  return p.swap ? (N + 127) / 128 : (N + p.bn - 1) / p.bn;
+}
+
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
                         GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s) {
+  return gemm_launch_epi(dtype, X, ldx, W, M, N, K, out, o, sem, dev_status, probe_op, nullptr, s);
+}
+
+cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
+                            GemmOut* o, int* sem, int* dev_status, int probe_op, const GemmEpi* epi,
+                            cudaStream_t s) {
   if (M <= 0 || N <= 0) {
     if (o) *o = GemmOut{out, N, 1, 0};
     return cudaSuccess;
@@ -713,6 +847,18 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
   args.N = N;
   args.sem = sem;
   args.status = dev_status;
+  args.op = EPI_STORE;
+  if (epi) {
+    args.op = epi->op;
+    args.part_ld = p.swap ? (N + 127) / 128 : (N + p.bn - 1) / p.bn;
+    args.logits = epi->logits;
+    args.logits_ld = epi->logits_ld;
+    args.p_max = epi->p_max;
+    args.p_sum = epi->p_sum;
+    args.p_lab = epi->p_lab;
+    args.p_idx = epi->p_idx;
+    args.labels = epi->labels;
+  }
   CUtensorMap ma, mb;
   bool ok;
   if (p.swap) {

@@ -373,6 +373,45 @@ __global__ void ce_rows_kernel(GemmOut in, int V, int row0, const int* row_label
   }
 }
 
+// Row cross-entropy and argmax from the fused head epilogue's per-tile
+// partials: logsumexp = M + log(sum_t s_t exp(m_t - M)); the label's logit
+// comes from the one tile that holds it. A warp per row.
+__global__ void ce_merge_kernel(int rows, int part_ld, int row0, const float* p_max, const float* p_sum,
+                                const float* p_lab, const int* p_idx, const int* row_label, float* row_ce,
+                                int* row_am) {
+  pdl_trigger();
+  const int rl = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (rl >= rows) return;
+  const size_t base = (size_t)rl * part_ld;
+  float M = -INFINITY, ll = -INFINITY, bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int t = lane; t < part_ld; t += 32) {
+    const float mt = p_max[base + t];
+    M = fmaxf(M, mt);
+    ll = fmaxf(ll, p_lab[base + t]);
+    if (am_better(mt, p_idx[base + t], bv, bi)) {
+      bv = mt;
+      bi = p_idx[base + t];
+    }
+  }
+  M = warp_max(M);
+  ll = warp_max(ll);
+  warp_argmax(bv, bi);
+  float sum = 0.f;
+  for (int t = lane; t < part_ld; t += 32) {
+    const float mt = p_max[base + t];
+    if (mt != -INFINITY) sum += p_sum[base + t] * expf(mt - M);
+  }
+  sum = warp_sum(sum);
+  if (lane == 0) {
+    const int r = row0 + rl;
+    const int lab = row_label[r];
+    row_ce[r] = lab >= 0 ? (M + logf(sum)) - ll : __int_as_float(0x7fc00000);
+    row_am[r] = bi;
+  }
+}
+
 // Per-depth means and the decay-weighted total (#2376, Changelog: 0.8**d
 // weighted-mean schedule). One block; fixed summation order.
 __global__ void ce_reduce_kernel(CeReduceArgs a) {
@@ -687,6 +726,22 @@ cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const i
                            float* logits_out, float* row_ce, int* row_am, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   ce_rows_kernel<<<rows, 256, 0, st>>>(in, V, row0, row_label, logits_out, row_ce, row_am);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_ce_merge(int rows, int part_ld, int row0, const float* p_max, const float* p_sum,
+                            const float* p_lab, const int* p_idx, const int* row_label, float* row_ce, int* row_am,
+                            cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  ce_merge_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, part_ld, row0, p_max, p_sum, p_lab, p_idx, row_label, row_ce,
+                                                  row_am);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, const int* pidx, const int* d2t,
+                                   int* tokens, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  lm_argmax_final_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, nchunks, pval, pidx, d2t, tokens);
   PE_LAUNCH_END();
 }
 

@@ -120,6 +120,11 @@ cudaError_t launch_lm_argmax(const GemmOut& in, int rows, int V, float* logits, 
 cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const int* row_label,
                            float* logits_out, float* row_ce, int* row_am, cudaStream_t st);
 cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st);
+cudaError_t launch_ce_merge(int rows, int part_ld, int row0, const float* p_max, const float* p_sum,
+                            const float* p_lab, const int* p_idx, const int* row_label, float* row_ce, int* row_am,
+                            cudaStream_t st);
+cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, const int* pidx, const int* d2t,
+                                   int* tokens, cudaStream_t st);
 cudaError_t launch_train_meta(const TrainMetaArgs& a, cudaStream_t st);
 cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, int* next, cudaStream_t st);
 cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st);
