@@ -195,6 +195,44 @@ struct HeadAcc {
       if (n == lab) ll = v;
     }
   }
+  // 32 consecutive columns at once: independent max / exp / compare steps
+  // instead of a dependent chain per element (NaN falls back to add()).
+  __device__ __forceinline__ void add_chunk(const float (&v)[32], int n0, int nvalid, int lab, bool ce) {
+    bool nan = false;
+    float cm = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float x = c < nvalid ? v[c] : -INFINITY;
+      nan |= (x != x);
+      cm = fmaxf(cm, x);
+    }
+    if (nan) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) add(v[c], n0 + c, lab, ce);
+      return;
+    }
+    int ci = 0x7fffffff;
+#pragma unroll
+    for (int c = 31; c >= 0; --c)
+      if (c < nvalid && v[c] == cm) ci = n0 + c;
+    if (am_better(cm, ci, bv, bi)) {
+      bv = cm;
+      bi = ci;
+    }
+    if (ce && cm != -INFINITY) {
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sum += (c < nvalid) ? __expf(v[c] - cm) : 0.f;
+      const float nm = fmaxf(mx, cm);
+      se = (mx == -INFINITY ? 0.f : se * __expf(mx - nm)) + sum * __expf(cm - nm);
+      mx = nm;
+      const int off = lab - n0;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c == off && c < nvalid) ll = v[c];
+    }
+  }
   __device__ __forceinline__ void warp_merge(bool ce) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -523,18 +561,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r[16];
+          float v[32];
           tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            stg[lane * C::STG_LD + c] = __uint_as_float(r[c]);
-            if (fuse && tb * BN + c0 + c < g.N) acc.add(__uint_as_float(r[c]), tb * BN + c0 + c, lab, ce);
-          }
+          for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
           tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + 16, r);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            stg[lane * C::STG_LD + 16 + c] = __uint_as_float(r[c]);
-            if (fuse && tb * BN + c0 + 16 + c < g.N)
-              acc.add(__uint_as_float(r[c]), tb * BN + c0 + 16 + c, lab, ce);
+          for (int c = 0; c < 16; ++c) v[16 + c] = __uint_as_float(r[c]);
+          if (fuse) acc.add_chunk(v, tb * BN + c0, min(32, g.N - (tb * BN + c0)), lab, ce);
+          if (tgt) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) stg[lane * C::STG_LD + c] = v[c];
           }
           __syncwarp();
           if (tgt) {
