@@ -327,6 +327,24 @@ peagle_status peagle_clear_device_status(const peagle_model* m, void* stream) {
   return PEAGLE_OK;
 }
 
+// gate/up projection and SwiGLU over rows of width K: bf16 with 2I % 256 == 0
+// writes silu(gate) * up straight from the GEMM epilogue; otherwise the fp32
+// result goes through the SwiGLU row kernel.
+static cudaError_t gate_up_swiglu(int dt, const void* X, int K, const void* W, int rows, int I, float* part,
+                                  void* act, int* sem, int* status, cudaStream_t s) {
+  GemmOut go;
+  if (dt == PEAGLE_BF16 && (2 * I) % 256 == 0) {
+    GemmEpi ep{};
+    ep.op = GEMM_EPI_SWIGLU;
+    ep.act = act;
+    ep.act_ld = I;
+    return gemm_launch_epi(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, &ep, s);
+  }
+  cudaError_t e = gemm_launch(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, s);
+  if (e != cudaSuccess) return e;
+  return launch_swiglu(dt, go, rows, I, act, s);
+}
+
 // =============================================================== draft step
 struct DraftWs {
   int* sem;
@@ -507,8 +525,7 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ra.y = ws.xin;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
 
-    CUDA_TRY(gemm_launch(dt, ws.xin, H, W.gate_up_w, rows, 2 * I, H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_GATE_UP, s));
-    CUDA_TRY(launch_swiglu(dt, go, rows, I, ws.act, s));
+    CUDA_TRY(gate_up_swiglu(dt, ws.xin, H, W.gate_up_w, rows, I, ws.part, ws.act, ws.sem, m->status, s));
     CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, ws.sem, m->status, PEAGLE_OP_DOWN, s));
     ra.in = go;
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
@@ -897,9 +914,8 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
         ra.eps = eps;
         ra.y = ws.xin;
         CUDA_TRY(launch_resid_norm(dt, mr, ra, s));
-        CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.gate_up_w, mr, 2 * I, H, ws.part, &go, ws.sem, m->status,
-                             PEAGLE_OP_GATE_UP, s));
-        CUDA_TRY(launch_swiglu(dt, go, mr, I, ws.act, s));
+        CUDA_TRY(gate_up_swiglu(dt, atc(ws.xin, (size_t)c0 * H), H, W.gate_up_w, mr, I, ws.part, ws.act, ws.sem,
+                                m->status, s));
         CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, mr, H, I, ws.part, &go, ws.sem, m->status, PEAGLE_OP_DOWN, s));
         ra.in = go;
         ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;

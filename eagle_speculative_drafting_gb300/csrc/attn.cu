@@ -41,6 +41,7 @@ __device__ __forceinline__ void online_add(float s, const float (&v)[E], float& 
 template <typename T, int E>
 __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
   pdl_trigger();
+  pdl_wait();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
 template <typename T, int E>
 __global__ void decode_combine(DecodeAttnArgs a) {
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int b = r / a.K, d = r % a.K;
   const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
@@ -189,6 +191,7 @@ struct MmaAttnCfg {
 template <int MT, int HD>
 __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
   pdl_trigger();
+  pdl_wait();
   using C = MmaAttnCfg<MT, HD>;
   constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP;
   constexpr int DW = HD / 4;          // head dims per warp in the PV product
@@ -392,7 +395,7 @@ static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  decode_split_mma<MT, HD><<<dim3(a.nsplit, a.nkv, a.B), 128, C::SMEM, st>>>(a);
+  launch_pdl(decode_split_mma<MT, HD>, dim3(a.nsplit, a.nkv, a.B), 128, C::SMEM, st, a);
   return cudaGetLastError();
 }
 
@@ -424,11 +427,11 @@ static cudaError_t decode_attn_t(const DecodeAttnArgs& a, int probe_op, cudaStre
     cudaError_t e = (E == 4) ? split_mma_hd<128>(a, st) : split_mma_hd<64>(a, st);
     if (e != cudaSuccess) return e;
   } else {
-    decode_split_simt<T, E><<<grid, 256, 0, st>>>(a);
+    launch_pdl(decode_split_simt<T, E>, grid, 256, 0, st, a);
   }
   note_launch();
   probe_stop(probe_op, st);
-  decode_combine<T, E><<<dim3(a.B * a.K, (a.nq + 3) / 4), 128, 0, st>>>(a);
+  launch_pdl(decode_combine<T, E>, dim3(a.B * a.K, (a.nq + 3) / 4), 128, 0, st, a);
   note_launch();
   return cudaGetLastError();
 }
@@ -445,6 +448,7 @@ cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op,
 template <typename T, int E>
 __global__ void __launch_bounds__(128) train_attn_simt(TrainAttnArgs a) {
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int G = a.nq / a.nkv, hd = a.hd;
@@ -508,6 +512,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int HD>
 __global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTileArgs tt) {
   pdl_trigger();
+  pdl_wait();
   using C = TrainMmaCfg<HD>;
   constexpr int TQ = C::TQ, TK = C::TK, LDS = C::LDS, NTO = HD / 8;
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -693,7 +698,7 @@ static cudaError_t launch_train_mma(const TrainAttnArgs& a, const TrainTileArgs&
     attr = true;
   }
   probe_start(probe_op, st);
-  train_attn_mma<HD><<<dim3(tt.tile_off[tt.K], a.nq), 128, C::SMEM, st>>>(a, tt);
+  launch_pdl(train_attn_mma<HD>, dim3(tt.tile_off[tt.K], a.nq), 128, C::SMEM, st, a, tt);
   note_launch();
   probe_stop(probe_op, st);
   return cudaGetLastError();
@@ -703,7 +708,7 @@ template <typename T, int E>
 static cudaError_t train_attn_t(const TrainAttnArgs& a, int probe_op, cudaStream_t st) {
   dim3 grid(a.R, (a.nq + 3) / 4);
   probe_start(probe_op, st);
-  train_attn_simt<T, E><<<grid, 128, 0, st>>>(a);
+  launch_pdl(train_attn_simt<T, E>, grid, 128, 0, st, a);
   note_launch();
   probe_stop(probe_op, st);
   return cudaGetLastError();

@@ -64,14 +64,33 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may start before its predecessor finishes; it must wait
-// before touching anything the predecessor writes or reads. Every kernel of
-// the library lets its dependents launch as soon as it starts.
+// Programmatic dependent launch: every kernel of the library is launched
+// with programmatic stream serialization, lets its dependents launch as soon
+// as it starts (pdl_trigger), and waits for its predecessor to complete and
+// flush (pdl_wait) before it reads or writes anything the predecessor
+// touches. Without the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- host side
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor finishes, and waits (pdl_wait) before touching its data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 void note_launch();                       // counts one kernel launch
 void set_error(const char* fmt, ...);     // records peagle_last_error()
 void probe_start(int op, cudaStream_t s); // timing probe around main kernels
@@ -105,9 +124,14 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
 // fp32 result, per (row, column tile) partials of the row's argmax (value,
 // lowest index) and, for cross-entropy, the max, the sum of exp(x - max) and
 // the label's logit (-inf when the label is in another tile).
-enum { GEMM_EPI_ARGMAX = 1, GEMM_EPI_CE = 2 };
+// GEMM_EPI_SWIGLU: W is a [2I, K] gate/up weight (gate rows first); the
+// result silu(gate) * up [M, I] is written as bf16 to act (row stride
+// act_ld). Needs 2I % 256 == 0.
+enum { GEMM_EPI_ARGMAX = 1, GEMM_EPI_CE = 2, GEMM_EPI_SWIGLU = 3 };
 struct GemmEpi {
   int op;
+  void* act;
+  int act_ld;
   float* logits;        // optional fp32 copy of D [M, logits_ld]
   int logits_ld;
   float *p_max, *p_sum, *p_lab;   // [M, gemm_col_tiles]

@@ -145,7 +145,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 // =========================================================================
 // The tcgen05 kernel
 // =========================================================================
-enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_CE = 2 };
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_CE = 2, EPI_SWIGLU = 3 };
 
 struct TcArgs {
   int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
@@ -165,6 +165,11 @@ struct TcArgs {
   float *p_max, *p_sum, *p_lab;
   int* p_idx;
   const int* labels;       // EPI_CE: draft-vocab label per GEMM row, -1 = none
+  // EPI_SWIGLU: each weight tile pairs gate rows with the matching up rows
+  // (rows gate_off + ...); the epilogue writes silu(gate) * up as bf16
+  int gate_off;
+  void* act;
+  int act_ld;
 };
 
 // Running head statistics of one row over some columns: argmax (lowest
@@ -366,6 +371,20 @@ struct TcCfg {
   static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
 };
 
+// silu(gate) * up of finished rows read back from slab 0, where a tile's
+// columns [src0, src0 + half) are gate and [src0 + half, src0 + 2 half) up.
+__device__ void swiglu_finish_rows(const TcArgs& g, int m_begin, int m_end, int m_step, int src0, int half,
+                                   int dst0, int lane) {
+  bf16* act = static_cast<bf16*>(g.act);
+  for (int m = m_begin; m < m_end; m += m_step) {
+    for (int j = lane; j < half; j += 32) {
+      const float gt = __ldcg(g.out + (size_t)m * g.ldo + src0 + j);
+      const float up = __ldcg(g.out + (size_t)m * g.ldo + src0 + half + j);
+      act[(size_t)m * g.act_ld + dst0 + j] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
+    }
+  }
+}
+
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -404,6 +423,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
+  pdl_trigger();   // the next kernel may launch now and wait for this one
 
   const int tilesA = (g.rowsA + 127) / 128;
   const int tilesB = (g.rowsB + BN - 1) / BN;
@@ -416,6 +436,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // weight rows of tile t (row block of the weight operand) into one
+      // sub-box; a gated tile takes its first half from the gate rows and its
+      // second half from the matching up rows
+      auto load_w = [&](uint8_t* dst, int x, int t, uint64_t* bar) {
+        if (SWAP) {
+          if (g.gate_off) {
+            tc::tma_load_2d(dst, &tmA, x, t * 64, bar);
+            tc::tma_load_2d(dst + 64 * 128, &tmA, x, g.gate_off + t * 64, bar);
+          } else {
+            tc::tma_load_2d(dst, &tmA, x, t * 128, bar);
+          }
+        } else {
+          if (g.gate_off) {
+            tc::tma_load_2d(dst, &tmB, x, t * (BN / 2), bar);
+            tc::tma_load_2d(dst + (BN / 2) * 128, &tmB, x, g.gate_off + t * (BN / 2), bar);
+          } else {
+            tc::tma_load_2d(dst, &tmB, x, t * BN, bar);
+          }
+        }
+      };
       int it = 0, pre = 0;
       bool waited = false;
       while (!*abort_flag && sc.next(sg)) {
@@ -429,8 +469,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int k = kb + q, nv = nsub(k);
             tc::mbar_expect_tx(&full[q], nv * (C::A_SUB + C::B_SUB));
             for (int i = 0; i < nv; ++i) {
-              if (SWAP) tc::tma_load_2d(sA + q * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[q]);
-              else tc::tma_load_2d(sB + q * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[q]);
+              if (SWAP) load_w(sA + q * C::A_BYTES + i * C::A_SUB, k * C::KT + i * 64, ta, &full[q]);
+              else load_w(sB + q * C::B_BYTES + i * C::B_SUB, k * C::KT + i * 64, tb, &full[q]);
             }
           }
           pdl_wait();
@@ -454,8 +494,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           tc::mbar_expect_tx(&full[s], nv * (C::A_SUB + C::B_SUB));
           for (int i = 0; i < nv; ++i) {
-            tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
-            tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
+            if (SWAP) {
+              load_w(sA + s * C::A_BYTES + i * C::A_SUB, k * C::KT + i * 64, ta, &full[s]);
+              tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
+            } else {
+              tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
+              load_w(sB + s * C::B_BYTES + i * C::B_SUB, k * C::KT + i * 64, tb, &full[s]);
+            }
           }
         }
       }
@@ -550,7 +595,54 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // stores fp32 only if the caller asked for logits.
         float* stg = staging + (warp - 2) * 32 * C::STG_LD;
         const int m0 = ta * 128 + quad * 32;
-        const bool fuse = g.op != EPI_STORE && sg.nslab == 1;
+        const bool head = g.op == EPI_ARGMAX || g.op == EPI_CE;
+        if (g.op == EPI_SWIGLU && sg.nslab == 1) {
+          // columns c and BN/2 + c are gate and up of output column
+          // tb * BN/2 + c: write silu(gate) * up as bf16, coalesced
+          constexpr int HALF = BN / 2;
+          bf16* act = static_cast<bf16*>(g.act);
+          const int I = g.N / 2;
+#pragma unroll 1
+          for (int c0 = 0; c0 < HALF; c0 += 32) {
+#pragma unroll
+            for (int h16 = 0; h16 < 32; h16 += 16) {
+              uint32_t rg[16], ru[16];
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + h16, rg);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + HALF + c0 + h16, ru);
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const float gt = __uint_as_float(rg[c]);
+                stg[lane * C::STG_LD + h16 + c] = gt / (1.f + __expf(-gt)) * __uint_as_float(ru[c]);
+              }
+            }
+            __syncwarp();
+            const int cc = (lane & 7) * 4;
+            const int n = tb * HALF + c0 + cc;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + (lane >> 3);
+              const int m = m0 + rr;
+              if (m < g.M) {
+                const float* srow = stg + rr * C::STG_LD + cc;
+                bf16* dst = act + (size_t)m * g.act_ld + n;
+                if (n + 4 <= I && ((reinterpret_cast<uintptr_t>(dst) & 7) == 0)) {
+                  __nv_bfloat162 lo = __floats2bfloat162_rn(srow[0], srow[1]);
+                  __nv_bfloat162 hi = __floats2bfloat162_rn(srow[2], srow[3]);
+                  uint2 pk;
+                  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+                  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+                  *reinterpret_cast<uint2*>(dst) = pk;
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c)
+                    if (n + c < I) dst[c] = __float2bfloat16_rn(srow[c]);
+                }
+              }
+            }
+            __syncwarp();
+          }
+        } else {
+        const bool fuse = head && sg.nslab == 1;
         float* tgt = fuse ? g.logits : slab;
         const int ldt = fuse ? g.logits_ld : g.ldo;
         const bool ce = g.op == EPI_CE;
@@ -597,6 +689,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           __syncwarp();
         }
         if (fuse && my_m < g.M) acc.write(g, my_m, tb);
+        }
       }
       tc::fence_before();
       __syncwarp();
@@ -652,7 +745,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (warp == 2 && lane == 0) g.sem[tile] = 0;
         }
       }
-      if (g.op != EPI_STORE && (SWAP || sg.nslab > 1)) {
+      if (g.op == EPI_SWIGLU && (SWAP || sg.nslab > 1)) {
+        // silu(gate) * up of a finished tile, from slab 0
+        const bool fin = (sg.nslab == 1) || *s_last;
+        if (fin) {
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (SWAP)
+            swiglu_finish_rows(g, warp - 2, g.M, 4, ta * 128, 64, ta * 64, lane);
+          else
+            swiglu_finish_rows(g, ta * 128 + quad * 32, min(g.M, ta * 128 + quad * 32 + 32), 1, tb * BN, BN / 2,
+                               tb * (BN / 2), lane);
+        }
+      }
+      if ((g.op == EPI_ARGMAX || g.op == EPI_CE) && (SWAP || sg.nslab > 1)) {
         // head statistics of a finished tile, from slab 0: by the only CTA
         // of an unsplit tile, or by the CTA that summed the slabs
         const bool fin = (sg.nslab == 1) || *s_last;
@@ -885,7 +990,17 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.sem = sem;
   args.status = dev_status;
   args.op = EPI_STORE;
-  if (epi) {
+  args.gate_off = 0;
+  if (epi && epi->op == GEMM_EPI_SWIGLU) {
+    if (N % 256 != 0) {
+      set_error("fused SwiGLU needs the gate/up width %d to be a multiple of 256", N);
+      return cudaErrorInvalidValue;
+    }
+    args.op = EPI_SWIGLU;
+    args.gate_off = N / 2;
+    args.act = epi->act;
+    args.act_ld = epi->act_ld;
+  } else if (epi) {
     args.op = epi->op;
     args.part_ld = p.swap ? (N + 127) / 128 : (N + p.bn - 1) / p.bn;
     args.logits = epi->logits;
@@ -898,14 +1013,16 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   }
   CUtensorMap ma, mb;
   bool ok;
+  // a gated weight tile is loaded as two half-height boxes
+  const int wdiv = args.gate_off ? 2 : 1;
   if (p.swap) {
     args.rowsA = N;
     args.rowsB = M;
-    ok = make_map(&ma, W, N, K, K, 128) && make_map(&mb, X, M, K, ldx, p.bn);
+    ok = make_map(&ma, W, N, K, K, 128 / wdiv) && make_map(&mb, X, M, K, ldx, p.bn);
   } else {
     args.rowsA = M;
     args.rowsB = N;
-    ok = make_map(&ma, X, M, K, ldx, 128) && make_map(&mb, W, N, K, K, p.bn);
+    ok = make_map(&ma, X, M, K, ldx, 128) && make_map(&mb, W, N, K, K, p.bn / wdiv);
   }
   if (!ok) {
     set_error("cuTensorMapEncodeTiled failed (M=%d N=%d K=%d)", M, N, K);

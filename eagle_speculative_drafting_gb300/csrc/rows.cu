@@ -23,6 +23,7 @@ __device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
 // -------------------------------------------------------------------------
 __global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int half, int hd, double theta) {
   pdl_trigger();
+  pdl_wait();
   const long long total = (long long)max_pos * half;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -45,6 +46,7 @@ __global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int hal
 template <typename T>
 __global__ void fc_finish_kernel(FcFinishArgs a) {
   pdl_trigger();
+  pdl_wait();
   extern __shared__ float sh[];
   __shared__ float red[33];
   const int r = blockIdx.x, H = a.H;
@@ -108,6 +110,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
 template <typename T>
 __global__ void qkv_finish_kernel(QkvArgs a) {
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x + a.row0;
   const int half = a.hd / 2;
   int src;
@@ -193,6 +196,7 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
 template <typename T>
 __global__ void resid_norm_kernel(ResidNormArgs a) {
   pdl_trigger();
+  pdl_wait();
   extern __shared__ float sh[];
   __shared__ float red[33];
   const int rl = blockIdx.x;           // row within the chunk
@@ -220,6 +224,7 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
 template <typename T>
 __global__ void swiglu_kernel(GemmOut in, int rows, int I, void* act_) {
   pdl_trigger();
+  pdl_wait();
   T* act = static_cast<T*>(act_);
   const long long total = (long long)rows * I;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -250,6 +255,7 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 __global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* logits, float* pval,
                                          int* pidx) {
   pdl_trigger();
+  pdl_wait();
   __shared__ float sv[32];
   __shared__ int si[32];
   const int r = blockIdx.y, c = blockIdx.x, nchunks = gridDim.x;
@@ -287,6 +293,7 @@ __global__ void lm_argmax_partial_kernel(GemmOut in, int V, int chunk, float* lo
 __global__ void lm_argmax_final_kernel(int rows, int nchunks, const float* pval, const int* pidx,
                                        const int* d2t, int* tokens) {
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -312,6 +319,7 @@ __global__ void lm_argmax_final_kernel(int rows, int nchunks, const float* pval,
 __global__ void ce_rows_kernel(GemmOut in, int V, int row0, const int* row_label, float* logits_out,
                                float* row_ce, int* row_am) {
   pdl_trigger();
+  pdl_wait();
   __shared__ float sm[32], ss[32], sv[32];
   __shared__ int si[32];
   const int rl = blockIdx.x, r = row0 + rl;
@@ -380,6 +388,7 @@ __global__ void ce_merge_kernel(int rows, int part_ld, int row0, const float* p_
                                 const float* p_lab, const int* p_idx, const int* row_label, float* row_ce,
                                 int* row_am) {
   pdl_trigger();
+  pdl_wait();
   const int rl = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (rl >= rows) return;
@@ -416,6 +425,7 @@ __global__ void ce_merge_kernel(int rows, int part_ld, int row0, const float* p_
 // weighted-mean schedule). One block; fixed summation order.
 __global__ void ce_reduce_kernel(CeReduceArgs a) {
   pdl_trigger();
+  pdl_wait();
   __shared__ double red_d[32];
   __shared__ int red_i[32], red_j[32];
   __shared__ double loss_acc;
@@ -472,6 +482,7 @@ __global__ void ce_reduce_kernel(CeReduceArgs a) {
 // -------------------------------------------------------------------------
 __global__ void train_meta_kernel(TrainMetaArgs a) {
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     bool ok = a.cu[0] == 0 && a.cu[a.S] == a.n;
@@ -524,6 +535,7 @@ __global__ void train_meta_kernel(TrainMetaArgs a) {
 // -------------------------------------------------------------------------
 __global__ void verify_kernel(int B, int K, const int* draft, const int* target, int* acc, int* next) {
   pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int* d = draft + (size_t)b * K;
@@ -550,6 +562,7 @@ __device__ __forceinline__ uint64_t splitmix64_out(uint64_t seed, uint64_t i) {
 
 __global__ void __launch_bounds__(1024) cod_select_kernel(CodArgs a) {
   pdl_trigger();
+  pdl_wait();
   __shared__ unsigned hist[16][256];
   __shared__ uint64_t prefix[16], maskv[16], thr[16];
   __shared__ int rank_left[16], wsum[32], base[16];
@@ -636,6 +649,7 @@ __global__ void __launch_bounds__(1024) cod_select_kernel(CodArgs a) {
 // D = sum of the partial slabs (the plain GEMM entry point).
 __global__ void sum_splits_kernel(GemmOut in, int M, int N, float* D) {
   pdl_trigger();
+  pdl_wait();
   const long long total = (long long)M * N;
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
        e += (long long)gridDim.x * blockDim.x) {
@@ -671,7 +685,7 @@ static int row_threads(int rows, int H) {
 
 cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double theta, cudaStream_t st) {
   const long long total = (long long)max_pos * (hd / 2);
-  rope_table_kernel<<<grid_for(total, 256), 256, 0, st>>>(c, s, max_pos, hd / 2, hd, theta);
+  launch_pdl(rope_table_kernel, grid_for(total, 256), 256, 0, st, c, s, max_pos, hd / 2, hd, theta);
   PE_LAUNCH_END();
 }
 
@@ -679,8 +693,8 @@ cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStr
   if (rows <= 0) return cudaSuccess;
   const size_t sm = (size_t)a.H * sizeof(float);
   const int threads = row_threads(rows, a.H);
-  if (dtype == PEAGLE_BF16) fc_finish_kernel<bf16><<<rows, threads, sm, st>>>(a);
-  else fc_finish_kernel<float><<<rows, threads, sm, st>>>(a);
+  if (dtype == PEAGLE_BF16) launch_pdl(fc_finish_kernel<bf16>, rows, threads, sm, st, a);
+  else launch_pdl(fc_finish_kernel<float>, rows, threads, sm, st, a);
   PE_LAUNCH_END();
 }
 
@@ -688,8 +702,8 @@ cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_
   if (rows <= 0) return cudaSuccess;
   const int total = (a.nq + a.nkv) * (a.hd / 2) + a.nkv * a.hd + (a.h ? a.H : 0);
   const dim3 grid(rows, (total + kQkvChunk - 1) / kQkvChunk);
-  if (dtype == PEAGLE_BF16) qkv_finish_kernel<bf16><<<grid, 256, 0, st>>>(a);
-  else qkv_finish_kernel<float><<<grid, 256, 0, st>>>(a);
+  if (dtype == PEAGLE_BF16) launch_pdl(qkv_finish_kernel<bf16>, grid, 256, 0, st, a);
+  else launch_pdl(qkv_finish_kernel<float>, grid, 256, 0, st, a);
   PE_LAUNCH_END();
 }
 
@@ -697,16 +711,16 @@ cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaS
   if (rows <= 0) return cudaSuccess;
   const size_t sm = (size_t)a.H * sizeof(float);
   const int threads = row_threads(rows, a.H);
-  if (dtype == PEAGLE_BF16) resid_norm_kernel<bf16><<<rows, threads, sm, st>>>(a);
-  else resid_norm_kernel<float><<<rows, threads, sm, st>>>(a);
+  if (dtype == PEAGLE_BF16) launch_pdl(resid_norm_kernel<bf16>, rows, threads, sm, st, a);
+  else launch_pdl(resid_norm_kernel<float>, rows, threads, sm, st, a);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_swiglu(int dtype, const GemmOut& in, int rows, int I, void* act, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const long long total = (long long)rows * I;
-  if (dtype == PEAGLE_BF16) swiglu_kernel<bf16><<<grid_for(total, 256), 256, 0, st>>>(in, rows, I, act);
-  else swiglu_kernel<float><<<grid_for(total, 256), 256, 0, st>>>(in, rows, I, act);
+  if (dtype == PEAGLE_BF16) launch_pdl(swiglu_kernel<bf16>, grid_for(total, 256), 256, 0, st, in, rows, I, act);
+  else launch_pdl(swiglu_kernel<float>, grid_for(total, 256), 256, 0, st, in, rows, I, act);
   PE_LAUNCH_END();
 }
 
@@ -716,16 +730,16 @@ cudaError_t launch_lm_argmax(const GemmOut& in, int rows, int V, float* logits, 
                              const int* d2t, int* tokens, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int nch = lm_argmax_chunks(V);
-  lm_argmax_partial_kernel<<<dim3(nch, rows), 256, 0, st>>>(in, V, 2048, logits, pval, pidx);
+  launch_pdl(lm_argmax_partial_kernel, dim3(nch, rows), 256, 0, st, in, V, 2048, logits, pval, pidx);
   note_launch();
-  lm_argmax_final_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, nch, pval, pidx, d2t, tokens);
+  launch_pdl(lm_argmax_final_kernel, (rows + 7) / 8, 256, 0, st, rows, nch, pval, pidx, d2t, tokens);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const int* row_label,
                            float* logits_out, float* row_ce, int* row_am, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  ce_rows_kernel<<<rows, 256, 0, st>>>(in, V, row0, row_label, logits_out, row_ce, row_am);
+  launch_pdl(ce_rows_kernel, rows, 256, 0, st, in, V, row0, row_label, logits_out, row_ce, row_am);
   PE_LAUNCH_END();
 }
 
@@ -733,7 +747,7 @@ cudaError_t launch_ce_merge(int rows, int part_ld, int row0, const float* p_max,
                             const float* p_lab, const int* p_idx, const int* row_label, float* row_ce, int* row_am,
                             cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  ce_merge_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, part_ld, row0, p_max, p_sum, p_lab, p_idx, row_label, row_ce,
+  launch_pdl(ce_merge_kernel, (rows + 7) / 8, 256, 0, st, rows, part_ld, row0, p_max, p_sum, p_lab, p_idx, row_label, row_ce,
                                                   row_am);
   PE_LAUNCH_END();
 }
@@ -741,37 +755,37 @@ cudaError_t launch_ce_merge(int rows, int part_ld, int row0, const float* p_max,
 cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, const int* pidx, const int* d2t,
                                    int* tokens, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  lm_argmax_final_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, nchunks, pval, pidx, d2t, tokens);
+  launch_pdl(lm_argmax_final_kernel, (rows + 7) / 8, 256, 0, st, rows, nchunks, pval, pidx, d2t, tokens);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st) {
-  ce_reduce_kernel<<<1, 1024, 0, st>>>(a);
+  launch_pdl(ce_reduce_kernel, 1, 1024, 0, st, a);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_train_meta(const TrainMetaArgs& a, cudaStream_t st) {
   if (a.R <= 0) return cudaSuccess;
-  train_meta_kernel<<<(a.R + 255) / 256, 256, 0, st>>>(a);
+  launch_pdl(train_meta_kernel, (a.R + 255) / 256, 256, 0, st, a);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, int* next, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  verify_kernel<<<(B + 127) / 128, 128, 0, st>>>(B, K, d, t, acc, next);
+  launch_pdl(verify_kernel, (B + 127) / 128, 128, 0, st, B, K, d, t, acc, next);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st) {
   if (a.n <= 0) return cudaSuccess;
-  cod_select_kernel<<<1, 1024, 0, st>>>(a);
+  launch_pdl(cod_select_kernel, 1, 1024, 0, st, a);
   PE_LAUNCH_END();
 }
 
 cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStream_t st) {
   const long long total = (long long)M * N;
   if (total <= 0) return cudaSuccess;
-  sum_splits_kernel<<<grid_for(total, 256), 256, 0, st>>>(in, M, N, D);
+  launch_pdl(sum_splits_kernel, grid_for(total, 256), 256, 0, st, in, M, N, D);
   PE_LAUNCH_END();
 }
 

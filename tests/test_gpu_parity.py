@@ -162,7 +162,8 @@ def test_decode_tiny_f32():
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(batch=80, K=3), dict(num_layers=1, K=1),
-                                dict(kv_len_range=(0, 0)), dict(batch=1, K=16, kv_len_range=(700, 700))])
+                                dict(kv_len_range=(0, 0)), dict(batch=1, K=16, kv_len_range=(700, 700)),
+                                dict(intermediate=200)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
@@ -267,6 +268,12 @@ def test_train_f32_all_rows_and_loss_mask():
 def test_train_bf16_small():
     wl, inp = small_train(dtype="bf16", n=300, lens=(120, 7, 100, 73), K=5)
     check_train(wl, inp, 5, 0.7, 0.2, 99, BF16_TOL)
+
+
+def test_train_bf16_unfused_swiglu_width():
+    # 2I not a multiple of 256: the SwiGLU runs as its own kernel
+    wl, inp = small_train(dtype="bf16", n=300, lens=(120, 180), K=3, intermediate=200)
+    check_train(wl, inp, 3, 0.7, 0.2, 4, BF16_TOL)
 
 
 def test_train_bf16_multi_chunk_rows():
