@@ -69,6 +69,7 @@ struct peagle_model {
   float* mask_qkv0 = nullptr;   // [QKV] pre-rotary q/k/v of a masked layer-0 row
   float* mask_resid0 = nullptr; // [H] its layer-0 residual
   int* status = nullptr;
+  int* sem = nullptr;           // [kGemmSemCount] draft-step arrival counters, zero between launches
 };
 
 #define FAIL(code, ...)      \
@@ -236,6 +237,7 @@ peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights
       cudaFree(m->mask_qkv0);
       cudaFree(m->mask_resid0);
       cudaFree(m->status);
+      cudaFree(m->sem);
       delete m;
     }
     return code;
@@ -254,6 +256,8 @@ peagle_status peagle_model_create(const peagle_config* cfg, const peagle_weights
   CREATE_TRY(cudaMalloc(&m->mask_resid0, (size_t)H * sizeof(float)));
   CREATE_TRY(cudaMalloc(&m->status, sizeof(int)));
   CREATE_TRY(cudaMemsetAsync(m->status, 0, sizeof(int), s));
+  CREATE_TRY(cudaMalloc(&m->sem, kGemmSemCount * sizeof(int)));
+  CREATE_TRY(cudaMemsetAsync(m->sem, 0, kGemmSemCount * sizeof(int), s));
   CREATE_TRY(launch_rope_table(m->rcos, m->rsin, c.max_position, c.head_dim, c.rope_theta, s));
 
   // masked-row constants: fc_norm(fc(mask_hidden)), the ptd embedding, and
@@ -307,6 +311,7 @@ peagle_status peagle_model_destroy(peagle_model* m) {
   cudaFree(m->mask_qkv0);
   cudaFree(m->mask_resid0);
   cudaFree(m->status);
+  cudaFree(m->sem);
   delete m;
   return PEAGLE_OK;
 }
@@ -324,30 +329,35 @@ peagle_status peagle_get_device_status(const peagle_model* m, void* stream, int3
 peagle_status peagle_clear_device_status(const peagle_model* m, void* stream) {
   if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "clear_device_status: NULL model");
   CUDA_TRY(cudaMemsetAsync(m->status, 0, sizeof(int), static_cast<cudaStream_t>(stream)));
+  CUDA_TRY(cudaMemsetAsync(m->sem, 0, kGemmSemCount * sizeof(int), static_cast<cudaStream_t>(stream)));
   return PEAGLE_OK;
 }
 
 // gate/up projection and SwiGLU over rows of width K: bf16 with 2I % 256 == 0
 // writes silu(gate) * up straight from the GEMM epilogue; otherwise the fp32
 // result goes through the SwiGLU row kernel.
+// Weight bytes each decode contraction pulls into L2 for the next one: about
+// what HBM streams in the gap between two contractions, and half of L2.
+static const size_t kL2PrefetchBytes = size_t(64) << 20;
+
 static cudaError_t gate_up_swiglu(int dt, const void* X, int K, const void* W, int rows, int I, float* part,
-                                  void* act, int* sem, int* status, cudaStream_t s) {
+                                  void* act, int* sem, int* status, cudaStream_t s,
+                                  const GemmNext* next = nullptr) {
   GemmOut go;
   if (dt == PEAGLE_BF16 && (2 * I) % 256 == 0) {
     GemmEpi ep{};
     ep.op = GEMM_EPI_SWIGLU;
     ep.act = act;
     ep.act_ld = I;
-    return gemm_launch_epi(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, &ep, s);
+    return gemm_launch_epi(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, &ep, s, next);
   }
-  cudaError_t e = gemm_launch(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, s);
+  cudaError_t e = gemm_launch(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, s, next);
   if (e != cudaSuccess) return e;
   return launch_swiglu(dt, go, rows, I, act, s);
 }
 
 // =============================================================== draft step
 struct DraftWs {
-  int* sem;
   void *x0, *xin, *act, *q, *kc, *vc, *ao;
   float *h, *resid0, *part, *attn_o, *attn_ml, *am_val;
   int* am_idx;
@@ -358,7 +368,6 @@ static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, B
   const size_t es = esize(c);
   const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K;
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
-  ws.sem = bp.take<int>(kGemmSemCount);
   ws.x0 = bp.take_bytes((size_t)B * 2 * H * es);
   ws.xin = bp.take_bytes((size_t)rows * H * es);
   ws.act = bp.take_bytes((size_t)rows * I * es);
@@ -432,10 +441,18 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   const int dt = c.dtype;
   const float eps = (float)c.rms_eps;
   GemmOut go;
-  CUDA_TRY(cudaMemsetAsync(ws.sem, 0, kGemmSemCount * sizeof(int), s));
+  // each contraction pulls the leading weight tiles of the next one into L2
+  // while it drains and the row kernels between the two run
+  const bool gated = dt == PEAGLE_BF16 && (2 * I) % 256 == 0;
+  auto nx_qkv = [&](int l) { return GemmNext{m->layers[l].qkv_w, l == 0 ? B : rows, QKV, l == 0 ? 2 * H : H, 0,
+                                              kL2PrefetchBytes}; };
+  const GemmNext nx_head{m->w.lm_head_w, rows, c.draft_vocab, H, 0, kL2PrefetchBytes};
 
   // fc + fc_norm over the anchors' aux states, then the layer-0 input rows
-  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, ws.sem, m->status, PEAGLE_OP_FC, s));
+  {
+    const GemmNext nx = nx_qkv(0);
+    CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->sem, m->status, PEAGLE_OP_FC, s, &nx));
+  }
   FcFinishArgs fa{};
   fa.u = go;
   fa.H = H;
@@ -455,14 +472,20 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   for (int l = 0; l < L; ++l) {
     const peagle_layer_weights& W = m->layers[l];
     QkvArgs qa{};
+    const GemmNext nx_o{W.o_w, rows, H, nq * hd, 0, kL2PrefetchBytes};
+    const GemmNext nx_gu{W.gate_up_w, rows, 2 * I, H, gated ? 1 : 0, kL2PrefetchBytes};
+    const GemmNext nx_down{W.down_w, rows, H, I, 0, kL2PrefetchBytes};
+    const GemmNext nx_after = (l + 1 < L) ? nx_qkv(l + 1) : nx_head;
     if (l == 0) {
-      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV, s));
+      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s,
+                           &nx_o));
       qa.mode = 1;
       qa.resid0 = ws.resid0;
       qa.mask_resid = m->mask_resid0;
       qa.h = ws.h;
     } else {
-      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV, s));
+      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s,
+                           &nx_o));
       qa.mode = 0;
     }
     qa.in = go;
@@ -514,7 +537,8 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     da.status = m->status;
     CUDA_TRY(launch_decode_attn(dt, da, PEAGLE_OP_ATTN, s));
 
-    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, ws.sem, m->status, PEAGLE_OP_O, s));
+    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, m->sem, m->status, PEAGLE_OP_O, s,
+                         &nx_gu));
     ResidNormArgs ra{};
     ra.in = go;
     ra.H = H;
@@ -525,8 +549,9 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ra.y = ws.xin;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
 
-    CUDA_TRY(gate_up_swiglu(dt, ws.xin, H, W.gate_up_w, rows, I, ws.part, ws.act, ws.sem, m->status, s));
-    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, ws.sem, m->status, PEAGLE_OP_DOWN, s));
+    CUDA_TRY(gate_up_swiglu(dt, ws.xin, H, W.gate_up_w, rows, I, ws.part, ws.act, m->sem, m->status, s, &nx_down));
+    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->sem, m->status, PEAGLE_OP_DOWN, s,
+                         &nx_after));
     ra.in = go;
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
@@ -540,12 +565,12 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ep.logits_ld = c.draft_vocab;
     ep.p_max = ws.am_val;
     ep.p_idx = ws.am_idx;
-    CUDA_TRY(gemm_launch_epi(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem,
+    CUDA_TRY(gemm_launch_epi(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->sem,
                              m->status, PEAGLE_OP_LM_HEAD, &ep, s));
     CUDA_TRY(launch_lm_argmax_final(rows, gemm_col_tiles(rows, c.draft_vocab, H), ws.am_val, ws.am_idx, m->w.d2t,
                                     draft_tokens, s));
   } else {
-    CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, ws.sem, m->status,
+    CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->sem, m->status,
                          PEAGLE_OP_LM_HEAD, s));
     CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
   }

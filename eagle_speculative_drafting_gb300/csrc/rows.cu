@@ -3,11 +3,13 @@
 // tensor-core GEMM wrote, then applies the row operation in fp32.
 #include <math.h>
 
+#include <algorithm>
+
 #include "rows.cuh"
 
 namespace pe {
 
-constexpr int kQkvChunk = 1024;   // per-row elements one qkv_finish block handles
+constexpr int kQkvChunk = 256;    // per-row elements one qkv_finish block handles (one per thread)
 
 __device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
   float v = 0.f;
@@ -42,56 +44,89 @@ __global__ void rope_table_kernel(float* cosb, float* sinb, int max_pos, int hal
 // Row r: u = sum of partials; h = RMSNorm_fc(u);
 //   x0[r] = [RMSNorm_in(E[tok]) , RMSNorm_hidden(h)]   (2H wide)
 //   resid[r] = RMSNorm_hidden(h) if norm_before_residual else h.
+// One block per row, EPT columns per thread held in registers: the gains are
+// read before waiting on the producer, u and the token in one round, the
+// embedding row in a second, and the three sums of squares in one block
+// reduction (sum h^2 = inv_fc^2 * sum (u g_fc)^2).
 // -------------------------------------------------------------------------
-template <typename T>
+// Sums three per-thread values over the block; every thread gets the totals.
+__device__ __forceinline__ void block_sum3(float& x, float& y, float& z, float (*red)[32]) {
+  x = warp_sum(x);
+  y = warp_sum(y);
+  z = warp_sum(z);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  if (lane == 0) {
+    red[0][w] = x;
+    red[1][w] = y;
+    red[2][w] = z;
+  }
+  __syncthreads();
+  x = warp_sum(lane < nw ? red[0][lane] : 0.f);
+  y = warp_sum(lane < nw ? red[1][lane] : 0.f);
+  z = warp_sum(lane < nw ? red[2][lane] : 0.f);
+}
+
+template <typename T, int EPT>
 __global__ void fc_finish_kernel(FcFinishArgs a) {
   pdl_trigger();
-  pdl_wait();
-  extern __shared__ float sh[];
-  __shared__ float red[33];
-  const int r = blockIdx.x, H = a.H;
+  __shared__ float red[3][32];
+  const int r = blockIdx.x, H = a.H, bd = blockDim.x, tid = threadIdx.x;
   const T* g_fc = static_cast<const T*>(a.g_fc);
   const T* g_in = static_cast<const T*>(a.g_in);
   const T* g_h = static_cast<const T*>(a.g_h);
-  float ss = 0.f;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float v = sum_parts(a.u, (size_t)r * a.u.ldo + j);
-    sh[j] = v;
-    ss += v * v;
+  float gf[EPT], gi[EPT], gh[EPT], u[EPT], ev[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    gf[i] = j < H ? to_f(g_fc[j]) : 0.f;
+    gi[i] = j < H ? to_f(g_in[j]) : 0.f;
+    gh[i] = j < H ? to_f(g_h[j]) : 0.f;
   }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / H + a.eps);
-  float ss2 = 0.f;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float h = sh[j] * inv * to_f(g_fc[j]);
-    sh[j] = h;
-    ss2 += h * h;
-  }
-  ss2 = block_sum(ss2, red);
-  const float inv2 = rsqrtf(ss2 / H + a.eps);
+  pdl_wait();
   int t = a.tok ? a.tok[r] : a.tok_const;
+  const float* ur = a.u.out + (size_t)r * a.u.ldo;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    u[i] = j < H ? ur[j] : 0.f;
+  }
+  for (int q = 1; q < a.u.splits; ++q) {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int j = tid + i * bd;
+      if (j < H) u[i] += ur[(size_t)q * a.u.split_stride + j];
+    }
+  }
   if (t < 0 || t >= a.Vt) {
-    if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+    if (tid == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
     t = 0;
   }
   const T* e = static_cast<const T*>(a.embed) + (size_t)t * H;
-  float ss3 = 0.f;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float v = to_f(e[j]);
-    ss3 += v * v;
+  float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    ev[i] = j < H ? to_f(e[j]) : 0.f;
+    const float ug = u[i] * gf[i];
+    s1 += u[i] * u[i];
+    s2 += ug * ug;
+    s3 += ev[i] * ev[i];
   }
-  ss3 = block_sum(ss3, red);
-  const float inv3 = rsqrtf(ss3 / H + a.eps);
+  block_sum3(s1, s2, s3, red);
+  const float inv = rsqrtf(s1 / H + a.eps);
+  const float inv2 = rsqrtf(inv * inv * s2 / H + a.eps);
+  const float inv3 = rsqrtf(s3 / H + a.eps);
   T* x0 = static_cast<T*>(a.x0) + (size_t)r * 2 * H;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < H; j += blockDim.x) {
-    const float hn = sh[j] * inv2 * to_f(g_h[j]);
-    x0[j] = from_f<T>(to_f(e[j]) * inv3 * to_f(g_in[j]));
-    x0[H + j] = from_f<T>(hn);
-    if (a.resid) a.resid[(size_t)r * H + j] = a.nbr ? hn : sh[j];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    if (j < H) {
+      const float h = u[i] * inv * gf[i];
+      const float hn = h * inv2 * gh[i];
+      x0[j] = from_f<T>(ev[i] * inv3 * gi[i]);
+      x0[H + j] = from_f<T>(hn);
+      if (a.resid) a.resid[(size_t)r * H + j] = a.nbr ? hn : h;
+    }
   }
 }
 
@@ -193,29 +228,49 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
 // (Llama layer: after O-proj with the post-attention gain; after the MLP
 // down-proj with the next layer's input gain or the final gain.)
 // -------------------------------------------------------------------------
-template <typename T>
+template <typename T, int EPT>
 __global__ void resid_norm_kernel(ResidNormArgs a) {
   pdl_trigger();
-  pdl_wait();
-  extern __shared__ float sh[];
-  __shared__ float red[33];
+  __shared__ float red[3][32];
   const int rl = blockIdx.x;           // row within the chunk
   const int r = a.row0 + rl;           // global row
-  float* h = a.h + (size_t)r * a.H;
-  float ss = 0.f;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < a.H; j += blockDim.x) {
-    const float v = h[j] + sum_parts(a.in, (size_t)rl * a.in.ldo + j);
-    h[j] = v;
-    sh[j] = v;
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / a.H + a.eps);
+  const int H = a.H, bd = blockDim.x, tid = threadIdx.x;
   const T* g = static_cast<const T*>(a.gain);
-  T* y = static_cast<T*>(a.y) + (size_t)r * a.H;
-#pragma unroll 4
-  for (int j = threadIdx.x; j < a.H; j += blockDim.x) y[j] = from_f<T>(sh[j] * inv * to_f(g[j]));
+  float gv[EPT], v[EPT];
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    gv[i] = j < H ? to_f(g[j]) : 0.f;
+  }
+  pdl_wait();
+  float* h = a.h + (size_t)r * H;
+  const float* ur = a.in.out + (size_t)rl * a.in.ldo;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    v[i] = j < H ? h[j] + ur[j] : 0.f;
+  }
+  for (int q = 1; q < a.in.splits; ++q) {
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int j = tid + i * bd;
+      if (j < H) v[i] += ur[(size_t)q * a.in.split_stride + j];
+    }
+  }
+  float ss = 0.f, d1 = 0.f, d2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) ss += v[i] * v[i];
+  block_sum3(ss, d1, d2, red);
+  const float inv = rsqrtf(ss / H + a.eps);
+  T* y = static_cast<T*>(a.y) + (size_t)r * H;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int j = tid + i * bd;
+    if (j < H) {
+      h[j] = v[i];
+      y[j] = from_f<T>(v[i] * inv * gv[i]);
+    }
+  }
 }
 
 // -------------------------------------------------------------------------
@@ -668,13 +723,16 @@ static int grid_for(long long total, int threads) {
   return (int)(g < 1 ? 1 : g);
 }
 
-// Threads per row of a row-reduction kernel: few rows get wide blocks so the
-// row's loads are all in flight at once; many rows keep blocks small.
-static int row_threads(int rows, int H) {
-  if (rows >= 2 * num_sms()) return 256;
-  int t = 256;
-  while (t < 1024 && t * 4 < H) t *= 2;
-  return t;
+// Block shape of a one-row-per-block kernel: EPT columns per thread in
+// registers (4, 8 or 16). Few rows get wide blocks so each thread holds few
+// columns; many rows keep blocks near 256 threads.
+static int row_threads(int rows, int H, int* ept) {
+  const int t0 = rows >= 2 * num_sms() ? 256 : 1024;
+  int e = 4;
+  while (e < 16 && e * t0 < H) e *= 2;
+  *ept = e;
+  const int t = ((H + e - 1) / e + 31) / 32 * 32;
+  return std::max(32, std::min(1024, t));
 }
 
 #define PE_LAUNCH_END() \
@@ -689,12 +747,19 @@ cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double th
   PE_LAUNCH_END();
 }
 
+template <typename T>
+static void fc_finish_dispatch(int rows, int threads, int ept, const FcFinishArgs& a, cudaStream_t st) {
+  if (ept == 4) launch_pdl(fc_finish_kernel<T, 4>, rows, threads, 0, st, a);
+  else if (ept == 8) launch_pdl(fc_finish_kernel<T, 8>, rows, threads, 0, st, a);
+  else launch_pdl(fc_finish_kernel<T, 16>, rows, threads, 0, st, a);
+}
+
 cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  const size_t sm = (size_t)a.H * sizeof(float);
-  const int threads = row_threads(rows, a.H);
-  if (dtype == PEAGLE_BF16) launch_pdl(fc_finish_kernel<bf16>, rows, threads, sm, st, a);
-  else launch_pdl(fc_finish_kernel<float>, rows, threads, sm, st, a);
+  int ept;
+  const int threads = row_threads(rows, a.H, &ept);
+  if (dtype == PEAGLE_BF16) fc_finish_dispatch<bf16>(rows, threads, ept, a, st);
+  else fc_finish_dispatch<float>(rows, threads, ept, a, st);
   PE_LAUNCH_END();
 }
 
@@ -707,12 +772,19 @@ cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_
   PE_LAUNCH_END();
 }
 
+template <typename T>
+static void resid_norm_dispatch(int rows, int threads, int ept, const ResidNormArgs& a, cudaStream_t st) {
+  if (ept == 4) launch_pdl(resid_norm_kernel<T, 4>, rows, threads, 0, st, a);
+  else if (ept == 8) launch_pdl(resid_norm_kernel<T, 8>, rows, threads, 0, st, a);
+  else launch_pdl(resid_norm_kernel<T, 16>, rows, threads, 0, st, a);
+}
+
 cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  const size_t sm = (size_t)a.H * sizeof(float);
-  const int threads = row_threads(rows, a.H);
-  if (dtype == PEAGLE_BF16) launch_pdl(resid_norm_kernel<bf16>, rows, threads, sm, st, a);
-  else launch_pdl(resid_norm_kernel<float>, rows, threads, sm, st, a);
+  int ept;
+  const int threads = row_threads(rows, a.H, &ept);
+  if (dtype == PEAGLE_BF16) resid_norm_dispatch<bf16>(rows, threads, ept, a, st);
+  else resid_norm_dispatch<float>(rows, threads, ept, a, st);
   PE_LAUNCH_END();
 }
 

@@ -129,7 +129,9 @@ uint64_t peagle_kernel_launches(void);
 
 /* ---- model -------------------------------------------------------------- */
 /* Validates the config, borrows the weights, allocates the model's own small
- * device state (rotary table, status word, constants) and precomputes what
+ * device state (rotary table, status word, constants, and the zeroed
+ * arrival counters of the draft step's contractions, which every launch
+ * leaves zero again) and precomputes what
  * every masked row shares: fc_norm(fc(mask_hidden)), the ptd embedding, the
  * layer-0 pre-rotary q/k/v and residual of a masked row (#2376, Changelog:
  * masked_projected_hidden). Synchronizes `stream` before returning. */
@@ -141,7 +143,8 @@ peagle_status peagle_model_destroy(peagle_model* model);
  * (PEAGLE_DEV_* bits) to *host_status. */
 peagle_status peagle_get_device_status(const peagle_model* model, void* stream,
                                        int32_t* host_status);
-/* Clears the device status word (enqueued on `stream`). */
+/* Clears the device status word and re-zeroes the model's arrival counters
+ * (a launch that timed out may leave them set); enqueued on `stream`. */
 peagle_status peagle_clear_device_status(const peagle_model* model, void* stream);
 
 /* ---- draft step (decode) ------------------------------------------------ */
@@ -171,7 +174,9 @@ peagle_status peagle_draft_step_workspace_size(const peagle_model* model, int32_
  *                  lowest index among equal maxima
  *   logits         device float [B, K, Vd] out, or NULL
  * K in [1, 16]. Violations of the device-side ranges set PEAGLE_DEV_BOUNDS
- * and the offending row is skipped. */
+ * and the offending row is skipped. The step uses the model's arrival
+ * counters: draft steps of one model must not run concurrently (enqueue them
+ * on one stream, or order their streams). */
 peagle_status peagle_draft_step(const peagle_model* model, int32_t B, int32_t K,
                                 const void* aux, const int32_t* anchor_tokens,
                                 const int32_t* anchor_pos, void* const* k_cache,
