@@ -336,22 +336,17 @@ peagle_status peagle_clear_device_status(const peagle_model* m, void* stream) {
 // gate/up projection and SwiGLU over rows of width K: bf16 with 2I % 256 == 0
 // writes silu(gate) * up straight from the GEMM epilogue; otherwise the fp32
 // result goes through the SwiGLU row kernel.
-// Weight bytes each decode contraction pulls into L2 for the next one: about
-// what HBM streams in the gap between two contractions, and half of L2.
-static const size_t kL2PrefetchBytes = size_t(64) << 20;
-
 static cudaError_t gate_up_swiglu(int dt, const void* X, int K, const void* W, int rows, int I, float* part,
-                                  void* act, int* sem, int* status, cudaStream_t s,
-                                  const GemmNext* next = nullptr) {
+                                  void* act, int* sem, int* status, cudaStream_t s) {
   GemmOut go;
   if (dt == PEAGLE_BF16 && (2 * I) % 256 == 0) {
     GemmEpi ep{};
     ep.op = GEMM_EPI_SWIGLU;
     ep.act = act;
     ep.act_ld = I;
-    return gemm_launch_epi(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, &ep, s, next);
+    return gemm_launch_epi(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, &ep, s);
   }
-  cudaError_t e = gemm_launch(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, s, next);
+  cudaError_t e = gemm_launch(dt, X, K, W, rows, 2 * I, K, part, &go, sem, status, PEAGLE_OP_GATE_UP, s);
   if (e != cudaSuccess) return e;
   return launch_swiglu(dt, go, rows, I, act, s);
 }
@@ -441,20 +436,9 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   const int dt = c.dtype;
   const float eps = (float)c.rms_eps;
   GemmOut go;
-  // each contraction pulls the leading weight tiles of the next one into L2
-  // while it drains and the row kernels between the two run
-  const bool gated = dt == PEAGLE_BF16 && (2 * I) % 256 == 0;
-  auto nx_qkv = [&](int l) { return GemmNext{m->layers[l].qkv_w, l == 0 ? B : rows, QKV, l == 0 ? 2 * H : H, 0,
-                                              kL2PrefetchBytes}; };
-  const GemmNext nx_head{m->w.lm_head_w, rows, c.draft_vocab, H, 0, kL2PrefetchBytes};
 
   // fc + fc_norm over the anchors' aux states, then the layer-0 input rows
-  {
-    const GemmNext nx = nx_qkv(0);
-    CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->sem, m->status, PEAGLE_OP_FC, s, &nx));
-  }
   FcFinishArgs fa{};
-  fa.u = go;
   fa.H = H;
   fa.Vt = c.target_vocab;
   fa.tok = anchor_tokens;
@@ -467,25 +451,21 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   fa.x0 = ws.x0;
   fa.resid = ws.resid0;
   fa.status = m->status;
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->sem, m->status, PEAGLE_OP_FC, s));
+  fa.u = go;
   CUDA_TRY(launch_fc_finish(dt, B, fa, s));
 
   for (int l = 0; l < L; ++l) {
     const peagle_layer_weights& W = m->layers[l];
     QkvArgs qa{};
-    const GemmNext nx_o{W.o_w, rows, H, nq * hd, 0, kL2PrefetchBytes};
-    const GemmNext nx_gu{W.gate_up_w, rows, 2 * I, H, gated ? 1 : 0, kL2PrefetchBytes};
-    const GemmNext nx_down{W.down_w, rows, H, I, 0, kL2PrefetchBytes};
-    const GemmNext nx_after = (l + 1 < L) ? nx_qkv(l + 1) : nx_head;
     if (l == 0) {
-      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s,
-                           &nx_o));
+      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s));
       qa.mode = 1;
       qa.resid0 = ws.resid0;
       qa.mask_resid = m->mask_resid0;
       qa.h = ws.h;
     } else {
-      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s,
-                           &nx_o));
+      CUDA_TRY(gemm_launch(dt, ws.xin, H, W.qkv_w, rows, QKV, H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s));
       qa.mode = 0;
     }
     qa.in = go;
@@ -537,21 +517,19 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     da.status = m->status;
     CUDA_TRY(launch_decode_attn(dt, da, PEAGLE_OP_ATTN, s));
 
-    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, m->sem, m->status, PEAGLE_OP_O, s,
-                         &nx_gu));
     ResidNormArgs ra{};
-    ra.in = go;
     ra.H = H;
     ra.row0 = 0;
     ra.h = ws.h;
     ra.gain = W.post_norm_w;
     ra.eps = eps;
     ra.y = ws.xin;
+    CUDA_TRY(gemm_launch(dt, ws.ao, nq * hd, W.o_w, rows, H, nq * hd, ws.part, &go, m->sem, m->status, PEAGLE_OP_O, s));
+    ra.in = go;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
 
-    CUDA_TRY(gate_up_swiglu(dt, ws.xin, H, W.gate_up_w, rows, I, ws.part, ws.act, m->sem, m->status, s, &nx_down));
-    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->sem, m->status, PEAGLE_OP_DOWN, s,
-                         &nx_after));
+    CUDA_TRY(gate_up_swiglu(dt, ws.xin, H, W.gate_up_w, rows, I, ws.part, ws.act, m->sem, m->status, s));
+    CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->sem, m->status, PEAGLE_OP_DOWN, s));
     ra.in = go;
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));

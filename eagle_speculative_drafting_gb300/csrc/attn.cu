@@ -86,65 +86,123 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
   }
 }
 
+// Output row (r = (b, d), head h) from the chunks' (m, l, o) plus the chain
+// keys (b, 0..d); one warp, lane owns dims [lane*E, lane*E + E). The query,
+// the chunk statistics, the first chunk outputs and the first chain keys /
+// values are all loaded before any of them is used, so the row costs about
+// two memory round trips.
+template <typename T, int E>
+__device__ void combine_row(const DecodeAttnArgs& a, int r, int h, int lane) {
+  constexpr int SB = 8, CB = 4;   // chunk outputs / chain rows per load round
+  const int b = r / a.K, d = r % a.K;
+  const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
+  const int g = h / G, qi = d * G + h % G;
+  const int ns = a.nsplit;
+  const T* Q = static_cast<const T*>(a.Q);
+  const T* Kc = static_cast<const T*>(a.Kc);
+  const T* Vc = static_cast<const T*>(a.Vc);
+  const size_t prow = (size_t)(b * a.nkv + g) * ns * KG;
+  auto ml = [&](int s) { return a.part_ml + (prow + (size_t)s * KG + qi) * 2; };
+  auto po_at = [&](int s) { return a.part_o + (prow + (size_t)s * KG + qi) * hd + lane * E; };
+  auto kv_at = [&](int j) { return ((size_t)(b * a.K + j) * a.nkv + g) * hd + lane * E; };
+
+  float q[E];
+  load_vec<T, E>(Q + ((size_t)r * a.nq + h) * hd + lane * E, q);
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;   // chunks lane, lane + 32
+  if (lane < ns) {
+    m0 = ml(lane)[0];
+    l0 = ml(lane)[1];
+  }
+  if (lane + 32 < ns) {
+    m1 = ml(lane + 32)[0];
+    l1 = ml(lane + 32)[1];
+  }
+  float po[SB][E], kk[CB][E], vv[CB][E];
+#pragma unroll
+  for (int i = 0; i < SB; ++i) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) po[i][e] = i < ns ? po_at(i)[e] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < CB; ++i) {
+    if (i <= d) {
+      load_vec<T, E>(Kc + kv_at(i), kk[i]);
+      load_vec<T, E>(Vc + kv_at(i), vv[i]);
+    }
+  }
+  // merged statistics of the chunks
+  float M = fmaxf(m0, m1);
+  for (int s = lane + 64; s < ns; s += 32) M = fmaxf(M, ml(s)[0]);
+  M = warp_max(M);
+  float l = (m0 == -INFINITY ? 0.f : l0 * __expf(m0 - M)) + (m1 == -INFINITY ? 0.f : l1 * __expf(m1 - M));
+  for (int s = lane + 64; s < ns; s += 32) {
+    const float ms = ml(s)[0];
+    if (ms != -INFINITY) l += ml(s)[1] * __expf(ms - M);
+  }
+  l = warp_sum(l);
+  float o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[e] = 0.f;
+  if (M != -INFINITY) {
+    for (int s0 = 0; s0 < ns; s0 += SB) {
+      if (s0 > 0) {
+#pragma unroll
+        for (int i = 0; i < SB; ++i) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) po[i][e] = s0 + i < ns ? po_at(s0 + i)[e] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < SB; ++i) {
+        const int s = s0 + i;
+        if (s >= ns) break;
+        const float ms = s < 64 ? __shfl_sync(0xffffffffu, s < 32 ? m0 : m1, s & 31) : ml(s)[0];
+        const float c = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] += po[i][e] * c;
+      }
+    }
+  }
+  // chain rows (b, 0..d), CB at a time
+  float m = M;
+  for (int j0 = 0; j0 <= d; j0 += CB) {
+    if (j0 > 0) {
+#pragma unroll
+      for (int i = 0; i < CB; ++i) {
+        if (j0 + i <= d) {
+          load_vec<T, E>(Kc + kv_at(j0 + i), kk[i]);
+          load_vec<T, E>(Vc + kv_at(j0 + i), vv[i]);
+        }
+      }
+    }
+    float dot[CB];
+#pragma unroll
+    for (int i = 0; i < CB; ++i) {
+      dot[i] = 0.f;
+      if (j0 + i <= d) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) dot[i] = fmaf(q[e], kk[i][e], dot[i]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CB; ++i) dot[i] = warp_sum(dot[i]) * a.scale;
+#pragma unroll
+    for (int i = 0; i < CB; ++i)
+      if (j0 + i <= d) online_add<E>(dot[i], vv[i], m, l, o);
+  }
+  const float inv = 1.f / l;
+  T* out = static_cast<T*>(a.O) + ((size_t)r * a.nq + h) * hd + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] = from_f<T>(o[e] * inv);
+}
+
 template <typename T, int E>
 __global__ void decode_combine(DecodeAttnArgs a) {
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
-  const int b = r / a.K, d = r % a.K;
-  const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const T* Q = static_cast<const T*>(a.Q);
-  const T* Kc = static_cast<const T*>(a.Kc);
-  const T* Vc = static_cast<const T*>(a.Vc);
-  T* O = static_cast<T*>(a.O);
-  for (int h = blockIdx.y * nw + w; h < a.nq; h += gridDim.y * nw) {
-    const int g = h / G, qi = d * G + h % G;
-    const size_t prow = (size_t)(b * a.nkv + g) * a.nsplit * KG;
-    // the chunks' (m, l): lanes over chunks, then warp reductions
-    float M = -INFINITY;
-    for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, a.part_ml[(prow + (size_t)s * KG + qi) * 2]);
-    M = warp_max(M);
-    float l = 0.f;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const size_t pr = prow + (size_t)s * KG + qi;
-      const float ms = a.part_ml[pr * 2];
-      if (ms != -INFINITY) l += a.part_ml[pr * 2 + 1] * __expf(ms - M);
-    }
-    l = warp_sum(l);
-    float o[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll 8
-      for (int s = 0; s < a.nsplit; ++s) {
-        const size_t pr = prow + (size_t)s * KG + qi;
-        const float ms = a.part_ml[pr * 2];
-        const float c = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-        const float* po = a.part_o + pr * hd + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] += po[e] * c;
-      }
-    }
-    float m = M;
-    float q[E];
-    load_vec<T, E>(Q + ((size_t)r * a.nq + h) * hd + lane * E, q);
-    for (int j = 0; j <= d; ++j) {  // chain rows (b, 0..d)
-      const size_t base = ((size_t)(b * a.K + j) * a.nkv + g) * hd + lane * E;
-      float k[E], v[E];
-      load_vec<T, E>(Kc + base, k);
-      float dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) dot = fmaf(q[e], k[e], dot);
-      dot = warp_sum(dot) * a.scale;
-      load_vec<T, E>(Vc + base, v);
-      online_add<E>(dot, v, m, l, o);
-    }
-    const float inv = 1.f / l;
-    T* out = O + ((size_t)r * a.nq + h) * hd + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = from_f<T>(o[e] * inv);
-  }
+  for (int h = blockIdx.y * nw + w; h < a.nq; h += gridDim.y * nw) combine_row<T, E>(a, r, h, lane);
 }
 
 // ------------------------------------------------- decode, bf16 tensor cores
@@ -420,7 +478,8 @@ void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit) {
 }
 
 template <typename T, int E>
-static cudaError_t decode_attn_t(const DecodeAttnArgs& a, int probe_op, cudaStream_t st) {
+static cudaError_t decode_attn_t(const DecodeAttnArgs& a_in, int probe_op, cudaStream_t st) {
+  const DecodeAttnArgs& a = a_in;
   dim3 grid(a.nsplit, a.nkv, a.B);
   probe_start(probe_op, st);
   if (sizeof(T) == 2 && a.K * (a.nq / a.nkv) <= 128) {

@@ -117,10 +117,8 @@ constexpr int kGemmSemCount = 4096;
 // Runs D = X W^T into out (planning the split itself; fills *o). The K
 // slices are summed inside the kernel, so *o always describes one slab.
 // X [M, K] with row stride ldx elements, W [N, K] contiguous.
-struct GemmNext;
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
-                        float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s,
-                        const GemmNext* next = nullptr);
+                        float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s);
 
 // Fused head epilogue of a bf16 contraction: instead of (or besides) the
 // fp32 result, per (row, column tile) partials of the row's argmax (value,
@@ -142,20 +140,8 @@ struct GemmEpi {
 };
 // Column tiles (partials per row) of the fused head epilogue.
 int gemm_col_tiles(int M, int N, int K);
-// The contraction that follows on the same stream. Its weights do not depend
-// on this one's result, so once a CTA has issued its own last load it pulls
-// the first weight tiles that the same-numbered CTA of the next launch will
-// read into L2 (up to `bytes` over the whole grid), and the next launch
-// starts from L2 while this one drains. Only a next contraction with few
-// activation rows (the swapped stream-K schedule) is prefetched.
-struct GemmNext {
-  const void* W;   // [N, K] weight, contiguous
-  int M, N, K;
-  int gated;       // W is a fused SwiGLU gate/up weight
-  size_t bytes;
-};
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
                             float* out, GemmOut* o, int* sem, int* dev_status, int probe_op,
-                            const GemmEpi* epi, cudaStream_t s, const GemmNext* next = nullptr);
+                            const GemmEpi* epi, cudaStream_t s);
 
 }  // namespace pe

@@ -77,13 +77,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// Pulls one box of a tensor into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -177,10 +170,6 @@ struct TcArgs {
   int gate_off;
   void* act;
   int act_ld;
-  // L2 prefetch of the next contraction (swapped stream-K): its schedule
-  // (tiles x ktiles units over pf_grid CTAs, pf_sub boxes per k-tile, K
-  // width pf_K, gate rows offset pf_gate or 0) and pf_units units per CTA
-  int pf_tiles, pf_ktiles, pf_grid, pf_units, pf_sub, pf_K, pf_gate;
 };
 
 // Running head statistics of one row over some columns: argmax (lowest
@@ -399,7 +388,7 @@ __device__ void swiglu_finish_rows(const TcArgs& g, int m_begin, int m_end, int 
 template <int BN, bool SWAP>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmP, TcArgs g) {
+                   TcArgs g) {
   using C = TcCfg<BN, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -516,32 +505,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
       if (!waited) pdl_wait();
-      if (g.pf_units > 0 && !*abort_flag) {
-        // this CTA's loads are all issued: pull the leading units of the next
-        // contraction's CTA blockIdx.x (and of any CTA beyond this grid) into
-        // L2, in the order that CTA will read them
-        tc::prefetch_map(&tmP);
-        for (int c = blockIdx.x; c < g.pf_grid; c += gridDim.x) {
-          Sched ps;
-          ps.init(g.pf_tiles, g.pf_ktiles, 1, 1, g.pf_grid, c);
-          Seg q;
-          int left = g.pf_units;
-          while (left > 0 && ps.next(q)) {
-            for (int k = q.kb; k < q.ke && left > 0; ++k, --left) {
-              const int nv = min(g.pf_sub, (g.pf_K - k * 64 * g.pf_sub + 63) / 64);
-              for (int i = 0; i < nv; ++i) {
-                const int x = (k * g.pf_sub + i) * 64;
-                if (g.pf_gate) {
-                  tc::tma_prefetch_2d(&tmP, x, q.tile * 64);
-                  tc::tma_prefetch_2d(&tmP, x, g.pf_gate + q.tile * 64);
-                } else {
-                  tc::tma_prefetch_2d(&tmP, x, q.tile * 128);
-                }
-              }
-            }
-          }
-        }
-      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -962,8 +925,8 @@ size_t gemm_out_floats(int dtype, int M, int N, int K) {
 }
 
 template <int BN, bool SWAP>
-static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& pf,
-                             const TcArgs& args, int grid, cudaStream_t s) {
+static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
+                             cudaStream_t s) {
   using C = TcCfg<BN, SWAP>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -982,7 +945,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const C
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP>, a, b, pf, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP>, a, b, args);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -993,14 +956,13 @@ int gemm_col_tiles(int M, int N, int K) {
 }
 
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
-                        GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s,
-                        const GemmNext* next) {
-  return gemm_launch_epi(dtype, X, ldx, W, M, N, K, out, o, sem, dev_status, probe_op, nullptr, s, next);
+                        GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s) {
+  return gemm_launch_epi(dtype, X, ldx, W, M, N, K, out, o, sem, dev_status, probe_op, nullptr, s);
 }
 
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
                             GemmOut* o, int* sem, int* dev_status, int probe_op, const GemmEpi* epi,
-                            cudaStream_t s, const GemmNext* next) {
+                            cudaStream_t s) {
   if (M <= 0 || N <= 0) {
     if (o) *o = GemmOut{out, N, 1, 0};
     return cudaSuccess;
@@ -1066,26 +1028,6 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
     set_error("cuTensorMapEncodeTiled failed (M=%d N=%d K=%d)", M, N, K);
     return cudaErrorInvalidValue;
   }
-  // the next contraction's leading weight units, if it is a swapped one
-  CUtensorMap mp = (p.swap ? ma : mb);
-  args.pf_units = 0;
-  args.pf_tiles = args.pf_ktiles = args.pf_grid = args.pf_sub = args.pf_K = args.pf_gate = 0;
-  if (next && next->W && next->bytes > 0 && next->M > 0 && next->N > 0 && next->K > 0 &&
-      (!next->gated || next->N % 256 == 0)) {
-    const Plan q = plan_gemm(next->M, next->N, next->K);
-    if (q.swap && q.streamk &&
-        make_map(&mp, next->W, next->N, next->K, next->K, next->gated ? 64 : 128)) {
-      const size_t unit = (size_t)sub_boxes(q.bn) * 128 * 64 * 2;
-      const size_t per_cta = (next->bytes + (size_t)q.grid * unit - 1) / ((size_t)q.grid * unit);
-      args.pf_units = (int)std::min<size_t>(per_cta, (size_t)q.tiles * q.ktiles);
-      args.pf_tiles = q.tiles;
-      args.pf_ktiles = q.ktiles;
-      args.pf_grid = q.grid;
-      args.pf_sub = sub_boxes(q.bn);
-      args.pf_K = next->K;
-      args.pf_gate = next->gated ? next->N / 2 : 0;
-    }
-  }
   // the kernel folds the K slices into slab 0
   if (o) *o = GemmOut{out, N, 1, 0};
   const int items = p.grid;
@@ -1093,15 +1035,15 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   probe_start(probe_op, s);
   if (p.swap) {
     switch (p.bn) {
-      case 16: e = launch_tc<16, true>(ma, mb, mp, args, items, s); break;
-      case 32: e = launch_tc<32, true>(ma, mb, mp, args, items, s); break;
-      case 64: e = launch_tc<64, true>(ma, mb, mp, args, items, s); break;
-      case 128: e = launch_tc<128, true>(ma, mb, mp, args, items, s); break;
-      default: e = launch_tc<256, true>(ma, mb, mp, args, items, s); break;
+      case 16: e = launch_tc<16, true>(ma, mb, args, items, s); break;
+      case 32: e = launch_tc<32, true>(ma, mb, args, items, s); break;
+      case 64: e = launch_tc<64, true>(ma, mb, args, items, s); break;
+      case 128: e = launch_tc<128, true>(ma, mb, args, items, s); break;
+      default: e = launch_tc<256, true>(ma, mb, args, items, s); break;
     }
   } else {
-    e = (p.bn == 128) ? launch_tc<128, false>(ma, mb, mp, args, items, s)
-                      : launch_tc<256, false>(ma, mb, mp, args, items, s);
+    e = (p.bn == 128) ? launch_tc<128, false>(ma, mb, args, items, s)
+                      : launch_tc<256, false>(ma, mb, args, items, s);
   }
   probe_stop(probe_op, s);
   return e;

@@ -270,6 +270,13 @@ def test_train_bf16_small():
     check_train(wl, inp, 5, 0.7, 0.2, 99, BF16_TOL)
 
 
+def test_train_bf16_swapped_rows():
+    # at most 256 rows: every GEMM runs swapped, so the cross-entropy
+    # statistics come from the swapped epilogue
+    wl, inp = small_train(dtype="bf16", n=100, lens=(60, 40), K=2)
+    check_train(wl, inp, 2, 0.7, 0.2, 8, BF16_TOL)
+
+
 def test_train_bf16_unfused_swiglu_width():
     # 2I not a multiple of 256: the SwiGLU runs as its own kernel
     wl, inp = small_train(dtype="bf16", n=300, lens=(120, 180), K=3, intermediate=200)
