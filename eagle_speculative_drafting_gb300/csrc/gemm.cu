@@ -376,11 +376,21 @@ struct TcCfg {
 __device__ void swiglu_finish_rows(const TcArgs& g, int m_begin, int m_end, int m_step, int src0, int half,
                                    int dst0, int lane) {
   bf16* act = static_cast<bf16*>(g.act);
+  constexpr int U = 4;   // columns per lane whose loads issue before their stores
   for (int m = m_begin; m < m_end; m += m_step) {
-    for (int j = lane; j < half; j += 32) {
-      const float gt = __ldcg(g.out + (size_t)m * g.ldo + src0 + j);
-      const float up = __ldcg(g.out + (size_t)m * g.ldo + src0 + half + j);
-      act[(size_t)m * g.act_ld + dst0 + j] = __float2bfloat16_rn(gt / (1.f + __expf(-gt)) * up);
+    for (int j0 = 0; j0 < half; j0 += 32 * U) {
+      float gt[U], up[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * 32 + lane;
+        gt[u] = j < half ? __ldcg(g.out + (size_t)m * g.ldo + src0 + j) : 0.f;
+        up[u] = j < half ? __ldcg(g.out + (size_t)m * g.ldo + src0 + half + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = j0 + u * 32 + lane;
+        if (j < half) act[(size_t)m * g.act_ld + dst0 + j] = __float2bfloat16_rn(gt[u] / (1.f + __expf(-gt[u])) * up[u]);
+      }
     }
   }
 }
@@ -724,22 +734,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               }
             }
           } else {
-            // warp sums its 32 rows; lanes walk 32 consecutive columns
+            // warp sums its 32 rows; lanes walk 32 consecutive columns.
+            // A row's loads (up to four slabs at a time) all issue before
+            // its stores, which could alias them.
+            constexpr int NC = BN >= 32 ? BN / 32 : 1;
             const int n0 = tb * BN;
             for (int rr = 0; rr < 32; ++rr) {
               const int m = ta * 128 + quad * 32 + rr;
               if (m >= g.M) break;
-#pragma unroll 2
-              for (int c0 = 0; c0 < BN; c0 += 32) {
-                const int n = n0 + c0 + lane;
-                if (n < g.N) {
-                  const size_t idx = (size_t)m * g.ldo + n;
-                  float acc = 0.f;
-#pragma unroll 4
-                  for (int q = 0; q < sg.nslab; ++q) acc += __ldcg(g.out + (size_t)q * g.split_stride + idx);
-                  g.out[idx] = acc;
-                }
+              const size_t base = (size_t)m * g.ldo + n0 + lane;
+              float acc[NC];
+#pragma unroll
+              for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+              for (int q0 = 0; q0 < sg.nslab; q0 += 4) {
+                float t[4][NC];
+#pragma unroll
+                for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+                  for (int c = 0; c < NC; ++c)
+                    t[qi][c] = (q0 + qi < sg.nslab && n0 + c * 32 + lane < g.N)
+                                   ? __ldcg(g.out + (size_t)(q0 + qi) * g.split_stride + base + c * 32)
+                                   : 0.f;
+#pragma unroll
+                for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+                  for (int c = 0; c < NC; ++c)
+                    if (q0 + qi < sg.nslab) acc[c] += t[qi][c];
               }
+#pragma unroll
+              for (int c = 0; c < NC; ++c)
+                if (n0 + c * 32 + lane < g.N) g.out[base + c * 32] = acc[c];
             }
           }
           if (warp == 2 && lane == 0) g.sem[tile] = 0;
@@ -881,6 +905,9 @@ static Plan plan_gemm(int M, int N, int K) {
   p.swap = M <= 256;
   p.bn = p.swap ? swap_bn(M) : 256;
   if (!p.swap && N <= 128 * 6) p.bn = 128;
+  // too few 256-wide tiles to give every SM work: halve the tile width
+  // before cutting K into slices, which need a cross-CTA sum
+  if (!p.swap && p.bn == 256 && 2LL * ((M + 127) / 128) * ((N + 255) / 256) < num_sms()) p.bn = 128;
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
