@@ -9,7 +9,8 @@
 
 namespace pe {
 
-constexpr int kQkvChunk = 256;    // per-row elements one qkv_finish block handles (one per thread)
+constexpr int kQkvThreads = 256, kQkvEpt = 8;
+constexpr int kQkvChunk = kQkvThreads * kQkvEpt;   // per-row elements one qkv_finish block handles
 
 __device__ __forceinline__ float sum_parts(const GemmOut& g, size_t idx) {
   float v = 0.f;
@@ -142,12 +143,12 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
 // Layer 0 also seeds the residual stream h with the row's layer-0 residual.
 // Decode can append the anchor row's K/V to its cache.
 // -------------------------------------------------------------------------
-template <typename T>
-__global__ void qkv_finish_kernel(QkvArgs a) {
+template <typename T, int HD>
+__global__ void __launch_bounds__(kQkvThreads) qkv_finish_kernel(QkvArgs a) {
   pdl_trigger();
   pdl_wait();
+  constexpr int HALF = HD / 2;
   const int r = blockIdx.x + a.row0;
-  const int half = a.hd / 2;
   int src;
   if (a.mode == 0) src = r - a.src0;
   else if (a.mode == 1) src = (r % a.K == 0) ? r / a.K : -1;
@@ -159,11 +160,13 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
     if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
     pos = pos < 0 ? 0 : a.max_pos - 1;
   }
-  T* Q = static_cast<T*>(a.Q) + (size_t)r * a.nq * a.hd;
-  T* Ko = static_cast<T*>(a.Kout) + (size_t)r * a.nkv * a.hd;
-  T* Vo = static_cast<T*>(a.Vout) + (size_t)r * a.nkv * a.hd;
-  const float* cs = a.rcos + (size_t)pos * half;
-  const float* sn = a.rsin + (size_t)pos * half;
+  T* Q = static_cast<T*>(a.Q) + (size_t)r * a.nq * HD;
+  T* Ko = static_cast<T*>(a.Kout) + (size_t)r * a.nkv * HD;
+  T* Vo = static_cast<T*>(a.Vout) + (size_t)r * a.nkv * HD;
+  const float* cs = a.rcos + (size_t)pos * HALF;
+  const float* sn = a.rsin + (size_t)pos * HALF;
+  const float* in = src >= 0 ? a.in.out + (size_t)src * a.in.ldo : a.mask_qkv;
+  const float* hin = !a.h ? nullptr : (src >= 0 ? a.resid0 + (size_t)src * a.H : a.mask_resid);
 
   bool append = false;
   size_t cache_row = 0;
@@ -177,48 +180,56 @@ __global__ void qkv_finish_kernel(QkvArgs a) {
       set_status(a.status, PEAGLE_DEV_BOUNDS);
     }
   }
-  // this block's slice of the row's work: rotary pairs of q/k heads, then v
-  // elements, then (layer 0) the residual seed
-  const int pairs = (a.nq + a.nkv) * half;
-  const int vcount = a.nkv * a.hd;
+  // this block's slice of the row: rotary pairs of q/k heads, then v
+  // elements, then (layer 0) the residual seed; every operand of the
+  // thread's elements is loaded before the first store
+  const int pairs = (a.nq + a.nkv) * HALF;
+  const int vcount = a.nkv * HD;
   const int total = pairs + vcount + (a.h ? a.H : 0);
-  const int e0 = blockIdx.y * kQkvChunk, e1 = min(total, e0 + kQkvChunk);
-  const int v0 = (a.nq + a.nkv) * a.hd;
-  for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+  const int v0 = (a.nq + a.nkv) * HD;
+  const int e0 = blockIdx.y * kQkvChunk + threadIdx.x;
+  float x[kQkvEpt], y[kQkvEpt], c[kQkvEpt], sv[kQkvEpt];
+#pragma unroll
+  for (int i = 0; i < kQkvEpt; ++i) {
+    const int e = e0 + i * kQkvThreads;
+    x[i] = y[i] = c[i] = sv[i] = 0.f;
     if (e < pairs) {
-      const int head = e / half, j = e % half;
-      const int lo = head * a.hd + j, hi = lo + half;
-      float xl, xh;
-      if (src >= 0) {
-        xl = sum_parts(a.in, (size_t)src * a.in.ldo + lo);
-        xh = sum_parts(a.in, (size_t)src * a.in.ldo + hi);
-      } else {
-        xl = a.mask_qkv[lo];
-        xh = a.mask_qkv[hi];
-      }
-      const float c = cs[j], sv = sn[j];
-      const float ol = xl * c - xh * sv, oh = xh * c + xl * sv;
+      const int lo = (e / HALF) * HD + e % HALF;
+      x[i] = in[lo];
+      y[i] = in[lo + HALF];
+      c[i] = cs[e % HALF];
+      sv[i] = sn[e % HALF];
+    } else if (e < pairs + vcount) {
+      x[i] = in[v0 + e - pairs];
+    } else if (e < total) {
+      x[i] = hin[e - pairs - vcount];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kQkvEpt; ++i) {
+    const int e = e0 + i * kQkvThreads;
+    if (e < pairs) {
+      const int head = e / HALF, j = e % HALF;
+      const float ol = x[i] * c[i] - y[i] * sv[i], oh = y[i] * c[i] + x[i] * sv[i];
       if (head < a.nq) {
-        Q[head * a.hd + j] = from_f<T>(ol);
-        Q[head * a.hd + j + half] = from_f<T>(oh);
+        Q[head * HD + j] = from_f<T>(ol);
+        Q[head * HD + j + HALF] = from_f<T>(oh);
       } else {
         const int kh = head - a.nq;
-        Ko[kh * a.hd + j] = from_f<T>(ol);
-        Ko[kh * a.hd + j + half] = from_f<T>(oh);
+        Ko[kh * HD + j] = from_f<T>(ol);
+        Ko[kh * HD + j + HALF] = from_f<T>(oh);
         if (append) {
-          T* kc = static_cast<T*>(a.kcache) + cache_row * a.nkv * a.hd;
-          kc[kh * a.hd + j] = from_f<T>(ol);
-          kc[kh * a.hd + j + half] = from_f<T>(oh);
+          T* kc = static_cast<T*>(a.kcache) + cache_row * a.nkv * HD;
+          kc[kh * HD + j] = from_f<T>(ol);
+          kc[kh * HD + j + HALF] = from_f<T>(oh);
         }
       }
     } else if (e < pairs + vcount) {
       const int ev = e - pairs;
-      const float v = (src >= 0) ? sum_parts(a.in, (size_t)src * a.in.ldo + v0 + ev) : a.mask_qkv[v0 + ev];
-      Vo[ev] = from_f<T>(v);
-      if (append) static_cast<T*>(a.vcache)[cache_row * a.nkv * a.hd + ev] = from_f<T>(v);
-    } else {
-      const int j = e - pairs - vcount;
-      a.h[(size_t)r * a.H + j] = (src >= 0) ? a.resid0[(size_t)src * a.H + j] : a.mask_resid[j];
+      Vo[ev] = from_f<T>(x[i]);
+      if (append) static_cast<T*>(a.vcache)[cache_row * a.nkv * HD + ev] = from_f<T>(x[i]);
+    } else if (e < total) {
+      a.h[(size_t)r * a.H + e - pairs - vcount] = x[i];
     }
   }
 }
@@ -724,10 +735,10 @@ static int grid_for(long long total, int threads) {
 }
 
 // Block shape of a one-row-per-block kernel: EPT columns per thread in
-// registers (4, 8 or 16). Few rows get wide blocks so each thread holds few
-// columns; many rows keep blocks near 256 threads.
-static int row_threads(int rows, int H, int* ept) {
-  const int t0 = rows >= 2 * num_sms() ? 256 : 1024;
+// registers (4, 8 or 16, the fewest that cover the row with at most 1024
+// threads), so each thread keeps all its loads in flight at once.
+static int row_threads(int /*rows*/, int H, int* ept) {
+  const int t0 = 1024;
   int e = 4;
   while (e < 16 && e * t0 < H) e *= 2;
   *ept = e;
@@ -766,9 +777,18 @@ cudaError_t launch_fc_finish(int dtype, int rows, const FcFinishArgs& a, cudaStr
 cudaError_t launch_qkv_finish(int dtype, int rows, const QkvArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int total = (a.nq + a.nkv) * (a.hd / 2) + a.nkv * a.hd + (a.h ? a.H : 0);
+  if (a.in.splits != 1) {
+    set_error("qkv_finish expects one partial slab");
+    return cudaErrorInvalidValue;
+  }
   const dim3 grid(rows, (total + kQkvChunk - 1) / kQkvChunk);
-  if (dtype == PEAGLE_BF16) launch_pdl(qkv_finish_kernel<bf16>, grid, 256, 0, st, a);
-  else launch_pdl(qkv_finish_kernel<float>, grid, 256, 0, st, a);
+  if (dtype == PEAGLE_BF16) {
+    if (a.hd == 128) launch_pdl(qkv_finish_kernel<bf16, 128>, grid, kQkvThreads, 0, st, a);
+    else launch_pdl(qkv_finish_kernel<bf16, 64>, grid, kQkvThreads, 0, st, a);
+  } else {
+    if (a.hd == 128) launch_pdl(qkv_finish_kernel<float, 128>, grid, kQkvThreads, 0, st, a);
+    else launch_pdl(qkv_finish_kernel<float, 64>, grid, kQkvThreads, 0, st, a);
+  }
   PE_LAUNCH_END();
 }
 
