@@ -673,6 +673,8 @@ struct TrainWs {
   int* sem;
   int *indices, *row_of, *anchor, *depth, *pos, *start, *label;
   void *x0, *xin, *act, *q, *kr, *vr, *ao;
+  void* vt;  // V transposed [nkv*hd, rp] for the tensor-core attention, or NULL
+  int rp;
   float *resid0, *h, *part, *row_ce;
   int* row_am;
   float *p_max, *p_sum, *p_lab;   // fused head partials of one chunk
@@ -713,6 +715,8 @@ static void train_layout(const peagle_config& c, int n, int K, int R, Bump& bp, 
   ws.kr = bp.take_bytes((size_t)R * nkv * hd * es);
   ws.vr = bp.take_bytes((size_t)R * nkv * hd * es);
   ws.ao = bp.take_bytes((size_t)R * nq * hd * es);
+  ws.rp = (R + 63) / 64 * 64;
+  ws.vt = (dt == PEAGLE_BF16 && hd == 128) ? bp.take_bytes((size_t)nkv * hd * ws.rp * es) : nullptr;
   size_t pf = chunk_part_floats(dt, n, rc, H, AHt);
   pf = std::max(pf, chunk_part_floats(dt, n, rc, QKV, 2 * H));
   pf = std::max(pf, chunk_part_floats(dt, R, rc, QKV, H));
@@ -897,11 +901,12 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
       aa.row_of = ws.row_of;
       aa.O = ws.ao;
       aa.scale = 1.0f / sqrtf((float)hd);
+      aa.Vt = ws.vt;
+      aa.Rp = ws.rp;
+      aa.status = m->status;
       TrainTileArgs tt{};
       tt.K = K;
       for (int d = 0; d <= K; ++d) tt.row_off[d] = off[d];
-      tt.tile_off[0] = 0;
-      for (int d = 0; d < K; ++d) tt.tile_off[d + 1] = tt.tile_off[d] + (counts[d] + 63) / 64;
       CUDA_TRY(launch_train_attn(dt, aa, tt, PEAGLE_OP_ATTN, s));
 
       for (int c0 = 0; c0 < R; c0 += rc) {

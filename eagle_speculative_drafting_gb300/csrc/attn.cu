@@ -748,8 +748,12 @@ __global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTile
 }
 
 template <int HD>
-static cudaError_t launch_train_mma(const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op, cudaStream_t st) {
+static cudaError_t launch_train_mma(const TrainAttnArgs& a, const TrainTileArgs& tt_in, int probe_op, cudaStream_t st) {
   using C = TrainMmaCfg<HD>;
+  TrainTileArgs tt = tt_in;
+  tt.tile_off[0] = 0;
+  for (int d = 0; d < tt.K; ++d)
+    tt.tile_off[d + 1] = tt.tile_off[d] + (tt.row_off[d + 1] - tt.row_off[d] + C::TQ - 1) / C::TQ;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(train_attn_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -776,6 +780,12 @@ static cudaError_t train_attn_t(const TrainAttnArgs& a, int probe_op, cudaStream
 cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op,
                               cudaStream_t st) {
   if (a.R <= 0) return cudaSuccess;
+  if (train_attn_tc_supported(dtype, a)) {
+    probe_start(probe_op, st);
+    cudaError_t e = launch_train_attn_tc(a, tt, st);
+    probe_stop(probe_op, st);
+    return e;
+  }
   if (dtype == PEAGLE_BF16)
     return a.hd == 128 ? launch_train_mma<128>(a, tt, probe_op, st) : launch_train_mma<64>(a, tt, probe_op, st);
   return a.hd == 128 ? train_attn_t<float, 4>(a, probe_op, st) : train_attn_t<float, 2>(a, probe_op, st);

@@ -1,0 +1,525 @@
+// Training attention of the P-EAGLE parallel forward on the 5th-generation
+// tensor cores ("feat(speculative) ... #2376": depth-0 rows see their own
+// conversation causally, a depth-d row sees the depth-0 rows of its
+// conversation up to its anchor plus its own chain rows (anchor, 1..d);
+// "P_Eagle" README: packed conversations isolated by cu_seqlens).
+//
+// One CTA = 128 consecutive rows of one depth (anchors ascending) x one
+// query head, 192 threads:
+//   warp 0     one thread loads Q once and streams 128-key tiles of K and
+//              of V transposed (V^T, so both products take K-major
+//              operands) with TMA: K into a 3-stage ring released by the
+//              score product, V^T into a 2-stage ring released by P V;
+//   warp 1     one thread issues tcgen05.mma: S = Q K^T (M = 128 rows,
+//              N = 128 keys, K = hd) into one of two TMEM score buffers,
+//              and O += P V (N = hd, K = 128 keys) into a TMEM accumulator;
+//   warps 2-5  one thread per row: read the row's scores from TMEM, mask
+//              (start(i) <= key <= anchor(i)), online softmax in exp2 units,
+//              write P (bf16) into shared memory in the 128B-swizzled
+//              K-major layout the second product reads;
+//   warps 6-9  meanwhile, one thread per row: the <= d chain keys of the
+//              row on the CUDA cores (their maximum, sum and weighted value
+//              sum, the latter in spare TMEM columns), merged at the end.
+// The reference maximum of a row is only raised when the tile maximum
+// exceeds it by more than 2^8 (then O is rescaled in TMEM); in between,
+// probabilities relative to the older maximum stay below 256.
+// Every mbarrier wait is bounded (1 s); on expiry the kernel sets
+// PEAGLE_DEV_TIMEOUT and stops.
+#include "rows.cuh"
+#include "tc.cuh"
+
+namespace pe {
+
+namespace ta {
+constexpr int TQ = 128, TK = 128, HD = 128, NK = 3, NV = 2, THREADS = 320;
+constexpr int QB = TQ * HD * 2;    // Q tile (two 64-column boxes)
+constexpr int KB = TK * HD * 2;    // K tile
+constexpr int VB = HD * TK * 2;    // V^T tile
+constexpr int PB = TQ * TK * 2;    // P tile
+constexpr int BOX = 128 * 128;     // one 64-column x 128-row box
+constexpr int SMEM = 1024 + QB + NK * KB + NV * VB + PB + 2 * TQ * 4 + 256;
+constexpr float kRescale = 8.f;    // log2 headroom before the reference max moves
+}  // namespace ta
+
+__global__ void __launch_bounds__(ta::THREADS, 1)
+    train_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, TrainAttnArgs a, TrainTileArgs tt) {
+  using namespace ta;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + QB;              // [NK][KB]
+  uint8_t* sV = sK + NK * KB;         // [NV][VB]
+  uint8_t* sP = sV + NV * VB;
+  float* sCm = reinterpret_cast<float*>(sP + PB);   // [TQ] chain maximum per row
+  float* sCl = sCm + TQ;                            // [TQ] chain sum per row
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(sCl + TQ);
+  uint64_t* kfull = qfull + 1;        // [NK]
+  uint64_t* kempty = kfull + NK;      // [NK]
+  uint64_t* vfull = kempty + NK;      // [NV]
+  uint64_t* vempty = vfull + NV;      // [NV]
+  uint64_t* sfull = vempty + NV;      // [2]
+  uint64_t* sfree = sfull + 2;        // [2]
+  uint64_t* pfull = sfree + 2;
+  uint64_t* pfree = pfull + 1;        // one completion per P V product
+  uint64_t* chfull = pfree + 1;       // chain results of every row
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(chfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(qfull, 1);
+    for (int s = 0; s < NK; ++s) {
+      tc::mbar_init(&kfull[s], 1);
+      tc::mbar_init(&kempty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      tc::mbar_init(&vfull[s], 1);
+      tc::mbar_init(&vempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&sfull[b], 1);
+      tc::mbar_init(&sfree[b], 128);
+    }
+    tc::mbar_init(pfull, 128);
+    tc::mbar_init(pfree, 1);
+    tc::mbar_init(chfull, 128);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_map(&tmQ);
+    tc::prefetch_map(&tmK);
+    tc::prefetch_map(&tmV);
+  }
+  if (warp == 1) tc::tmem_alloc(tslot, 512);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+  pdl_trigger();
+  pdl_wait();   // Q, K, V^T and the row metadata come from earlier kernels
+
+  // this CTA's rows and key range
+  const int tile = blockIdx.x, h = blockIdx.y;
+  int d = 0;
+  while (d + 1 < tt.K && tile >= tt.tile_off[d + 1]) ++d;
+  const int row0 = tt.row_off[d] + (tile - tt.tile_off[d]) * TQ;
+  const int nrows = min(TQ, tt.row_off[d + 1] - row0);
+  const int G = a.nq / a.nkv, g = h / G;
+  // conversation starts are non-decreasing in the anchor: row0 has the
+  // smallest start, the last row the largest anchor. Tiles begin on a
+  // 64-key boundary so every TMA column coordinate is 16-byte aligned.
+  const int kend = a.row_anchor[row0 + nrows - 1];
+  const int kbeg = a.row_start[row0] & ~63;
+  const int ntiles = (kend - kbeg) / TK + 1;
+  const float sl2 = a.scale * 1.4426950408889634f;
+  constexpr uint32_t idesc = tc::idesc_bf16(128, 128);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::mbar_expect_tx(qfull, QB);
+      tc::tma_load_2d(sQ, &tmQ, h * HD, row0, qfull);
+      tc::tma_load_2d(sQ + BOX, &tmQ, h * HD + 64, row0, qfull);
+      for (int t = 0; t < ntiles && !*abort_flag; ++t) {
+        const int sk = t % NK, sv = t % NV;
+        const int key0 = kbeg + t * TK;
+        if (!tc::mbar_wait(&kempty[sk], ((t / NK) & 1) ^ 1)) {
+          *abort_flag = 1;
+          set_status(a.status, PEAGLE_DEV_TIMEOUT);
+          break;
+        }
+        tc::mbar_expect_tx(&kfull[sk], KB);
+        tc::tma_load_2d(sK + sk * KB, &tmK, g * HD, key0, &kfull[sk]);
+        tc::tma_load_2d(sK + sk * KB + BOX, &tmK, g * HD + 64, key0, &kfull[sk]);
+        if (!tc::mbar_wait(&vempty[sv], ((t / NV) & 1) ^ 1)) {
+          *abort_flag = 1;
+          set_status(a.status, PEAGLE_DEV_TIMEOUT);
+          break;
+        }
+        tc::mbar_expect_tx(&vfull[sv], VB);
+        tc::tma_load_2d(sV + sv * VB, &tmV, key0, g * HD, &vfull[sv]);
+        tc::tma_load_2d(sV + sv * VB + BOX, &tmV, key0 + 64, g * HD, &vfull[sv]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t tO = tbase + 256;
+      // O += P_u V_u, then release the P buffer and the tile's stage
+      auto pv = [&](int u) -> bool {
+        const int su = u % NV;
+        if (!tc::mbar_wait(pfull, u & 1) || !tc::mbar_wait(&vfull[su], (u / NV) & 1)) return false;
+        tc::fence_after();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t a0 = tc::smem_u32(sP + i * BOX), b0 = tc::smem_u32(sV + su * VB + i * BOX);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tO, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
+                         (u > 0 || i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(pfree);
+        tc::mma_commit(&vempty[su]);
+        return true;
+      };
+      bool ok = tc::mbar_wait(qfull, 0);
+      for (int t = 0; ok && t < ntiles && !*abort_flag; ++t) {
+        const int s = t % NK, b = t & 1;
+        ok = tc::mbar_wait(&kfull[s], (t / NK) & 1) && tc::mbar_wait(&sfree[b], ((t >> 1) & 1) ^ 1);
+        if (!ok) break;
+        tc::fence_after();
+        const uint32_t tS = tbase + b * 128;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t a0 = tc::smem_u32(sQ + i * BOX), b0 = tc::smem_u32(sK + s * KB + i * BOX);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_bf16(tS, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
+                         (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&sfull[b]);
+        tc::mma_commit(&kempty[s]);
+        if (t >= 1) ok = pv(t - 1);
+      }
+      if (ok && !*abort_flag) ok = pv(ntiles - 1);
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, PEAGLE_DEV_TIMEOUT);
+      }
+    }
+  } else if (warp < 6) {
+    // ---- softmax: thread = row quad*32 + lane (TMEM lane quadrant = warp % 4)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const bool live = row < nrows;
+    const int anc = live ? a.row_anchor[row0 + row] : -1;
+    const int st = live ? a.row_start[row0 + row] : 0x7fffffff;
+    const uint32_t tl = (uint32_t)(quad * 32) << 16;
+    const uint32_t tO = tbase + 256 + tl;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sfull[b], (t >> 1) & 1)) && !*abort_flag;
+      if (!ok) break;
+      tc::fence_after();
+      float sv[TK];
+      {
+        uint32_t r[TK / 16][16];
+#pragma unroll
+        for (int c = 0; c < TK / 16; ++c) tc::tmem_ld16_nowait(tbase + tl + b * 128 + c * 16, r[c]);
+#pragma unroll
+        for (int c = 0; c < TK / 16; ++c) tc::tmem_ld_wait16(r[c]);
+#pragma unroll
+        for (int c = 0; c < TK / 16; ++c)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) sv[c * 16 + k] = __uint_as_float(r[c][k]);
+      }
+      tc::fence_before();
+      tc::mbar_arrive(&sfree[b]);   // the score buffer may be rewritten
+      // mask to the row's visible columns [lo, hi] of this tile and take the
+      // row maximum of the raw scores (the scale is positive, so it is
+      // applied to the maximum and folded into the exponent below); eight
+      // independent partial maxima keep the reduction off one dependency chain
+      const int key0 = kbeg + t * TK;
+      const int lo = max(st - key0, 0), hi = min(anc - key0, TK - 1);
+      float pm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
+      if (lo == 0 && hi == TK - 1) {   // the whole tile is visible to this row
+#pragma unroll
+        for (int c = 0; c < TK; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+      } else {
+        // hi < lo (nothing visible) leaves span negative: no column passes
+        const int span = hi - lo;
+#pragma unroll
+        for (int c = 0; c < TK; ++c) {
+          const bool vis = (unsigned)(c - lo) <= (unsigned)span && span >= 0;
+          sv[c] = vis ? sv[c] : -INFINITY;
+          pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+        }
+      }
+      const float mraw = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl2;
+      // the previous P V product must be done before P is overwritten or O
+      // rescaled
+      if (t >= 1) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(pfree, (t - 1) & 1)) && !*abort_flag;
+        if (!ok) break;
+        tc::fence_after();
+      }
+      // a row raises its reference maximum when the tile exceeds it by more
+      // than 2^8; O holds earlier tiles' products only from tile 1 on, and a
+      // row whose reference was still -inf contributed zeros, so only the
+      // others rescale (the TMEM accesses are warp-wide)
+      const bool raise = mx > m_ref + kRescale;
+      const float corr = !raise ? 1.f : (m_ref == -INFINITY ? 0.f : tc::ex2_approx(m_ref - mx));
+      const bool rescale = raise && t >= 1 && m_ref != -INFINITY;
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 16; ++c) {
+          uint32_t r[16];
+          tc::tmem_ld16(tO + c * 16, r);
+          if (rescale) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * corr);
+          }
+          tc::tmem_st16(tO + c * 16, r);
+        }
+      }
+      if (raise) {
+        l *= corr;
+        m_ref = mx;
+      }
+      // probabilities (bf16, summed as rounded) into the swizzled P rows;
+      // eight partial sums
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+      const float nref = m_ref == -INFINITY ? -INFINITY : -m_ref;   // -inf rows: every p = 0
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint8_t* prow = sP + i * BOX + row * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = i * 64 + q * 8 + e * 2;
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(tc::ex2_approx(fmaf(sv[c], sl2, nref)),
+                                                            tc::ex2_approx(fmaf(sv[c + 1], sl2, nref)));
+            const float2 pf = __bfloat1622float2(pp);
+            ps[q] += pf.x + pf.y;
+            w[e] = *reinterpret_cast<const uint32_t*>(&pp);
+          }
+          *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      tc::fence_proxy_async();
+      tc::fence_before();
+      tc::mbar_arrive(pfull);
+    }
+    // ---- chain keys, then the output row
+    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(pfree, (ntiles - 1) & 1)) && !*abort_flag;
+    if (!ok) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        set_status(a.status, PEAGLE_DEV_TIMEOUT);
+      }
+    } else {
+      tc::fence_after();
+      // merge with the chain keys' (maximum, sum, weighted value sum)
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(chfull, 0));
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          set_status(a.status, PEAGLE_DEV_TIMEOUT);
+        }
+      } else {
+        const float m_c = sCm[row], l_c = sCl[row];
+        const float m_f = fmaxf(m_ref, m_c);
+        const float so = (m_ref == -INFINITY) ? 0.f : tc::ex2_approx(m_ref - m_f);
+        const float sc = (m_c == -INFINITY) ? 0.f : tc::ex2_approx(m_c - m_f);
+        const float lf = l * so + l_c * sc;
+        const float inv = lf > 0.f ? 1.f / lf : 0.f;
+        const uint32_t tA = tbase + 384 + tl;
+        uint4* Og = reinterpret_cast<uint4*>(static_cast<bf16*>(a.O) + ((size_t)(row0 + row) * a.nq + h) * HD);
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ro[4][16], ra[4][16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tO + half * 64 + c * 16, ro[c]);
+          if (d > 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tA + half * 64 + c * 16, ra[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ra[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int k = 0; k < 16; ++k) ra[c][k] = 0u;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ro[c]);
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t w[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float x0 = (__uint_as_float(ro[c][2 * k]) * so + __uint_as_float(ra[c][2 * k]) * sc) * inv;
+                const float x1 =
+                    (__uint_as_float(ro[c][2 * k + 1]) * so + __uint_as_float(ra[c][2 * k + 1]) * sc) * inv;
+                const __nv_bfloat162 pp = __floats2bfloat162_rn(x0, x1);
+                w[k] = *reinterpret_cast<const uint32_t*>(&pp);
+              }
+              Og[half * 8 + c * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+              Og[half * 8 + c * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ---- chain keys (anchor, 1..d) of row quad*32 + lane, while the tiles
+    // run: their maximum m_c, sum l_c and value sum relative to m_c (in TMEM
+    // columns 384..511 of the row's lane)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const bool live = row < nrows;
+    const uint32_t tA = tbase + 384 + ((uint32_t)(quad * 32) << 16);
+    float m_c = -INFINITY, l_c = 0.f;
+    bool ok = true;
+    if (d > 0) {
+      const int anc = live ? a.row_anchor[row0 + row] : -1;
+      const bf16* Kg = static_cast<const bf16*>(a.Kr);
+      const bf16* Vg = static_cast<const bf16*>(a.Vr);
+      int kc[16];
+      float sc[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        kc[c] = -1;
+        if (live && c < d) {
+          const int kr = a.row_of[(size_t)(c + 1) * a.n + anc];
+          kc[c] = (kr >= 0 && kr < a.R) ? kr : -1;   // nested COD sets always provide it
+        }
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(qfull, 0));   // q is read from the Q tile
+      if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < d; ++c) {
+          sc[c] = -INFINITY;
+          if (kc[c] < 0) continue;
+          const uint4* kp = reinterpret_cast<const uint4*>(Kg + ((size_t)kc[c] * a.nkv + g) * HD);
+          uint4 kv[HD / 8];
+#pragma unroll
+          for (int e = 0; e < HD / 8; ++e) kv[e] = kp[e];
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < HD / 8; ++e) {
+            // 16-byte chunk e of the row in the swizzled Q tile
+            const uint4 qa = *reinterpret_cast<const uint4*>(sQ + (e / 8) * BOX + row * 128 +
+                                                             (((e & 7) ^ (row & 7)) << 4));
+            const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qa);
+            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv[e]);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              const float2 qf = __bfloat1622float2(q2[z]), kf = __bfloat1622float2(k2[z]);
+              dot = fmaf(qf.x, kf.x, dot);
+              dot = fmaf(qf.y, kf.y, dot);
+            }
+          }
+          sc[c] = dot * sl2;
+          m_c = fmaxf(m_c, sc[c]);
+        }
+        // value sum: the chain loop is uniform over the warp (d is the
+        // tile's depth), so every lane takes part in the TMEM accesses
+#pragma unroll 1
+        for (int c = 0; c < d; ++c) {
+          const bool has = kc[c] >= 0 && m_c != -INFINITY;
+          const float w = has ? tc::ex2_approx(sc[c] - m_c) : 0.f;
+          l_c += w;
+          uint4 vv[HD / 8];
+          if (has) {
+            const uint4* vp = reinterpret_cast<const uint4*>(Vg + ((size_t)kc[c] * a.nkv + g) * HD);
+#pragma unroll
+            for (int e = 0; e < HD / 8; ++e) vv[e] = vp[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < HD / 8; ++e) vv[e] = make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int cc = 0; cc < HD / 16; ++cc) {
+            uint32_t r[16];
+            if (c > 0) tc::tmem_ld16(tA + cc * 16, r);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vv[cc * 2 + e]);
+#pragma unroll
+              for (int z = 0; z < 4; ++z) {
+                const float2 vf = __bfloat1622float2(v2[z]);
+                const int k0 = e * 8 + 2 * z;
+                r[k0] = __float_as_uint((c > 0 ? __uint_as_float(r[k0]) : 0.f) + w * vf.x);
+                r[k0 + 1] = __float_as_uint((c > 0 ? __uint_as_float(r[k0 + 1]) : 0.f) + w * vf.y);
+              }
+            }
+            tc::tmem_st16(tA + cc * 16, r);
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        set_status(a.status, PEAGLE_DEV_TIMEOUT);
+      }
+    }
+    sCm[row] = m_c;
+    sCl[row] = l_c;
+    tc::fence_before();
+    tc::mbar_arrive(chfull);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::tmem_dealloc(tbase, 512);
+  }
+}
+
+// V [R, nkv*hd] -> V^T [nkv*hd, Rp] (bf16), 32 x 32 tiles through shared memory
+__global__ void __launch_bounds__(256) transpose_v_kernel(const bf16* __restrict__ V, int R, int C, bf16* __restrict__ Vt,
+                                                          int Rp) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ bf16 tileb[32][34];
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 8 rows per pass
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int r = r0 + ty + k, c = c0 + tx;
+    tileb[ty + k][tx] = (r < R && c < C) ? V[(size_t)r * C + c] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int c = c0 + ty + k, r = r0 + tx;
+    if (c < C && r < Rp) Vt[(size_t)c * Rp + r] = tileb[tx][ty + k];
+  }
+}
+
+bool train_attn_tc_supported(int dtype, const TrainAttnArgs& a) {
+  return dtype == PEAGLE_BF16 && a.hd == 128 && a.Vt != nullptr && a.Rp >= a.R && a.Rp % 64 == 0 &&
+         a.nq % a.nkv == 0;
+}
+
+cudaError_t launch_train_attn_tc(const TrainAttnArgs& a, const TrainTileArgs& tt_in, cudaStream_t st) {
+  using namespace ta;
+  TrainTileArgs tt = tt_in;
+  tt.tile_off[0] = 0;
+  for (int d = 0; d < tt.K; ++d) tt.tile_off[d + 1] = tt.tile_off[d] + (tt.row_off[d + 1] - tt.row_off[d] + TQ - 1) / TQ;
+  const int C = a.nkv * HD;
+  launch_pdl(transpose_v_kernel, dim3((a.Rp + 31) / 32, (C + 31) / 32), 256, 0, st,
+             static_cast<const bf16*>(a.Vr), a.R, C, static_cast<bf16*>(a.Vt), a.Rp);
+  note_launch();
+  CUtensorMap mq, mk, mv;
+  if (!make_tma_2d(&mq, a.Q, a.R, a.nq * HD, a.nq * HD, 128) ||
+      !make_tma_2d(&mk, a.Kr, a.R, C, C, 128) || !make_tma_2d(&mv, a.Vt, C, a.R, a.Rp, 128)) {
+    set_error("train attention: cuTensorMapEncodeTiled failed");
+    return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(train_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  if (tt.tile_off[tt.K] > 0) {
+    launch_pdl(train_attn_tc, dim3(tt.tile_off[tt.K], a.nq), THREADS, SMEM, st, mq, mk, mv, a, tt);
+    note_launch();
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pe

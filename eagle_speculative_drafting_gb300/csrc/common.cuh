@@ -2,6 +2,7 @@
 // the device status word, launch bookkeeping and the launchers each .cu file
 // exports to the host API (api.cu).
 #pragma once
+#include <cuda.h>
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -138,6 +139,10 @@ struct GemmEpi {
   int* p_idx;
   const int* labels;    // GEMM_EPI_CE: label per row, -1 = none
 };
+// 2-D bf16 tensor map over a [rows, cols] matrix (row stride ld elements),
+// box = 64 columns x box_rows rows, 128-byte swizzle. False if the driver
+// rejects it.
+bool make_tma_2d(CUtensorMap* map, const void* base, int rows, int cols, int ld, int box_rows);
 // Column tiles (partials per row) of the fused head epilogue.
 int gemm_col_tiles(int M, int N, int K);
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,

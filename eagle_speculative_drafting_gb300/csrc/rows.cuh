@@ -107,6 +107,9 @@ struct TrainAttnArgs {
   const int *row_anchor, *row_depth, *row_start, *row_of;  // row_of [K, n]
   void* O;
   float scale;
+  void* Vt;                  // bf16 scratch [nkv*hd, Rp] for V transposed (tensor-core path) or NULL
+  int Rp;                    // row stride of Vt: R rounded up to 64
+  int* status;
 };
 
 cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double theta, cudaStream_t st);
@@ -136,9 +139,12 @@ cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op,
 struct TrainTileArgs {
   int K;
   int row_off[17];   // depth d rows [row_off[d], row_off[d+1])
-  int tile_off[17];  // depth d tiles [tile_off[d], tile_off[d+1])
+  int tile_off[17];  // depth d tiles [tile_off[d], tile_off[d+1]) (filled by the launcher)
 };
 cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op,
                               cudaStream_t st);
+// tcgen05 training attention (bf16, hd = 128); false when it does not apply
+bool train_attn_tc_supported(int dtype, const TrainAttnArgs& a);
+cudaError_t launch_train_attn_tc(const TrainAttnArgs& a, const TrainTileArgs& tt, cudaStream_t st);
 
 }  // namespace pe

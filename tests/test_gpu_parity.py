@@ -277,6 +277,16 @@ def test_train_bf16_swapped_rows():
     check_train(wl, inp, 2, 0.7, 0.2, 8, BF16_TOL)
 
 
+@pytest.mark.parametrize("n,lens,K", [(300, (120, 7, 100, 73), 5), (300, (70, 230), 3), (100, (60, 40), 2),
+                                     (700, (300, 400), 2)])
+def test_train_bf16_hd128_tensor_core_attention(n, lens, K):
+    # head_dim 128 routes the training attention through the tcgen05 kernel:
+    # several 128-key tiles, conversation starts off the 64-key grid, chain
+    # keys up to depth 4, and one or several 128-row query tiles per depth
+    wl, inp = small_train(dtype="bf16", n=n, lens=lens, K=K, head_dim=128)
+    check_train(wl, inp, K, 0.7, 0.2, 13, BF16_TOL)
+
+
 def test_train_bf16_unfused_swiglu_width():
     # 2I not a multiple of 256: the SwiGLU runs as its own kernel
     wl, inp = small_train(dtype="bf16", n=300, lens=(120, 180), K=3, intermediate=200)
