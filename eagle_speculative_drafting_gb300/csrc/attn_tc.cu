@@ -13,11 +13,12 @@
 //   warp 1     one thread issues tcgen05.mma: S = Q K^T (M = 128 rows,
 //              N = 128 keys, K = hd) into one of two TMEM score buffers,
 //              and O += P V (N = hd, K = 128 keys) into a TMEM accumulator;
-//   warps 2-5  one thread per row: read the row's scores from TMEM, mask
-//              (start(i) <= key <= anchor(i)), online softmax in exp2 units,
-//              write P (bf16) into shared memory in the 128B-swizzled
-//              K-major layout the second product reads;
-//   warps 6-9  meanwhile, one thread per row: the <= d chain keys of the
+//   warps 2-9  two threads per row (64 columns each): read the scores from
+//              TMEM, mask (start(i) <= key <= anchor(i)), online softmax in
+//              exp2 units (the halves meet in shared memory for the row
+//              maximum), write P (bf16) into shared memory in the
+//              128B-swizzled K-major layout the second product reads;
+//   warps 10-13 meanwhile, one thread per row: the <= d chain keys of the
 //              row on the CUDA cores (their maximum, sum and weighted value
 //              sum, the latter in spare TMEM columns), merged at the end.
 // The reference maximum of a row is only raised when the tile maximum
@@ -31,13 +32,13 @@
 namespace pe {
 
 namespace ta {
-constexpr int TQ = 128, TK = 128, HD = 128, NK = 3, NV = 2, THREADS = 320;
+constexpr int TQ = 128, TK = 128, HD = 128, NK = 2, NV = 2, THREADS = 448;
 constexpr int QB = TQ * HD * 2;    // Q tile (two 64-column boxes)
 constexpr int KB = TK * HD * 2;    // K tile
 constexpr int VB = HD * TK * 2;    // V^T tile
 constexpr int PB = TQ * TK * 2;    // P tile
 constexpr int BOX = 128 * 128;     // one 64-column x 128-row box
-constexpr int SMEM = 1024 + QB + NK * KB + NV * VB + PB + 2 * TQ * 4 + 256;
+constexpr int SMEM = 1024 + QB + NK * KB + NV * VB + PB + 8 * TQ * 4 + 256;
 constexpr float kRescale = 8.f;    // log2 headroom before the reference max moves
 }  // namespace ta
 
@@ -53,7 +54,8 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   uint8_t* sP = sV + NV * VB;
   float* sCm = reinterpret_cast<float*>(sP + PB);   // [TQ] chain maximum per row
   float* sCl = sCm + TQ;                            // [TQ] chain sum per row
-  uint64_t* qfull = reinterpret_cast<uint64_t*>(sCl + TQ);
+  float* sX = sCl + TQ;                             // [2 tiles][2 halves][TQ] partial row maxima, then sums
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(sX + 4 * TQ);
   uint64_t* kfull = qfull + 1;        // [NK]
   uint64_t* kempty = kfull + NK;      // [NK]
   uint64_t* vfull = kempty + NK;      // [NV]
@@ -63,7 +65,9 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   uint64_t* pfull = sfree + 2;
   uint64_t* pfree = pfull + 1;        // one completion per P V product
   uint64_t* chfull = pfree + 1;       // chain results of every row
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(chfull + 1);
+  uint64_t* xfull = chfull + 1;       // [2] both halves' partial maxima of a tile (by parity)
+  uint64_t* lfull = xfull + 2;        // both halves' partial sums
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(lfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,11 +83,14 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&sfull[b], 1);
-      tc::mbar_init(&sfree[b], 128);
+      tc::mbar_init(&sfree[b], 256);
     }
-    tc::mbar_init(pfull, 128);
+    tc::mbar_init(pfull, 256);
     tc::mbar_init(pfree, 1);
     tc::mbar_init(chfull, 128);
+    tc::mbar_init(&xfull[0], 256);
+    tc::mbar_init(&xfull[1], 256);
+    tc::mbar_init(lfull, 256);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_map(&tmQ);
@@ -185,78 +192,98 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         set_status(a.status, PEAGLE_DEV_TIMEOUT);
       }
     }
-  } else if (warp < 6) {
-    // ---- softmax: thread = row quad*32 + lane (TMEM lane quadrant = warp % 4)
-    const int quad = warp & 3;
+  } else if (warp < 10) {
+    // ---- softmax: warp w holds row quad*32 + lane (TMEM lane quadrant =
+    // warp % 4) and columns [hf*64, hf*64 + 64) of every score tile and of O
+    const int quad = warp & 3, hf = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
     const bool live = row < nrows;
     const int anc = live ? a.row_anchor[row0 + row] : -1;
     const int st = live ? a.row_start[row0 + row] : 0x7fffffff;
     const uint32_t tl = (uint32_t)(quad * 32) << 16;
-    const uint32_t tO = tbase + 256 + tl;
+    const uint32_t tO = tbase + 256 + tl + hf * 64;
+    constexpr int HC = TK / 2;   // columns per thread
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
+    // every wait is skipped once the kernel has aborted, so a timeout never
+    // leaves the other threads waiting on this one
+    auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
+      bool ok = !*abort_flag && tc::mbar_wait(bar, par);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0 && !*abort_flag) {
+        *abort_flag = 1;
+        set_status(a.status, PEAGLE_DEV_TIMEOUT);
+      }
+      return ok;
+    };
     for (int t = 0; t < ntiles; ++t) {
       const int b = t & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sfull[b], (t >> 1) & 1)) && !*abort_flag;
-      if (!ok) break;
+      const bool have = wait(&sfull[b], (t >> 1) & 1);
       tc::fence_after();
-      float sv[TK];
-      {
-        uint32_t r[TK / 16][16];
+      float sv[HC];
+      if (have) {
+        uint32_t r[HC / 16][16];
 #pragma unroll
-        for (int c = 0; c < TK / 16; ++c) tc::tmem_ld16_nowait(tbase + tl + b * 128 + c * 16, r[c]);
+        for (int c = 0; c < HC / 16; ++c) tc::tmem_ld16_nowait(tbase + tl + b * 128 + hf * HC + c * 16, r[c]);
 #pragma unroll
-        for (int c = 0; c < TK / 16; ++c) tc::tmem_ld_wait16(r[c]);
+        for (int c = 0; c < HC / 16; ++c) tc::tmem_ld_wait16(r[c]);
 #pragma unroll
-        for (int c = 0; c < TK / 16; ++c)
+        for (int c = 0; c < HC / 16; ++c)
 #pragma unroll
           for (int k = 0; k < 16; ++k) sv[c * 16 + k] = __uint_as_float(r[c][k]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < HC; ++c) sv[c] = -INFINITY;
       }
       tc::fence_before();
       tc::mbar_arrive(&sfree[b]);   // the score buffer may be rewritten
-      // mask to the row's visible columns [lo, hi] of this tile and take the
-      // row maximum of the raw scores (the scale is positive, so it is
+      // mask to the row's visible columns [lo, hi] of this half tile and take
+      // the row maximum of the raw scores (the scale is positive, so it is
       // applied to the maximum and folded into the exponent below); eight
       // independent partial maxima keep the reduction off one dependency chain
-      const int key0 = kbeg + t * TK;
-      const int lo = max(st - key0, 0), hi = min(anc - key0, TK - 1);
+      const int key0 = kbeg + t * TK + hf * HC;
+      const int lo = max(st - key0, 0), hi = min(anc - key0, HC - 1);
       float pm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) pm[k] = -INFINITY;
-      if (lo == 0 && hi == TK - 1) {   // the whole tile is visible to this row
+      if (lo == 0 && hi == HC - 1) {   // the whole half tile is visible to this row
 #pragma unroll
-        for (int c = 0; c < TK; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
+        for (int c = 0; c < HC; ++c) pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
       } else {
         // hi < lo (nothing visible) leaves span negative: no column passes
         const int span = hi - lo;
 #pragma unroll
-        for (int c = 0; c < TK; ++c) {
+        for (int c = 0; c < HC; ++c) {
           const bool vis = (unsigned)(c - lo) <= (unsigned)span && span >= 0;
           sv[c] = vis ? sv[c] : -INFINITY;
           pm[c & 7] = fmaxf(pm[c & 7], sv[c]);
         }
       }
-      const float mraw = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                               fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      // the row maximum from both halves (slots alternate by tile parity, so
+      // a slot is rewritten only after both halves have passed the next tile)
+      float* xs = sX + b * 2 * TQ;
+      xs[hf * TQ + row] = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      tc::mbar_arrive(&xfull[b]);
+      wait(&xfull[b], (t >> 1) & 1);
+      const float mraw = fmaxf(xs[row], xs[TQ + row]);
       const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl2;
       // the previous P V product must be done before P is overwritten or O
       // rescaled
       if (t >= 1) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(pfree, (t - 1) & 1)) && !*abort_flag;
-        if (!ok) break;
+        wait(pfree, (t - 1) & 1);
         tc::fence_after();
       }
       // a row raises its reference maximum when the tile exceeds it by more
-      // than 2^8; O holds earlier tiles' products only from tile 1 on, and a
-      // row whose reference was still -inf contributed zeros, so only the
-      // others rescale (the TMEM accesses are warp-wide)
+      // than 2^8 (both halves decide alike); O holds earlier tiles' products
+      // only from tile 1 on, and a row whose reference was still -inf
+      // contributed zeros, so only the others rescale (TMEM accesses are
+      // warp-wide)
       const bool raise = mx > m_ref + kRescale;
       const float corr = !raise ? 1.f : (m_ref == -INFINITY ? 0.f : tc::ex2_approx(m_ref - mx));
       const bool rescale = raise && t >= 1 && m_ref != -INFINITY;
-      if (__any_sync(0xffffffffu, rescale)) {
+      if (__any_sync(0xffffffffu, rescale) && !*abort_flag) {
 #pragma unroll 1
-        for (int c = 0; c < HD / 16; ++c) {
+        for (int c = 0; c < HC / 16; ++c) {
           uint32_t r[16];
           tc::tmem_ld16(tO + c * 16, r);
           if (rescale) {
@@ -270,94 +297,80 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         l *= corr;
         m_ref = mx;
       }
-      // probabilities (bf16, summed as rounded) into the swizzled P rows;
-      // eight partial sums
+      // probabilities (bf16) into this half's box of the swizzled P rows,
+      // eight partial sums; a quarter of the exponentials run on the FMA pipe
       float ps[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ps[k] = 0.f;
       const float nref = m_ref == -INFINITY ? -INFINITY : -m_ref;   // -inf rows: every p = 0
+      uint8_t* prow = sP + hf * BOX + row * 128;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        uint8_t* prow = sP + i * BOX + row * 128;
+      for (int q = 0; q < 8; ++q) {
+        uint32_t w[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = i * 64 + q * 8 + e * 2;
-            const __nv_bfloat162 pp = __floats2bfloat162_rn(tc::ex2_approx(fmaf(sv[c], sl2, nref)),
-                                                            tc::ex2_approx(fmaf(sv[c + 1], sl2, nref)));
-            const float2 pf = __bfloat1622float2(pp);
-            ps[q] += pf.x + pf.y;
-            w[e] = *reinterpret_cast<const uint32_t*>(&pp);
-          }
-          *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 4; ++e) {
+          const int c = q * 8 + e * 2;
+          const float x0 = fmaf(sv[c], sl2, nref), x1 = fmaf(sv[c + 1], sl2, nref);
+          const bool poly = (q & 3) == 3;
+          const float p0 = poly ? tc::ex2_poly(x0) : tc::ex2_approx(x0);
+          const float p1 = poly ? tc::ex2_poly(x1) : tc::ex2_approx(x1);
+          ps[q] += p0 + p1;
+          const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+          w[e] = *reinterpret_cast<const uint32_t*>(&pp);
         }
+        *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       tc::fence_proxy_async();
       tc::fence_before();
       tc::mbar_arrive(pfull);
     }
-    // ---- chain keys, then the output row
-    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(pfree, (ntiles - 1) & 1)) && !*abort_flag;
-    if (!ok) {
-      if (lane == 0) {
-        *abort_flag = 1;
-        set_status(a.status, PEAGLE_DEV_TIMEOUT);
-      }
-    } else {
-      tc::fence_after();
-      // merge with the chain keys' (maximum, sum, weighted value sum)
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(chfull, 0));
-      if (!ok) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          set_status(a.status, PEAGLE_DEV_TIMEOUT);
-        }
+    // ---- the row sum from both halves, the chain keys, then the output
+    const bool done = wait(pfree, (ntiles - 1) & 1);
+    tc::fence_after();
+    sX[hf * TQ + row] = l;   // tile slots are free: every tile's maxima were read
+    tc::mbar_arrive(lfull);
+    const bool summed = wait(lfull, 0) && wait(chfull, 0);
+    if (done && summed) {
+      const float lt = sX[row] + sX[TQ + row];
+      const float m_c = sCm[row], l_c = sCl[row];
+      const float m_f = fmaxf(m_ref, m_c);
+      const float so = (m_ref == -INFINITY) ? 0.f : tc::ex2_approx(m_ref - m_f);
+      const float sc = (m_c == -INFINITY) ? 0.f : tc::ex2_approx(m_c - m_f);
+      const float lf = lt * so + l_c * sc;
+      const float inv = lf > 0.f ? 1.f / lf : 0.f;
+      const uint32_t tA = tbase + 384 + tl + hf * 64;
+      uint4* Og = reinterpret_cast<uint4*>(static_cast<bf16*>(a.O) + ((size_t)(row0 + row) * a.nq + h) * HD + hf * 64);
+      uint32_t ro[4][16], ra[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tO + c * 16, ro[c]);
+      if (d > 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tA + c * 16, ra[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ra[c]);
       } else {
-        const float m_c = sCm[row], l_c = sCl[row];
-        const float m_f = fmaxf(m_ref, m_c);
-        const float so = (m_ref == -INFINITY) ? 0.f : tc::ex2_approx(m_ref - m_f);
-        const float sc = (m_c == -INFINITY) ? 0.f : tc::ex2_approx(m_c - m_f);
-        const float lf = l * so + l_c * sc;
-        const float inv = lf > 0.f ? 1.f / lf : 0.f;
-        const uint32_t tA = tbase + 384 + tl;
-        uint4* Og = reinterpret_cast<uint4*>(static_cast<bf16*>(a.O) + ((size_t)(row0 + row) * a.nq + h) * HD);
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ro[4][16], ra[4][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tO + half * 64 + c * 16, ro[c]);
-          if (d > 0) {
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_ld16_nowait(tA + half * 64 + c * 16, ra[c]);
+          for (int k = 0; k < 16; ++k) ra[c][k] = 0u;
+      }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ra[c]);
-          } else {
+      for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ro[c]);
+      if (live) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[8];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) ra[c][k] = 0u;
+          for (int k = 0; k < 8; ++k) {
+            const float x0 = (__uint_as_float(ro[c][2 * k]) * so + __uint_as_float(ra[c][2 * k]) * sc) * inv;
+            const float x1 =
+                (__uint_as_float(ro[c][2 * k + 1]) * so + __uint_as_float(ra[c][2 * k + 1]) * sc) * inv;
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(x0, x1);
+            w[k] = *reinterpret_cast<const uint32_t*>(&pp);
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tc::tmem_ld_wait16(ro[c]);
-          if (live) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t w[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float x0 = (__uint_as_float(ro[c][2 * k]) * so + __uint_as_float(ra[c][2 * k]) * sc) * inv;
-                const float x1 =
-                    (__uint_as_float(ro[c][2 * k + 1]) * so + __uint_as_float(ra[c][2 * k + 1]) * sc) * inv;
-                const __nv_bfloat162 pp = __floats2bfloat162_rn(x0, x1);
-                w[k] = *reinterpret_cast<const uint32_t*>(&pp);
-              }
-              Og[half * 8 + c * 2] = make_uint4(w[0], w[1], w[2], w[3]);
-              Og[half * 8 + c * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-          }
+          Og[c * 2] = make_uint4(w[0], w[1], w[2], w[3]);
+          Og[c * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
     }
