@@ -179,9 +179,12 @@ __device__ void head_finish_rows(const TcArgs& g, int m_begin, int m_end, int m_
 }
 
 // Work of one persistent CTA, as segments (tile, k-tiles [kb, ke)).
-//   stream-K: the tiles x ktiles (tile, k-tile) units are cut into gridDim
-//     equal contiguous ranges, so every CTA streams the same number of
-//     k-tiles (+-1). The CTAs sharing a tile each write one partial slab:
+//   stream-K: with at least as many tiles as CTAs, every CTA ends with
+//     tiles/gridDim whole tiles of its own (no cross-CTA sum, so the
+//     kernel's last epilogues are local), and the leftover tiles come
+//     first: their (tile, k-tile) units are cut into gridDim equal
+//     contiguous ranges, so every CTA streams the same number of k-tiles
+//     (+-1). The CTAs sharing a tile each write one partial slab:
 //     slab = CTA - first CTA of the tile.
 //   split: items (tile, slice) are dealt round-robin; slice s writes slab s.
 struct Seg {
@@ -189,8 +192,9 @@ struct Seg {
 };
 
 struct Sched {
-  long long U, u, ue;
+  long long U, u, ue;   // stream-K units of the leftover tiles, this CTA's range
   int tiles, ktiles, splits, streamk, grid, cta, w;
+  int skt, dpt, dp;     // leftover tiles, whole tiles per CTA, whole tiles taken
 
   __host__ __device__ static long long begin(long long U, int G, long long c) { return c * U / G; }
   __host__ __device__ static int owner(long long u, long long U, int G) {
@@ -206,14 +210,32 @@ struct Sched {
     streamk = streamk_;
     grid = grid_;
     cta = cta_;
-    U = (long long)tiles * ktiles;
+    dpt = (streamk && tiles >= grid) ? tiles / grid : 0;
+    skt = tiles - dpt * grid;
+    // a stream-K share needs at least one unit per CTA (an empty range
+    // would count as a partial slab of its tile)
+    if (dpt > 0 && skt > 0 && (long long)skt * ktiles < grid) {
+      --dpt;
+      skt += grid;
+    }
+    dp = 0;
+    U = (long long)skt * ktiles;
     u = begin(U, grid, cta);
     ue = begin(U, grid, cta + 1);
     w = cta;
   }
   __host__ __device__ bool next(Seg& s) {
     if (streamk) {
-      if (u >= ue) return false;
+      if (u >= ue) {
+        if (dp >= dpt) return false;
+        s.tile = skt + cta * dpt + dp;
+        s.kb = 0;
+        s.ke = ktiles;
+        s.slab = 0;
+        s.nslab = 1;
+        ++dp;
+        return true;
+      }
       s.tile = (int)(u / ktiles);
       s.kb = (int)(u % ktiles);
       s.ke = (int)((long long)s.kb + (ue - u) < ktiles ? s.kb + (ue - u) : ktiles);
@@ -810,10 +832,16 @@ static Plan plan_gemm(int M, int N, int K) {
     p.streamk = 1;
     const long long U = (long long)p.tiles * p.ktiles;
     p.grid = (int)std::min<long long>(U, sms);
+    // the tiles stream-K cuts (all of them when there are fewer tiles than
+    // CTAs; see Sched)
+    Sched ref;
+    ref.init(p.tiles, p.ktiles, 1, 1, p.grid, 0);
+    const int skt = ref.skt;
+    const long long Usk = ref.U;
     int most = 1;
-    for (int t = 0; t < p.tiles; ++t) {
-      const int first = Sched::owner((long long)t * p.ktiles, U, p.grid);
-      const int last = Sched::owner((long long)t * p.ktiles + p.ktiles - 1, U, p.grid);
+    for (int t = 0; t < skt; ++t) {
+      const int first = Sched::owner((long long)t * p.ktiles, Usk, p.grid);
+      const int last = Sched::owner((long long)t * p.ktiles + p.ktiles - 1, Usk, p.grid);
       most = std::max(most, last - first + 1);
     }
     p.splits = most;

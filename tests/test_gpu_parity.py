@@ -42,7 +42,10 @@ def pe():
 # ------------------------------------------------------------------ GEMM
 GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17, 1000, 256),
                (64, 4096, 4096), (100, 1000, 2048), (256, 512, 256), (257, 640, 512),
-               (512, 4096, 1024), (1000, 300, 200), (333, 32000, 128)]
+               (512, 4096, 1024), (1000, 300, 200), (333, 32000, 128),
+               # swapped with at least as many tiles as SMs: whole tiles per CTA
+               # after the stream-K share of the leftover tiles
+               (4, 32000, 256), (16, 20480, 512), (2, 39040, 1040)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
