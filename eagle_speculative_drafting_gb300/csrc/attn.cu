@@ -240,27 +240,33 @@ template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 }  // namespace mm
 
-template <int MT, int HD>
+// NW warps: warp w scores keys [w*KW, (w+1)*KW) of each 64-key tile for
+// every row and owns head dims [w*DW, (w+1)*DW) of the P V product. Eight
+// warps (8 keys, 16 dims each) pay off only for a single 16-row block,
+// where the kernel is latency bound; larger row blocks use four.
+template <int MT, int HD, int NW>
 struct MmaAttnCfg {
-  static constexpr int QR = 16 * MT, TK = 64, LDS = HD + 8, LDP = TK + 8;
-  static constexpr int SMEM = (QR * LDS + 4 * TK * LDS + QR * LDP) * 2 + 2 * 4 * QR * 4;
+  static constexpr int THREADS = 32 * NW;
+  static constexpr int QR = 16 * MT, TK = 64, KW = TK / NW, NK8 = KW / 8, DW = HD / NW, NP = DW / 16;
+  static constexpr int LDS = HD + 8, LDP = TK + 8;
+  static constexpr int SMEM = (QR * LDS + 4 * TK * LDS + QR * LDP) * 2 + 2 * NW * QR * 4;
 };
 
-template <int MT, int HD>
-__global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
+template <int MT, int HD, int NW>
+__global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_mma(DecodeAttnArgs a) {
   pdl_trigger();
   pdl_wait();
-  using C = MmaAttnCfg<MT, HD>;
-  constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP;
-  constexpr int DW = HD / 4;          // head dims per warp in the PV product
-  constexpr int NTO = DW / 8;         // n-tiles of 8 dims per warp
+  using C = MmaAttnCfg<MT, HD, NW>;
+  constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP, KW = C::KW, NK8 = C::NK8, DW = C::DW;
+  constexpr int NP = C::NP, NT = C::THREADS;
+  static_assert((NK8 == 1 || NK8 == 2) && NP >= 1 && DW == 16 * NP, "8 or 16 keys and 16k dims per warp");
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
   bf16* sK = sQ + QR * LDS;           // [2][TK][LDS]
   bf16* sV = sK + 2 * TK * LDS;       // [2][TK][LDS]
   bf16* sP = sV + 2 * TK * LDS;       // [QR][LDP]
-  float* sMax = reinterpret_cast<float*>(sP + QR * LDP);  // [4][QR]
-  float* sSum = sMax + 4 * QR;                             // [4][QR]
+  float* sMax = reinterpret_cast<float*>(sP + QR * LDP);  // [NW][QR]
+  float* sSum = sMax + NW * QR;                            // [NW][QR]
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.nq / a.nkv, KG = a.K * G;
@@ -278,19 +284,9 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
   const bf16* vc = static_cast<const bf16*>(a.vcache);
   const bf16* Q = static_cast<const bf16*>(a.Q);
 
-  // queries of this KV head: row qi = d*G + (h % G)
-  for (int e = tid; e < QR * (HD / 8); e += 128) {
-    const int qi = e / (HD / 8), c8 = e % (HD / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (qi < KG) {
-      const int r = b * a.K + qi / G, h = g * G + qi % G;
-      v = *reinterpret_cast<const uint4*>(Q + ((size_t)r * a.nq + h) * HD + c8 * 8);
-    }
-    *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
-  }
   auto load_tile = [&](int t, int buf) {
     const int base = k0 + t * TK;
-    for (int e = tid; e < TK * (HD / 8); e += 128) {
+    for (int e = tid; e < TK * (HD / 8); e += NT) {
       const int kr = e / (HD / 8), c8 = e % (HD / 8);
       const int key = base + kr;
       const bool in = key < k1;
@@ -299,18 +295,29 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
       mm::cp16(mm::sa(sV + (buf * TK + kr) * LDS + c8 * 8), vc + src, in ? 16 : 0);
     }
   };
+  // the first tile's keys stream while the queries are staged
   if (ntiles > 0) load_tile(0, 0);
   mm::cp_commit();
+  // queries of this KV head: row qi = d*G + (h % G)
+  for (int e = tid; e < QR * (HD / 8); e += NT) {
+    const int qi = e / (HD / 8), c8 = e % (HD / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (qi < KG) {
+      const int r = b * a.K + qi / G, h = g * G + qi % G;
+      v = *reinterpret_cast<const uint4*>(Q + ((size_t)r * a.nq + h) * HD + c8 * 8);
+    }
+    *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
+  }
 
   const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
   float m_run[MT][2], l_run[MT][2];
-  float O[MT][NTO][4];
+  float O[MT][2 * NP][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     m_run[mt][0] = m_run[mt][1] = -INFINITY;
     l_run[mt][0] = l_run[mt][1] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NTO; ++nt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
+    for (int nt = 0; nt < 2 * NP; ++nt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
   }
 
   for (int t = 0; t < ntiles; ++t) {
@@ -325,33 +332,50 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
     __syncthreads();
     const bf16* tK = sK + buf * TK * LDS;
     const bf16* tV = sV + buf * TK * LDS;
-    // ---- S = Q K^T for keys 16w..16w+15
-    float S[MT][2][4];
+    // ---- S = Q K^T for keys w*KW .. w*KW + KW - 1
+    float S[MT][NK8][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+      for (int nt = 0; nt < NK8; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+    if constexpr (NK8 == 2) {
 #pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-      uint32_t bk[4];
-      mm::ldsm4(bk, mm::sa(tK + (16 * w + (lane >> 4) * 8 + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8));
+      for (int ks = 0; ks < HD / 16; ++ks) {
+        uint32_t bk[4];   // keys (2 x 8) x 16 dims
+        mm::ldsm4(bk, mm::sa(tK + (KW * w + (lane >> 4) * 8 + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8));
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t aq[4];
-        mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
-        mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
-        mm::mma16816(S[mt][1], aq, bk[2], bk[3]);
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t aq[4];
+          mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+          mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
+          mm::mma16816(S[mt][NK8 - 1], aq, bk[2], bk[3]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kp = 0; kp < HD / 32; ++kp) {
+        uint32_t bk[4];   // 8 keys x (2 x 16) dims
+        mm::ldsm4(bk, mm::sa(tK + (KW * w + (lane & 7)) * LDS + kp * 32 + (lane >> 3) * 8));
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            uint32_t aq[4];
+            mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + kp * 32 + h2 * 16 + (lane >> 4) * 8));
+            mm::mma16816(S[mt][0], aq, bk[2 * h2], bk[2 * h2 + 1]);
+          }
+        }
       }
     }
-    // ---- scale, mask the tail, per-row maxima of this warp's 16 keys
-    const int kbase = k0 + t * TK + 16 * w + (lane & 3) * 2;
+    // ---- scale, mask the tail, per-row maxima of this warp's keys
+    const int kbase = k0 + t * TK + KW * w + (lane & 3) * 2;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NK8; ++nt)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const int key = kbase + nt * 8 + c;
@@ -373,16 +397,18 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int row = mt * 16 + hf * 8 + (lane >> 2);
-        const float tmax = fmaxf(fmaxf(sMax[row], sMax[QR + row]), fmaxf(sMax[2 * QR + row], sMax[3 * QR + row]));
+        float tmax = sMax[row];
+#pragma unroll
+        for (int q = 1; q < NW; ++q) tmax = fmaxf(tmax, sMax[q * QR + row]);
         const float mn = fmaxf(m_run[mt][hf], tmax);
         corr[mt][hf] = (mn == -INFINITY) ? 1.f : exp2f(m_run[mt][hf] - mn);
         float sum = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < NK8; ++nt) {
           float p0 = (mn == -INFINITY) ? 0.f : exp2f(S[mt][nt][hf * 2] - mn);
           float p1 = (mn == -INFINITY) ? 0.f : exp2f(S[mt][nt][hf * 2 + 1] - mn);
           const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-          *reinterpret_cast<__nv_bfloat162*>(sP + row * LDP + 16 * w + nt * 8 + (lane & 3) * 2) = pp;
+          *reinterpret_cast<__nv_bfloat162*>(sP + row * LDP + KW * w + nt * 8 + (lane & 3) * 2) = pp;
           sum += __low2float(pp) + __high2float(pp);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -397,9 +423,12 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int row = mt * 16 + hf * 8 + (lane >> 2);
-        l_run[mt][hf] = l_run[mt][hf] * corr[mt][hf] + (sSum[row] + sSum[QR + row] + sSum[2 * QR + row] + sSum[3 * QR + row]);
+        float ts = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NTO; ++nt) {
+        for (int q = 0; q < NW; ++q) ts += sSum[q * QR + row];
+        l_run[mt][hf] = l_run[mt][hf] * corr[mt][hf] + ts;
+#pragma unroll
+        for (int nt = 0; nt < 2 * NP; ++nt) {
           O[mt][nt][hf * 2] *= corr[mt][hf];
           O[mt][nt][hf * 2 + 1] *= corr[mt][hf];
         }
@@ -412,7 +441,7 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
       for (int mt = 0; mt < MT; ++mt)
         mm::ldsm4(ap[mt], mm::sa(sP + (mt * 16 + (lane & 15)) * LDP + ks * 16 + (lane >> 4) * 8));
 #pragma unroll
-      for (int np = 0; np < NTO / 2; ++np) {
+      for (int np = 0; np < NP; ++np) {
         uint32_t bv[4];
         mm::ldsm4t(bv, mm::sa(tV + (ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + w * DW + np * 16 +
                                   (lane >> 4) * 8));
@@ -435,7 +464,7 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
       if (row >= KG) continue;
       float* po = a.part_o + (prow + row) * HD + w * DW + (lane & 3) * 2;
 #pragma unroll
-      for (int nt = 0; nt < NTO; ++nt)
+      for (int nt = 0; nt < 2 * NP; ++nt)
         *reinterpret_cast<float2*>(po + nt * 8) = make_float2(O[mt][nt][hf * 2], O[mt][nt][hf * 2 + 1]);
       if (w == 0 && (lane & 3) == 0) {
         a.part_ml[(prow + row) * 2 + 0] = m_run[mt][hf] * 0.6931471805599453f;
@@ -444,23 +473,24 @@ __global__ void __launch_bounds__(128) decode_split_mma(DecodeAttnArgs a) {
     }
 }
 
-template <int MT, int HD>
+template <int MT, int HD, int NW = 4>
 static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
-  using C = MmaAttnCfg<MT, HD>;
+  using C = MmaAttnCfg<MT, HD, NW>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_mma<MT, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_split_mma<MT, HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  launch_pdl(decode_split_mma<MT, HD>, dim3(a.nsplit, a.nkv, a.B), 128, C::SMEM, st, a);
+  launch_pdl(decode_split_mma<MT, HD, NW>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
   return cudaGetLastError();
 }
 
 template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
   const int KG = a.K * (a.nq / a.nkv);
-  if (KG <= 16) return launch_split_mma<1, HD>(a, st);
+  if (KG <= 16) return launch_split_mma<1, HD, HD / 16>(a, st);
   if (KG <= 32) return launch_split_mma<2, HD>(a, st);
   if (KG <= 64) return launch_split_mma<4, HD>(a, st);
   return launch_split_mma<8, HD>(a, st);
