@@ -244,27 +244,35 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 // every row and owns head dims [w*DW, (w+1)*DW) of the P V product. Eight
 // warps (8 keys, 16 dims each) pay off only for a single 16-row block,
 // where the kernel is latency bound; larger row blocks use four.
-template <int MT, int HD, int NW>
+// K and V tiles rotate through NS stages; their rows are unpadded with the
+// 16-byte chunks of row r XOR-swizzled by r & 7 (conflict-free ldmatrix),
+// so three stages of two 32-row-block CTAs still fit one SM.
+template <int MT, int HD, int NW, int NS>
 struct MmaAttnCfg {
   static constexpr int THREADS = 32 * NW;
   static constexpr int QR = 16 * MT, TK = 64, KW = TK / NW, NK8 = KW / 8, DW = HD / NW, NP = DW / 16;
   static constexpr int LDS = HD + 8, LDP = TK + 8;
-  static constexpr int SMEM = (QR * LDS + 4 * TK * LDS + QR * LDP) * 2 + 2 * NW * QR * 4;
+  static constexpr int SMEM = (QR * LDS + 2 * NS * TK * HD + QR * LDP) * 2 + 2 * NW * QR * 4;
 };
+// element offset of (row, 16-byte chunk c8) in a swizzled K/V tile
+template <int HD>
+__device__ __forceinline__ int kv_sw(int row, int c8) {
+  return row * HD + ((c8 ^ (row & 7)) << 3);
+}
 
-template <int MT, int HD, int NW>
-__global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_mma(DecodeAttnArgs a) {
+template <int MT, int HD, int NW, int NS>
+__global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_split_mma(DecodeAttnArgs a) {
   pdl_trigger();
   pdl_wait();
-  using C = MmaAttnCfg<MT, HD, NW>;
+  using C = MmaAttnCfg<MT, HD, NW, NS>;
   constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, LDP = C::LDP, KW = C::KW, NK8 = C::NK8, DW = C::DW;
   constexpr int NP = C::NP, NT = C::THREADS;
   static_assert((NK8 == 1 || NK8 == 2) && NP >= 1 && DW == 16 * NP, "8 or 16 keys and 16k dims per warp");
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
-  bf16* sK = sQ + QR * LDS;           // [2][TK][LDS]
-  bf16* sV = sK + 2 * TK * LDS;       // [2][TK][LDS]
-  bf16* sP = sV + 2 * TK * LDS;       // [QR][LDP]
+  bf16* sK = sQ + QR * LDS;           // [NS][TK][HD] swizzled
+  bf16* sV = sK + NS * TK * HD;       // [NS][TK][HD] swizzled
+  bf16* sP = sV + NS * TK * HD;       // [QR][LDP]
   float* sMax = reinterpret_cast<float*>(sP + QR * LDP);  // [NW][QR]
   float* sSum = sMax + NW * QR;                            // [NW][QR]
 
@@ -291,13 +299,17 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
       const int key = base + kr;
       const bool in = key < k1;
       const size_t src = ((size_t)(off + (in ? key : k0)) * a.nkv + g) * HD + c8 * 8;
-      mm::cp16(mm::sa(sK + (buf * TK + kr) * LDS + c8 * 8), kc + src, in ? 16 : 0);
-      mm::cp16(mm::sa(sV + (buf * TK + kr) * LDS + c8 * 8), vc + src, in ? 16 : 0);
+      mm::cp16(mm::sa(sK + buf * TK * HD + kv_sw<HD>(kr, c8)), kc + src, in ? 16 : 0);
+      mm::cp16(mm::sa(sV + buf * TK * HD + kv_sw<HD>(kr, c8)), vc + src, in ? 16 : 0);
     }
   };
-  // the first tile's keys stream while the queries are staged
-  if (ntiles > 0) load_tile(0, 0);
-  mm::cp_commit();
+  // the first tiles' keys stream while the queries are staged (one commit
+  // group per stage, empty groups included, so the waits below count tiles)
+#pragma unroll
+  for (int q = 0; q < NS - 1; ++q) {
+    if (q < ntiles) load_tile(q, q);
+    mm::cp_commit();
+  }
   // queries of this KV head: row qi = d*G + (h % G)
   for (int e = tid; e < QR * (HD / 8); e += NT) {
     const int qi = e / (HD / 8), c8 = e % (HD / 8);
@@ -321,17 +333,15 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
   }
 
   for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(t + 1, buf ^ 1);
-      mm::cp_commit();
-      mm::cp_wait<1>();
-    } else {
-      mm::cp_wait<0>();
-    }
+    const int buf = t % NS;
+    // tile t + NS - 1 goes to the stage tile t - 1 used (free since the
+    // barrier that ended the previous iteration)
+    if (t + NS - 1 < ntiles) load_tile(t + NS - 1, (t + NS - 1) % NS);
+    mm::cp_commit();
+    mm::cp_wait<NS - 1>();
     __syncthreads();
-    const bf16* tK = sK + buf * TK * LDS;
-    const bf16* tV = sV + buf * TK * LDS;
+    const bf16* tK = sK + buf * TK * HD;
+    const bf16* tV = sV + buf * TK * HD;
     // ---- S = Q K^T for keys w*KW .. w*KW + KW - 1
     float S[MT][NK8][4];
 #pragma unroll
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
         uint32_t bk[4];   // keys (2 x 8) x 16 dims
-        mm::ldsm4(bk, mm::sa(tK + (KW * w + (lane >> 4) * 8 + (lane & 7)) * LDS + ks * 16 + ((lane >> 3) & 1) * 8));
+        mm::ldsm4(bk, mm::sa(tK + kv_sw<HD>(KW * w + (lane >> 4) * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1))));
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t aq[4];
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
 #pragma unroll
       for (int kp = 0; kp < HD / 32; ++kp) {
         uint32_t bk[4];   // 8 keys x (2 x 16) dims
-        mm::ldsm4(bk, mm::sa(tK + (KW * w + (lane & 7)) * LDS + kp * 32 + (lane >> 3) * 8));
+        mm::ldsm4(bk, mm::sa(tK + kv_sw<HD>(KW * w + (lane & 7), kp * 4 + (lane >> 3))));
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
@@ -443,8 +453,8 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
 #pragma unroll
       for (int np = 0; np < NP; ++np) {
         uint32_t bv[4];
-        mm::ldsm4t(bv, mm::sa(tV + (ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + w * DW + np * 16 +
-                                  (lane >> 4) * 8));
+        mm::ldsm4t(bv, mm::sa(tV + kv_sw<HD>(ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8,
+                                             (w * DW + np * 16) / 8 + (lane >> 4))));
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           mm::mma16816(O[mt][2 * np], ap[mt], bv[0], bv[1]);
@@ -473,17 +483,17 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW>::THREADS) decode_split_
     }
 }
 
-template <int MT, int HD, int NW = 4>
+template <int MT, int HD, int NW = 4, int NS = 2>
 static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
-  using C = MmaAttnCfg<MT, HD, NW>;
+  using C = MmaAttnCfg<MT, HD, NW, NS>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_split_mma<MT, HD, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(decode_split_mma<MT, HD, NW, NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  launch_pdl(decode_split_mma<MT, HD, NW>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
+  launch_pdl(decode_split_mma<MT, HD, NW, NS>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
   return cudaGetLastError();
 }
 
@@ -491,7 +501,7 @@ template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
   const int KG = a.K * (a.nq / a.nkv);
   if (KG <= 16) return launch_split_mma<1, HD, HD / 16>(a, st);
-  if (KG <= 32) return launch_split_mma<2, HD>(a, st);
+  if (KG <= 32) return launch_split_mma<2, HD, 4, 3>(a, st);
   if (KG <= 64) return launch_split_mma<4, HD>(a, st);
   return launch_split_mma<8, HD>(a, st);
 }
