@@ -500,7 +500,7 @@ static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
 template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
   const int KG = a.K * (a.nq / a.nkv);
-  if (KG <= 16) return launch_split_mma<1, HD, HD / 16>(a, st);
+  if (KG <= 16) return launch_split_mma<1, HD, HD / 16, 3>(a, st);
   if (KG <= 32) return launch_split_mma<2, HD, 4, 3>(a, st);
   if (KG <= 64) return launch_split_mma<4, HD>(a, st);
   return launch_split_mma<8, HD>(a, st);
