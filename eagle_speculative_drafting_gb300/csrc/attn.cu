@@ -320,6 +320,25 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
     }
     *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
   }
+  // up to two row blocks keep their query fragments in registers
+  constexpr bool QREG = MT <= 2;
+  uint32_t qf[QREG ? MT : 1][HD / 16][4];
+  if constexpr (QREG) {
+    __syncthreads();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks)
+        mm::ldsm4(qf[mt][ks], mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+  }
+  auto qfrag = [&](int mt, int ks, uint32_t(&aq)[4]) {
+    if constexpr (QREG) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) aq[i] = qf[mt][ks][i];
+    } else {
+      mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+    }
+  };
 
   const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
   float m_run[MT][2], l_run[MT][2];
@@ -342,12 +361,17 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
     __syncthreads();
     const bf16* tK = sK + buf * TK * HD;
     const bf16* tV = sV + buf * TK * HD;
-    // ---- S = Q K^T for keys w*KW .. w*KW + KW - 1
-    float S[MT][NK8][4];
+    // ---- S = Q K^T for keys w*KW .. w*KW + KW - 1; with up to two row
+    // blocks, even and odd 16-dim steps accumulate separately (twice the
+    // independent MMA chains)
+    constexpr bool SPLIT = MT <= 2;
+    float S[MT][NK8][4], S2[MT][NK8][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NK8; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+      for (int nt = 0; nt < NK8; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[mt][nt][i] = S2[mt][nt][i] = 0.f;
     if constexpr (NK8 == 2) {
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
@@ -356,9 +380,10 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t aq[4];
-          mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
-          mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
-          mm::mma16816(S[mt][NK8 - 1], aq, bk[2], bk[3]);
+          qfrag(mt, ks, aq);
+          float(&acc)[NK8][4] = (SPLIT && (ks & 1)) ? S2[mt] : S[mt];
+          mm::mma16816(acc[0], aq, bk[0], bk[1]);
+          mm::mma16816(acc[NK8 - 1], aq, bk[2], bk[3]);
         }
       }
     } else {
@@ -371,11 +396,20 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             uint32_t aq[4];
-            mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + kp * 32 + h2 * 16 + (lane >> 4) * 8));
-            mm::mma16816(S[mt][0], aq, bk[2 * h2], bk[2 * h2 + 1]);
+            qfrag(mt, kp * 2 + h2, aq);
+            float(&acc)[NK8][4] = (SPLIT && h2) ? S2[mt] : S[mt];
+            mm::mma16816(acc[0], aq, bk[2 * h2], bk[2 * h2 + 1]);
           }
         }
       }
+    }
+    if constexpr (SPLIT) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NK8; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) S[mt][nt][i] += S2[mt][nt][i];
     }
     // ---- scale, mask the tail, per-row maxima of this warp's keys
     const int kbase = k0 + t * TK + KW * w + (lane & 3) * 2;
