@@ -166,7 +166,9 @@ def test_decode_tiny_f32():
 
 @pytest.mark.parametrize("kw", [dict(), dict(batch=80, K=3), dict(num_layers=1, K=1),
                                 dict(kv_len_range=(0, 0)), dict(batch=1, K=16, kv_len_range=(700, 700)),
-                                dict(intermediate=200)])
+                                dict(intermediate=200),
+                                # head tiles whole in one CTA (register argmax path), mixed with split ones
+                                dict(vocab=24000, batch=2, K=8), dict(vocab=40000, hidden=512, batch=1)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
