@@ -624,7 +624,53 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*s_last) {
           __threadfence();
-          if (SWAP) {
+          const bool vec = SWAP && (g.N & 3) == 0 && (g.ldo & 3) == 0 && (g.split_stride & 3) == 0 &&
+                           (reinterpret_cast<uintptr_t>(g.out) & 15) == 0;
+          if (vec) {
+            // warp w of the epilogue sums rows w, w + 4, ... of the tile;
+            // lanes take 4 consecutive columns each (float4). Four rows of
+            // four slabs are in flight per thread before any of their sums
+            // is stored (slab 0 is read and rewritten by the same thread).
+            const int m0 = tb * BN, mc = min(BN, g.M - m0);
+            const int et = threadIdx.x - 64, rg = et >> 5;
+            const int n0 = ta * 128 + (et & 31) * 4;
+            if (n0 < g.N) {
+              constexpr int RB = 4;
+              for (int r0 = rg; r0 < mc; r0 += 4 * RB) {
+                float4 acc[RB];
+#pragma unroll
+                for (int i = 0; i < RB; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q0 = 0; q0 < sg.nslab; q0 += 4) {
+                  float4 t[4][RB];
+#pragma unroll
+                  for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+                    for (int i = 0; i < RB; ++i) {
+                      const int m = r0 + 4 * i;
+                      t[qi][i] = (q0 + qi < sg.nslab && m < mc)
+                                     ? __ldcg(reinterpret_cast<const float4*>(
+                                           g.out + (size_t)(q0 + qi) * g.split_stride + (size_t)(m0 + m) * g.ldo + n0))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                  for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+                    for (int i = 0; i < RB; ++i)
+                      if (q0 + qi < sg.nslab) {
+                        acc[i].x += t[qi][i].x;
+                        acc[i].y += t[qi][i].y;
+                        acc[i].z += t[qi][i].z;
+                        acc[i].w += t[qi][i].w;
+                      }
+                }
+#pragma unroll
+                for (int i = 0; i < RB; ++i) {
+                  const int m = r0 + 4 * i;
+                  if (m < mc) *reinterpret_cast<float4*>(g.out + (size_t)(m0 + m) * g.ldo + n0) = acc[i];
+                }
+              }
+            }
+          } else if (SWAP) {
             const int n = arow, m0 = tb * BN, mc = min(BN, g.M - m0);
             if (n < g.N) {
               for (int c0 = 0; c0 < mc; c0 += 8) {

@@ -45,7 +45,9 @@ GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17,
                (512, 4096, 1024), (1000, 300, 200), (333, 32000, 128),
                # swapped with at least as many tiles as SMs: whole tiles per CTA
                # after the stream-K share of the leftover tiles
-               (4, 32000, 256), (16, 20480, 512), (2, 39040, 1040)]
+               (4, 32000, 256), (16, 20480, 512), (2, 39040, 1040),
+               # wide tiles, ragged in every dimension, several rounds
+               (300, 40000, 320), (512, 32000, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -168,7 +170,9 @@ def test_decode_tiny_f32():
                                 dict(kv_len_range=(0, 0)), dict(batch=1, K=16, kv_len_range=(700, 700)),
                                 dict(intermediate=200),
                                 # head tiles whole in one CTA (register argmax path), mixed with split ones
-                                dict(vocab=24000, batch=2, K=8), dict(vocab=40000, hidden=512, batch=1)])
+                                dict(vocab=24000, batch=2, K=8), dict(vocab=40000, hidden=512, batch=1),
+                                # 320 rows: wide head tiles with the fused argmax
+                                dict(vocab=40000, batch=40, K=8)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
