@@ -172,7 +172,13 @@ def test_decode_tiny_f32():
                                 # head tiles whole in one CTA (register argmax path), mixed with split ones
                                 dict(vocab=24000, batch=2, K=8), dict(vocab=40000, hidden=512, batch=1),
                                 # 320 rows: wide head tiles with the fused argmax
-                                dict(vocab=40000, batch=40, K=8)])
+                                dict(vocab=40000, batch=40, K=8),
+                                # head dim 128, chunks of 512-1024 keys (32 and 6 query rows per
+                                # KV head, chunks past the context end, ragged last tiles)
+                                dict(head_dim=128, num_q_heads=8, num_kv_heads=2, hidden=1024, batch=12, K=8,
+                                     kv_len_range=(0, 4000), max_position=8192),
+                                dict(head_dim=128, num_q_heads=4, num_kv_heads=2, hidden=512, batch=9, K=3,
+                                     kv_len_range=(200, 2600), max_position=8192)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
