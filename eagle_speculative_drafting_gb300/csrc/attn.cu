@@ -97,11 +97,15 @@ __device__ void combine_row(const DecodeAttnArgs& a, int r, int h, int lane) {
   const int b = r / a.K, d = r % a.K;
   const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
   const int g = h / G, qi = d * G + h % G;
-  const int ns = a.nsplit;
+  // only the chunks that hold context keys of request b carry partials
+  const long long off = a.kv_off[b];
+  int L = a.kv_len[b];
+  if (!(L >= 0 && L <= a.max_kv_len && off >= 0 && off + L <= a.kv_off[b + 1] && off + L <= a.kv_cap)) L = 0;
+  const int ns = min(a.nsplit, (L + a.chunk - 1) / a.chunk);
   const T* Q = static_cast<const T*>(a.Q);
   const T* Kc = static_cast<const T*>(a.Kc);
   const T* Vc = static_cast<const T*>(a.Vc);
-  const size_t prow = (size_t)(b * a.nkv + g) * ns * KG;
+  const size_t prow = (size_t)(b * a.nkv + g) * a.nsplit * KG;
   auto ml = [&](int s) { return a.part_ml + (prow + (size_t)s * KG + qi) * 2; };
   auto po_at = [&](int s) { return a.part_o + (prow + (size_t)s * KG + qi) * hd + lane * E; };
   auto kv_at = [&](int j) { return ((size_t)(b * a.K + j) * a.nkv + g) * hd + lane * E; };
@@ -288,6 +292,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
   }
   const int k0 = split * a.chunk, k1 = min(L, k0 + a.chunk);
   const int ntiles = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
+  if (ntiles == 0) return;   // a chunk past the context end: the merge skips it
   const bf16* kc = static_cast<const bf16*>(a.kcache);
   const bf16* vc = static_cast<const bf16*>(a.vcache);
   const bf16* Q = static_cast<const bf16*>(a.Q);
