@@ -209,6 +209,29 @@ def test_decode_f32_multilayer_gqa_append():
             assert H().max_abs_rel(vc[row], rv) <= F32_TOL
 
 
+@pytest.mark.parametrize("kw", [dict(batch=2, K=4), dict(batch=1, K=3, head_dim=128, hidden=512)])
+def test_decode_bf16_few_rows_append(kw):
+    # few bf16 decode rows over two layers: rotary q/k, the anchor rows'
+    # k/v appended to their context slots, the layer-0 residual seed
+    wl = small_bf16_decode(kv_len_range=(1, 40), **kw)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    got = H().run_decode(wl, model, inp, want_logits=True, append=True)
+    ref = H().oracle_decode(wl, W, inp, append=True)
+    check_decode(wl, got, ref, BF16_TOL)
+    d = got["dev"]
+    for l in range(wl.num_layers):
+        kc = d["k_cache"][l].float().cpu().numpy()
+        vc = d["v_cache"][l].float().cpu().numpy()
+        for b in range(wl.batch):
+            row = int(inp["kv_offsets"][b] + inp["kv_lens"][b])
+            rk, rv = ref["appended"][l][b]
+            assert H().max_abs_rel(kc[row], rk) <= BF16_TOL
+            assert H().max_abs_rel(vc[row], rv) <= BF16_TOL
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
 def test_decode_prefix_consistency_on_gpu():
     wl = small_bf16_decode(dtype="f32", batch=2)
     W = synth.make_weights(wl)
