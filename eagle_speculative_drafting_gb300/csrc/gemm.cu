@@ -624,9 +624,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (*s_last) {
           __threadfence();
-          const bool vec = SWAP && (g.N & 3) == 0 && (g.ldo & 3) == 0 && (g.split_stride & 3) == 0 &&
+          const bool al4 = (g.N & 3) == 0 && (g.ldo & 3) == 0 && (g.split_stride & 3) == 0 &&
                            (reinterpret_cast<uintptr_t>(g.out) & 15) == 0;
-          if (vec) {
+          if (SWAP && al4) {
             // warp w of the epilogue sums rows w, w + 4, ... of the tile;
             // lanes take 4 consecutive columns each (float4). Four rows of
             // four slabs are in flight per thread before any of their sums
@@ -688,6 +688,56 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int c = 0; c < 8; ++c)
                   if (c0 + c < mc) g.out[(size_t)(m0 + c0 + c) * g.ldo + n] = acc[c];
               }
+            }
+          } else if (!SWAP && al4) {
+            // warp sums its 32 rows, four at a time; lanes take float4
+            // columns lane*4 + 128j. Four rows of two slabs are in flight
+            // per thread before any of their sums is stored.
+            constexpr int NV = BN >= 128 ? BN / 128 : 1;
+            constexpr int RB = 4;
+            const int n0 = tb * BN;
+            for (int r0 = 0; r0 < 32; r0 += RB) {
+              const int mb = ta * 128 + quad * 32 + r0;
+              if (mb >= g.M) break;
+              float4 acc[RB][NV];
+#pragma unroll
+              for (int i = 0; i < RB; ++i)
+#pragma unroll
+                for (int jv = 0; jv < NV; ++jv) acc[i][jv] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int q0 = 0; q0 < sg.nslab; q0 += 2) {
+                float4 t[2][RB][NV];
+#pragma unroll
+                for (int qi = 0; qi < 2; ++qi)
+#pragma unroll
+                  for (int i = 0; i < RB; ++i)
+#pragma unroll
+                    for (int jv = 0; jv < NV; ++jv) {
+                      const int m = mb + i, n = n0 + jv * 128 + lane * 4;
+                      t[qi][i][jv] = (q0 + qi < sg.nslab && m < g.M && n < g.N)
+                                         ? __ldcg(reinterpret_cast<const float4*>(
+                                               g.out + (size_t)(q0 + qi) * g.split_stride + (size_t)m * g.ldo + n))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                for (int qi = 0; qi < 2; ++qi)
+#pragma unroll
+                  for (int i = 0; i < RB; ++i)
+#pragma unroll
+                    for (int jv = 0; jv < NV; ++jv)
+                      if (q0 + qi < sg.nslab) {
+                        acc[i][jv].x += t[qi][i][jv].x;
+                        acc[i][jv].y += t[qi][i][jv].y;
+                        acc[i][jv].z += t[qi][i][jv].z;
+                        acc[i][jv].w += t[qi][i][jv].w;
+                      }
+              }
+#pragma unroll
+              for (int i = 0; i < RB; ++i)
+#pragma unroll
+                for (int jv = 0; jv < NV; ++jv) {
+                  const int m = mb + i, n = n0 + jv * 128 + lane * 4;
+                  if (m < g.M && n < g.N) *reinterpret_cast<float4*>(g.out + (size_t)m * g.ldo + n) = acc[i][jv];
+                }
             }
           } else {
             // warp sums its 32 rows; lanes walk 32 consecutive columns.
@@ -866,8 +916,12 @@ static Plan plan_gemm(int M, int N, int K) {
   p.bn = p.swap ? swap_bn(M) : 256;
   if (!p.swap && N <= 128 * 6) p.bn = 128;
   // too few 256-wide tiles to give every SM work: halve the tile width
-  // before cutting K into slices, which need a cross-CTA sum
-  if (!p.swap && p.bn == 256 && 2LL * ((M + 127) / 128) * ((N + 255) / 256) < num_sms()) p.bn = 128;
+  // before cutting K into slices, which need a cross-CTA sum -- unless K is
+  // long: there 128-wide tiles re-read the operands from L2 twice as often
+  // per flop and the contraction stalls on the L2 stream (b64 down
+  // projection, K = 14336: 85 us at 128 wide, about 18 us less at 256 wide
+  // in two K slices)
+  if (!p.swap && p.bn == 256 && K < 8192 && 2LL * ((M + 127) / 128) * ((N + 255) / 256) < num_sms()) p.bn = 128;
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
