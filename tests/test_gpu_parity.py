@@ -47,7 +47,9 @@ GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17,
                # after the stream-K share of the leftover tiles
                (4, 32000, 256), (16, 20480, 512), (2, 39040, 1040),
                # wide tiles, ragged in every dimension, several rounds
-               (300, 40000, 320), (512, 32000, 512)]
+               (300, 40000, 320), (512, 32000, 512),
+               # few wide tiles with a long K: 256-wide tiles in four K slices
+               (300, 1024, 9000)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
