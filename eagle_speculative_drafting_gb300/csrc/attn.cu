@@ -551,7 +551,7 @@ void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit) {
   const long long work = (long long)B * nkv * (max_kv_len > 0 ? max_kv_len : 1);
   long long c = work / num_sms();
   int ch = 64;
-  while (ch < c && ch < 1024) ch *= 2;
+  while (ch < c && ch < 2048) ch *= 2;
   *chunk = ch;
   *nsplit = max_kv_len > 0 ? (max_kv_len + ch - 1) / ch : 1;
 }
