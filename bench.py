@@ -103,12 +103,38 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest():
+def _code_only(text):
+    """C++/CUDA source without comments and blank space: edits to comments
+    leave the kernels, and so the digest, unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":   # string / char literal, copied as is
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def source_digest(root=None):
+    """Digest of the kernel sources (code only) that recorded ncu counters
+    are tied to."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "eagle_speculative_drafting_gb300", "csrc")
+    csrc = os.path.join(root or ROOT, "eagle_speculative_drafting_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -615,9 +615,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
       if (sg.nslab > 1) {
-        // the CTA that stores a tile's last K slice sums every slab of the
-        // tile into slab 0, in slab order (deterministic), and re-arms the
-        // tile's counter for the next launch
+        // the last of the tile's CTAs to arrive sums every slab of the tile
+        // into slab 0, in slab order (deterministic), and re-arms the tile's
+        // counter for the next launch
         __threadfence();
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (warp == 2 && lane == 0) *s_last = (atomicAdd(&g.sem[tile], 1) == sg.nslab - 1) ? 1 : 0;
@@ -918,9 +918,9 @@ static Plan plan_gemm(int M, int N, int K) {
   // too few 256-wide tiles to give every SM work: halve the tile width
   // before cutting K into slices, which need a cross-CTA sum -- unless K is
   // long: there 128-wide tiles re-read the operands from L2 twice as often
-  // per flop and the contraction stalls on the L2 stream (b64 down
-  // projection, K = 14336: 85 us at 128 wide, about 18 us less at 256 wide
-  // in two K slices)
+  // per flop and the contraction stalls on the L2 stream (the down
+  // projection of a 512-row batched decode step, K = 14336: 85 us at 128
+  // wide, about 18 us less at 256 wide in two K slices)
   if (!p.swap && p.bn == 256 && K < 8192 && 2LL * ((M + 127) / 128) * ((N + 255) / 256) < num_sms()) p.bn = 128;
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
