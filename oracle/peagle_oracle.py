@@ -19,8 +19,7 @@ Sources (page title, then section):
          (EAGLE-3 injection concatenates [embeddings (+) hidden]) and the
          variable-length attention note (cu_seqlens isolation).
 
-Readings taken where the pages are silent (each is listed with its reason
-in the design notes):
+Readings taken where the pages are silent:
   * layer-0 input is [RMSNorm_in(embedding) (+) RMSNorm_hidden(hidden)]
     (2H wide); later layers take RMSNorm_in(h) (H wide);
   * norm_before_residual (default on) makes the layer-0 residual the

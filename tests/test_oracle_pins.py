@@ -323,9 +323,12 @@ def test_decode_structured_equals_dense_bruteforce():
             assert np.allclose(a["appended"][l][r][0], b["appended"][l][r][0], atol=1e-12)
 
 
-def _eagle3_step0(W, cfg, aux, token, pos, k_ctx, v_ctx):
+def _eagle3_step0(W, cfg, aux, token, pos, k_ctx, v_ctx, norm_before_residual=True):
     """A plain EAGLE-3 first draft step for one request, written without any
-    of the parallel-drafting machinery (no depths, no mask_hidden, no ptd)."""
+    of the parallel-drafting machinery (no depths, no mask_hidden, no ptd).
+    With norm_before_residual off, the layer-0 residual is the fc-projected
+    hidden state itself rather than its hidden-norm output ("P-EAGLE" user
+    guide, Key Parameters: --no-norm-before-residual)."""
     f64 = lambda a: np.asarray(a, dtype=np.float64)
     eps = cfg["rms_eps"]
     nq, nkv, hd = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
@@ -349,7 +352,7 @@ def _eagle3_step0(W, cfg, aux, token, pos, k_ctx, v_ctx):
         if l == 0:
             hn = norm(hid, L["hidden_norm_w"])
             x = np.concatenate([norm(f64(W["embed"])[token], L["in_norm_w"]), hn])
-            resid = hn
+            resid = hn if norm_before_residual else hid
         else:
             x = norm(h, L["in_norm_w"])
             resid = h
@@ -396,6 +399,64 @@ def test_k1_equals_eagle3_step0_and_ignores_masked_inputs():
         pytest.skip("anchor token hit the ptd id")
     out2 = O.draft_step(O.DraftModel(model.cfg, W2), *args)
     assert np.array_equal(out2["logits"], out["logits"])
+
+
+def test_k1_without_norm_before_residual_equals_eagle3_step0():
+    # the residual branch the flag switches: the fc-projected hidden state
+    # (not its hidden-norm output) seeds the layer-0 residual stream
+    wl = tiny_workload(K=1)
+    model, W = tiny_model(wl, norm_before_residual=False)
+    inp = synth.make_decode_inputs(wl)
+    out = O.draft_step(model, inp["aux"], inp["anchor_tokens"], inp["anchor_pos"], inp["k_cache"],
+                       inp["v_cache"], inp["kv_offsets"], inp["kv_lens"], 1)
+    on, _ = tiny_model(wl)
+    out_on = O.draft_step(on, inp["aux"], inp["anchor_tokens"], inp["anchor_pos"], inp["k_cache"],
+                          inp["v_cache"], inp["kv_offsets"], inp["kv_lens"], 1)
+    for b in range(wl.batch):
+        o, L = int(inp["kv_offsets"][b]), int(inp["kv_lens"][b])
+        ctx = ([kc[o:o + L] for kc in inp["k_cache"]], [vc[o:o + L] for vc in inp["v_cache"]])
+        ref = _eagle3_step0(W, model.cfg, inp["aux"][b], int(inp["anchor_tokens"][b]),
+                            int(inp["anchor_pos"][b]), *ctx, norm_before_residual=False)
+        assert np.allclose(out["logits"][b, 0], ref, atol=1e-12)
+        ref_on = _eagle3_step0(W, model.cfg, inp["aux"][b], int(inp["anchor_tokens"][b]),
+                               int(inp["anchor_pos"][b]), *ctx, norm_before_residual=True)
+        # the flag matters: the two readings give different logits
+        assert not np.allclose(ref, ref_on, atol=1e-6)
+        assert np.allclose(out_on["logits"][b, 0], ref_on, atol=1e-12)
+
+
+def test_to_target_maps_the_argmax_id_through_d2t():
+    # a hand-built draft-vocab logits row: the maximum 3.0 sits at draft ids
+    # 1 and 2, so the lowest (1) wins and d2t turns it into a target id
+    wl = tiny_workload()
+    model, W = tiny_model(wl)
+    perm = np.random.default_rng(4).permutation(wl.vocab)
+    W2 = dict(W, d2t=perm)
+    m2 = O.DraftModel(model.cfg, W2)
+    row = np.full((1, wl.vocab), -2.0)
+    row[0, 1] = row[0, 2] = 3.0
+    row[0, 7] = 2.5
+    assert int(m2.to_target(O.argmax_lowest(row))[0]) == int(perm[1])
+    assert int(model.to_target(O.argmax_lowest(row))[0]) == 1
+    # in a draft step the map acts on the argmax id only: the logits are
+    # unchanged, and every token is perm[argmax of its own logits row]
+    inp = synth.make_decode_inputs(wl)
+    args = (inp["aux"], inp["anchor_tokens"], inp["anchor_pos"], inp["k_cache"], inp["v_cache"],
+            inp["kv_offsets"], inp["kv_lens"], wl.K)
+    a = O.draft_step(model, *args)
+    b = O.draft_step(m2, *args)
+    assert np.array_equal(a["logits"], b["logits"])
+    assert np.array_equal(b["draft_tokens"], perm[np.argmax(a["logits"], axis=-1)])
+    assert np.array_equal(a["draft_tokens"], np.argmax(a["logits"], axis=-1))
+    # a draft vocab smaller than the target vocab: draft id j -> target id d2t[j]
+    Vd = wl.vocab // 2
+    d2t = np.sort(np.random.default_rng(5).choice(wl.vocab, Vd, replace=False))
+    W3 = dict(W, lm_head_w=W["lm_head_w"][:Vd], d2t=d2t)
+    cfg3 = dict(model.cfg, draft_vocab=Vd)
+    c = O.draft_step(O.DraftModel(cfg3, W3), *args)
+    assert c["logits"].shape[-1] == Vd
+    assert np.array_equal(c["logits"], a["logits"][..., :Vd])
+    assert np.array_equal(c["draft_tokens"], d2t[np.argmax(a["logits"][..., :Vd], axis=-1)])
 
 
 def test_prefix_consistency_and_no_recurrence():
