@@ -6,14 +6,16 @@ parallel draft step (fc/fc_norm, masked-depth inputs, rotary-by-position,
 depth-masked attention over context + chain, MLP, draft-vocab head and
 argmax) followed by greedy verify/accept, all through the C ABI.
 
-Workload (default): bf16 decode, batch 1, KV context 2048, K = 4 depths,
-target hidden 4096 with 3 aux layers, one Llama-3-8B-sized draft layer
-(32 q / 8 kv heads x 128, SwiGLU 14336), draft vocab 32000. Weights and
-inputs are seeded synthetic data; the 849 MB of weights streamed every step
-exceed the 129 MB L2, so no L2 flush is needed between steps.
+Workload (default): bf16 batched decode, 64 requests with context lengths
+uniform in [512, 8192], K = 8 depths, target hidden 4096 with 3 aux layers,
+one Llama-3-8B-sized draft layer (32 q / 8 kv heads x 128, SwiGLU 14336),
+draft vocab 32000. Weights and inputs are seeded synthetic data; every step
+streams 849 MB of weights and about 1.2 GB of context K/V, far more than the
+129 MB L2, so no L2 flush is needed between steps.
 
 Metric: drafted tokens/s = B * K / step time (whole job over all ranks).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME]
 """
 import argparse
 import hashlib
@@ -32,8 +34,10 @@ if ROOT not in sys.path:
 
 METRIC = "drafted tokens/s per P-EAGLE draft step"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "decode_b1_ctx2048_k4"
+DEFAULT_WORKLOAD = "decode_b64_ragged_k8"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 OP_IDS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6}
 
 
@@ -75,32 +79,55 @@ def job_throughput(world, B, K, ms_step):
 
 
 def algorithmic_bytes(wl, B, kv_lens):
-    """Bytes each operation must move at minimum, per launch: weights once,
-    activations in, fp32 results out; attention reads the context K/V once."""
+    """Bytes each operation must move at minimum in one step, summed over the
+    layers: weights once, activations in, fp32 results out; attention reads
+    the context K/V once. Layer 0's QKV reads only the B anchor rows (the
+    masked rows share one precomputed q/k/v); later layers read all rows."""
     es = 2 if wl.dtype == "bf16" else 4
-    K, H, I, V = wl.K, wl.hidden, wl.intermediate, wl.vocab
+    K, H, I, V, L = wl.K, wl.hidden, wl.intermediate, wl.vocab, wl.num_layers
     AHt = wl.num_aux * wl.target_hidden
     QKV, nqhd = wl.qkv_out, wl.num_q_heads * wl.head_dim
     rows = B * K
     kv = int(np.sum(kv_lens)) * wl.num_kv_heads * wl.head_dim * 2 * es
     return {
         "fc": es * (H * AHt + B * AHt) + 4 * B * H,
-        "qkv": es * (QKV * 2 * H + B * 2 * H) + 4 * B * QKV,   # layer 0 (one-layer draft)
-        "attn": kv + 2 * rows * nqhd * es + rows * 2 * wl.num_kv_heads * wl.head_dim * es,
-        "o_proj": es * (H * nqhd + rows * nqhd) + 4 * rows * H,
-        "gate_up": es * (2 * I * H + rows * H) + 4 * rows * 2 * I,
-        "down": es * (H * I + rows * I) + 4 * rows * H,
+        "qkv": (es * (QKV * 2 * H + B * 2 * H) + 4 * B * QKV
+                + (L - 1) * (es * (QKV * H + rows * H) + 4 * rows * QKV)),
+        "attn": L * (kv + 2 * rows * nqhd * es + rows * 2 * wl.num_kv_heads * wl.head_dim * es),
+        "o_proj": L * (es * (H * nqhd + rows * nqhd) + 4 * rows * H),
+        "gate_up": L * (es * (2 * I * H + rows * H) + 2 * rows * I),
+        "down": L * (es * (H * I + rows * I) + 4 * rows * H),
         "lm_head": es * (V * H + rows * H) + 4 * rows * V,
     }
 
 
+def algorithmic_flops(wl, B):
+    """Multiply-add flops of each contraction in one step (2 per MAC), over
+    the rows that exist: B anchor rows for fc and layer-0 QKV, B*K rows for
+    the rest."""
+    K, H, I, V, L = wl.K, wl.hidden, wl.intermediate, wl.vocab, wl.num_layers
+    AHt = wl.num_aux * wl.target_hidden
+    QKV, nqhd = wl.qkv_out, wl.num_q_heads * wl.head_dim
+    rows = B * K
+    return {
+        "fc": 2.0 * B * H * AHt,
+        "qkv": 2.0 * B * QKV * 2 * H + (L - 1) * 2.0 * rows * QKV * H,
+        "o_proj": 2.0 * L * rows * H * nqhd,
+        "gate_up": 2.0 * L * rows * 2 * I * H,
+        "down": 2.0 * L * rows * H * I,
+        "lm_head": 2.0 * rows * V * H,
+    }
+
+
 def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 def _code_only(text):
@@ -128,13 +155,26 @@ def _code_only(text):
 
 
 def source_digest(root=None):
-    """Digest of the kernel sources (code only) that recorded ncu counters
-    are tied to."""
+    """Digest of what the recorded ncu counters depend on: the kernel sources
+    and the public header they include (code only), plus the nvcc target
+    and flags the library is built with."""
+    root = root or ROOT
     h = hashlib.sha256()
-    csrc = os.path.join(root or ROOT, "eagle_speculative_drafting_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
-            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
+    pkg = os.path.join(root, "eagle_speculative_drafting_gb300")
+    csrc = os.path.join(pkg, "csrc")
+    files = [(f, os.path.join(csrc, f)) for f in sorted(os.listdir(csrc))]
+    files.append(("include/peagle.h", os.path.join(root, "include", "peagle.h")))
+    for name, path in files:
+        with open(path, encoding="utf-8") as fh:
+            h.update(name.encode() + b"\0" + _code_only(fh.read()).encode())
+    build = os.path.join(pkg, "_build.py")
+    if os.path.exists(build):
+        with open(build, encoding="utf-8") as fh:
+            text = fh.read()
+        for key in ("ARCH", "FLAGS"):
+            for ln in text.splitlines():
+                if ln.startswith(key + " ="):
+                    h.update(ln.encode())
     return h.hexdigest()[:16]
 
 
@@ -353,12 +393,12 @@ def run_train(args, wl):
     __graft_entry__.build()
     import eagle_speculative_drafting_gb300 as pe
     import synth
-    from tests import harness
+    from eagle_speculative_drafting_gb300 import marshal
 
     W = synth.make_weights(wl)
     inp = synth.make_train_inputs(wl)
-    model = harness.make_model(wl, W)
-    d = harness.upload_train(wl, inp)
+    model = marshal.make_model(wl, W)
+    d = marshal.upload_train(wl, inp)
     n, K, r, rmin, seed = wl.n_tokens, inp["K"], inp["r"], inp["r_min"], inp["seed"]
     counts = pe.peagle_cod_counts(n, K, r, rmin)
     R = sum(counts)
@@ -382,6 +422,7 @@ def run_train(args, wl):
     for _ in range(max(args.warmup, 3)):
         step(d)
     torch.cuda.synchronize()
+    clk = ClockSampler(local).__enter__()   # through the probe, timed and e2e passes
     shares = {}
     for name, op in TRAIN_OPS.items():
         pe.peagle_probe_begin(op, 4096)
@@ -393,13 +434,12 @@ def run_train(args, wl):
     launches0 = pe.peagle_kernel_launches()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step(d)
-        e1.record(stream)
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(d)
+    e1.record(stream)
+    torch.cuda.synchronize()
     launches = pe.peagle_kernel_launches() - launches0
     ms_step = e0.elapsed_time(e1) / args.steps
     # the dominant op, timed with CUDA events around its launches in a pass
@@ -431,14 +471,10 @@ def run_train(args, wl):
         h_out[3 * K:].copy_(outs[3], non_blocking=True)
     e3.record(stream)
     torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
     e2e_ms = e2.elapsed_time(e3) / e_steps
-    peak = 1728.9
-    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    src = "fallback"
-    if os.path.exists(pk):
-        with open(pk) as f:
-            peak = float(json.load(f)["bf16_tflops_sustained"])
-        src = "measured (sustained)"
+    _, _, peak, src = measured_peaks()
+    src += " (sustained)"
     total_dom_ms = float(np.sum(dom_ms)) / probe_steps if dom_ms else None
     achieved = flops[dom] / (total_dom_ms / 1000.0) / 1e12 if total_dom_ms else None
     line = {
@@ -491,12 +527,12 @@ def main():
     if dist:
         dist.barrier()
     import eagle_speculative_drafting_gb300 as pe
-    from tests import harness
+    from eagle_speculative_drafting_gb300 import marshal
 
     W = synth.make_weights(wl)
     inp = synth.make_decode_inputs(wl)
-    model = harness.make_model(wl, W)
-    d = harness.upload_decode(wl, inp)
+    model = marshal.make_model(wl, W)
+    d = marshal.upload_decode(wl, inp)
     B, K = wl.batch, wl.K
     kv_cap = int(inp["kv_capacity"])
     max_kv = int(np.max(inp["kv_lens"]))
@@ -524,45 +560,48 @@ def main():
         step(d, targets)
     torch.cuda.synchronize()
 
-    # which kernel dominates: probe each projection / attention class briefly
     abytes = algorithmic_bytes(wl, B, inp["kv_lens"])
-    shares = {}
+    aflops = algorithmic_flops(wl, B)
+    hbm_peak, tc_peak, _, peak_src = measured_peaks()
+    # Clocks are sampled from here to the end of the end-to-end pass: the
+    # per-op probe pass, the timed region, the dominant-kernel pass and the
+    # end-to-end pass all run the same steps under load.
+    clk = ClockSampler(local).__enter__()
+
+    # ---- per-op time: CUDA events around every launch of one op class
+    # (the contraction's kernel, or the attention's split kernel) on its own
+    # launch stream, one class at a time
+    probe_steps = min(max(args.steps, 300), 2000)
+    per_op_ms = {}
     for name, op in OP_IDS.items():
-        pe.peagle_probe_begin(op, 64)
-        for _ in range(8):
+        cap = probe_steps * wl.num_layers + 8
+        pe.peagle_probe_begin(op, cap)
+        for _ in range(probe_steps):
             step(d, targets)
-        ms = pe.peagle_probe_end(64)
-        shares[name] = float(np.sum(ms)) / 8.0 if ms else 0.0
+        torch.cuda.synchronize()
+        ms = pe.peagle_probe_end(cap)
+        per_op_ms[name] = (float(np.sum(ms)) / probe_steps if ms else 0.0, len(ms) / probe_steps if ms else 0)
+    shares = {k: v[0] for k, v in per_op_ms.items()}
     dom = max(shares, key=shares.get)
 
     # ---- timed region: K steps, device events, barrier + sync both sides.
     # No probe events inside it: an event recorded between two PDL-chained
-    # kernels serializes them, so the dominant kernel is timed in its own
-    # pass below.
+    # kernels serializes them, so the per-op times come from the pass above.
     launches0 = pe.peagle_kernel_launches()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step(d, targets)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(d, targets)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     launches = pe.peagle_kernel_launches() - launches0
     ms_total = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
-    # ---- the dominant kernel: CUDA events on the launch stream around each
-    # of its launches, over a pass of the same steps
-    probe_steps = max(1, min(args.steps, 1000))
-    pe.peagle_probe_begin(OP_IDS[dom], probe_steps * wl.num_layers + 8)
-    for _ in range(probe_steps):
-        step(d, targets)
-    torch.cuda.synchronize()
-    dom_ms = pe.peagle_probe_end(probe_steps * wl.num_layers + 8)
     ms_step = ms_total / args.steps
     value = job_throughput(world, B, K, ms_step)
 
@@ -570,7 +609,7 @@ def main():
     # inputs leave one pinned host buffer in one copy (16-byte aligned
     # segments: aux, anchor tokens/positions, KV offsets/lengths, targets)
     # and the drafts / accept lengths / next tokens come back in one copy
-    segs = [("aux", torch.from_numpy(inp["aux"]).to(harness.tdtype(wl))),
+    segs = [("aux", torch.from_numpy(inp["aux"]).to(marshal.tdtype(wl))),
             ("anchor_tokens", torch.from_numpy(inp["anchor_tokens"].astype(np.int32))),
             ("anchor_pos", torch.from_numpy(inp["anchor_pos"].astype(np.int32))),
             ("kv_offsets", torch.from_numpy(inp["kv_offsets"].astype(np.int64))),
@@ -600,7 +639,7 @@ def main():
 
     h2d = int(h_stage.numel())
     d2h = int(h_out.numel() * h_out.element_size())
-    e_steps = max(1, min(args.steps, 2000))
+    e_steps = min(max(args.steps, 300), 2000)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -613,6 +652,7 @@ def main():
         h_out.copy_(d_out, non_blocking=True)
     e3.record(stream)
     torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
     e2e_ms = max_over_ranks(e2.elapsed_time(e3) / e_steps, dist, "cuda")
     e2e_value = job_throughput(world, B, K, e2e_ms)
     status = pe.peagle_get_device_status(model.handle)
@@ -623,9 +663,24 @@ def main():
             dist.destroy_process_group()
         return
 
-    peak, peak_src = measured_peaks()
-    dom_avg_ms = float(np.mean(dom_ms)) if dom_ms else None
-    achieved = abytes[dom] / (dom_avg_ms / 1000.0) / 1e9 if dom_avg_ms else None
+    # per-op roofline: every op by algorithmic bytes against HBM; the
+    # contractions also by algorithmic flops against the bf16 tensor-core
+    # burst peak (each op is timed alone, launch by launch)
+    ops = {}
+    for name, (ms, nl) in per_op_ms.items():
+        if ms <= 0:
+            continue
+        e = {"ms_per_step": round(ms, 5), "launches_per_step": nl,
+             "hbm_gbs": abytes[name] / (ms / 1000.0) / 1e9}
+        e["hbm_frac"] = e["hbm_gbs"] / hbm_peak
+        if name in aflops:
+            e["tflops"] = aflops[name] / (ms / 1000.0) / 1e12
+            e["tc_frac"] = e["tflops"] / tc_peak
+        ops[name] = e
+    dom_ms = per_op_ms[dom][0]
+    dom_launches = max(1, per_op_ms[dom][1])
+    dom_avg_ms = dom_ms / dom_launches
+    achieved = (abytes[dom] / dom_launches) / (dom_avg_ms / 1000.0) / 1e9 if dom_avg_ms > 0 else None
     traffic = recorded_traffic(dom, wl.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -635,14 +690,15 @@ def main():
         "gpu_launches": int(launches),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
                      "peak_source": peak_src, "unit": "GB/s",
-                     "frac": (achieved / peak) if achieved else None,
-                     "traffic": traffic, "algorithmic_bytes": abytes[dom],
+                     "frac": (achieved / hbm_peak) if achieved else None,
+                     "traffic": traffic, "algorithmic_bytes": abytes[dom] / dom_launches,
                      "avg_launch_ms": dom_avg_ms,
-                     "timing": f"CUDA events around each launch, {len(dom_ms) if dom_ms else 0} launches "
-                               f"in a probe pass after the timed region"},
-        "step_shares_ms": {k: round(v, 5) for k, v in shares.items()},
+                     "timing": f"CUDA events around each launch on its stream, {probe_steps} steps "
+                               f"in a probe pass before the timed region"},
+        "ops": ops,
+        "tc_peak_tflops": tc_peak,
         "device_status": status,
     }
     line["clocks"] = clk.summary()
@@ -650,7 +706,7 @@ def main():
         v, steps, el, cores = oracle_leg(wl, W, inp, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{steps} whole float64 oracle draft steps "
-                                          f"({B} request x {K} depths) in {el:.1f} s"}
+                                          f"({B} requests x {K} depths each) in {el:.1f} s"}
     print(json.dumps(line), flush=True)
     model.close()
     if dist:

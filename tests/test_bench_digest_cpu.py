@@ -24,10 +24,18 @@ def test_code_changes_and_literals_are_kept():
     assert bench._code_only('s = "\\"//"; // tail') == 's = "\\"//";'
 
 
-def test_digest_follows_code_not_comments(tmp_path):
-    src = os.path.join(ROOT, "eagle_speculative_drafting_gb300", "csrc")
+def _copy_sources(tmp_path):
+    pkg = os.path.join(ROOT, "eagle_speculative_drafting_gb300")
     dst = tmp_path / "eagle_speculative_drafting_gb300" / "csrc"
-    shutil.copytree(src, dst)
+    shutil.copytree(os.path.join(pkg, "csrc"), dst)
+    shutil.copy(os.path.join(pkg, "_build.py"), tmp_path / "eagle_speculative_drafting_gb300" / "_build.py")
+    (tmp_path / "include").mkdir()
+    shutil.copy(os.path.join(ROOT, "include", "peagle.h"), tmp_path / "include" / "peagle.h")
+    return dst
+
+
+def test_digest_follows_code_not_comments(tmp_path):
+    dst = _copy_sources(tmp_path)
     base = bench.source_digest(str(tmp_path))
     assert base == bench.source_digest()
     f = dst / sorted(os.listdir(dst))[0]
@@ -51,3 +59,18 @@ def test_recorded_counters_are_keyed_and_summarised():
         if e["source_digest"] == bench.source_digest():
             workload, op = key.split(":")
             assert bench.recorded_traffic(op, workload) == e["dram_bytes_per_launch"]
+
+
+def test_digest_covers_the_header_and_build_flags(tmp_path):
+    _copy_sources(tmp_path)
+    base = bench.source_digest(str(tmp_path))
+    hdr = tmp_path / "include" / "peagle.h"
+    text = hdr.read_text()
+    hdr.write_text(text.replace("#define PEAGLE_DEV_TIMEOUT 0x2", "#define PEAGLE_DEV_TIMEOUT 0x4"))
+    assert bench.source_digest(str(tmp_path)) != base
+    hdr.write_text(text)
+    assert bench.source_digest(str(tmp_path)) == base
+    b = tmp_path / "eagle_speculative_drafting_gb300" / "_build.py"
+    bt = b.read_text()
+    b.write_text(bt.replace('"-O3"', '"-O2"'))
+    assert bench.source_digest(str(tmp_path)) != base
