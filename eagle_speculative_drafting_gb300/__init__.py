@@ -102,6 +102,9 @@ _sig("peagle_gemm", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_voi
      c_void_p, c_size_t, c_void_p)
 _sig("peagle_gemm_noalloc", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
      c_void_p, c_void_p)
+_sig("peagle_get_library_status", c_int32, c_void_p, ctypes.POINTER(c_int32))
+_sig("peagle_clear_library_status", c_int32, c_void_p)
+_sig("peagle_set_wait_limit_ns", c_int32, ctypes.c_uint64)
 _sig("peagle_op_name", ctypes.c_char_p, c_int32)
 _sig("peagle_probe_begin", c_int32, c_int32, c_int32)
 _sig("peagle_probe_end", c_int32, ctypes.POINTER(ctypes.c_float), c_int32, ctypes.POINTER(c_int32))
@@ -251,6 +254,20 @@ def peagle_gemm(dtype, M, N, K, X, W, D, workspace, workspace_bytes, stream=None
 def peagle_gemm_noalloc(dtype, M, N, K, X, W, D, stream=None):
     _check(_lib.peagle_gemm_noalloc(dtype, M, N, K, ptr(X), ptr(W), ptr(D), _stream(stream)),
            "peagle_gemm_noalloc")
+
+
+def peagle_get_library_status(stream=None):
+    v = c_int32()
+    _check(_lib.peagle_get_library_status(_stream(stream), ctypes.byref(v)), "peagle_get_library_status")
+    return v.value
+
+
+def peagle_clear_library_status(stream=None):
+    _check(_lib.peagle_clear_library_status(_stream(stream)), "peagle_clear_library_status")
+
+
+def peagle_set_wait_limit_ns(ns):
+    _check(_lib.peagle_set_wait_limit_ns(int(ns)), "peagle_set_wait_limit_ns")
 
 
 def peagle_op_name(op):

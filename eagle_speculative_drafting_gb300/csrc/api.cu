@@ -30,15 +30,47 @@ void set_error(const char* fmt, ...) {
   va_end(ap);
   g_err = buf;
 }
+int current_device() {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+std::mutex& setup_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+// SM count of the current device, looked up once per device
 int num_sms() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
+  static std::atomic<int> sms[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-    sms = v;
+    sms[dev].store(v, std::memory_order_relaxed);
   }
-  return sms;
+  return v;
+}
+
+// ---- status word of the calls that take no model handle (peagle_gemm,
+// peagle_gemm_noalloc): a device variable, so it exists on every device that
+// loads the library without any allocation. Its device address is looked up
+// once per device (cudaGetSymbolAddress with that device current) and
+// cached; a cached address does not survive a device reset.
+static __device__ int g_lib_status;
+static void* g_lib_status_addr[kMaxDevices];
+
+cudaError_t library_status_word(int** out) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(setup_mutex());
+  if (!g_lib_status_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_lib_status);
+    if (e != cudaSuccess) return e;
+    g_lib_status_addr[dev] = p;
+  }
+  *out = static_cast<int*>(g_lib_status_addr[dev]);
+  return cudaSuccess;
 }
 
 // ---- timing probe: event pairs around the main kernel of one op class
@@ -628,6 +660,29 @@ peagle_status peagle_cod_select(int32_t n, int32_t K, double r, double r_min, ui
 }
 
 // ============================================================= dense GEMM
+peagle_status peagle_get_library_status(void* stream, int32_t* host_status) {
+  if (!host_status) FAIL(PEAGLE_ERR_INVALID_ARG, "get_library_status: host_status is NULL");
+  int* w = nullptr;
+  CUDA_TRY(library_status_word(&w));
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int v = 0;
+  CUDA_TRY(cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost));
+  *host_status = v;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_clear_library_status(void* stream) {
+  int* w = nullptr;
+  CUDA_TRY(library_status_word(&w));
+  CUDA_TRY(cudaMemsetAsync(w, 0, sizeof(int), static_cast<cudaStream_t>(stream)));
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_set_wait_limit_ns(uint64_t ns) {
+  gemm_set_wait_limit(ns);
+  return PEAGLE_OK;
+}
+
 static size_t gemm_slab_bytes(int M, int N, int K) {
   return ((gemm_out_floats(PEAGLE_BF16, M, N, K) * sizeof(float)) + 255) & ~size_t(255);
 }
@@ -659,8 +714,10 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
     FAIL(PEAGLE_ERR_WORKSPACE, "gemm: workspace %zu bytes, need %zu", workspace_bytes, need);
   GemmOut go;
   int* sem = reinterpret_cast<int*>(static_cast<char*>(workspace) + gemm_slab_bytes(M, N, K));
+  int* lib_status = nullptr;
+  CUDA_TRY(library_status_word(&lib_status));
   CUDA_TRY(cudaMemsetAsync(sem, 0, kGemmSemCount * sizeof(int), s));
-  CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, static_cast<float*>(workspace), &go, sem, nullptr, -1, s));
+  CUDA_TRY(gemm_launch(dtype, X, K, W, M, N, K, static_cast<float*>(workspace), &go, sem, lib_status, -1, s));
   CUDA_TRY(launch_sum_splits(go, M, N, D, s));
   return PEAGLE_OK;
 }

@@ -525,13 +525,12 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
 template <int MT, int HD, int NW = 4, int NS = 2>
 static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
   using C = MmaAttnCfg<MT, HD, NW, NS>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_mma<MT, HD, NW, NS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(decode_split_mma<MT, HD, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM);
+  });
+  if (e != cudaSuccess) return e;
   launch_pdl(decode_split_mma<MT, HD, NW, NS>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
   return cudaGetLastError();
 }
@@ -833,12 +832,11 @@ static cudaError_t launch_train_mma(const TrainAttnArgs& a, const TrainTileArgs&
   tt.tile_off[0] = 0;
   for (int d = 0; d < tt.K; ++d)
     tt.tile_off[d + 1] = tt.tile_off[d] + (tt.row_off[d + 1] - tt.row_off[d] + C::TQ - 1) / C::TQ;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(train_attn_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(train_attn_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (e != cudaSuccess) return e;
   probe_start(probe_op, st);
   launch_pdl(train_attn_mma<HD>, dim3(tt.tile_off[tt.K], a.nq), 128, C::SMEM, st, a, tt);
   note_launch();

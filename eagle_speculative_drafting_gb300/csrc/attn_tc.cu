@@ -25,7 +25,8 @@
 // exceeds it by more than 2^8 (then O is rescaled in TMEM); in between,
 // probabilities relative to the older maximum stay below 256.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel sets
-// PEAGLE_DEV_TIMEOUT and stops.
+// PEAGLE_DEV_TIMEOUT and stops, after waiting (again bounded) for the TMA
+// copies and tensor-core products it has already issued.
 #include "rows.cuh"
 #include "tc.cuh"
 
@@ -67,7 +68,8 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   uint64_t* chfull = pfree + 1;       // chain results of every row
   uint64_t* xfull = chfull + 1;       // [2] both halves' partial maxima of a tile (by parity)
   uint64_t* lfull = xfull + 2;        // both halves' partial sums
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(lfull + 1);
+  uint64_t* drain = lfull + 1;        // completion of every product issued, on abort
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     tc::mbar_init(&xfull[0], 256);
     tc::mbar_init(&xfull[1], 256);
     tc::mbar_init(lfull, 256);
+    tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_map(&tmQ);
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   const int ntiles = (kend - kbeg) / TK + 1;
   const float sl2 = a.scale * 1.4426950408889634f;
   constexpr uint32_t idesc = tc::idesc_bf16(128, 128);
+  int k_issued = 0, v_issued = 0;   // K and V^T tiles whose copies warp 0 issued
 
   if (warp == 0) {
     if (lane == 0) {
@@ -137,6 +141,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         tc::mbar_expect_tx(&kfull[sk], KB);
         tc::tma_load_2d(sK + sk * KB, &tmK, g * HD, key0, &kfull[sk]);
         tc::tma_load_2d(sK + sk * KB + BOX, &tmK, g * HD + 64, key0, &kfull[sk]);
+        k_issued = t + 1;
         if (!tc::mbar_wait(&vempty[sv], ((t / NV) & 1) ^ 1)) {
           *abort_flag = 1;
           set_status(a.status, PEAGLE_DEV_TIMEOUT);
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         tc::mbar_expect_tx(&vfull[sv], VB);
         tc::tma_load_2d(sV + sv * VB, &tmV, key0, g * HD, &vfull[sv]);
         tc::tma_load_2d(sV + sv * VB + BOX, &tmV, key0 + 64, g * HD, &vfull[sv]);
+        v_issued = t + 1;
       }
     }
   } else if (warp == 1) {
@@ -474,7 +480,21 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     tc::mbar_arrive(chfull);
   }
   tc::fence_before();
-  __syncthreads();
+  __syncthreads();   // every role has stopped issuing
+  if (*abort_flag) {
+    // an aborted CTA drains what it issued before its shared memory and TMEM
+    // go: Q, the last phase of every K and V^T stage, then every product
+    if (warp == 0 && lane == 0) {
+      tc::mbar_wait(qfull, 0);
+      for (int t = max(0, k_issued - NK); t < k_issued; ++t) tc::mbar_wait(&kfull[t % NK], (t / NK) & 1);
+      for (int t = max(0, v_issued - NV); t < v_issued; ++t) tc::mbar_wait(&vfull[t % NV], (t / NV) & 1);
+    } else if (warp == 1 && lane == 0) {
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0);
+    }
+    tc::fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc::fence_after();
     tc::tmem_dealloc(tbase, 512);
@@ -522,12 +542,11 @@ cudaError_t launch_train_attn_tc(const TrainAttnArgs& a, const TrainTileArgs& tt
     set_error("train attention: cuTensorMapEncodeTiled failed");
     return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(train_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(train_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  });
+  if (e != cudaSuccess) return e;
   if (tt.tile_off[tt.K] > 0) {
     launch_pdl(train_attn_tc, dim3(tt.tile_off[tt.K], a.nq), THREADS, SMEM, st, mq, mk, mv, a, tt);
     note_launch();

@@ -9,6 +9,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/peagle.h"
 
 namespace pe {
@@ -96,7 +99,32 @@ void note_launch();                       // counts one kernel launch
 void set_error(const char* fmt, ...);     // records peagle_last_error()
 void probe_start(int op, cudaStream_t s); // timing probe around main kernels
 void probe_stop(int op, cudaStream_t s);
-int num_sms();
+int num_sms();                            // SMs of the current device
+
+// Devices the per-device set-up below tracks (device ordinals 0..63).
+constexpr int kMaxDevices = 64;
+int current_device();                     // cudaGetDevice, or -1 on failure
+std::mutex& setup_mutex();
+// Device address of the current device's status word for calls that take
+// no model handle (PEAGLE_DEV_* bits, sticky).
+cudaError_t library_status_word(int** out);
+
+// Runs fn() on the current device once: `done` holds one bit per device,
+// set after fn() succeeded there. Launch attributes such as the dynamic
+// shared-memory limit apply to the device current when they are set, so
+// every device a kernel runs on needs its own set-up. Safe across threads.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& fn) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(setup_mutex());
+  if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+  const cudaError_t e = fn();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // ---------------------------------------------------------------- GEMM
 // Partial-sum output of a contraction D = X W^T: `splits` slabs of
@@ -143,6 +171,9 @@ struct GemmEpi {
 // box = 64 columns x box_rows rows, 128-byte swizzle. False if the driver
 // rejects it.
 bool make_tma_2d(CUtensorMap* map, const void* base, int rows, int cols, int ld, int box_rows);
+// Bound of every in-kernel wait of the tensor-core contractions launched
+// from now on (default 1 s; 0 = a single try). A test hook.
+void gemm_set_wait_limit(unsigned long long ns);
 // Column tiles (partials per row) of the fused head epilogue.
 int gemm_col_tiles(int M, int N, int K);
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,

@@ -14,8 +14,11 @@
 // through the 128-lane side, activations sit in the narrow N side). Work
 // items are (output tile, K slice); the K slices of a tile land in separate
 // partial slabs that the consumer kernel sums, so no item waits on another.
-// Every mbarrier wait is bounded (1 s); on expiry the kernel sets
-// PEAGLE_DEV_TIMEOUT, stops issuing, frees its TMEM and returns.
+// Every mbarrier wait is bounded (1 s by default, TcArgs::wait_ns); on
+// expiry the kernel sets PEAGLE_DEV_TIMEOUT and stops issuing. Before it
+// frees its TMEM and returns it waits (again bounded) for the TMA copies and
+// tensor-core products it has already issued, so nothing lands in shared
+// memory or TMEM after the CTA has gone.
 //
 // fp32: a tiled CUDA-core kernel (FFMA), exact fp32 accumulation.
 #include <cuda.h>
@@ -45,6 +48,7 @@ struct TcArgs {
   int M, N;                // D is M x N
   int* sem;                // per-tile arrival counters (zero between launches)
   int* status;
+  unsigned long long wait_ns;  // bound of every wait of the roles (0: one try)
   // fused head epilogue (op != EPI_STORE): one partial per (row, column tile)
   int op;
   int part_ld;             // column tiles per row
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;   // completion of every product issued, on abort
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   volatile int* s_last = abort_flag + 1;
   float* staging = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE + 256);
@@ -333,6 +338,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc::mbar_init(&tfull[b], 1);
       tc::mbar_init(&tempty[b], 4);
     }
+    tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_map(&tmA);
@@ -351,6 +357,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   Sched sc;
   sc.init(tilesA * tilesB, ktiles, g.splits, g.streamk, gridDim.x, blockIdx.x);
   Seg sg;
+  int p_issued = 0;   // ring iterations whose TMA copies the producer issued
   // boxes of 64 K-columns that exist in k-tile k (the last one may be short)
   auto nsub = [&](int k) { return min(C::SUB, (g.K - k * C::KT + 63) / 64); };
 
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             continue;
           }
-          if (!tc::mbar_wait(&empty[s], ph ^ 1)) {
+          if (!tc::mbar_wait_for(&empty[s], ph ^ 1, g.wait_ns)) {
             *abort_flag = 1;
             set_status(g.status, PEAGLE_DEV_TIMEOUT);
             break;
@@ -425,6 +432,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
       }
       if (!waited) pdl_wait();
+      p_issued = max(it, pre);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -434,7 +442,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int kb = sg.kb, ke = sg.ke;
         const int buf = j & 1;
         const uint32_t use = j >> 1;
-        if (!tc::mbar_wait(&tempty[buf], (use & 1) ^ 1)) {
+        if (!tc::mbar_wait_for(&tempty[buf], (use & 1) ^ 1, g.wait_ns)) {
           *abort_flag = 1;
           set_status(g.status, PEAGLE_DEV_TIMEOUT);
           break;
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int k = kb; k < ke; ++k, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
-          if (!tc::mbar_wait(&full[s], ph)) {
+          if (!tc::mbar_wait_for(&full[s], ph, g.wait_ns)) {
             ok = false;
             break;
           }
@@ -481,14 +489,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int ta = tile % tilesA, tb = tile / tilesA;
       const int buf = j & 1;
       const uint32_t use = j >> 1;
-      if (*abort_flag) break;
-      // the wait result must be warp-uniform before the .sync.aligned loads
-      const bool ready = __all_sync(0xffffffffu, tc::mbar_wait(&tfull[buf], use & 1));
-      if (!ready) {
+      // Whether to go on is decided by the four epilogue warps together (an
+      // OR over the named barrier they share): a warp that left alone would
+      // leave the others waiting at the barriers of the tile's finish.
+      const bool ready = !*abort_flag && tc::mbar_wait_for(&tfull[buf], use & 1, g.wait_ns);
+      if (!ready && !*abort_flag) {
         *abort_flag = 1;
         set_status(g.status, PEAGLE_DEV_TIMEOUT);
-        break;
       }
+      if (tc::bar_or_epilogue(!ready)) break;
       tc::fence_after();
       float* slab = g.out + (size_t)sp * g.split_stride;
       const int arow = ta * 128 + quad * 32 + lane;
@@ -803,7 +812,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   tc::fence_before();
-  __syncthreads();
+  __syncthreads();   // every role has stopped issuing
+  if (*abort_flag) {
+    // an aborted CTA drains what it issued before its shared memory and TMEM
+    // go: the last TMA phase of every ring stage, then (one commit tracks
+    // all of them) every tensor-core product
+    if (warp == 0 && lane == 0) {
+      for (int q = max(0, p_issued - C::STAGES); q < p_issued; ++q)
+        tc::mbar_wait(&full[q % C::STAGES], (q / C::STAGES) & 1);
+    } else if (warp == 1 && lane == 0) {
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0);
+    }
+    tc::fence_before();
+    __syncthreads();
+  }
   if (warp == 1) {
     tc::fence_after();
     tc::tmem_dealloc(tbase, C::TMEM_COLS);
@@ -857,6 +880,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X,
 // =========================================================================
 // Host side: tensor maps, planning, launch
 // =========================================================================
+static std::atomic<unsigned long long> g_wait_ns{tc::kWaitLimitNs};
+void gemm_set_wait_limit(unsigned long long ns) { g_wait_ns.store(ns, std::memory_order_relaxed); }
+
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;
 
@@ -975,13 +1001,11 @@ template <int BN, bool SWAP>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
                              cudaStream_t s) {
   using C = TcCfg<BN, SWAP>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e0 = once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
@@ -1036,6 +1060,7 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.N = N;
   args.sem = sem;
   args.status = dev_status;
+  args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   args.op = EPI_STORE;
   args.gate_off = 0;
   if (epi && epi->op == GEMM_EPI_SWIGLU) {

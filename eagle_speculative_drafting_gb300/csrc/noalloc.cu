@@ -18,6 +18,13 @@
 // make that first call before any stream capture. The caller still passes
 // the inputs and the output.
 //
+// The cached address does not survive a device reset (cudaDeviceReset):
+// after one, restart the process before calling this entry point again.
+//
+// A bounded wait that runs out inside the contraction sets PEAGLE_DEV_TIMEOUT
+// in the library status word (peagle_get_library_status), which also needs
+// no allocation: it is a device variable of the library.
+//
 // All calls share the array, and it keeps the last call's contents. The
 // per-tile counters must start at zero, so every call clears them first.
 // The slabs need no clearing: every element a call reads was written by the
@@ -32,7 +39,7 @@ namespace {
 constexpr size_t kSlabFloats = (size_t)2 << 20;    // 8 MiB of partial sums
 constexpr size_t kSlabBytes = kSlabFloats * sizeof(float);
 constexpr size_t kScratchBytes = kSlabBytes + pe::kGemmSemCount * sizeof(int);
-constexpr int kMaxDevices = 64;
+using pe::kMaxDevices;
 
 static __device__ __align__(256) unsigned char g_gemm_scratch[kScratchBytes];
 
@@ -97,9 +104,14 @@ extern "C" peagle_status peagle_gemm_noalloc(int32_t dtype, int32_t M, int32_t N
   }
   float* slabs = static_cast<float*>(base);
   int* sem = reinterpret_cast<int*>(static_cast<char*>(base) + kSlabBytes);
+  int* lib_status = nullptr;
+  if ((e = library_status_word(&lib_status)) != cudaSuccess) {
+    set_error("gemm_noalloc: cudaGetSymbolAddress (status word): %s", cudaGetErrorString(e));
+    return PEAGLE_ERR_CUDA;
+  }
   GemmOut go;
   if ((e = cudaMemsetAsync(sem, 0, kGemmSemCount * sizeof(int), s)) != cudaSuccess ||
-      (e = gemm_launch(dtype, X, K, W, M, N, K, slabs, &go, sem, nullptr, -1, s)) != cudaSuccess ||
+      (e = gemm_launch(dtype, X, K, W, M, N, K, slabs, &go, sem, lib_status, -1, s)) != cudaSuccess ||
       (e = launch_sum_splits(go, M, N, D, s)) != cudaSuccess) {
     set_error("gemm_noalloc: %s", cudaGetErrorString(e));
     return PEAGLE_ERR_CUDA;

@@ -108,9 +108,11 @@ def upload_train(wl, inp):
     }
 
 
-def run_train(wl, model, inp, K, r, r_min, seed, decay=0.8, want_logits=False, d=None):
+def run_train(wl, model, inp, K, r, r_min, seed, decay=0.8, want_logits=False, d=None,
+              logit_rows=None):
     """One training-shaped forward; per-depth outputs and per-row results as
-    numpy arrays."""
+    numpy arrays. ``logit_rows`` (row indices) limits the logits copied back
+    to those rows, in that order."""
     d = upload_train(wl, inp) if d is None else d
     n = len(inp["input_ids"])
     counts = peagle_cod_counts(n, K, r, r_min)
@@ -127,6 +129,10 @@ def run_train(wl, model, inp, K, r, r_min, seed, decay=0.8, want_logits=False, d
     res["row_argmax"] = row_am.cpu().numpy()[:R]
     res["row_ce"] = row_ce.cpu().numpy()[:R].astype(np.float64)
     if want_logits:
-        res["logits"] = logits.cpu().numpy()[:R].astype(np.float64)
+        if logit_rows is not None:
+            sel = torch.as_tensor(np.asarray(logit_rows, dtype=np.int64), device="cuda")
+            res["logits"] = logits.index_select(0, sel).cpu().numpy().astype(np.float64)
+        else:
+            res["logits"] = logits.cpu().numpy()[:R].astype(np.float64)
     res["counts"] = counts
     return res

@@ -264,7 +264,10 @@ peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, in
  * projection of the draft (fc, QKV, O, gate/up, down, lm_head; user guide,
  * Architecture). X device [M, K] and W device [N, K] of `dtype` (nn.Linear
  * layout), D device float [M, N]. bf16 runs on the tcgen05 tensor cores
- * (K % 8 == 0, 16-byte aligned X and W), fp32 on the CUDA cores. */
+ * (K % 8 == 0, 16-byte aligned X and W), fp32 on the CUDA cores.
+ * Asynchronous: a bounded wait that runs out inside the kernel sets
+ * PEAGLE_DEV_TIMEOUT in the library status word (peagle_get_library_status)
+ * and leaves D undefined. */
 peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
                           const void* W, float* D, void* workspace, size_t workspace_bytes,
                           void* stream);
@@ -286,11 +289,30 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current. Make that first call
  *     before any stream capture.
+ *   - The looked-up address is cached per device and does not survive a
+ *     device reset (cudaDeviceReset); restart the process after one.
  *   - Every call clears the counters before use. Calls share the array, so
  *     calls that may overlap on the GPU race: serialise them, e.g. on one
- *     stream. */
+ *     stream.
+ *   - As for peagle_gemm, a bounded wait that runs out sets
+ *     PEAGLE_DEV_TIMEOUT in the library status word. */
 peagle_status peagle_gemm_noalloc(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
                                   const void* W, float* D, void* stream);
+
+/* ---- library status word -------------------------------------------------- */
+/* The calls that take no model handle (peagle_gemm, peagle_gemm_noalloc)
+ * report faults their kernels detect (PEAGLE_DEV_* bits) in one sticky
+ * status word per device, a device variable of the library (no allocation).
+ * get synchronizes `stream`, then copies the word of the current device to
+ * *host_status; clear zeroes it, enqueued on `stream`. */
+peagle_status peagle_get_library_status(void* stream, int32_t* host_status);
+peagle_status peagle_clear_library_status(void* stream);
+/* Test hook for the timeout path: every in-kernel wait of the tensor-core
+ * contractions launched after this call gives up after `ns` nanoseconds
+ * (default 1e9; 0 = at the first try that finds the awaited phase still
+ * open) and sets PEAGLE_DEV_TIMEOUT. Process-wide. A contraction whose wait
+ * gave up drains the copies and products it issued before it exits. */
+peagle_status peagle_set_wait_limit_ns(uint64_t ns);
 
 /* ---- per-kernel timing probe -------------------------------------------- */
 /* Operation classes the probe can time (one class at a time). */

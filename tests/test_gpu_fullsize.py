@@ -42,13 +42,14 @@ def test_decode_b1_ctx2048_k4_full():
     assert err <= BF16_TOL, err
     assert np.array_equal(got["draft_tokens"], np.argmax(got["logits"], -1))
     assert not H().token_mismatches_explained(got["draft_tokens"], ref["logits"])
-    # greedy verify of the drafts against geometric-accept targets
+    # greedy verify of the GPU's own drafts against geometric-accept targets,
+    # on the GPU and in the oracle (the same drafts go to both)
     acc = synth.draw_accept_lengths(wl, wl.batch, wl.K)
-    tgt = synth.make_targets_with_accept(wl, ref["draft_tokens"], acc)
-    if np.array_equal(got["draft_tokens"], ref["draft_tokens"]):
-        a, n = H().run_verify(got["draft_tokens"], tgt)
-        ra, rn = O.verify_accept(ref["draft_tokens"], tgt)
-        assert np.array_equal(a, ra) and np.array_equal(n, rn)
+    tgt = synth.make_targets_with_accept(wl, got["draft_tokens"], acc)
+    a, n = H().run_verify(got["draft_tokens"], tgt)
+    ra, rn = O.verify_accept(got["draft_tokens"], tgt)
+    assert np.array_equal(a, ra) and np.array_equal(n, rn)
+    assert np.array_equal(a, acc)
     import eagle_speculative_drafting_gb300 as pe
     assert pe.peagle_get_device_status(model.handle) == 0
     model.close()
@@ -73,28 +74,39 @@ def test_decode_b64_ragged_k8_sampled_requests():
     model.close()
 
 
-def test_train_n4096_k4_sampled_conversation():
-    wl = synth.WORKLOADS["train_n4096_k4"]
+def check_train_conversations(wl, convs):
+    """Full-size forward on the GPU; the oracle on whole conversations
+    (exact on their own: conversations never attend to one another)."""
     W = synth.make_weights(wl)
     inp = synth.make_train_inputs(wl)
     model = H().make_model(wl, W)
     K, r, rmin, seed = inp["K"], inp["r"], inp["r_min"], inp["seed"]
-    got = H().run_train(wl, model, inp, K, r, rmin, seed, want_logits=True)
     cu = inp["cu_seqlens"]
-    conv = int(np.argmin(np.diff(cu)))
+    n = wl.n_tokens
+    counts, sets = O.cod_select(n, K, r, rmin, seed)
+    anchor, depth = O.train_rows(n, counts, sets)
+    conv_of_anchor = np.searchsorted(cu, anchor, side="right") - 1
+    rows = np.flatnonzero(np.isin(conv_of_anchor, convs))
+    got = H().run_train(wl, model, inp, K, r, rmin, seed, want_logits=True, logit_rows=rows)
     fwd_in = {k: inp[k] for k in ("aux", "input_ids", "position_ids", "cu_seqlens", "labels", "loss_mask")}
     ref = O.parallel_forward(H().oracle_model(wl, W), **fwd_in, K=K, r=r, r_min=rmin, seed=seed,
-                             conversations=[conv])
-    rows = np.flatnonzero(ref["row_argmax"] >= 0)
-    assert rows.size > 0
-    assert H().max_abs_rel(got["logits"][rows], ref["logits"][rows]) <= BF16_TOL
-    lab = rows[ref["row_label"][rows] >= 0]
-    assert H().max_abs_rel(got["row_ce"][lab], ref["row_ce"][lab]) <= BF16_TOL
+                             conversations=list(convs), keep_logits=True)
+    assert np.array_equal(np.flatnonzero(ref["row_argmax"] >= 0), rows)
+    assert H().max_abs_rel(got["logits"], ref["logits"][rows]) <= BF16_TOL
+    lab = ref["row_label"][rows] >= 0
+    lrows = rows[lab]
+    assert H().max_abs_rel(got["row_ce"][lrows], ref["row_ce"][lrows]) <= BF16_TOL
     assert not H().token_mismatches_explained(got["row_argmax"][rows], ref["logits"][rows])
+    # per-depth mean CE over the sampled conversations' rows: GPU rows against
+    # the oracle's CE of the same rows
+    for d in range(K):
+        m = lrows[depth[lrows] == d]
+        if m.size:
+            g, o = float(np.mean(got["row_ce"][m])), float(np.mean(ref["row_ce"][m]))
+            assert abs(g - o) <= BF16_TOL * max(1.0, abs(o)), (d, g, o)
     # every row's label presence, for the whole packed sequence
-    labels, counts = O.row_labels(wl.n_tokens, K, r, rmin, seed, cu, inp["labels"])
-    assert got["counts"] == counts
-    depth = np.repeat(np.arange(K), counts)
+    labels, counts2 = O.row_labels(n, K, r, rmin, seed, cu, inp["labels"])
+    assert got["counts"] == counts2 == counts
     want_valid = [int(np.sum((depth == d) & (labels >= 0))) for d in range(K)]
     assert got["per_depth_valid"].tolist() == want_valid
     assert np.all(np.isnan(got["row_ce"][labels < 0]))
@@ -107,3 +119,22 @@ def test_train_n4096_k4_sampled_conversation():
     import eagle_speculative_drafting_gb300 as pe
     assert pe.peagle_get_device_status(model.handle) == 0
     model.close()
+    return rows
+
+
+def test_train_n4096_k4_shortest_and_longest_conversations():
+    # the shortest conversation (132 tokens: about one 128-key tile) and the
+    # longest (889 tokens: many 128-key tiles of the tensor-core attention)
+    wl = synth.WORKLOADS["train_n4096_k4"]
+    cu = synth.make_train_inputs(wl)["cu_seqlens"]
+    lens = np.diff(cu)
+    rows = check_train_conversations(wl, [int(np.argmin(lens)), int(np.argmax(lens))])
+    assert rows.size > 2000
+
+
+def test_train_n32768_k8_sampled_conversation():
+    # the long-context training workload: n = 32768, K = 8, H = 4096, four
+    # layers; the oracle computes the shortest conversation (670 tokens)
+    wl = synth.WORKLOADS["train_n32768_k8"]
+    cu = synth.make_train_inputs(wl)["cu_seqlens"]
+    check_train_conversations(wl, [int(np.argmin(np.diff(cu)))])

@@ -144,15 +144,16 @@ def small_bf16_decode(**kw):
     return wl.scaled(**kw) if kw else wl
 
 
-def check_decode(wl, got, ref, tol):
+def check_decode(wl, got, ref, tol, d2t=None):
     err = H().max_abs_rel(got["logits"], ref["logits"])
     assert err <= tol, f"logits max-abs-rel {err:.3e} > {tol}"
-    # every GPU token is the argmax of the GPU's own logits
-    assert np.array_equal(got["draft_tokens"], np.argmax(got["logits"], axis=-1))
+    # every GPU token is (the target id of) the argmax of the GPU's own logits
+    own = np.argmax(got["logits"], axis=-1)
+    assert np.array_equal(got["draft_tokens"], own if d2t is None else np.asarray(d2t)[own])
     if tol <= F32_TOL:
         assert np.array_equal(got["draft_tokens"], ref["draft_tokens"])
     else:
-        bad = H().token_mismatches_explained(got["draft_tokens"], ref["logits"])
+        bad = H().token_mismatches_explained(got["draft_tokens"], ref["logits"], d2t=d2t)
         assert not bad, bad
     return err
 
@@ -234,6 +235,52 @@ def test_decode_bf16_few_rows_append(kw):
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
+def draft_vocab_maps(V, Vd, seed):
+    """A draft vocab of Vd target ids (sorted): d2t[j] = target id of draft
+    id j; t2d[t] = j, or -1 for target ids outside the draft vocab."""
+    d2t = np.sort(np.random.default_rng(seed).choice(V, Vd, replace=False)).astype(np.int32)
+    t2d = np.full(V, -1, dtype=np.int32)
+    t2d[d2t] = np.arange(Vd, dtype=np.int32)
+    return d2t, t2d
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", F32_TOL), ("bf16", BF16_TOL)])
+def test_decode_draft_vocab_smaller_than_target_vocab(dtype, tol):
+    # the head projects onto a 600-id draft vocab and every token comes back
+    # as the target id d2t[argmax] ("feat(speculative) ... #2376", Changelog:
+    # the draft-vocab projection)
+    wl = small_bf16_decode(dtype=dtype, batch=7)
+    W = synth.make_weights(wl)
+    Vd = 600
+    d2t, t2d = draft_vocab_maps(wl.vocab, Vd, 31)
+    W = dict(W, lm_head_w=W["lm_head_w"][:Vd].copy(), d2t=d2t, t2d=t2d)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    got = H().run_decode(wl, model, inp, want_logits=True)
+    ref = H().oracle_decode(wl, W, inp)
+    assert got["logits"].shape[-1] == Vd
+    check_decode(wl, got, ref, tol, d2t=d2t)
+    assert np.isin(got["draft_tokens"], d2t).all()
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", F32_TOL), ("bf16", BF16_TOL)])
+def test_decode_without_norm_before_residual(dtype, tol):
+    # --no-norm-before-residual ("P-EAGLE" user guide, Key Parameters): the
+    # layer-0 residual is the fc-projected hidden state itself, for the anchor
+    # rows and for the masked rows' shared constant alike
+    wl = small_bf16_decode(dtype=dtype, batch=4)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W, norm_before_residual=0)
+    got = H().run_decode(wl, model, inp, want_logits=True, append=True)
+    ref = H().oracle_decode(wl, W, inp, append=True, norm_before_residual=False)
+    check_decode(wl, got, ref, tol)
+    on = H().oracle_decode(wl, W, inp)
+    assert H().max_abs_rel(on["logits"], ref["logits"]) > 10 * tol   # the flag is seen
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
 def test_decode_prefix_consistency_on_gpu():
     wl = small_bf16_decode(dtype="f32", batch=2)
     W = synth.make_weights(wl)
@@ -271,11 +318,12 @@ def small_train(dtype="f32", n=64, lens=(20, 1, 30, 13), K=4, **kw):
     return wl, inp
 
 
-def check_train(wl, inp, K, r, rmin, seed, tol, got=None):
-    W = synth.make_weights(wl)
-    model = H().make_model(wl, W)
+def check_train(wl, inp, K, r, rmin, seed, tol, W=None, norm_before_residual=True):
+    W = synth.make_weights(wl) if W is None else W
+    model = H().make_model(wl, W, norm_before_residual=int(norm_before_residual))
     got = H().run_train(wl, model, inp, K, r, rmin, seed, want_logits=True)
-    ref = O.parallel_forward(H().oracle_model(wl, W), **inp, K=K, r=r, r_min=rmin, seed=seed)
+    ref = O.parallel_forward(H().oracle_model(wl, W, norm_before_residual), **inp, K=K, r=r, r_min=rmin,
+                             seed=seed)
     assert got["counts"] == ref["counts"]
     assert H().max_abs_rel(got["logits"], ref["logits"]) <= tol
     assert np.array_equal(got["per_depth_valid"], ref["per_depth_valid"])
@@ -337,3 +385,26 @@ def test_train_bf16_multi_chunk_rows():
     # more than 256 rows per GEMM so the wide (non-swapped) tensor-core tiles run
     wl, inp = small_train(dtype="bf16", n=700, lens=(300, 400), K=2)
     check_train(wl, inp, 2, 0.7, 0.2, 5, BF16_TOL)
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", F32_TOL), ("bf16", BF16_TOL)])
+def test_train_labels_outside_the_draft_vocab(dtype, tol):
+    # labels are target ids; t2d maps them into the 600-id draft vocab, and a
+    # label with t2d = -1 has no draft id, so its row carries no loss
+    # ("feat(speculative) ... #2376", Pre checks: out-of-draft-vocab masking)
+    wl, inp = small_train(dtype=dtype, n=300, lens=(120, 7, 100, 73), K=4)
+    W = synth.make_weights(wl)
+    Vd = 600
+    d2t, t2d = draft_vocab_maps(wl.vocab, Vd, 32)
+    W = dict(W, lm_head_w=W["lm_head_w"][:Vd].copy(), d2t=d2t, t2d=t2d)
+    got, ref = check_train(wl, inp, 4, 0.7, 0.2, 21, tol, W=W)
+    # about 40% of the uniform labels fall outside the draft vocab
+    lab_all, _ = O.row_labels(wl.n_tokens, 4, 0.7, 0.2, 21, inp["cu_seqlens"], inp["labels"])
+    assert got["per_depth_valid"].sum() < 0.8 * (lab_all >= 0).sum()
+    assert np.array_equal(got["per_depth_valid"], ref["per_depth_valid"])
+
+
+@pytest.mark.parametrize("dtype,tol", [("f32", F32_TOL), ("bf16", BF16_TOL)])
+def test_train_without_norm_before_residual(dtype, tol):
+    wl, inp = small_train(dtype=dtype, n=300, lens=(120, 7, 100, 73), K=4)
+    check_train(wl, inp, 4, 0.7, 0.2, 17, tol, norm_before_residual=False)

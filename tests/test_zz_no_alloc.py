@@ -47,7 +47,10 @@ def _max_abs_rel(a, b):
 
 
 @pytest.mark.parametrize("shapes", [[(4, 4096, 4096), (16, 1000, 2048)],
-                                    [(64, 4096, 1024), (4, 4096, 4096)]])
+                                    [(64, 4096, 1024), (4, 4096, 4096)],
+                                    # more than 256 rows: wide tiles whose long K is cut into
+                                    # four slices, summed through the fixed array
+                                    [(300, 1024, 9000), (16, 1000, 2048)]])
 def test_noalloc_matches_workspace_gemm_twice_in_a_row(pe, shapes):
     ops = [_operands(M, N, K, seed=M + N + K + i) for i, (M, N, K) in enumerate(shapes)]
     refs = [_with_workspace(pe, M, N, K, X, W) for (M, N, K), (X, W) in zip(shapes, ops)]
@@ -69,3 +72,18 @@ def test_noalloc_rejects_sizes_beyond_its_array(pe):
         pe.peagle_gemm_noalloc(pe.PEAGLE_BF16, M, N, K, X, W, D)
     assert e.value.status == pe.PEAGLE_ERR_UNSUPPORTED
     assert "partial floats" in pe.peagle_last_error()
+
+
+def test_noalloc_f32_matches_workspace_gemm(pe):
+    # the fp32 contraction runs on the CUDA cores straight into D
+    rng = np.random.default_rng(5)
+    M, N, K = 65, 130, 100
+    X = torch.from_numpy(rng.standard_normal((M, K), dtype=np.float32)).cuda()
+    W = torch.from_numpy(rng.standard_normal((N, K), dtype=np.float32)).cuda()
+    ref = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    pe.peagle_gemm(pe.PEAGLE_F32, M, N, K, X, W, ref, None, 0)
+    for _ in range(2):
+        D = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        pe.peagle_gemm_noalloc(pe.PEAGLE_F32, M, N, K, X, W, D)
+        torch.cuda.synchronize()
+        assert _max_abs_rel(D, ref) <= 1e-6
