@@ -31,6 +31,8 @@ PEAGLE_DEV_BOUNDS = 0x1
 PEAGLE_DEV_TIMEOUT = 0x2
 PEAGLE_F32 = 0
 PEAGLE_BF16 = 1
+PEAGLE_MEM_DEVICE = 0
+PEAGLE_MEM_HOST = 1
 OPS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6,
        "verify": 7, "cod": 8, "ce": 9}
 
@@ -102,6 +104,11 @@ _sig("peagle_gemm", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_voi
      c_void_p, c_size_t, c_void_p)
 _sig("peagle_gemm_noalloc", c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
      c_void_p, c_void_p)
+_sig("peagle_checkpoint_save", c_int32, ctypes.c_char_p, ctypes.POINTER(peagle_config),
+     ctypes.POINTER(peagle_weights), c_int32, c_void_p)
+_sig("peagle_checkpoint_load_config", c_int32, ctypes.c_char_p, ctypes.POINTER(peagle_config))
+_sig("peagle_checkpoint_load", c_int32, ctypes.c_char_p, ctypes.POINTER(peagle_config),
+     ctypes.POINTER(peagle_weights), c_int32, c_void_p)
 _sig("peagle_get_library_status", c_int32, c_void_p, ctypes.POINTER(c_int32))
 _sig("peagle_clear_library_status", c_int32, c_void_p)
 _sig("peagle_set_wait_limit_ns", c_int32, ctypes.c_uint64)
@@ -123,12 +130,15 @@ def _check(status, where):
 
 
 def ptr(x):
-    """Device (or host) address of a tensor, an int, or None (NULL)."""
+    """Address of a torch tensor (device or host), a numpy array (host), an
+    int, or None (NULL)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data
 
 
 def _stream(stream):
@@ -254,6 +264,28 @@ def peagle_gemm(dtype, M, N, K, X, W, D, workspace, workspace_bytes, stream=None
 def peagle_gemm_noalloc(dtype, M, N, K, X, W, D, stream=None):
     _check(_lib.peagle_gemm_noalloc(dtype, M, N, K, ptr(X), ptr(W), ptr(D), _stream(stream)),
            "peagle_gemm_noalloc")
+
+
+def _stream_or_null(stream, memory):
+    # host-memory checkpoint calls make no CUDA call and need no stream
+    return None if memory == PEAGLE_MEM_HOST and stream is None else _stream(stream)
+
+
+def peagle_checkpoint_save(directory, cfg, weights, memory=PEAGLE_MEM_DEVICE, stream=None):
+    _check(_lib.peagle_checkpoint_save(os.fsencode(directory), ctypes.byref(cfg), ctypes.byref(weights), memory,
+                                       _stream_or_null(stream, memory)), "peagle_checkpoint_save")
+
+
+def peagle_checkpoint_load_config(directory):
+    cfg = peagle_config()
+    _check(_lib.peagle_checkpoint_load_config(os.fsencode(directory), ctypes.byref(cfg)),
+           "peagle_checkpoint_load_config")
+    return cfg
+
+
+def peagle_checkpoint_load(directory, cfg, weights, memory=PEAGLE_MEM_DEVICE, stream=None):
+    _check(_lib.peagle_checkpoint_load(os.fsencode(directory), ctypes.byref(cfg), ctypes.byref(weights), memory,
+                                       _stream_or_null(stream, memory)), "peagle_checkpoint_load")
 
 
 def peagle_get_library_status(stream=None):

@@ -22,6 +22,61 @@ def make_config(hidden, target_hidden, num_aux, num_layers, num_q_heads, num_kv_
                          float(rope_theta), float(rms_eps))
 
 
+def weights_struct(weights: dict):
+    """peagle_weights over a dict of buffers (torch tensors or numpy arrays,
+    all in one kind of memory) named like the struct's fields;
+    ``weights["layers"]`` is a list of per-layer dicts. Returns the struct and
+    the per-layer array it points to (keep both alive)."""
+    Ls = weights["layers"]
+    layers = (peagle_layer_weights * len(Ls))(*[
+        peagle_layer_weights(ptr(L["in_norm_w"]), ptr(L.get("hidden_norm_w")), ptr(L["qkv_w"]),
+                             ptr(L["o_w"]), ptr(L["post_norm_w"]), ptr(L["gate_up_w"]),
+                             ptr(L["down_w"])) for L in Ls])
+    w = peagle_weights(ptr(weights["embed"]), ptr(weights["fc_w"]), ptr(weights["fc_norm_w"]),
+                       ptr(weights["mask_hidden"]), ptr(weights["final_norm_w"]),
+                       ptr(weights["lm_head_w"]), ptr(weights.get("d2t")), ptr(weights.get("t2d")),
+                       ctypes.cast(layers, ctypes.POINTER(peagle_layer_weights)))
+    return w, layers
+
+
+def weight_shapes(cfg: peagle_config) -> dict:
+    """Shape of every weight buffer a config implies (same keys as
+    weights_struct; d2t / t2d are int32)."""
+    H, A, Ht, I = cfg.hidden, cfg.num_aux, cfg.target_hidden, cfg.intermediate
+    qkv = (cfg.num_q_heads + 2 * cfg.num_kv_heads) * cfg.head_dim
+    out = {"embed": (cfg.target_vocab, H), "fc_w": (H, A * Ht), "fc_norm_w": (H,),
+           "mask_hidden": (1, A * Ht), "final_norm_w": (H,), "lm_head_w": (cfg.draft_vocab, H),
+           "d2t": (cfg.draft_vocab,), "t2d": (cfg.target_vocab,), "layers": []}
+    for l in range(cfg.num_layers):
+        out["layers"].append({
+            "in_norm_w": (H,), "hidden_norm_w": (H,) if l == 0 else None,
+            "qkv_w": (qkv, 2 * H if l == 0 else H), "o_w": (H, cfg.num_q_heads * cfg.head_dim),
+            "post_norm_w": (H,), "gate_up_w": (2 * I, H), "down_w": (H, I)})
+    return out
+
+
+def load_checkpoint(directory, stream=None):
+    """Reads a P-EAGLE draft checkpoint (config.json + model.safetensors) into
+    fresh device tensors and creates the model over them."""
+    import torch
+    from . import peagle_checkpoint_load, peagle_checkpoint_load_config
+    cfg = peagle_checkpoint_load_config(directory)
+    dt = torch.bfloat16 if cfg.dtype == PEAGLE_BF16 else torch.float32
+    shapes = weight_shapes(cfg)
+    W = {}
+    for k, v in shapes.items():
+        if k == "layers":
+            W["layers"] = [{kk: (None if sh is None else torch.empty(sh, dtype=dt, device="cuda"))
+                            for kk, sh in L.items()} for L in v]
+        elif k in ("d2t", "t2d"):
+            W[k] = torch.empty(v, dtype=torch.int32, device="cuda")
+        else:
+            W[k] = torch.empty(v, dtype=dt, device="cuda")
+    w, keep = weights_struct(W)
+    peagle_checkpoint_load(directory, cfg, w, stream=stream)
+    return Model(cfg, W, stream)
+
+
 class Model:
     """A created draft model. ``weights`` maps the names of peagle_weights /
     peagle_layer_weights to device tensors; ``weights["layers"]`` is a list
@@ -30,16 +85,7 @@ class Model:
     def __init__(self, cfg: peagle_config, weights: dict, stream=None):
         self.cfg = cfg
         self._keep = weights
-        Ls = weights["layers"]
-        self._layers = (peagle_layer_weights * len(Ls))(*[
-            peagle_layer_weights(ptr(L["in_norm_w"]), ptr(L.get("hidden_norm_w")), ptr(L["qkv_w"]),
-                                 ptr(L["o_w"]), ptr(L["post_norm_w"]), ptr(L["gate_up_w"]),
-                                 ptr(L["down_w"])) for L in Ls])
-        self._w = peagle_weights(ptr(weights["embed"]), ptr(weights["fc_w"]),
-                                 ptr(weights["fc_norm_w"]), ptr(weights["mask_hidden"]),
-                                 ptr(weights["final_norm_w"]), ptr(weights["lm_head_w"]),
-                                 ptr(weights.get("d2t")), ptr(weights.get("t2d")),
-                                 ctypes.cast(self._layers, ctypes.POINTER(peagle_layer_weights)))
+        self._w, self._layers = weights_struct(weights)
         self.handle = peagle_model_create(cfg, self._w, stream)
         self._ws = {}
 
@@ -82,6 +128,11 @@ class Model:
                                 out["per_depth_valid"], out["loss"], row_argmax, row_ce, logits,
                                 ws, nbytes, stream)
         return out
+
+    def save_checkpoint(self, directory, stream=None):
+        """Writes the model's weights as a vLLM-loadable P-EAGLE checkpoint."""
+        from . import peagle_checkpoint_save
+        peagle_checkpoint_save(directory, self.cfg, self._w, stream=stream)
 
     def close(self):
         if getattr(self, "handle", None):

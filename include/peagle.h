@@ -299,6 +299,41 @@ peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const 
 peagle_status peagle_gemm_noalloc(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
                                   const void* W, float* D, void* stream);
 
+/* ---- checkpoint I/O ------------------------------------------------------ */
+/* Where the weight buffers of a checkpoint call live. */
+typedef enum peagle_memory { PEAGLE_MEM_DEVICE = 0, PEAGLE_MEM_HOST = 1 } peagle_memory;
+/* Writes `dir`/config.json and `dir`/model.safetensors in the layout vLLM's
+ * parallel-drafting loader reads: a standard EAGLE-3 draft checkpoint with
+ * the placeholder saved under the key "mask_hidden" ([1, A*Ht]) and
+ * "parallel_drafting": true plus "ptd_token_id" in config.json (#2376,
+ * Checkpoint contract). Tensor names: embed_tokens.weight, fc.weight,
+ * fc_norm.weight, mask_hidden, layers.<l>.{input_layernorm, hidden_norm (layer 0),
+ * self_attn.{q,k,v,o}_proj, post_attention_layernorm, mlp.{gate,up,down}_proj}.weight,
+ * norm.weight, lm_head.weight, d2t (int64 [Vd], target id - draft id) and t2d
+ * (bool [Vt], target id in the draft vocab). The fused q/k/v and gate/up
+ * matrices of peagle_layer_weights are split into their row blocks.
+ *   w       the weights, in `memory` (device pointers are read with
+ *           cudaMemcpyAsync on `stream`, which is synchronized); d2t / t2d
+ *           may be NULL (identity)
+ * The directory must exist. Host memory only is touched on the way; nothing
+ * is allocated on the device. */
+peagle_status peagle_checkpoint_save(const char* dir, const peagle_config* cfg, const peagle_weights* w,
+                                     int32_t memory, void* stream);
+/* Reads `dir`/config.json into *cfg. Requires "parallel_drafting": true and a
+ * "ptd_token_id" (#2376: no silent default). The number of aux states comes
+ * from num_aux_hidden_states, else the length of
+ * eagle_aux_hidden_state_layer_ids, else the width of fc.weight; dtype from
+ * torch_dtype (float32, else bf16); max_position from max_position_embeddings. */
+peagle_status peagle_checkpoint_load_config(const char* dir, peagle_config* cfg);
+/* Fills caller-owned buffers `w` (sized for *cfg, all in `memory`) from
+ * `dir`/model.safetensors: every tensor must be present with the shape *cfg
+ * implies; F32 and BF16 files convert to the model dtype on the host. d2t /
+ * t2d are rebuilt from the stored offsets (t2d = the inverse map, checked
+ * against the stored membership mask); they may be NULL only if the stored
+ * map is the identity. Synchronizes `stream` (device memory). */
+peagle_status peagle_checkpoint_load(const char* dir, const peagle_config* cfg, const peagle_weights* w,
+                                     int32_t memory, void* stream);
+
 /* ---- library status word -------------------------------------------------- */
 /* The calls that take no model handle (peagle_gemm, peagle_gemm_noalloc)
  * report faults their kernels detect (PEAGLE_DEV_* bits) in one sticky

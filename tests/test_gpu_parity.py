@@ -275,9 +275,11 @@ def test_decode_without_norm_before_residual(dtype, tol):
     model = H().make_model(wl, W, norm_before_residual=0)
     got = H().run_decode(wl, model, inp, want_logits=True, append=True)
     ref = H().oracle_decode(wl, W, inp, append=True, norm_before_residual=False)
-    check_decode(wl, got, ref, tol)
+    err = check_decode(wl, got, ref, tol)
+    # the flag is seen: the GPU sits far closer to the flag-off oracle than
+    # the flag-on oracle does
     on = H().oracle_decode(wl, W, inp)
-    assert H().max_abs_rel(on["logits"], ref["logits"]) > 10 * tol   # the flag is seen
+    assert err < 0.25 * H().max_abs_rel(on["logits"], ref["logits"])
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
@@ -408,3 +410,24 @@ def test_train_labels_outside_the_draft_vocab(dtype, tol):
 def test_train_without_norm_before_residual(dtype, tol):
     wl, inp = small_train(dtype=dtype, n=300, lens=(120, 7, 100, 73), K=4)
     check_train(wl, inp, 4, 0.7, 0.2, 17, tol, norm_before_residual=False)
+
+
+# ------------------------------------------------------------- checkpoint
+def test_checkpoint_round_trip_gives_the_same_draft_step(tmp_path):
+    # save the device weights in vLLM's P-EAGLE layout, load them into fresh
+    # device buffers, and draft again: identical logits and tokens
+    from eagle_speculative_drafting_gb300.model import load_checkpoint
+    wl = small_bf16_decode(batch=3)
+    W = synth.make_weights(wl)
+    d2t, t2d = draft_vocab_maps(wl.vocab, 700, 5)
+    W = dict(W, lm_head_w=W["lm_head_w"][:700].copy(), d2t=d2t, t2d=t2d)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    a = H().run_decode(wl, model, inp, want_logits=True)
+    model.save_checkpoint(str(tmp_path))
+    model2 = load_checkpoint(str(tmp_path))
+    assert model2.cfg.draft_vocab == 700 and model2.cfg.ptd_token_id == wl.ptd_token_id
+    b = H().run_decode(wl, model2, inp, want_logits=True)
+    assert np.array_equal(a["logits"], b["logits"])
+    assert np.array_equal(a["draft_tokens"], b["draft_tokens"])
+    assert np.array_equal(model2._keep["t2d"].cpu().numpy(), t2d)
