@@ -111,6 +111,67 @@ def verify_accept(drafts: np.ndarray, targets: np.ndarray):
 
 
 # --------------------------------------------------------------------------
+# Stochastic verification  ["P_Eagle" README, "How Speculative Decoding
+# Works" row 6: accepted tokens are used, rejected ones resampled; output
+# quality "probabilistically same" as the target]
+# The published speculative-sampling rule (Leviathan, Kalman, Matias, ICML
+# 2023; Chen et al., 2023): draft token x at depth i is kept with probability
+# min(1, p_i(x) / q_i(x)); at the first rejection the next token is drawn
+# from the normalised residual max(0, p_i - q_i); when all K drafts are kept
+# it is drawn from p_K (the bonus token). The random numbers are inputs:
+#   accept_u[b, i] in [0, 1): keep x iff fl32(u * q_i(x)) < p_i(x), in fp32;
+#   draws[b]: a uniform 32-bit integer for the one inverse-CDF draw.
+# The draw is exact integer arithmetic: each weight (the fp32 residual or
+# p_K, clamped to [0, 1], NaN as 0) becomes W_j = floor(w_j * 2^40) (int64),
+# S = sum W_j, T = (draw * S) >> 32, and the token is the smallest j whose
+# inclusive prefix sum of W exceeds T. Weights below 2^-40 thus count as 0.
+# If S == 0 (the draft was rejected where p and q agree to 2^-40), the token
+# is the lowest-index argmax of p_i.
+# --------------------------------------------------------------------------
+SAMPLE_SCALE = 2.0 ** 40
+
+
+def sample_weights(w):
+    """Integer weights of the inverse-CDF draw from fp32 weights w."""
+    w = np.asarray(w, dtype=np.float32).astype(np.float64)
+    w = np.where(np.isnan(w), 0.0, np.clip(w, 0.0, 1.0))
+    return np.floor(w * SAMPLE_SCALE).astype(np.int64)
+
+
+def verify_sample(drafts, draft_probs, target_probs, accept_u, draws):
+    """drafts [B, K] target ids; draft_probs q [B, K, V] and target_probs
+    p [B, K+1, V] (fp32 values); accept_u [B, K] fp32; draws [B] uint32.
+    Returns (accept_len [B], next_token [B])."""
+    drafts = np.asarray(drafts, dtype=np.int64)
+    q = np.asarray(draft_probs, dtype=np.float32)
+    p = np.asarray(target_probs, dtype=np.float32)
+    u = np.asarray(accept_u, dtype=np.float32)
+    B, K = drafts.shape
+    accept = np.zeros(B, dtype=np.int32)
+    nxt = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        a = 0
+        while a < K:
+            x = int(drafts[b, a])
+            if not (np.float32(u[b, a] * q[b, a, x]) < p[b, a, x]):
+                break
+            a += 1
+        if a < K:
+            w = np.maximum(p[b, a] - q[b, a], np.float32(0.0))
+        else:
+            w = p[b, K]
+        W = sample_weights(w)
+        S = int(W.sum())
+        if S == 0:
+            nxt[b] = int(argmax_lowest(p[b, a]))
+        else:
+            T = (int(draws[b]) * S) >> 32
+            nxt[b] = int(np.searchsorted(np.cumsum(W), T, side="right"))
+        accept[b] = a
+    return accept, nxt
+
+
+# --------------------------------------------------------------------------
 # Dense pieces
 # --------------------------------------------------------------------------
 def rms_norm(x, gain, eps):

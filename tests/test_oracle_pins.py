@@ -598,3 +598,99 @@ def test_row_labels_agree_with_forward():
     lab, counts = O.row_labels(wl.n_tokens, wl.K, 0.7, 0.2, 9, inp["cu_seqlens"], inp["labels"])
     assert counts == res["counts"]
     assert np.array_equal(lab, res["row_label"])
+
+
+# -------------------------------------------------------- stochastic verify
+def _probs(rng, V, sharp=1.0):
+    x = rng.standard_normal(V) * sharp
+    e = np.exp(x - x.max())
+    return (e / e.sum()).astype(np.float32)
+
+
+def test_verify_sample_one_hot_is_greedy_verify():
+    # one-hot target and draft distributions reduce rejection sampling to
+    # greedy longest-prefix acceptance, the brute-force-pinned rule
+    rng = np.random.default_rng(3)
+    B, K, V = 400, 4, 3
+    d = rng.integers(0, V, (B, K))
+    t = rng.integers(0, V, (B, K + 1))
+    t[:, :K] = np.where(rng.random((B, K)) < 0.6, d, t[:, :K])
+    q = np.eye(V, dtype=np.float32)[d]
+    p = np.eye(V, dtype=np.float32)[t]
+    u = rng.random((B, K)).astype(np.float32)
+    draws = rng.integers(0, 2 ** 32, B, dtype=np.uint64)
+    a, n = O.verify_sample(d, q, p, u, draws)
+    ga, gn = O.verify_accept(d, t)
+    assert np.array_equal(a, ga) and np.array_equal(n, gn)
+
+
+def test_verify_sample_first_token_follows_the_target_distribution():
+    # the speculative-sampling theorem: whatever the draft distribution q,
+    # the first emitted token is distributed as the target's p. Acceptance
+    # depends only on u and the resample only on the draw, so each is
+    # integrated on its own uniform grid.
+    rng = np.random.default_rng(8)
+    V, Nu, Nd = 6, 2000, 4000
+    for trial in range(3):
+        p0 = _probs(rng, V, 1.5)
+        q0 = _probs(rng, V, 1.5)
+        p = np.stack([p0, _probs(rng, V)])[None]          # [1, K+1=2, V]
+        ugrid = ((np.arange(Nu) + 0.5) / Nu).astype(np.float32)
+        A = np.zeros(V)
+        for x in range(V):
+            a, _ = O.verify_sample(np.full((Nu, 1), x), np.broadcast_to(q0, (Nu, 1, V)),
+                                   np.broadcast_to(p, (Nu, 2, V)), ugrid[:, None], np.zeros(Nu, np.uint64))
+            A[x] = a.mean()
+            assert abs(A[x] - min(1.0, p0[x] / q0[x])) <= 1.5 / Nu
+        xr = int(np.argmin(p0 / q0))                        # a draft that is rejected at u ~ 1
+        assert p0[xr] < 0.99 * q0[xr]
+        dgrid = (np.arange(Nd, dtype=np.uint64) * (2 ** 32 // Nd)).astype(np.uint64)
+        a, nxt = O.verify_sample(np.full((Nd, 1), xr), np.broadcast_to(q0, (Nd, 1, V)),
+                                 np.broadcast_to(p, (Nd, 2, V)), np.full((Nd, 1), 0.999999, np.float32), dgrid)
+        assert (a == 0).all()
+        R = np.bincount(nxt, minlength=V) / Nd
+        resid = np.maximum(p0.astype(np.float64) - q0, 0)
+        assert np.allclose(R, resid / resid.sum(), atol=2.0 / Nd)
+        first = q0 * A + (1 - np.sum(q0 * A)) * R
+        assert np.allclose(first, p0, atol=3e-3), (first, p0)
+
+
+def test_verify_sample_bonus_token_follows_the_last_target_distribution():
+    # drafts drawn from q = p are always kept (u < 1), and the bonus token is
+    # then distributed as p_K
+    rng = np.random.default_rng(9)
+    V, K, Nd = 7, 3, 5000
+    p = np.stack([_probs(rng, V) for _ in range(K + 1)])
+    q = p[:K]
+    d = np.argmax(q, -1)
+    dgrid = (np.arange(Nd, dtype=np.uint64) * (2 ** 32 // Nd)).astype(np.uint64)
+    a, nxt = O.verify_sample(np.broadcast_to(d, (Nd, K)), np.broadcast_to(q, (Nd, K, V)),
+                             np.broadcast_to(p, (Nd, K + 1, V)), np.full((Nd, K), 0.9999, np.float32), dgrid)
+    assert (a == K).all()
+    assert np.allclose(np.bincount(nxt, minlength=V) / Nd, p[K], atol=2.0 / Nd)
+
+
+def test_verify_sample_degenerate_residual_takes_the_argmax():
+    # a draft with p(x) = q(x) = 0 is rejected (0 < 0 fails); when p == q the
+    # residual is empty and the token is the lowest-index argmax of p
+    V = 5
+    p = np.array([0.1, 0.4, 0.0, 0.4, 0.1], dtype=np.float32)
+    a, n = O.verify_sample(np.array([[2]]), p[None, None], np.stack([p, p])[None],
+                           np.array([[0.5]], np.float32), np.array([123], np.uint64))
+    assert a[0] == 0 and n[0] == 1
+    # integer weights: floor(w * 2^40), NaN as 0, clamped to [0, 1]
+    W = O.sample_weights(np.array([0.5, np.nan, 2.0, -1.0, 2.0 ** -41], np.float32))
+    assert W.tolist() == [2 ** 39, 0, 2 ** 40, 0, 0]
+
+
+def test_verify_sample_draw_intervals_are_half_open():
+    # hand-worked: bonus weights [1/4, 1/4, 0, 1/2] give integer weights
+    # [2^38, 2^38, 0, 2^39], S = 2^40 and T = draw * 2^8. Token j owns the
+    # draws with prefix(j-1) <= T < prefix(j): [0, 2^30) -> 0,
+    # [2^30, 2^31) -> 1, token 2 never, [2^31, 2^32) -> 3
+    p = np.array([[0.0, 1.0, 0.0, 0.0], [0.25, 0.25, 0.0, 0.5]], dtype=np.float32)[None]
+    q = np.array([[0.0, 1.0, 0.0, 0.0]], dtype=np.float32)[None]
+    cases = {0: 0, 2 ** 30 - 1: 0, 2 ** 30: 1, 2 ** 31 - 1: 1, 2 ** 31: 3, 2 ** 32 - 1: 3}
+    for draw, want in cases.items():
+        a, n = O.verify_sample(np.array([[1]]), q, p, np.array([[0.3]], np.float32), np.array([draw], np.uint64))
+        assert a[0] == 1 and n[0] == want, (draw, n[0], want)
