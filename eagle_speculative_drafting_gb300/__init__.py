@@ -88,6 +88,8 @@ _sig("peagle_draft_step", c_int32, c_void_p, c_int32, c_int32, c_void_p, c_void_
      c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
 _sig("peagle_verify_accept", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
      c_void_p)
+_sig("peagle_verify_sample", c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+     c_void_p, c_void_p, c_void_p, c_void_p)
 _sig("peagle_cod_counts", c_int32, c_int32, c_int32, c_double, c_double, ctypes.POINTER(c_int32))
 _sig("peagle_cod_select_workspace_size", c_int32, c_int32, c_int32, ctypes.POINTER(c_size_t))
 _sig("peagle_cod_select", c_int32, c_int32, c_int32, c_double, c_double, ctypes.c_uint64,
@@ -206,6 +208,13 @@ def peagle_draft_step(model, B, K, aux, anchor_tokens, anchor_pos, k_cache, v_ca
 def peagle_verify_accept(B, K, draft_tokens, target_tokens, accept_len, next_token, stream=None):
     _check(_lib.peagle_verify_accept(B, K, ptr(draft_tokens), ptr(target_tokens), ptr(accept_len),
                                      ptr(next_token), _stream(stream)), "peagle_verify_accept")
+
+
+def peagle_verify_sample(B, K, V, draft_tokens, draft_probs, target_probs, accept_u, draws, accept_len,
+                         next_token, stream=None):
+    _check(_lib.peagle_verify_sample(B, K, V, ptr(draft_tokens), ptr(draft_probs), ptr(target_probs),
+                                     ptr(accept_u), ptr(draws), ptr(accept_len), ptr(next_token),
+                                     _stream(stream)), "peagle_verify_sample")
 
 
 def peagle_cod_counts(n, K, r, r_min):

@@ -601,6 +601,33 @@ peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_to
   return PEAGLE_OK;
 }
 
+peagle_status peagle_verify_sample(int32_t B, int32_t K, int32_t V, const int32_t* draft_tokens,
+                                   const float* draft_probs, const float* target_probs, const float* accept_u,
+                                   const uint32_t* draws, int32_t* accept_len, int32_t* next_token, void* stream) {
+  if (B < 0 || K < 1 || K > 64 || V < 1 || V > (1 << 23))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "verify_sample: B=%d K=%d V=%d (K in [1,64], V in [1, 2^23])", B, K, V);
+  if (B == 0) return PEAGLE_OK;
+  if (!draft_tokens || !draft_probs || !target_probs || !accept_u || !draws || !accept_len || !next_token)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "verify_sample: a pointer is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SampleArgs sa{};
+  sa.B = B;
+  sa.K = K;
+  sa.V = V;
+  sa.drafts = draft_tokens;
+  sa.q = draft_probs;
+  sa.p = target_probs;
+  sa.u = accept_u;
+  sa.draws = draws;
+  sa.accept = accept_len;
+  sa.next = next_token;
+  CUDA_TRY(library_status_word(&sa.status));
+  probe_start(PEAGLE_OP_VERIFY, s);
+  CUDA_TRY(launch_verify_sample(sa, s));
+  probe_stop(PEAGLE_OP_VERIFY, s);
+  return PEAGLE_OK;
+}
+
 // ======================================================================= COD
 peagle_status peagle_cod_counts(int32_t n, int32_t K, double r, double r_min, int32_t* counts) {
   if (n < 0 || n > (1 << 24) || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "cod_counts: n=%d K=%d", n, K);

@@ -133,6 +133,19 @@ cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, in
 cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st);
 cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStream_t st);
 
+// Stochastic verification (rejection sampling) of B requests' K drafts.
+struct SampleArgs {
+  int B, K, V;
+  const int* drafts;       // [B, K] target ids
+  const float* q;          // [B, K, V] draft probabilities
+  const float* p;          // [B, K+1, V] target probabilities
+  const float* u;          // [B, K] acceptance uniforms in [0, 1)
+  const uint32_t* draws;   // [B] uniform 32-bit draws
+  int *accept, *next;      // [B]
+  int* status;             // PEAGLE_DEV_BOUNDS for a draft id outside [0, V)
+};
+cudaError_t launch_verify_sample(const SampleArgs& a, cudaStream_t st);
+
 void decode_attn_plan(int B, int nkv, int max_kv_len, int* chunk, int* nsplit);
 cudaError_t launch_decode_attn(int dtype, const DecodeAttnArgs& a, int probe_op, cudaStream_t st);
 // Query tiles of the tensor-core training attention: 64 rows of one depth.

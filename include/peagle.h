@@ -197,6 +197,35 @@ peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_to
                                    const int32_t* target_tokens, int32_t* accept_len,
                                    int32_t* next_token, void* stream);
 
+/* ---- stochastic verification ------------------------------------------- */
+/* Rejection sampling of the drafts ("P_Eagle" README, How Speculative
+ * Decoding Works: accepted tokens are used, rejected ones resampled, and the
+ * output is distributed as the target's), by the published speculative-
+ * sampling rule (Leviathan, Kalman, Matias, ICML 2023; Chen et al. 2023):
+ *   depth i keeps draft x = draft_tokens[b, i] iff
+ *     fl32(accept_u[b, i] * q_i(x)) < p_i(x)          (fp32 product)
+ *   accept_len[b] = number of depths kept before the first rejection;
+ *   next_token[b] = a draw from max(0, p_a - q_a) at the first rejection a,
+ *   or from p_K when all K are kept (the bonus token).
+ * The draw is exact integer inverse-CDF: each weight (clamped to [0, 1], NaN
+ * as 0) becomes W_j = floor(w_j * 2^40), S = sum W_j, T = (draws[b] * S) >> 32,
+ * and the token is the smallest j whose inclusive prefix sum of W exceeds T.
+ * If S == 0 the token is the lowest-index argmax of p_a.
+ *   draft_tokens device int32 [B, K], target vocab ids
+ *   draft_probs  device float [B, K, V]: q_i, the draft distribution of depth
+ *                i over the target vocab (0 outside the draft vocab)
+ *   target_probs device float [B, K+1, V]: p_i, the target's distribution at
+ *                the position of depth i; row K is the bonus position
+ *   accept_u     device float [B, K], uniform in [0, 1)
+ *   draws        device uint32 [B], uniform 32-bit integers
+ *   accept_len, next_token device int32 [B]
+ * B >= 0, K in [1, 64], V in [1, 2^23]. A draft id outside [0, V) counts as
+ * rejected and sets PEAGLE_DEV_BOUNDS in the library status word. */
+peagle_status peagle_verify_sample(int32_t B, int32_t K, int32_t V, const int32_t* draft_tokens,
+                                   const float* draft_probs, const float* target_probs,
+                                   const float* accept_u, const uint32_t* draws, int32_t* accept_len,
+                                   int32_t* next_token, void* stream);
+
 /* ---- COD selection ------------------------------------------------------ */
 /* Host only: counts[0] = n, counts[d] = min(counts[d-1], max(floor(n*r^d),
  * floor(n*r_min))) with r^d formed by repeated multiplication in double

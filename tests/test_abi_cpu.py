@@ -122,3 +122,15 @@ def test_probe_api_validates(pe):
     with pytest.raises(pe.PeagleError):
         pe.peagle_probe_begin(99, 4)
     assert pe.peagle_op_name(4) == "gate_up"
+
+
+def test_verify_sample_rejects_bad_sizes_without_launch(pe):
+    before = pe.peagle_kernel_launches()
+    for B, K, V in ((2, 0, 10), (2, 65, 10), (2, 4, 0), (2, 4, (1 << 23) + 1), (-1, 4, 10)):
+        with pytest.raises(pe.PeagleError) as e:
+            pe.peagle_verify_sample(B, K, V, 1, 1, 1, 1, 1, 1, 1, stream=0)
+        assert e.value.status == pe.PEAGLE_ERR_INVALID_ARG
+    with pytest.raises(pe.PeagleError):
+        pe.peagle_verify_sample(2, 4, 10, None, 1, 1, 1, 1, 1, 1, stream=0)
+    pe.peagle_verify_sample(0, 4, 10, None, None, None, None, None, None, None, stream=0)
+    assert pe.peagle_kernel_launches() == before

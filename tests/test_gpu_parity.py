@@ -431,3 +431,80 @@ def test_checkpoint_round_trip_gives_the_same_draft_step(tmp_path):
     assert np.array_equal(a["logits"], b["logits"])
     assert np.array_equal(a["draft_tokens"], b["draft_tokens"])
     assert np.array_equal(model2._keep["t2d"].cpu().numpy(), t2d)
+
+
+# --------------------------------------------------- stochastic verification
+def _softmax32(x):
+    x = x - x.max(-1, keepdims=True)
+    e = np.exp(x)
+    return (e / e.sum(-1, keepdims=True)).astype(np.float32)
+
+
+def run_verify_sample(drafts, q, p, u, draws):
+    m = pe()
+    B, K = drafts.shape
+    V = p.shape[-1]
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dt).cuda()
+    a = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+    m.peagle_verify_sample(B, K, V, dev(drafts, torch.int32), dev(q, torch.float32), dev(p, torch.float32),
+                           dev(u, torch.float32), dev(np.asarray(draws, np.uint32).view(np.int32), torch.int32), a, n)
+    torch.cuda.synchronize()
+    return a.cpu().numpy(), n.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,K,V,temp", [(64, 8, 32000, 1.0), (64, 8, 32000, 0.3), (5, 1, 3, 1.0),
+                                        (300, 4, 7, 2.0), (3, 16, 1000, 0.05), (40, 64, 129, 1.0)])
+def test_verify_sample_bit_exact(B, K, V, temp):
+    rng = np.random.default_rng(B * 31 + K + V)
+    # draft and target distributions from nearby logits, drafts drawn from q
+    base = rng.standard_normal((B, K + 1, V)) * 3.0
+    p = _softmax32((base + 0.5 * rng.standard_normal(base.shape)) / temp)
+    q = _softmax32(base[:, :K] / temp)
+    cdf = np.cumsum(q.astype(np.float64), -1)
+    drafts = np.minimum((cdf > rng.random((B, K, 1))).argmax(-1), V - 1).astype(np.int32)
+    u = rng.random((B, K)).astype(np.float32)
+    draws = rng.integers(0, 2 ** 32, B, dtype=np.uint64)
+    a, n = run_verify_sample(drafts, q, p, u, draws)
+    ra, rn = O.verify_sample(drafts, q, p, u, draws)
+    assert np.array_equal(a, ra) and np.array_equal(n, rn)
+    assert 0 < a.mean() < K or K == 1
+    assert pe().peagle_get_library_status() == 0
+
+
+def test_verify_sample_edge_cases():
+    rng = np.random.default_rng(2)
+    B, K, V = 6, 3, 50
+    # one-hot distributions: greedy verify, on the GPU as in the oracle
+    d = rng.integers(0, V, (B, K)).astype(np.int32)
+    t = rng.integers(0, V, (B, K + 1)).astype(np.int32)
+    t[:3, :K] = d[:3]
+    q = np.eye(V, dtype=np.float32)[d]
+    p = np.eye(V, dtype=np.float32)[t]
+    u = rng.random((B, K)).astype(np.float32)
+    draws = rng.integers(0, 2 ** 32, B, dtype=np.uint64)
+    a, n = run_verify_sample(d, q, p, u, draws)
+    ga, gn = O.verify_accept(d, t)
+    assert np.array_equal(a, ga) and np.array_equal(n, gn)
+    # p == q, drafts of zero probability: rejected, empty residual -> argmax
+    pz = np.full((B, K + 1, V), 0.0, np.float32)
+    pz[..., 7] = 0.5
+    pz[..., 9] = 0.5
+    a, n = run_verify_sample(np.zeros((B, K), np.int32), pz[:, :K], pz, u, draws)
+    assert (a == 0).all() and (n == 7).all()
+    # NaN and out-of-[0,1] weights count as 0 / 1 on both sides
+    pn = _softmax32(rng.standard_normal((B, K + 1, V)))
+    pn[:, :, 3] = np.nan
+    pn[:, :, 4] = 5.0
+    qn = _softmax32(rng.standard_normal((B, K, V)))
+    a, n = run_verify_sample(d, qn, pn, u, draws)
+    ra, rn = O.verify_sample(d, qn, pn, u, draws)
+    assert np.array_equal(a, ra) and np.array_equal(n, rn)
+    # a draft id outside the vocab is a rejection and a bounds fault
+    pe().peagle_clear_library_status()
+    bad = d.copy()
+    bad[0, 0] = V + 3
+    a, n = run_verify_sample(bad, q, p, u, draws)
+    assert a[0] == 0
+    assert pe().peagle_get_library_status() & pe().PEAGLE_DEV_BOUNDS
+    pe().peagle_clear_library_status()
