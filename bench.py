@@ -386,20 +386,33 @@ def allowed_pairs(indices, counts, cu):
 
 
 def run_train(args, wl):
+    """Training-shaped forward. With N ranks every rank runs its own packed
+    sequence of the workload's shape (data parallel, weak scaling); the ranks
+    exchange their per-depth sums in one NCCL all-reduce per step and every
+    rank combines them into the batch loss."""
     import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     import __graft_entry__
-    __graft_entry__.build()
+    if rank == 0:
+        __graft_entry__.build()
+    if dist:
+        dist.barrier()
     import eagle_speculative_drafting_gb300 as pe
     import synth
-    from eagle_speculative_drafting_gb300 import marshal
+    from eagle_speculative_drafting_gb300 import dp, marshal
 
     W = synth.make_weights(wl)
-    inp = synth.make_train_inputs(wl)
+    # sequence `rank` of the global batch: its own conversations and tokens
+    inp = synth.make_train_inputs(wl.scaled(seed=wl.seed + 7919 * rank) if rank else wl)
     model = marshal.make_model(wl, W)
     d = marshal.upload_train(wl, inp)
-    n, K, r, rmin, seed = wl.n_tokens, inp["K"], inp["r"], inp["r_min"], inp["seed"]
+    n, K, r, rmin = wl.n_tokens, inp["K"], inp["r"], inp["r_min"]
+    seed = dp.sequence_seed(inp["seed"], rank) if world > 1 else inp["seed"]
     counts = pe.peagle_cod_counts(n, K, r, rmin)
     R = sum(counts)
     idx = torch.empty(R, dtype=torch.int32, device="cuda")
@@ -413,11 +426,23 @@ def run_train(args, wl):
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     S = len(inp["cu_seqlens"]) - 1
+    sums = torch.zeros(3 * K, dtype=torch.float64, **dev)
 
     def step(dd):
+        if dist is None:
+            pe.peagle_parallel_forward(model.handle, n, dd["aux"], dd["input_ids"], dd["position_ids"],
+                                       dd["cu_seqlens"], S, dd["labels"], None, K, r, rmin, seed,
+                                       inp["depth_decay"], *outs, None, None, None, ws, nbytes, stream)
+            return
+        # data parallel: this rank's sequence adds its depth sums, one
+        # all-reduce, then the batch loss on every rank
+        sums.zero_()
         pe.peagle_parallel_forward(model.handle, n, dd["aux"], dd["input_ids"], dd["position_ids"],
                                    dd["cu_seqlens"], S, dd["labels"], None, K, r, rmin, seed,
-                                   inp["depth_decay"], *outs, None, None, None, ws, nbytes, stream)
+                                   inp["depth_decay"], *outs, None, None, None, ws, nbytes, stream,
+                                   depth_sums=sums)
+        dp.allreduce_depth_sums(sums, dist)
+        pe.peagle_combine_depth_sums(K, inp["depth_decay"], sums, *outs, stream)
 
     for _ in range(max(args.warmup, 3)):
         step(d)
@@ -434,14 +459,18 @@ def run_train(args, wl):
     launches0 = pe.peagle_kernel_launches()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(args.steps):
         step(d)
     e1.record(stream)
     torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     launches = pe.peagle_kernel_launches() - launches0
-    ms_step = e0.elapsed_time(e1) / args.steps
+    ms_step = max_over_ranks(e0.elapsed_time(e1), dist, "cuda") / args.steps
     # the dominant op, timed with CUDA events around its launches in a pass
     # of its own (events between PDL-chained kernels serialize them)
     probe_steps = max(1, min(args.steps, 10))
@@ -457,6 +486,8 @@ def run_train(args, wl):
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in outs)
     e_steps = max(1, min(args.steps, 50))
+    if dist:
+        dist.barrier()
     torch.cuda.synchronize()
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
@@ -472,13 +503,19 @@ def run_train(args, wl):
     e3.record(stream)
     torch.cuda.synchronize()
     clk.__exit__(None, None, None)
-    e2e_ms = e2.elapsed_time(e3) / e_steps
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / e_steps, dist, "cuda")
+    status = pe.peagle_get_device_status(model.handle)
+    if rank != 0:
+        model.close()
+        if dist:
+            dist.destroy_process_group()
+        return
     _, _, peak, src = measured_peaks()
     src += " (sustained)"
     total_dom_ms = float(np.sum(dom_ms)) / probe_steps if dom_ms else None
     achieved = flops[dom] / (total_dom_ms / 1000.0) / 1e12 if total_dom_ms else None
     line = {
-        "metric": TRAIN_METRIC, "value": R / (ms_step / 1000.0), "unit": "rows/s", "n_gpus": world,
+        "metric": TRAIN_METRIC, "value": world * R / (ms_step / 1000.0), "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic",
@@ -486,9 +523,11 @@ def run_train(args, wl):
                    "cod_counts": counts, "layers": wl.num_layers, "hidden": wl.hidden,
                    "heads": f"{wl.num_q_heads}q/{wl.num_kv_heads}kv x {wl.head_dim}",
                    "intermediate": wl.intermediate, "draft_vocab": wl.vocab,
-                   "l2": "activations and weights far larger than L2, no flush"},
+                   "l2": "activations and weights far larger than L2, no flush",
+                   "parallelism": f"data parallel over {world} rank(s): one packed sequence each, "
+                                  "one all-reduce of the per-depth sums per step"},
         "gpu_launches": int(launches),
-        "e2e": {"value": R / (e2e_ms / 1000.0), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": world * R / (e2e_ms / 1000.0), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_source": src, "unit": "TFLOP/s",
@@ -496,11 +535,13 @@ def run_train(args, wl):
                      "algorithmic_flops_per_step": flops[dom], "ms_per_step": total_dom_ms},
         "step_shares_ms": {k: round(v, 4) for k, v in shares.items()},
         "flops_per_step": {k: v for k, v in flops.items()},
-        "device_status": pe.peagle_get_device_status(model.handle),
+        "device_status": status,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     model.close()
+    if dist:
+        dist.destroy_process_group()
 
 
 # ------------------------------------------------------------------- ours

@@ -840,8 +840,8 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
                                       const int32_t* labels, const uint8_t* loss_mask, int32_t K, double r,
                                       double r_min, uint64_t seed, double depth_decay, float* per_depth_loss,
                                       float* per_depth_acc, int32_t* per_depth_valid, float* loss,
-                                      int32_t* row_argmax, float* row_ce, float* logits, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
+                                      int32_t* row_argmax, float* row_ce, float* logits, double* depth_sums,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
   if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_forward: model is NULL");
   const peagle_config& c = m->cfg;
   int32_t counts[16];
@@ -1053,7 +1053,19 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
   cr.acc_d = per_depth_acc;
   cr.valid_d = per_depth_valid;
   cr.loss = loss;
+  cr.sums = depth_sums;
   CUDA_TRY(launch_ce_reduce(cr, s));
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_combine_depth_sums(int32_t K, double depth_decay, const double* depth_sums,
+                                        float* per_depth_loss, float* per_depth_acc, int32_t* per_depth_valid,
+                                        float* loss, void* stream) {
+  if (K < 1 || K > 16 || !isfinite(depth_decay)) FAIL(PEAGLE_ERR_INVALID_ARG, "combine_depth_sums: K=%d", K);
+  if (!depth_sums || !per_depth_loss || !per_depth_acc || !per_depth_valid || !loss)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "combine_depth_sums: a pointer is NULL");
+  CUDA_TRY(launch_depth_sums_combine(K, depth_decay, depth_sums, per_depth_loss, per_depth_acc, per_depth_valid,
+                                     loss, static_cast<cudaStream_t>(stream)));
   return PEAGLE_OK;
 }
 

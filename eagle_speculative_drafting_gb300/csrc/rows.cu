@@ -534,9 +534,34 @@ __global__ void ce_reduce_kernel(CeReduceArgs a) {
       a.acc_d[d] = C ? (float)((double)R / C) : 0.f;
       a.valid_d[d] = C;
       loss_acc += pow(a.decay, (double)d) * ld;
+      if (a.sums) {   // this sequence's share of a batch (one stream: no race)
+        a.sums[d] += S;
+        a.sums[a.K + d] += (double)R;
+        a.sums[2 * a.K + d] += (double)C;
+      }
     }
   }
   if (threadIdx.x == 0) a.loss[0] = (float)loss_acc;
+}
+
+// Per-depth mean CE, accuracy and label count, and the loss
+// sum_d decay^d * mean_d, from depth sums added over several packed
+// sequences (and ranks): the same arithmetic as the single-sequence reduction.
+__global__ void depth_sums_combine_kernel(int K, double decay, const double* sums, float* loss_d, float* acc_d,
+                                          int* valid_d, float* loss) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x != 0) return;
+  double acc = 0.0;
+  for (int d = 0; d < K; ++d) {
+    const double S = sums[d], R = sums[K + d], C = sums[2 * K + d];
+    const double ld = C > 0 ? S / C : 0.0;
+    loss_d[d] = (float)ld;
+    acc_d[d] = C > 0 ? (float)(R / C) : 0.f;
+    valid_d[d] = (int)C;
+    acc += pow(decay, (double)d) * ld;
+  }
+  loss[0] = (float)acc;
 }
 
 // -------------------------------------------------------------------------
@@ -853,6 +878,12 @@ cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, con
 
 cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st) {
   launch_pdl(ce_reduce_kernel, 1, 1024, 0, st, a);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_depth_sums_combine(int K, double decay, const double* sums, float* loss_d, float* acc_d,
+                                      int* valid_d, float* loss, cudaStream_t st) {
+  launch_pdl(depth_sums_combine_kernel, 1, 32, 0, st, K, decay, sums, loss_d, acc_d, valid_d, loss);
   PE_LAUNCH_END();
 }
 

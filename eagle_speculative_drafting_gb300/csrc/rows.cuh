@@ -59,6 +59,7 @@ struct CeReduceArgs {
   double decay;
   float *loss_d, *acc_d, *loss;
   int* valid_d;
+  double* sums;           // optional [3, K]: += sum CE, correct rows, labelled rows per depth
 };
 
 struct TrainMetaArgs {
@@ -123,6 +124,9 @@ cudaError_t launch_lm_argmax(const GemmOut& in, int rows, int V, float* logits, 
 cudaError_t launch_ce_rows(const GemmOut& in, int rows, int V, int row0, const int* row_label,
                            float* logits_out, float* row_ce, int* row_am, cudaStream_t st);
 cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st);
+// Per-depth means and the decay-weighted loss from summed [3, K] depth sums.
+cudaError_t launch_depth_sums_combine(int K, double decay, const double* sums, float* loss_d, float* acc_d,
+                                      int* valid_d, float* loss, cudaStream_t st);
 cudaError_t launch_ce_merge(int rows, int part_ld, int row0, const float* p_max, const float* p_sum,
                             const float* p_lab, const int* p_idx, const int* row_label, float* row_ce, int* row_am,
                             cudaStream_t st);

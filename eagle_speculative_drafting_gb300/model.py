@@ -111,7 +111,7 @@ class Model:
 
     def parallel_forward(self, aux, input_ids, position_ids, cu_seqlens, labels, K, r, r_min, seed,
                          depth_decay=0.8, loss_mask=None, row_argmax=None, row_ce=None,
-                         logits=None, stream=None):
+                         logits=None, stream=None, depth_sums=None):
         n = input_ids.numel()
         nbytes = peagle_parallel_forward_workspace_size(self.handle, n, K, r, r_min)
         ws = self.workspace(("train", n, K, r, r_min), nbytes)
@@ -126,7 +126,7 @@ class Model:
                                 cu_seqlens.numel() - 1, labels, loss_mask, K, r, r_min, seed,
                                 depth_decay, out["per_depth_loss"], out["per_depth_acc"],
                                 out["per_depth_valid"], out["loss"], row_argmax, row_ce, logits,
-                                ws, nbytes, stream)
+                                ws, nbytes, stream, depth_sums=depth_sums)
         return out
 
     def save_checkpoint(self, directory, stream=None):

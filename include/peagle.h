@@ -274,6 +274,9 @@ peagle_status peagle_parallel_forward_workspace_size(const peagle_model* model, 
  *   row_argmax     int32 [R] or NULL (draft-vocab argmax, lowest index on ties)
  *   row_ce         [R] or NULL (CE of the row, NaN if it has no label)
  *   logits         [R, Vd] or NULL
+ *   depth_sums     double [3, K] or NULL: the sequence's sum of CE, correct
+ *                  rows and labelled rows per depth are ADDED to it (see
+ *                  peagle_combine_depth_sums)
  * R = sum of the COD counts. */
 peagle_status peagle_parallel_forward(const peagle_model* model, int32_t n, const void* aux,
                                       const int32_t* input_ids, const int32_t* position_ids,
@@ -283,8 +286,20 @@ peagle_status peagle_parallel_forward(const peagle_model* model, int32_t n, cons
                                       double depth_decay, float* per_depth_loss,
                                       float* per_depth_acc, int32_t* per_depth_valid,
                                       float* loss, int32_t* row_argmax, float* row_ce,
-                                      float* logits, void* workspace, size_t workspace_bytes,
-                                      void* stream);
+                                      float* logits, double* depth_sums, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+/* Data-parallel training over several packed sequences (#2376, Validation:
+ * the 8-GPU run): the sequences are independent, so each rank runs its own
+ * whole sequences, each call adding its per-depth sums to depth_sums, and
+ * the ranks exchange those K*3 numbers in one all-reduce (sum). This call
+ * turns the summed depth_sums [3, K] (row 0: sum of CE over labelled rows,
+ * row 1: rows whose argmax is the label, row 2: labelled rows) into the
+ * per-depth means, counts and the loss sum_d depth_decay^d * mean_d, with
+ * the arithmetic of the single-sequence reduction (a depth without labelled
+ * rows contributes 0). All pointers device. K in [1, 16]. */
+peagle_status peagle_combine_depth_sums(int32_t K, double depth_decay, const double* depth_sums,
+                                        float* per_depth_loss, float* per_depth_acc,
+                                        int32_t* per_depth_valid, float* loss, void* stream);
 
 /* ---- dense contraction --------------------------------------------------- */
 peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, int32_t K,

@@ -660,6 +660,36 @@ def parallel_forward(model: DraftModel, aux, input_ids, position_ids, cu_seqlens
     return res
 
 
+# --------------------------------------------------------------------------
+# A batch of packed sequences  [PR: Validation (8-GPU training), Changelog
+# (0.8**d weighted-mean schedule)]: the loss of a batch averages each depth's
+# CE over the labelled rows of every sequence, then weights the depths.
+# --------------------------------------------------------------------------
+def depth_sums(res, K):
+    """[3, K] of one forward's result: sum of CE over labelled rows, labelled
+    rows whose argmax is the label, labelled rows -- per depth."""
+    out = np.zeros((3, K))
+    for d in range(K):
+        m = (res["depth"] == d) & (res["row_label"] >= 0)
+        out[0, d] = float(np.sum(res["row_ce"][m]))
+        out[1, d] = float(np.sum(res["row_argmax"][m] == res["row_label"][m]))
+        out[2, d] = float(np.sum(m))
+    return out
+
+
+def loss_from_depth_sums(sums, decay=0.8):
+    """Per-depth mean CE, accuracy and count, and sum_d decay^d * mean_d (a
+    depth without labelled rows contributes 0)."""
+    sums = np.asarray(sums, dtype=np.float64)
+    K = sums.shape[1]
+    C = sums[2]
+    loss_d = np.where(C > 0, sums[0] / np.maximum(C, 1), 0.0)
+    acc_d = np.where(C > 0, sums[1] / np.maximum(C, 1), 0.0)
+    loss = float(sum(decay ** d * loss_d[d] for d in range(K)))
+    return {"per_depth_loss": loss_d, "per_depth_acc": acc_d, "per_depth_valid": C.astype(np.int64),
+            "loss": loss}
+
+
 def model_config(wl, norm_before_residual=True) -> dict:
     """Config dict for a synthetic workload description (attribute access)."""
     return {

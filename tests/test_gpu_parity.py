@@ -508,3 +508,29 @@ def test_verify_sample_edge_cases():
     assert a[0] == 0
     assert pe().peagle_get_library_status() & pe().PEAGLE_DEV_BOUNDS
     pe().peagle_clear_library_status()
+
+
+# ------------------------------------------------------ data-parallel training
+def test_data_parallel_forward_sums_two_sequences_like_the_oracle():
+    # one process: two packed sequences accumulate their depth sums in one
+    # buffer; the combined loss is the oracle's batch loss. A single sequence
+    # combined reproduces the forward's own outputs exactly.
+    from eagle_speculative_drafting_gb300 import dp
+    wl, inp = small_train(dtype="bf16", n=300, lens=(120, 7, 100, 73), K=4)
+    _, inp2 = small_train(dtype="bf16", n=200, lens=(150, 50), K=4)
+    W = synth.make_weights(wl)
+    model = H().make_model(wl, W)
+    seqs = [(0, H().upload_train(wl, inp)), (1, H().upload_train(wl, inp2))]
+    fwd = dp.DataParallelForward(model, 4, 0.7, 0.2, base_seed=77)
+    out = {k: v.cpu().numpy() for k, v in fwd.step(seqs).items()}
+    om = H().oracle_model(wl, W)
+    ref = O.loss_from_depth_sums(sum(
+        O.depth_sums(O.parallel_forward(om, **x, K=4, r=0.7, r_min=0.2, seed=dp.sequence_seed(77, i)), 4)
+        for i, x in ((0, inp), (1, inp2))))
+    assert np.array_equal(out["per_depth_valid"], ref["per_depth_valid"])
+    assert H().max_abs_rel(out["per_depth_loss"], ref["per_depth_loss"]) <= BF16_TOL
+    assert abs(float(out["loss"][0]) - ref["loss"]) <= BF16_TOL * max(1.0, ref["loss"])
+    one = {k: v.cpu().numpy() for k, v in dp.DataParallelForward(model, 4, 0.7, 0.2, 77).step(seqs[:1]).items()}
+    direct = H().run_train(wl, model, inp, 4, 0.7, 0.2, dp.sequence_seed(77, 0))
+    for k in ("per_depth_loss", "per_depth_acc", "per_depth_valid", "loss"):
+        assert np.array_equal(one[k], direct[k]), k

@@ -694,3 +694,33 @@ def test_verify_sample_draw_intervals_are_half_open():
     for draw, want in cases.items():
         a, n = O.verify_sample(np.array([[1]]), q, p, np.array([[0.3]], np.float32), np.array([draw], np.uint64))
         assert a[0] == 1 and n[0] == want, (draw, n[0], want)
+
+
+# ------------------------------------------------------------ batch of sequences
+def test_depth_sums_of_one_sequence_give_its_loss():
+    wl, model, W, inp = tiny_train()
+    res = O.parallel_forward(model, **inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    got = O.loss_from_depth_sums(O.depth_sums(res, wl.K))
+    assert abs(got["loss"] - res["loss"]) < 1e-12
+    assert np.allclose(got["per_depth_loss"], res["per_depth_loss"], atol=1e-12)
+    assert np.allclose(got["per_depth_acc"], res["per_depth_acc"], atol=1e-15)
+    assert np.array_equal(got["per_depth_valid"], res["per_depth_valid"])
+
+
+def test_batch_loss_is_library_cross_entropy_over_all_sequences():
+    # two packed sequences: each depth's mean is taken over the labelled rows
+    # of both, then the depths are weighted by 0.8^d
+    wl, model, W, inp = tiny_train()
+    wl2, _, _, inp2 = tiny_train(n=17, S_lens=(10, 7), seed=6)
+    res = [O.parallel_forward(model, **x, K=wl.K, r=0.7, r_min=0.2, seed=sd)
+           for x, sd in ((inp, 9), (inp2, 4))]
+    got = O.loss_from_depth_sums(sum(O.depth_sums(r_, wl.K) for r_ in res))
+    total = 0.0
+    for d in range(wl.K):
+        lg = np.concatenate([r_["logits"][(r_["depth"] == d) & (r_["row_label"] >= 0)] for r_ in res])
+        lb = np.concatenate([r_["row_label"][(r_["depth"] == d) & (r_["row_label"] >= 0)] for r_ in res])
+        ce = float(torch.nn.functional.cross_entropy(torch.from_numpy(lg), torch.from_numpy(lb)))
+        assert abs(ce - got["per_depth_loss"][d]) < 1e-12
+        assert got["per_depth_valid"][d] == len(lb)
+        total += 0.8 ** d * ce
+    assert abs(total - got["loss"]) < 1e-12
