@@ -456,6 +456,71 @@ def _draft_step_dense(model, aux, anchor_tokens, anchor_pos, k_cache, v_cache,
 
 
 # --------------------------------------------------------------------------
+# Decode over new context rows  [PR: Equivalence to vLLM inference -- the
+# flat [context, new rows, mask_1..mask_{K-1}] layout; UG: Inference Process]
+# Each request brings n_b >= 1 new rows (token, aux state, position); the
+# last is the anchor. Row j of a request (its new rows, then its masked
+# depths 1..K-1) attends to the request's cached context and to its rows
+# 0..j. The new rows' K/V join the context.
+# --------------------------------------------------------------------------
+def draft_step_ctx(model: DraftModel, new_aux, new_tokens, new_pos, k_cache, v_cache, kv_offsets,
+                   kv_lens, K):
+    """new_aux / new_tokens / new_pos: per request, a list (or array) of its
+    new rows. Returns draft_tokens [B, K], logits [B, K, Vd] (depth rows:
+    the anchor, then the masked rows) and appended[l][b] = (k, v) of the
+    request's new rows."""
+    c = model.cfg
+    B = len(new_tokens)
+    ptd = c["ptd_token_id"]
+    h_mask = model.masked_hidden()
+    out_tok = np.zeros((B, K), dtype=np.int64)
+    out_logits = np.zeros((B, K, c["draft_vocab"]))
+    appended = [dict() for _ in range(c["num_layers"])]
+    for b in range(B):
+        n = len(new_tokens[b])
+        assert n >= 1
+        hp = model.project_hidden(np.asarray(new_aux[b], dtype=np.float64).reshape(n, -1))
+        toks = np.array(list(new_tokens[b]) + [ptd] * (K - 1), dtype=np.int64)
+        h = np.concatenate([hp, np.stack([h_mask] * (K - 1))]) if K > 1 else hp
+        emb = model.embed[toks]
+        anchor = int(new_pos[b][n - 1])
+        pos = np.array(list(new_pos[b]) + [anchor + d for d in range(1, K)], dtype=np.int64)
+        off, Lb = int(kv_offsets[b]), int(kv_lens[b])
+        rows = n + K - 1
+        allowed = np.zeros((rows, Lb + rows), dtype=bool)
+        allowed[:, :Lb] = True
+        for j in range(rows):
+            allowed[j, Lb:Lb + j + 1] = True
+        for l in range(c["num_layers"]):
+            ck = np.asarray(k_cache[l][off:off + Lb], dtype=np.float64)
+            cv = np.asarray(v_cache[l][off:off + Lb], dtype=np.float64)
+
+            def attend(q, k, v, ck=ck, cv=cv):
+                return masked_attention(q, np.concatenate([ck, k]), np.concatenate([cv, v]), allowed)
+
+            h, k, v = model.layer(l, h, emb, pos, attend)
+            appended[l][b] = (k[:n].copy(), v[:n].copy())
+        logits = model.head(h[n - 1:])
+        out_logits[b] = logits
+        out_tok[b] = model.to_target(argmax_lowest(logits))
+    return {"draft_tokens": out_tok, "logits": out_logits, "appended": appended}
+
+
+def next_context(drafts, accept, nxt, anchor_pos):
+    """The next step's new rows after verification [UG: Inference Process,
+    steps 3-4]: request b continues with its a_b accepted drafts and the
+    target's token, at the positions after its anchor. Returns per request
+    (tokens, positions)."""
+    out_tok, out_pos = [], []
+    for b in range(len(accept)):
+        a = int(accept[b])
+        toks = [int(t) for t in drafts[b, :a]] + [int(nxt[b])]
+        out_tok.append(toks)
+        out_pos.append([int(anchor_pos[b]) + 1 + j for j in range(a + 1)])
+    return out_tok, out_pos
+
+
+# --------------------------------------------------------------------------
 # Training-shaped parallel forward  [PR: description, Changelog (core:
 # PEagleTrainerModule), Equivalence to vLLM inference; UG: COD Sampling;
 # RM: cu_seqlens isolation]

@@ -724,3 +724,79 @@ def test_batch_loss_is_library_cross_entropy_over_all_sequences():
         assert got["per_depth_valid"][d] == len(lb)
         total += 0.8 ** d * ce
     assert abs(total - got["loss"]) < 1e-12
+
+
+# ------------------------------------------------------- new context rows
+def test_draft_step_ctx_with_one_new_row_is_the_anchor_step():
+    wl = tiny_workload()
+    model, W = tiny_model(wl)
+    inp = synth.make_decode_inputs(wl)
+    args = (inp["k_cache"], inp["v_cache"], inp["kv_offsets"], inp["kv_lens"], wl.K)
+    a = O.draft_step(model, inp["aux"], inp["anchor_tokens"], inp["anchor_pos"], *args, append_anchor_kv=True)
+    b = O.draft_step_ctx(model, [inp["aux"][i:i + 1] for i in range(wl.batch)],
+                         [[t] for t in inp["anchor_tokens"]], [[p] for p in inp["anchor_pos"]], *args)
+    assert np.array_equal(a["logits"], b["logits"]) and np.array_equal(a["draft_tokens"], b["draft_tokens"])
+    for l in range(wl.num_layers):
+        for r in range(wl.batch):
+            assert np.array_equal(a["appended"][l][r][0], b["appended"][l][r][0][0])
+
+
+def test_draft_step_ctx_equals_the_training_layout():
+    # a conversation prefix fed as new rows over an empty cache is the
+    # training layout's anchor: the depth logits equal parallel_forward's
+    # rows (i, d) (pinned against expanded decode), and the new rows' K/V
+    # equal its depth-0 K/V
+    wl, model, W, inp = tiny_train()
+    res = O.parallel_forward(model, **inp, K=wl.K, r=1.0, r_min=1.0, seed=3, keep_kv=True)
+    n = wl.n_tokens
+    cu = inp["cu_seqlens"]
+    empty = [np.zeros((1, wl.num_kv_heads, wl.head_dim))] * wl.num_layers
+    for i in (0, 5, 8, 9, 12, 22):
+        s = int(cu[np.searchsorted(cu, i, side="right") - 1])
+        out = O.draft_step_ctx(model, [inp["aux"][s:i + 1]], [inp["input_ids"][s:i + 1]],
+                               [inp["position_ids"][s:i + 1]], empty, empty, [0], [0], wl.K)
+        for d in range(wl.K):
+            assert np.allclose(out["logits"][0, d], res["logits"][d * n + i], atol=1e-12, rtol=0)
+        for l in range(wl.num_layers):
+            assert np.allclose(out["appended"][l][0][0], res["kv"][l][0][s:i + 1], atol=1e-12)
+
+
+def test_draft_step_ctx_split_over_two_calls_matches_one_call():
+    # feeding new rows in two steps (the first appending its rows to the
+    # cache) drafts what one step over all of them drafts
+    wl = tiny_workload(kv_len_range=(2, 5))
+    model, W = tiny_model(wl)
+    inp = synth.make_decode_inputs(wl, spare=8)
+    rng = np.random.default_rng(12)
+    B = wl.batch
+    n = [3, 1, 4]
+    aux = [rng.standard_normal((k, wl.num_aux * wl.target_hidden)) for k in n]
+    tok = [rng.integers(0, wl.vocab, k) for k in n]
+    pos = [list(range(int(inp["kv_lens"][b]), int(inp["kv_lens"][b]) + n[b])) for b in range(B)]
+    one = O.draft_step_ctx(model, aux, tok, pos, inp["k_cache"], inp["v_cache"], inp["kv_offsets"],
+                           inp["kv_lens"], wl.K)
+    m = [1, 0, 2]   # rows of the first call (a request needs at least one: b=1 takes all in call 2)
+    kc = [k.copy() for k in inp["k_cache"]]
+    vc = [v.copy() for v in inp["v_cache"]]
+    first = [b for b in range(B) if m[b] > 0]
+    o1 = O.draft_step_ctx(model, [aux[b][:m[b]] for b in first], [tok[b][:m[b]] for b in first],
+                          [pos[b][:m[b]] for b in first], kc, vc, inp["kv_offsets"][first],
+                          inp["kv_lens"][first], wl.K)
+    lens = inp["kv_lens"].copy()
+    for i, b in enumerate(first):
+        for l in range(wl.num_layers):
+            k, v = o1["appended"][l][i]
+            o = int(inp["kv_offsets"][b] + lens[b])
+            kc[l][o:o + m[b]] = k
+            vc[l][o:o + m[b]] = v
+        lens[b] += m[b]
+    two = O.draft_step_ctx(model, [aux[b][m[b]:] for b in range(B)], [tok[b][m[b]:] for b in range(B)],
+                           [pos[b][m[b]:] for b in range(B)], kc, vc, inp["kv_offsets"], lens, wl.K)
+    assert np.allclose(one["logits"], two["logits"], atol=1e-12)
+    assert np.array_equal(one["draft_tokens"], two["draft_tokens"])
+
+
+def test_next_context_hand_worked():
+    drafts = np.array([[5, 6, 7], [8, 9, 1]])
+    toks, pos = O.next_context(drafts, np.array([2, 0]), np.array([40, 41]), np.array([10, 20]))
+    assert toks == [[5, 6, 40], [41]] and pos == [[11, 12, 13], [21]]
