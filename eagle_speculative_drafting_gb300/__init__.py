@@ -86,6 +86,13 @@ _sig("peagle_draft_step_workspace_size", c_int32, c_void_p, c_int32, c_int32, c_
 _sig("peagle_draft_step", c_int32, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
      ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_void_p, c_void_p, c_int64, c_int32,
      c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
+_sig("peagle_draft_step_ctx_workspace_size", c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32,
+     ctypes.POINTER(c_size_t))
+_sig("peagle_draft_step_ctx", c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+     c_void_p, c_void_p, ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_void_p, c_void_p, c_int64,
+     c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p)
+_sig("peagle_next_context", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p)
 _sig("peagle_verify_accept", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
      c_void_p)
 _sig("peagle_verify_sample", c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -205,6 +212,32 @@ def peagle_draft_step(model, B, K, aux, anchor_tokens, anchor_pos, k_cache, v_ca
                                   int(append_anchor_kv), ptr(draft_tokens), ptr(logits),
                                   ptr(workspace), workspace_bytes, _stream(stream)),
            "peagle_draft_step")
+
+
+def peagle_draft_step_ctx_workspace_size(model, B, K, total_new, max_new, max_kv_len):
+    n = c_size_t()
+    _check(_lib.peagle_draft_step_ctx_workspace_size(model, B, K, total_new, max_new, max_kv_len,
+                                                     ctypes.byref(n)), "peagle_draft_step_ctx_workspace_size")
+    return n.value
+
+
+def peagle_draft_step_ctx(model, B, K, total_new, max_new, new_offsets, new_aux, new_tokens, new_pos, k_cache,
+                          v_cache, kv_offsets, kv_lens, kv_capacity, max_kv_len, append_new_kv, draft_tokens,
+                          logits, workspace, workspace_bytes, stream=None):
+    L = len(k_cache)
+    karr = (c_void_p * L)(*[ptr(t) for t in k_cache])
+    varr = (c_void_p * L)(*[ptr(t) for t in v_cache])
+    _check(_lib.peagle_draft_step_ctx(model, B, K, total_new, max_new, ptr(new_offsets), ptr(new_aux),
+                                      ptr(new_tokens), ptr(new_pos), karr, varr, ptr(kv_offsets), ptr(kv_lens),
+                                      kv_capacity, max_kv_len, int(append_new_kv), ptr(draft_tokens), ptr(logits),
+                                      ptr(workspace), workspace_bytes, _stream(stream)), "peagle_draft_step_ctx")
+
+
+def peagle_next_context(B, K, draft_tokens, accept_len, next_token, cur_offsets, cur_pos, kv_lens, next_offsets,
+                        next_tokens, next_pos, stream=None):
+    _check(_lib.peagle_next_context(B, K, ptr(draft_tokens), ptr(accept_len), ptr(next_token), ptr(cur_offsets),
+                                    ptr(cur_pos), ptr(kv_lens), ptr(next_offsets), ptr(next_tokens), ptr(next_pos),
+                                    _stream(stream)), "peagle_next_context")
 
 
 def peagle_verify_accept(B, K, draft_tokens, target_tokens, accept_len, next_token, stream=None):

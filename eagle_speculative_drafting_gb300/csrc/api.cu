@@ -391,11 +391,14 @@ struct DraftWs {
   int chunk, nsplit;
 };
 
-static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, Bump& bp, DraftWs& ws) {
+// Workspace of a step with N new rows in all (at most max_new per request);
+// rows = N + B*(K-1). The one-anchor step is N = B, max_new = 1.
+static void draft_layout(const peagle_config& c, int B, int K, int N, int max_new, int max_kv_len, Bump& bp,
+                         DraftWs& ws) {
   const size_t es = esize(c);
-  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K;
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = N + B * (K - 1), heads = B * K;
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
-  ws.x0 = bp.take_bytes((size_t)B * 2 * H * es);
+  ws.x0 = bp.take_bytes((size_t)N * 2 * H * es);
   ws.xin = bp.take_bytes((size_t)rows * H * es);
   ws.act = bp.take_bytes((size_t)rows * I * es);
   ws.q = bp.take_bytes((size_t)rows * nq * hd * es);
@@ -403,22 +406,22 @@ static void draft_layout(const peagle_config& c, int B, int K, int max_kv_len, B
   ws.vc = bp.take_bytes((size_t)rows * nkv * hd * es);
   ws.ao = bp.take_bytes((size_t)rows * nq * hd * es);
   ws.h = bp.take<float>((size_t)rows * H);
-  ws.resid0 = bp.take<float>((size_t)B * H);
-  size_t pf = gemm_out_floats(c.dtype, B, H, AHt);
-  pf = std::max(pf, gemm_out_floats(c.dtype, B, QKV, 2 * H));
+  ws.resid0 = bp.take<float>((size_t)N * H);
+  size_t pf = gemm_out_floats(c.dtype, N, H, AHt);
+  pf = std::max(pf, gemm_out_floats(c.dtype, N, QKV, 2 * H));
   pf = std::max(pf, gemm_out_floats(c.dtype, rows, QKV, H));
   pf = std::max(pf, gemm_out_floats(c.dtype, rows, H, nq * hd));
   pf = std::max(pf, gemm_out_floats(c.dtype, rows, 2 * I, H));
   pf = std::max(pf, gemm_out_floats(c.dtype, rows, H, I));
-  pf = std::max(pf, gemm_out_floats(c.dtype, rows, c.draft_vocab, H));
+  pf = std::max(pf, gemm_out_floats(c.dtype, heads, c.draft_vocab, H));
   ws.part = bp.take<float>(pf);
   decode_attn_plan(B, nkv, max_kv_len, &ws.chunk, &ws.nsplit);
-  const size_t prow = (size_t)B * nkv * ws.nsplit * K * (nq / nkv);
+  const size_t prow = (size_t)B * nkv * ws.nsplit * (max_new + K - 1) * (nq / nkv);
   ws.attn_o = bp.take<float>(prow * hd);
   ws.attn_ml = bp.take<float>(prow * 2);
   const size_t nch = std::max<size_t>(lm_argmax_chunks(c.draft_vocab), (c.draft_vocab + 127) / 128);
-  ws.am_val = bp.take<float>((size_t)rows * nch);
-  ws.am_idx = bp.take<int>((size_t)rows * nch);
+  ws.am_val = bp.take<float>((size_t)heads * nch);
+  ws.am_idx = bp.take<int>((size_t)heads * nch);
 }
 
 peagle_status peagle_draft_step_workspace_size(const peagle_model* m, int32_t B, int32_t K, int32_t max_kv_len,
@@ -428,52 +431,50 @@ peagle_status peagle_draft_step_workspace_size(const peagle_model* m, int32_t B,
     FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_workspace_size: B=%d K=%d max_kv_len=%d", B, K, max_kv_len);
   Bump bp(nullptr);
   DraftWs ws;
-  draft_layout(m->cfg, B, K, max_kv_len, bp, ws);
+  draft_layout(m->cfg, B, K, B, 1, max_kv_len, bp, ws);
   *bytes = bp.off;
   return PEAGLE_OK;
 }
 
-peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, const void* aux,
-                                const int32_t* anchor_tokens, const int32_t* anchor_pos, void* const* k_cache,
-                                void* const* v_cache, const int64_t* kv_offsets, const int32_t* kv_lens,
-                                int64_t kv_capacity, int32_t max_kv_len, int32_t append_anchor_kv,
-                                int32_t* draft_tokens, float* logits, void* workspace, size_t workspace_bytes,
-                                void* stream) {
-  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: model is NULL");
-  const peagle_config& c = m->cfg;
-  if (B < 0 || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: B=%d K=%d (K in [1,16])", B, K);
-  if (max_kv_len < 0 || kv_capacity < 0) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: negative KV bound");
-  if (append_anchor_kv != 0 && append_anchor_kv != 1) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: append_anchor_kv");
-  if (B == 0) return PEAGLE_OK;
-  if (!aux || !anchor_tokens || !anchor_pos || !k_cache || !v_cache || !kv_offsets || !kv_lens || !draft_tokens)
-    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: a required pointer is NULL");
-  for (int l = 0; l < c.num_layers; ++l) {
-    if (!k_cache[l] || !v_cache[l]) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is NULL", l);
-    if (!aligned16(k_cache[l]) || !aligned16(v_cache[l]))
-      FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is not 16-byte aligned", l);
-  }
-  if (c.dtype == PEAGLE_BF16 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: aux not 16-byte aligned");
-  size_t need = 0;
-  peagle_draft_step_workspace_size(m, B, K, max_kv_len, &need);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
-    FAIL(PEAGLE_ERR_WORKSPACE, "draft_step: workspace %zu bytes at %p, need %zu (256-byte aligned)",
-         workspace_bytes, workspace, need);
+peagle_status peagle_draft_step_ctx_workspace_size(const peagle_model* m, int32_t B, int32_t K, int32_t total_new,
+                                                   int32_t max_new, int32_t max_kv_len, size_t* bytes) {
+  if (!m || !bytes) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx_workspace_size: NULL argument");
+  if (B < 0 || K < 1 || K > 16 || max_kv_len < 0 || max_new < 1 || max_new > 64 || total_new < B ||
+      (long long)total_new > (long long)B * max_new)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx_workspace_size: B=%d K=%d total_new=%d max_new=%d max_kv_len=%d", B,
+         K, total_new, max_new, max_kv_len);
+  Bump bp(nullptr);
+  DraftWs ws;
+  draft_layout(m->cfg, B, K, total_new, max_new, max_kv_len, bp, ws);
+  *bytes = bp.off;
+  return PEAGLE_OK;
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// One draft step over the rows `dr` describes: new rows (aux, tok, pos per
+// new row; the last new row of a request is its anchor) and K-1 masked rows
+// per request.
+static peagle_status draft_step_impl(const peagle_model* m, const DecodeRows& dr, const void* aux, const int32_t* tok,
+                                     const int32_t* pos, void* const* k_cache, void* const* v_cache,
+                                     const int64_t* kv_offsets, const int32_t* kv_lens, int64_t kv_capacity,
+                                     int32_t max_kv_len, int32_t append_kv, int32_t* draft_tokens, float* logits,
+                                     void* workspace, cudaStream_t s) {
+  const peagle_config& c = m->cfg;
+  const int B = dr.B, K = dr.K, N = dr.total_new;
   Bump bp(workspace);
   DraftWs ws;
-  draft_layout(c, B, K, max_kv_len, bp, ws);
-  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = B * K, L = c.num_layers;
+  draft_layout(c, B, K, N, dr.max_new, max_kv_len, bp, ws);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), rows = N + B * (K - 1), L = c.num_layers;
+  const int heads = B * K;
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
   const int dt = c.dtype;
   const float eps = (float)c.rms_eps;
   GemmOut go;
 
-  // fc + fc_norm over the anchors' aux states, then the layer-0 input rows
+  // fc + fc_norm over the new rows' aux states, then their layer-0 inputs
   FcFinishArgs fa{};
   fa.H = H;
   fa.Vt = c.target_vocab;
-  fa.tok = anchor_tokens;
+  fa.tok = tok;
   fa.embed = m->w.embed;
   fa.g_fc = m->w.fc_norm_w;
   fa.g_in = m->layers[0].in_norm_w;
@@ -483,15 +484,15 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
   fa.x0 = ws.x0;
   fa.resid = ws.resid0;
   fa.status = m->status;
-  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, B, H, AHt, ws.part, &go, m->sem, m->status, PEAGLE_OP_FC, s));
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, N, H, AHt, ws.part, &go, m->sem, m->status, PEAGLE_OP_FC, s));
   fa.u = go;
-  CUDA_TRY(launch_fc_finish(dt, B, fa, s));
+  CUDA_TRY(launch_fc_finish(dt, N, fa, s));
 
   for (int l = 0; l < L; ++l) {
     const peagle_layer_weights& W = m->layers[l];
     QkvArgs qa{};
     if (l == 0) {
-      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, B, QKV, 2 * H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s));
+      CUDA_TRY(gemm_launch(dt, ws.x0, 2 * H, W.qkv_w, N, QKV, 2 * H, ws.part, &go, m->sem, m->status, PEAGLE_OP_QKV, s));
       qa.mode = 1;
       qa.resid0 = ws.resid0;
       qa.mask_resid = m->mask_resid0;
@@ -506,15 +507,16 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     qa.hd = hd;
     qa.H = H;
     qa.K = K;
+    qa.rows = dr;
     qa.mask_qkv = m->mask_qkv0;
     qa.rcos = m->rcos;
     qa.rsin = m->rsin;
     qa.max_pos = c.max_position;
-    qa.anchor_pos = anchor_pos;
+    qa.anchor_pos = pos;
     qa.Q = ws.q;
     qa.Kout = ws.kc;
     qa.Vout = ws.vc;
-    if (append_anchor_kv) {
+    if (append_kv) {
       qa.kcache = k_cache[l];
       qa.vcache = v_cache[l];
     }
@@ -522,7 +524,6 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     qa.kv_len = kv_lens;
     qa.kv_cap = kv_capacity;
     qa.status = m->status;
-    // mode 1 reads the GEMM row of the anchor; mode 0 row r
     CUDA_TRY(launch_qkv_finish(dt, rows, qa, s));
 
     DecodeAttnArgs da{};
@@ -531,6 +532,9 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     da.nq = nq;
     da.nkv = nkv;
     da.hd = hd;
+    da.rows = dr;
+    da.R = rows;
+    da.rows_max = dr.max_new + K - 1;
     da.Q = ws.q;
     da.Kc = ws.kc;
     da.Vc = ws.vc;
@@ -564,10 +568,15 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     CUDA_TRY(gemm_launch(dt, ws.act, I, W.down_w, rows, H, I, ws.part, &go, m->sem, m->status, PEAGLE_OP_DOWN, s));
     ra.in = go;
     ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
+    if (l + 1 == L && dr.new_off) {   // only the depth rows go on to the head
+      ra.compact = 1;
+      ra.crows = dr;
+    }
     CUDA_TRY(launch_resid_norm(dt, rows, ra, s));
   }
-  // draft-vocab head and argmax per depth: bf16 reduces each output tile
-  // inside the GEMM (warp argmax); fp32 stores the logits and reduces them
+  // draft-vocab head and argmax per depth over the B*K depth rows: bf16
+  // reduces each output tile inside the GEMM (warp argmax); fp32 stores the
+  // logits and reduces them
   if (dt == PEAGLE_BF16) {
     GemmEpi ep{};
     ep.op = GEMM_EPI_ARGMAX;
@@ -575,15 +584,116 @@ peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, con
     ep.logits_ld = c.draft_vocab;
     ep.p_max = ws.am_val;
     ep.p_idx = ws.am_idx;
-    CUDA_TRY(gemm_launch_epi(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->sem,
+    CUDA_TRY(gemm_launch_epi(dt, ws.xin, H, m->w.lm_head_w, heads, c.draft_vocab, H, ws.part, &go, m->sem,
                              m->status, PEAGLE_OP_LM_HEAD, &ep, s));
-    CUDA_TRY(launch_lm_argmax_final(rows, gemm_col_tiles(rows, c.draft_vocab, H), ws.am_val, ws.am_idx, m->w.d2t,
+    CUDA_TRY(launch_lm_argmax_final(heads, gemm_col_tiles(heads, c.draft_vocab, H), ws.am_val, ws.am_idx, m->w.d2t,
                                     draft_tokens, s));
   } else {
-    CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, rows, c.draft_vocab, H, ws.part, &go, m->sem, m->status,
+    CUDA_TRY(gemm_launch(dt, ws.xin, H, m->w.lm_head_w, heads, c.draft_vocab, H, ws.part, &go, m->sem, m->status,
                          PEAGLE_OP_LM_HEAD, s));
-    CUDA_TRY(launch_lm_argmax(go, rows, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
+    CUDA_TRY(launch_lm_argmax(go, heads, c.draft_vocab, logits, ws.am_val, ws.am_idx, m->w.d2t, draft_tokens, s));
   }
+  return PEAGLE_OK;
+}
+
+static peagle_status check_caches(const peagle_config& c, void* const* k_cache, void* const* v_cache) {
+  for (int l = 0; l < c.num_layers; ++l) {
+    if (!k_cache[l] || !v_cache[l]) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is NULL", l);
+    if (!aligned16(k_cache[l]) || !aligned16(v_cache[l]))
+      FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: cache of layer %d is not 16-byte aligned", l);
+  }
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_draft_step(const peagle_model* m, int32_t B, int32_t K, const void* aux,
+                                const int32_t* anchor_tokens, const int32_t* anchor_pos, void* const* k_cache,
+                                void* const* v_cache, const int64_t* kv_offsets, const int32_t* kv_lens,
+                                int64_t kv_capacity, int32_t max_kv_len, int32_t append_anchor_kv,
+                                int32_t* draft_tokens, float* logits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: model is NULL");
+  const peagle_config& c = m->cfg;
+  if (B < 0 || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: B=%d K=%d (K in [1,16])", B, K);
+  if (max_kv_len < 0 || kv_capacity < 0) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: negative KV bound");
+  if (append_anchor_kv != 0 && append_anchor_kv != 1) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: append_anchor_kv");
+  if (B == 0) return PEAGLE_OK;
+  if (!aux || !anchor_tokens || !anchor_pos || !k_cache || !v_cache || !kv_offsets || !kv_lens || !draft_tokens)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: a required pointer is NULL");
+  peagle_status st = check_caches(c, k_cache, v_cache);
+  if (st) return st;
+  if (c.dtype == PEAGLE_BF16 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step: aux not 16-byte aligned");
+  size_t need = 0;
+  peagle_draft_step_workspace_size(m, B, K, max_kv_len, &need);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "draft_step: workspace %zu bytes at %p, need %zu (256-byte aligned)",
+         workspace_bytes, workspace, need);
+  DecodeRows dr{};
+  dr.B = B;
+  dr.K = K;
+  dr.new_off = nullptr;   // one anchor row per request
+  dr.total_new = B;
+  dr.max_new = 1;
+  return draft_step_impl(m, dr, aux, anchor_tokens, anchor_pos, k_cache, v_cache, kv_offsets, kv_lens, kv_capacity,
+                         max_kv_len, append_anchor_kv, draft_tokens, logits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+peagle_status peagle_draft_step_ctx(const peagle_model* m, int32_t B, int32_t K, int32_t total_new, int32_t max_new,
+                                    const int32_t* new_offsets, const void* new_aux, const int32_t* new_tokens,
+                                    const int32_t* new_pos, void* const* k_cache, void* const* v_cache,
+                                    const int64_t* kv_offsets, const int32_t* kv_lens, int64_t kv_capacity,
+                                    int32_t max_kv_len, int32_t append_new_kv, int32_t* draft_tokens, float* logits,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx: model is NULL");
+  const peagle_config& c = m->cfg;
+  size_t need = 0;
+  peagle_status st = peagle_draft_step_ctx_workspace_size(m, B, K, total_new, max_new, max_kv_len, &need);
+  if (st) return st;
+  if (kv_capacity < 0) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx: negative KV capacity");
+  if (append_new_kv != 0 && append_new_kv != 1) FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx: append_new_kv");
+  if (B == 0) return PEAGLE_OK;
+  if (!new_offsets || !new_aux || !new_tokens || !new_pos || !k_cache || !v_cache || !kv_offsets || !kv_lens ||
+      !draft_tokens)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx: a required pointer is NULL");
+  st = check_caches(c, k_cache, v_cache);
+  if (st) return st;
+  if (c.dtype == PEAGLE_BF16 && !aligned16(new_aux))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "draft_step_ctx: new_aux not 16-byte aligned");
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "draft_step_ctx: workspace %zu bytes at %p, need %zu (256-byte aligned)",
+         workspace_bytes, workspace, need);
+  DecodeRows dr{};
+  dr.B = B;
+  dr.K = K;
+  dr.new_off = new_offsets;
+  dr.total_new = total_new;
+  dr.max_new = max_new;
+  return draft_step_impl(m, dr, new_aux, new_tokens, new_pos, k_cache, v_cache, kv_offsets, kv_lens, kv_capacity,
+                         max_kv_len, append_new_kv, draft_tokens, logits, workspace, static_cast<cudaStream_t>(stream));
+}
+
+peagle_status peagle_next_context(int32_t B, int32_t K, const int32_t* draft_tokens, const int32_t* accept_len,
+                                  const int32_t* next_token, const int32_t* cur_offsets, const int32_t* cur_pos,
+                                  int32_t* kv_lens, int32_t* next_offsets, int32_t* next_tokens, int32_t* next_pos,
+                                  void* stream) {
+  if (B < 0 || B > 65536 || K < 1 || K > 16) FAIL(PEAGLE_ERR_INVALID_ARG, "next_context: B=%d K=%d", B, K);
+  if (!next_offsets) FAIL(PEAGLE_ERR_INVALID_ARG, "next_context: next_offsets is NULL");
+  if (B > 0 && (!draft_tokens || !accept_len || !next_token || !cur_offsets || !cur_pos || !kv_lens ||
+                !next_tokens || !next_pos))
+    FAIL(PEAGLE_ERR_INVALID_ARG, "next_context: a pointer is NULL");
+  NextContextArgs na{};
+  na.B = B;
+  na.K = K;
+  na.drafts = draft_tokens;
+  na.accept = accept_len;
+  na.next = next_token;
+  na.cur_off = cur_offsets;
+  na.cur_pos = cur_pos;
+  na.kv_lens = kv_lens;
+  na.next_off = next_offsets;
+  na.next_tok = next_tokens;
+  na.next_pos = next_pos;
+  CUDA_TRY(library_status_word(&na.status));
+  CUDA_TRY(launch_next_context(na, static_cast<cudaStream_t>(stream)));
   return PEAGLE_OK;
 }
 

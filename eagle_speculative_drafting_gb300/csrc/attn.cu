@@ -3,13 +3,15 @@
 // flat [context, mask_1..mask_{K-1}] layout; "P_Eagle" README: packed
 // conversations isolated by cu_seqlens).
 //
-// Decode, row (b, d), query head h, KV head g = h / (nq/nkv):
+// Decode, row j of request b (DecodeRows: its new rows, the last of them the
+// anchor, then its masked depths), query head h, KV head g = h / (nq/nkv):
 //   keys = context rows kv_off[b] .. kv_off[b]+kv_len[b]-1 of the cache,
-//          then chain rows (b, 0..d) of this pass.
+//          then the request's rows 0..j of this pass (causal in the flat
+//          [context, new rows, mask_1..mask_{K-1}] layout).
 // The context is split into chunks; one CTA per (chunk, g, b) streams that
-// chunk once for all K*G query rows that read head g, keeping an online
-// softmax (max m, sum l, unnormalised o) per row. A combine kernel merges
-// the chunks' (m, l, o) and adds the chain keys.
+// chunk once for all the request's query rows that read head g, keeping an
+// online softmax (max m, sum l, unnormalised o) per row. A combine kernel
+// merges the chunks' (m, l, o) and adds the in-request keys.
 //
 // Training, row (i, d): keys = depth-0 rows start(i)..i, then chain rows
 // (i, 1..d).
@@ -43,7 +45,8 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
   pdl_trigger();
   pdl_wait();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
+  const int G = a.nq / a.nkv, hd = a.hd;
+  const int KGmax = a.rows_max * G;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const long long off = a.kv_off[b];
   int L = a.kv_len[b];
@@ -52,14 +55,16 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
     if (threadIdx.x == 0 && split == 0 && g == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
     L = 0;
   }
+  if (!dr_valid(a.rows, b)) return;   // flagged by the q/k/v kernel
+  const int KG = (dr_new(a.rows, b) + a.K - 1) * G, rb = dr_base(a.rows, b);
   const int k0 = split * a.chunk, k1 = min(L, k0 + a.chunk);
-  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KG;
+  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KGmax;
   const T* kc = static_cast<const T*>(a.kcache);
   const T* vc = static_cast<const T*>(a.vcache);
   const T* Q = static_cast<const T*>(a.Q);
   for (int qi = w; qi < KG; qi += nw) {
     const int d = qi / G, h = g * G + qi % G;
-    const int r = b * a.K + d;
+    const int r = rb + d;
     float q[E], o[E];
     load_vec<T, E>(Q + ((size_t)r * a.nq + h) * hd + lane * E, q);
 #pragma unroll
@@ -86,16 +91,19 @@ __global__ void __launch_bounds__(256) decode_split_simt(DecodeAttnArgs a) {
   }
 }
 
-// Output row (r = (b, d), head h) from the chunks' (m, l, o) plus the chain
-// keys (b, 0..d); one warp, lane owns dims [lane*E, lane*E + E). The query,
+// Output row r (row d of request b), head h, from the chunks' (m, l, o)
+// plus the request's rows 0..d; one warp, lane owns dims [lane*E, lane*E + E). The query,
 // the chunk statistics, the first chunk outputs and the first chain keys /
 // values are all loaded before any of them is used, so the row costs about
 // two memory round trips.
 template <typename T, int E>
 __device__ void combine_row(const DecodeAttnArgs& a, int r, int h, int lane) {
   constexpr int SB = 8, CB = 4;   // chunk outputs / chain rows per load round
-  const int b = r / a.K, d = r % a.K;
-  const int G = a.nq / a.nkv, KG = a.K * G, hd = a.hd;
+  int d;
+  const int b = dr_request(a.rows, r, &d);
+  if (!dr_valid(a.rows, b) || d < 0 || d >= dr_new(a.rows, b) + a.K - 1) return;   // flagged by the q/k/v kernel
+  const int rb = dr_base(a.rows, b);
+  const int G = a.nq / a.nkv, KG = a.rows_max * G, hd = a.hd;
   const int g = h / G, qi = d * G + h % G;
   // only the chunks that hold context keys of request b carry partials
   const long long off = a.kv_off[b];
@@ -108,7 +116,7 @@ __device__ void combine_row(const DecodeAttnArgs& a, int r, int h, int lane) {
   const size_t prow = (size_t)(b * a.nkv + g) * a.nsplit * KG;
   auto ml = [&](int s) { return a.part_ml + (prow + (size_t)s * KG + qi) * 2; };
   auto po_at = [&](int s) { return a.part_o + (prow + (size_t)s * KG + qi) * hd + lane * E; };
-  auto kv_at = [&](int j) { return ((size_t)(b * a.K + j) * a.nkv + g) * hd + lane * E; };
+  auto kv_at = [&](int j) { return ((size_t)(rb + j) * a.nkv + g) * hd + lane * E; };
 
   float q[E];
   load_vec<T, E>(Q + ((size_t)r * a.nq + h) * hd + lane * E, q);
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
   float* sSum = sMax + NW * QR;                            // [NW][QR]
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-  const int G = a.nq / a.nkv, KG = a.K * G;
+  const int G = a.nq / a.nkv;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const long long off = a.kv_off[b];
   int L = a.kv_len[b];
@@ -293,6 +301,10 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
   const int k0 = split * a.chunk, k1 = min(L, k0 + a.chunk);
   const int ntiles = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
   if (ntiles == 0) return;   // a chunk past the context end: the merge skips it
+  if (!dr_valid(a.rows, b)) return;   // flagged by the q/k/v kernel
+  // this request's query rows of KV head g: row qi = d*G + (h % G) for its
+  // rows d = 0 .. n_b + K - 2; the partials are laid out for rows_max rows
+  const int KG = (dr_new(a.rows, b) + a.K - 1) * G, KGmax = a.rows_max * G, rb = dr_base(a.rows, b);
   const bf16* kc = static_cast<const bf16*>(a.kcache);
   const bf16* vc = static_cast<const bf16*>(a.vcache);
   const bf16* Q = static_cast<const bf16*>(a.Q);
@@ -320,7 +332,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
     const int qi = e / (HD / 8), c8 = e % (HD / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
     if (qi < KG) {
-      const int r = b * a.K + qi / G, h = g * G + qi % G;
+      const int r = rb + qi / G, h = g * G + qi % G;
       v = *reinterpret_cast<const uint4*>(Q + ((size_t)r * a.nq + h) * HD + c8 * 8);
     }
     *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
     __syncthreads();
   }
   // ---- partial (unnormalised O, m in natural-log units, l)
-  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KG;
+  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KGmax;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -537,7 +549,7 @@ static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
 
 template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
-  const int KG = a.K * (a.nq / a.nkv);
+  const int KG = a.rows_max * (a.nq / a.nkv);
   if (KG <= 16) return launch_split_mma<1, HD, HD / 16, 3>(a, st);
   if (KG <= 32) return launch_split_mma<2, HD, 4, 3>(a, st);
   if (KG <= 64) return launch_split_mma<4, HD>(a, st);
@@ -560,7 +572,7 @@ static cudaError_t decode_attn_t(const DecodeAttnArgs& a_in, int probe_op, cudaS
   const DecodeAttnArgs& a = a_in;
   dim3 grid(a.nsplit, a.nkv, a.B);
   probe_start(probe_op, st);
-  if (sizeof(T) == 2 && a.K * (a.nq / a.nkv) <= 128) {
+  if (sizeof(T) == 2 && a.rows_max * (a.nq / a.nkv) <= 128) {
     cudaError_t e = (E == 4) ? split_mma_hd<128>(a, st) : split_mma_hd<64>(a, st);
     if (e != cudaSuccess) return e;
   } else {
@@ -568,7 +580,7 @@ static cudaError_t decode_attn_t(const DecodeAttnArgs& a_in, int probe_op, cudaS
   }
   note_launch();
   probe_stop(probe_op, st);
-  launch_pdl(decode_combine<T, E>, dim3(a.B * a.K, (a.nq + 3) / 4), 128, 0, st, a);
+  launch_pdl(decode_combine<T, E>, dim3(a.R, (a.nq + 3) / 4), 128, 0, st, a);
   note_launch();
   return cudaGetLastError();
 }

@@ -139,9 +139,12 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
 //           otherwise the precomputed masked q/k/v (every masked row of layer
 //           0 has the same input: ptd embedding + projected mask_hidden);
 //   mode 2  all rows masked (training layer 0, depths >= 1).
-// Position: decode pos = anchor_pos[b] + d; training pos = row_pos[r].
-// Layer 0 also seeds the residual stream h with the row's layer-0 residual.
-// Decode can append the anchor row's K/V to its cache.
+// Decode rows follow DecodeRows: row j of request b is new row j (its own
+// position; GEMM row new_off[b] + j in layer 0) for j < n_b, else masked
+// depth d = j - n_b + 1 at the anchor's position + d. Training: pos =
+// row_pos[r]. Layer 0 also seeds the residual stream h with the row's layer-0
+// residual. Decode can append the new rows' K/V to their cache slots
+// kv_off[b] + kv_len[b] + j.
 // -------------------------------------------------------------------------
 template <typename T, int HD>
 __global__ void __launch_bounds__(kQkvThreads) qkv_finish_kernel(QkvArgs a) {
@@ -149,13 +152,23 @@ __global__ void __launch_bounds__(kQkvThreads) qkv_finish_kernel(QkvArgs a) {
   pdl_wait();
   constexpr int HALF = HD / 2;
   const int r = blockIdx.x + a.row0;
-  int src;
-  if (a.mode == 0) src = r - a.src0;
-  else if (a.mode == 1) src = (r % a.K == 0) ? r / a.K : -1;
-  else src = -1;
-  int pos;
-  if (a.row_pos) pos = a.row_pos[r];
-  else pos = a.anchor_pos[r / a.K] + r % a.K;
+  int src = -1, pos = 0, b = 0, j = 0, nb = 1;
+  const bool decode = !a.row_pos;
+  if (!decode) {
+    src = a.mode == 0 ? r - a.src0 : -1;
+    pos = a.row_pos[r];
+  } else {
+    b = dr_request(a.rows, r, &j);
+    if (!dr_valid(a.rows, b) || j < 0 || j >= dr_new(a.rows, b) + a.K - 1) {
+      if (threadIdx.x == 0 && blockIdx.y == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+      return;
+    }
+    nb = dr_new(a.rows, b);
+    const int first = a.rows.new_off ? a.rows.new_off[b] : b;   // new-row index of (b, 0)
+    if (a.mode == 0) src = r - a.src0;
+    else src = j < nb ? first + j : -1;
+    pos = j < nb ? a.anchor_pos[first + j] : a.anchor_pos[first + nb - 1] + (j - nb + 1);
+  }
   if (pos < 0 || pos >= a.max_pos) {
     if (threadIdx.x == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
     pos = pos < 0 ? 0 : a.max_pos - 1;
@@ -170,9 +183,8 @@ __global__ void __launch_bounds__(kQkvThreads) qkv_finish_kernel(QkvArgs a) {
 
   bool append = false;
   size_t cache_row = 0;
-  if (a.kcache && !a.row_pos && (r % a.K) == 0) {   // decode anchor row, every layer
-    const int b = r / a.K;
-    const long long row = a.kv_off[b] + (long long)a.kv_len[b];
+  if (a.kcache && decode && j < nb) {   // a decode new row, every layer
+    const long long row = a.kv_off[b] + (long long)a.kv_len[b] + j;
     if (a.kv_len[b] >= 0 && row < a.kv_off[b + 1] && row < a.kv_cap && a.kv_off[b] >= 0) {
       append = true;
       cache_row = (size_t)row;
@@ -273,13 +285,22 @@ __global__ void resid_norm_kernel(ResidNormArgs a) {
   for (int i = 0; i < EPT; ++i) ss += v[i] * v[i];
   block_sum3(ss, d1, d2, red);
   const float inv = rsqrtf(ss / H + a.eps);
-  T* y = static_cast<T*>(a.y) + (size_t)r * H;
+  // the final norm of a decode step keeps only each request's depth rows
+  // (the anchor and the masked rows), packed as row b * K + depth
+  long long yrow = r;
+  if (a.compact) {
+    int jj;
+    const int b = dr_request(a.crows, r, &jj);
+    const int d = jj - (dr_new(a.crows, b) - 1);
+    yrow = (dr_valid(a.crows, b) && d >= 0 && d < a.crows.K) ? (long long)b * a.crows.K + d : -1;
+  }
+  T* y = static_cast<T*>(a.y) + (yrow >= 0 ? (size_t)yrow * H : 0);
 #pragma unroll
   for (int i = 0; i < EPT; ++i) {
     const int j = tid + i * bd;
     if (j < H) {
       h[j] = v[i];
-      y[j] = from_f<T>(v[i] * inv * gv[i]);
+      if (yrow >= 0) y[j] = from_f<T>(v[i] * inv * gv[i]);
     }
   }
 }
@@ -878,6 +899,67 @@ cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, con
 
 cudaError_t launch_ce_reduce(const CeReduceArgs& a, cudaStream_t st) {
   launch_pdl(ce_reduce_kernel, 1, 1024, 0, st, a);
+  PE_LAUNCH_END();
+}
+
+// -------------------------------------------------------------------------
+// The next draft step's new rows after verification ("P-EAGLE" user guide,
+// Inference Process: the accepted drafts are kept, the target supplies the
+// next token, and the next round continues from there). Request b: the
+// current step's n_b rows become context (kv_lens[b] += n_b); the next step
+// brings a_b + 1 rows -- drafts 0..a_b-1 and the next token -- at the
+// positions after the current anchor. One CTA: a block scan of the counts.
+// -------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) next_context_kernel(NextContextArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int s_warp[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < a.B; b0 += 1024) {
+    const int b = b0 + tid;
+    int n = 0, acc = 0, cur_lo = 0, cur_hi = 0;
+    if (b < a.B) {
+      cur_lo = a.cur_off[b];
+      cur_hi = a.cur_off[b + 1];
+      acc = a.accept[b];
+      if (acc < 0 || acc > a.K || cur_hi <= cur_lo) {
+        set_status(a.status, PEAGLE_DEV_BOUNDS);
+        acc = acc < 0 ? 0 : (acc > a.K ? a.K : acc);
+      }
+      n = acc + 1;
+    }
+    int incl = n;   // inclusive scan of n over the block
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp[w] = incl;
+    __syncthreads();
+    int before = s_carry;
+    for (int i = 0; i < w; ++i) before += s_warp[i];
+    const int off = before + incl - n;
+    if (b < a.B) {
+      a.next_off[b] = off;
+      if (cur_hi > cur_lo) a.kv_lens[b] += cur_hi - cur_lo;
+      const int p = cur_hi > cur_lo ? a.cur_pos[cur_hi - 1] : 0;   // the current anchor's position
+      for (int j = 0; j < n; ++j) {
+        a.next_tok[off + j] = j < acc ? a.drafts[(size_t)b * a.K + j] : a.next[b];
+        a.next_pos[off + j] = p + 1 + j;
+      }
+    }
+    __syncthreads();
+    if (tid == 1023) s_carry = off + n;
+    __syncthreads();
+  }
+  if (tid == 0) a.next_off[a.B] = s_carry;
+}
+
+cudaError_t launch_next_context(const NextContextArgs& a, cudaStream_t st) {
+  launch_pdl(next_context_kernel, 1, 1024, 0, st, a);
   PE_LAUNCH_END();
 }
 

@@ -4,6 +4,50 @@
 
 namespace pe {
 
+// Rows of a decode step. Request b owns rows [base(b), base(b) + n_b + K - 1):
+// its n_b new rows (context rows whose K/V are new; the last one is the
+// anchor, depth 0), then its K - 1 masked rows (depths 1..K-1). In this flat
+// layout ["feat(speculative) ... #2376", Equivalence to vLLM inference:
+// context, then the new rows, then mask_1..mask_{K-1}] row j of request b
+// attends to the cached context and to the request's rows 0..j.
+// new_off == NULL is the one-anchor step: n_b = 1, base(b) = b * K.
+struct DecodeRows {
+  int B, K;
+  const int* new_off;   // device [B+1], exclusive prefix sums of n_b, or NULL
+  int total_new;        // new_off[B] (host copy)
+  int max_new;          // host bound on n_b
+};
+__device__ __forceinline__ int dr_new(const DecodeRows& d, int b) {
+  return d.new_off ? d.new_off[b + 1] - d.new_off[b] : 1;
+}
+__device__ __forceinline__ int dr_base(const DecodeRows& d, int b) {
+  return d.new_off ? d.new_off[b] + b * (d.K - 1) : b * d.K;
+}
+// Whether request b's new-row range is well formed (1 <= n_b <= max_new,
+// inside [0, total_new]).
+__device__ __forceinline__ bool dr_valid(const DecodeRows& d, int b) {
+  if (!d.new_off) return true;
+  const int lo = d.new_off[b], hi = d.new_off[b + 1];
+  return lo >= 0 && hi <= d.total_new && hi - lo >= 1 && hi - lo <= d.max_new;
+}
+// Request of row r (the largest b with base(b) <= r), and r's index within it.
+__device__ __forceinline__ int dr_request(const DecodeRows& d, int r, int* j) {
+  int b;
+  if (!d.new_off) {
+    b = r / d.K;
+  } else {
+    int lo = 0, hi = d.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (dr_base(d, mid) <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    b = lo;
+  }
+  *j = r - dr_base(d, b);
+  return b;
+}
+
 struct FcFinishArgs {
   GemmOut u;              // fc partials, row r at u.out + r * ldo
   int H, Vt;
@@ -30,8 +74,9 @@ struct QkvArgs {
   float* h;               // residual stream to seed (layer 0) or NULL
   const float *rcos, *rsin;
   int max_pos;
-  const int* anchor_pos;  // decode positions (used when row_pos == NULL)
+  const int* anchor_pos;  // decode: position of each new row (one per request when rows.new_off is NULL)
   const int* row_pos;     // training positions per row
+  DecodeRows rows;        // decode row layout (mode 1 and decode mode 0)
   void *Q, *Kout, *Vout;  // [rows, nq*hd], [rows, nkv*hd] x2
   void *kcache, *vcache;  // decode append target (layer's cache) or NULL
   const int64_t* kv_off;
@@ -48,6 +93,9 @@ struct ResidNormArgs {
   const void* gain;
   float eps;
   void* y;                // out normalised rows (global rows)
+  int compact;            // decode final norm: write y only for each request's depth
+                          // rows, at row b * K + depth (the anchor is depth 0)
+  DecodeRows crows;       // the step's row layout when compact
 };
 
 struct CeReduceArgs {
@@ -87,17 +135,20 @@ struct CodArgs {
 // Depth-masked decode attention (split over the context) + combine.
 struct DecodeAttnArgs {
   int B, K, nq, nkv, hd;
-  const void* Q;          // [B*K, nq, hd]
-  const void *Kc, *Vc;    // chain rows [B*K, nkv, hd]
+  DecodeRows rows;        // request b's rows: [base(b), base(b) + n_b + K - 1)
+  int R;                  // rows of the step
+  int rows_max;           // max_new + K - 1: query rows per request the partials are sized for
+  const void* Q;          // [R, nq, hd]
+  const void *Kc, *Vc;    // the step's rows [R, nkv, hd]
   const void *kcache, *vcache;  // [cap, nkv, hd]
   const int64_t* kv_off;
   const int* kv_len;
   long long kv_cap;
   int max_kv_len;
   int chunk, nsplit;      // context keys per split, splits per (b, kv head)
-  float* part_o;          // [B, nkv, nsplit, K*G, hd]
-  float* part_ml;         // [B, nkv, nsplit, K*G, 2]
-  void* O;                // out [B*K, nq, hd]
+  float* part_o;          // [B, nkv, nsplit, rows_max*G, hd]
+  float* part_ml;         // [B, nkv, nsplit, rows_max*G, 2]
+  void* O;                // out [R, nq, hd]
   float scale;
   int* status;
 };
@@ -134,6 +185,13 @@ cudaError_t launch_lm_argmax_final(int rows, int nchunks, const float* pval, con
                                    int* tokens, cudaStream_t st);
 cudaError_t launch_train_meta(const TrainMetaArgs& a, cudaStream_t st);
 cudaError_t launch_verify(int B, int K, const int* d, const int* t, int* acc, int* next, cudaStream_t st);
+struct NextContextArgs {
+  int B, K;
+  const int *drafts, *accept, *next, *cur_off, *cur_pos;
+  int *kv_lens, *next_off, *next_tok, *next_pos;
+  int* status;
+};
+cudaError_t launch_next_context(const NextContextArgs& a, cudaStream_t st);
 cudaError_t launch_cod_select(const CodArgs& a, cudaStream_t st);
 cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStream_t st);
 

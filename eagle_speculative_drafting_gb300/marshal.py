@@ -11,7 +11,8 @@ max_position, rope_theta, rms_eps).
 import numpy as np
 import torch
 
-from . import peagle_cod_counts, peagle_verify_accept
+from . import (peagle_cod_counts, peagle_draft_step_ctx, peagle_draft_step_ctx_workspace_size,
+               peagle_verify_accept)
 from .model import Model, make_config
 
 
@@ -136,3 +137,33 @@ def run_train(wl, model, inp, K, r, r_min, seed, decay=0.8, want_logits=False, d
             res["logits"] = logits.cpu().numpy()[:R].astype(np.float64)
     res["counts"] = counts
     return res
+
+
+def run_decode_ctx(wl, model, new_aux, new_tokens, new_pos, d, kv_lens, kv_capacity, max_kv_len,
+                   want_logits=False, K=None):
+    """One draft step over new context rows: per request b, new_aux[b]
+    [n_b, A*Ht], new_tokens[b] and new_pos[b] (n_b each). ``d`` holds the
+    device caches and kv_offsets (as upload_decode returns); kv_lens is a
+    host array. The new rows' K/V are appended to the caches."""
+    K = wl.K if K is None else K
+    B = len(new_tokens)
+    n = np.array([len(t) for t in new_tokens], dtype=np.int32)
+    off = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    total, max_new = int(off[-1]), int(n.max())
+    aux = dev(np.concatenate([np.asarray(a, dtype=np.float32).reshape(len(t), -1)
+                              for a, t in zip(new_aux, new_tokens)]), tdtype(wl))
+    tok = dev(np.concatenate([np.asarray(t, dtype=np.int32) for t in new_tokens]))
+    pos = dev(np.concatenate([np.asarray(p, dtype=np.int32) for p in new_pos]))
+    Vd = model.cfg.draft_vocab
+    drafts = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    logits = torch.empty((B, K, Vd), dtype=torch.float32, device="cuda") if want_logits else None
+    nbytes = peagle_draft_step_ctx_workspace_size(model.handle, B, K, total, max_new, max_kv_len)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    peagle_draft_step_ctx(model.handle, B, K, total, max_new, dev(off), aux, tok, pos, d["k_cache"], d["v_cache"],
+                          d["kv_offsets"], dev(np.asarray(kv_lens, dtype=np.int32)), int(kv_capacity), max_kv_len,
+                          1, drafts, logits, ws, nbytes)
+    torch.cuda.synchronize()
+    out = {"draft_tokens": drafts.cpu().numpy()}
+    if want_logits:
+        out["logits"] = logits.cpu().numpy().astype(np.float64)
+    return out

@@ -186,6 +186,61 @@ peagle_status peagle_draft_step(const peagle_model* model, int32_t B, int32_t K,
                                 int32_t* draft_tokens, float* logits, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* ---- draft step over new context rows ------------------------------------ */
+peagle_status peagle_draft_step_ctx_workspace_size(const peagle_model* model, int32_t B, int32_t K,
+                                                   int32_t total_new, int32_t max_new,
+                                                   int32_t max_kv_len, size_t* bytes);
+/* One parallel draft step in which every request brings n_b >= 1 new rows:
+ * the tokens that joined its sequence since the last step (the accepted
+ * drafts and the target's next token: user guide, Inference Process), with
+ * the target's aux hidden states. The last new row is the anchor (depth 0);
+ * K - 1 masked rows follow it. In the flat layout [context, new rows,
+ * mask_1..mask_{K-1}] ("feat(speculative) ... #2376", Equivalence to vLLM
+ * inference) new row j attends to the cached context and new rows 0..j;
+ * masked depth d attends to the context, every new row and depths 1..d. The
+ * new rows' post-rotary K/V of every layer are written to cache rows
+ * kv_offsets[b] + kv_lens[b] + j when append_new_kv (kv_lens unchanged: the
+ * caller advances it, e.g. with peagle_next_context). With n_b = 1 this is
+ * peagle_draft_step.
+ *   total_new    HOST sum of n_b (= new_offsets[B]); max_new HOST bound on
+ *                n_b (1..64)
+ *   new_offsets  device int32 [B+1], new_offsets[0] = 0, n_b = new_offsets[b+1] -
+ *                new_offsets[b] in [1, max_new]
+ *   new_aux      device [total_new, A*Ht]; new_tokens, new_pos device int32
+ *                [total_new] (target ids, rotary positions; masked depth d of
+ *                request b is at the position of its last new row + d)
+ *   caches, kv_offsets, kv_lens, kv_capacity, max_kv_len: as peagle_draft_step;
+ *                kv_offsets[b] + kv_lens[b] + n_b <= kv_offsets[b+1]
+ *   draft_tokens device int32 [B, K] out; logits device float [B, K, Vd] or NULL
+ * A malformed new-row range sets PEAGLE_DEV_BOUNDS and the request is skipped. */
+peagle_status peagle_draft_step_ctx(const peagle_model* model, int32_t B, int32_t K, int32_t total_new,
+                                    int32_t max_new, const int32_t* new_offsets, const void* new_aux,
+                                    const int32_t* new_tokens, const int32_t* new_pos,
+                                    void* const* k_cache, void* const* v_cache,
+                                    const int64_t* kv_offsets, const int32_t* kv_lens,
+                                    int64_t kv_capacity, int32_t max_kv_len, int32_t append_new_kv,
+                                    int32_t* draft_tokens, float* logits, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+/* Closes the draft -> verify loop (user guide, Inference Process, steps 3-4:
+ * accepted drafts are kept and the next round starts from the target's
+ * token). After a peagle_draft_step_ctx whose new rows were cur_offsets /
+ * cur_pos (and appended) and a verification with accept_len / next_token:
+ *   kv_lens[b] += cur n_b (the appended rows are context now);
+ *   the next step's rows of request b are n_b' = accept_len[b] + 1 new rows:
+ *   tokens draft_tokens[b, 0..a-1] then next_token[b], at positions
+ *   p + 1 .. p + a + 1 with p the position of the current anchor (the last
+ *   current new row); next_offsets / next_tokens / next_pos receive them.
+ * All arrays device int32: draft_tokens [B, K]; accept_len, next_token, kv_lens
+ * [B]; cur_offsets, next_offsets [B+1]; cur_pos [cur total]; next_tokens,
+ * next_pos [at most B*(K+1)]. One CTA; B in [0, 65536], K in [1, 16]. The
+ * new total (next_offsets[B]) is on the device; read it before sizing the
+ * next step. */
+peagle_status peagle_next_context(int32_t B, int32_t K, const int32_t* draft_tokens,
+                                  const int32_t* accept_len, const int32_t* next_token,
+                                  const int32_t* cur_offsets, const int32_t* cur_pos, int32_t* kv_lens,
+                                  int32_t* next_offsets, int32_t* next_tokens, int32_t* next_pos,
+                                  void* stream);
+
 /* ---- greedy verification ------------------------------------------------ */
 /* accept_len[b] = the largest a <= K with draft_tokens[b, i] ==
  * target_tokens[b, i] for all i < a; next_token[b] = target_tokens[b, a]

@@ -4,7 +4,7 @@ parity tests and smoke() compare against."""
 import numpy as np
 
 from eagle_speculative_drafting_gb300.marshal import (  # noqa: F401  (re-exported for the tests)
-    config_of, dev, make_model, run_decode, run_train, run_verify, tdtype, upload_decode,
+    config_of, dev, make_model, run_decode, run_decode_ctx, run_train, run_verify, tdtype, upload_decode,
     upload_train, weights_to_device)
 from oracle import peagle_oracle as O
 

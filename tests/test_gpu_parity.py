@@ -534,3 +534,109 @@ def test_data_parallel_forward_sums_two_sequences_like_the_oracle():
     direct = H().run_train(wl, model, inp, 4, 0.7, 0.2, dp.sequence_seed(77, 0))
     for k in ("per_depth_loss", "per_depth_acc", "per_depth_valid", "loss"):
         assert np.array_equal(one[k], direct[k]), k
+
+
+# ------------------------------------------------- new context rows, closed loop
+def _ctx_rows(wl, inp, counts, seed):
+    rng = np.random.default_rng(seed)
+    aux, tok, pos = [], [], []
+    for b, n in enumerate(counts):
+        a = rng.standard_normal((n, wl.num_aux * wl.target_hidden)).astype(np.float32)
+        aux.append(synth.bf16_round(a) if wl.dtype == "bf16" else a)
+        tok.append(rng.integers(0, wl.vocab, n).astype(np.int32))
+        L = int(inp["kv_lens"][b])
+        pos.append(np.arange(L, L + n, dtype=np.int32))
+    return aux, tok, pos
+
+
+@pytest.mark.parametrize("dtype,tol,kw", [("f32", F32_TOL, dict()), ("bf16", BF16_TOL, dict()),
+                                          ("bf16", BF16_TOL, dict(head_dim=128, num_q_heads=8, num_kv_heads=2,
+                                                                  hidden=1024, batch=6, K=8,
+                                                                  kv_len_range=(0, 3000), max_position=8192))])
+def test_draft_step_over_new_context_rows(dtype, tol, kw):
+    # ragged new rows per request (1..9): causal among themselves over the
+    # cached context, K/V appended, masked depths after the anchor
+    wl = small_bf16_decode(dtype=dtype, **kw)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl, spare=12)
+    counts = [1 + (3 * b) % min(9, wl.K + 1) for b in range(wl.batch)]
+    aux, tok, pos = _ctx_rows(wl, inp, counts, 4)
+    model = H().make_model(wl, W)
+    d = H().upload_decode(wl, inp)
+    got = H().run_decode_ctx(wl, model, aux, tok, pos, d, inp["kv_lens"], inp["kv_capacity"],
+                             int(np.max(inp["kv_lens"])), want_logits=True)
+    ref = O.draft_step_ctx(H().oracle_model(wl, W), aux, tok, pos, inp["k_cache"], inp["v_cache"],
+                           inp["kv_offsets"], inp["kv_lens"], wl.K)
+    check_decode(wl, got, ref, tol)
+    for l in range(wl.num_layers):
+        kc = d["k_cache"][l].float().cpu().numpy()
+        vc = d["v_cache"][l].float().cpu().numpy()
+        for b in range(wl.batch):
+            o = int(inp["kv_offsets"][b] + inp["kv_lens"][b])
+            rk, rv = ref["appended"][l][b]
+            assert H().max_abs_rel(kc[o:o + counts[b]], rk) <= tol
+            assert H().max_abs_rel(vc[o:o + counts[b]], rv) <= tol
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
+def _target_aux(wl, b, p):
+    # the synthetic target's aux hidden state of request b at position p
+    a = np.random.default_rng([wl.seed, 77, b, int(p)]).standard_normal(wl.num_aux * wl.target_hidden)
+    a = a.astype(np.float32)
+    return synth.bf16_round(a) if wl.dtype == "bf16" else a
+
+
+def test_closed_draft_verify_loop_matches_the_oracle():
+    # four rounds of draft -> greedy verify -> next context on the GPU
+    # (DraftLoop) and in the oracle: the same drafts, accept lengths, next
+    # tokens and appended cache rows every round
+    from eagle_speculative_drafting_gb300.loop import DraftLoop
+    wl = small_bf16_decode(dtype="f32", batch=5, K=4, kv_len_range=(3, 40))
+    W = synth.make_weights(wl)
+    T = 4
+    inp = synth.make_decode_inputs(wl, spare=T * (wl.K + 1))
+    model = H().make_model(wl, W)
+    om = H().oracle_model(wl, W)
+    d = H().upload_decode(wl, inp)
+    B, K = wl.batch, wl.K
+    loop = DraftLoop(model, K, d["k_cache"], d["v_cache"], d["kv_offsets"], d["kv_lens"], inp["kv_capacity"])
+    first_tok, first_pos = inp["anchor_tokens"], inp["kv_lens"].copy()
+    loop.start(first_tok, first_pos)
+    kc = [k.copy() for k in inp["k_cache"]]
+    vc = [v.copy() for v in inp["v_cache"]]
+    lens = inp["kv_lens"].astype(np.int64).copy()
+    rtok = [[int(t)] for t in first_tok]
+    rpos = [[int(p)] for p in first_pos]
+    for t in range(T):
+        # the target's aux states of this round's new rows, both sides
+        gtok = loop.new_tokens.cpu().numpy()
+        gpos = loop.new_pos.cpu().numpy()
+        goff = loop.new_offsets.cpu().numpy()
+        assert [list(gtok[goff[b]:goff[b + 1]]) for b in range(B)] == rtok
+        assert [list(gpos[goff[b]:goff[b + 1]]) for b in range(B)] == rpos
+        aux_rows = np.stack([_target_aux(wl, b, p) for b in range(B) for p in rpos[b]])
+        drafts = loop.draft(H().dev(aux_rows)).cpu().numpy()
+        ref = O.draft_step_ctx(om, [aux_rows[goff[b]:goff[b + 1]] for b in range(B)], rtok, rpos, kc, vc,
+                               inp["kv_offsets"], lens, K)
+        assert np.array_equal(drafts, ref["draft_tokens"]), t
+        for b in range(B):   # the oracle's cache gains the new rows
+            o = int(inp["kv_offsets"][b] + lens[b])
+            for l in range(wl.num_layers):
+                k, v = ref["appended"][l][b]
+                kc[l][o:o + len(k)] = k
+                vc[l][o:o + len(v)] = v
+        acc_draw = synth.draw_accept_lengths(wl, B, K, salt=t)
+        tgt = synth.make_targets_with_accept(wl, drafts, acc_draw, salt=t)
+        a, nx = loop.verify_greedy(torch.from_numpy(tgt).cuda())
+        ra, rn = O.verify_accept(ref["draft_tokens"], tgt)
+        assert np.array_equal(a.cpu().numpy(), ra) and np.array_equal(nx.cpu().numpy(), rn)
+        anchor = [p[-1] for p in rpos]
+        lens += np.array([len(p) for p in rpos])
+        rtok, rpos = O.next_context(ref["draft_tokens"], ra, rn, anchor)
+        assert np.array_equal(loop.kv_lens.cpu().numpy(), lens)
+    for l in range(wl.num_layers):
+        g = d["k_cache"][l].cpu().numpy()
+        for b in range(B):
+            o = int(inp["kv_offsets"][b])
+            assert H().max_abs_rel(g[o:o + lens[b]], kc[l][o:o + lens[b]]) <= F32_TOL
+    assert pe().peagle_get_device_status(model.handle) == 0
