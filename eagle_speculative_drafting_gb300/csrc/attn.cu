@@ -252,13 +252,18 @@ template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 }  // namespace mm
 
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // NW warps: warp w scores keys [w*KW, (w+1)*KW) of each 64-key tile for
-// every row and owns head dims [w*DW, (w+1)*DW) of the P V product. Eight
-// warps (8 keys, 16 dims each) pay off only for a single 16-row block,
-// where the kernel is latency bound; larger row blocks use four.
+// every row and owns head dims [w*DW, (w+1)*DW) of the P V product. This
+// block-synchronous form (three barriers per tile) serves 64 or 128 query
+// rows per KV head (multi-row steps), where every K/V tile is shared by
+// many rows; up to 32 rows use the warp-independent kernel below.
 // K and V tiles rotate through NS stages; their rows are unpadded with the
-// 16-byte chunks of row r XOR-swizzled by r & 7 (conflict-free ldmatrix),
-// so three stages of two 32-row-block CTAs still fit one SM.
+// 16-byte chunks of row r XOR-swizzled by r & 7 (conflict-free ldmatrix).
 template <int MT, int HD, int NW, int NS>
 struct MmaAttnCfg {
   static constexpr int THREADS = 32 * NW;
@@ -534,6 +539,269 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
     }
 }
 
+// ------------------------------------ decode, bf16, warp-independent split
+// The same (chunk, KV head, request) CTAs, but no block barrier in the main
+// loop: warp w streams its own 16-key tiles t = w, w + NW, ... of the chunk
+// through its own NS-stage cp.async ring and keeps a private online softmax
+// over them for all 16*MT query rows and all HD dims:
+//   S = Q K^T   (rows x 16 keys; Q fragments from shared memory);
+//   row maxima within the quad of lanes that holds a row (two shuffles);
+//   the row's reference maximum moves only when a tile exceeds it by more
+//   than 2^8, so O is rescaled rarely; probabilities relative to it stay
+//   below 256 and are rounded to bf16;
+//   O += P V   (P straight from the score registers; V by ldmatrix.trans).
+// At the end the NW warps' (m, l, O) meet once in shared memory and the CTA
+// writes the chunk's partial as the block-synchronous kernel does, so the
+// combine is shared.
+template <int MT, int HD, int NW, int NS>
+struct WarpAttnCfg {
+  static constexpr int THREADS = 32 * NW;
+  static constexpr int QR = 16 * MT, TK = 16, LDS = HD + 8;
+  static constexpr int STAGE = 2 * TK * HD * 2;                  // K and V of one 16-key tile, bytes
+  static constexpr int RING = NW * NS * STAGE;
+  static constexpr int MERGE = NW * QR * (HD + 2) * 4;           // per-warp O, m, l at the end
+  static constexpr int SMEM = QR * LDS * 2 + (RING > MERGE ? RING : MERGE);
+};
+
+template <int MT, int HD, int NW, int NS>
+__global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_warp_mma(DecodeAttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  using C = WarpAttnCfg<MT, HD, NW, NS>;
+  constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, NT = HD / 8;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
+  uint8_t* ring = smem_raw + QR * LDS * 2;
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int G = a.nq / a.nkv;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const long long off = a.kv_off[b];
+  int L = a.kv_len[b];
+  const bool ok = L >= 0 && L <= a.max_kv_len && off >= 0 && off + L <= a.kv_off[b + 1] && off + L <= a.kv_cap;
+  if (!ok) {
+    if (tid == 0 && split == 0 && g == 0) set_status(a.status, PEAGLE_DEV_BOUNDS);
+    L = 0;
+  }
+  const int k0 = split * a.chunk, k1 = min(L, k0 + a.chunk);
+  const int ntiles = k1 > k0 ? (k1 - k0 + TK - 1) / TK : 0;
+  if (ntiles == 0) return;   // a chunk past the context end: the merge skips it
+  if (!dr_valid(a.rows, b)) return;   // flagged by the q/k/v kernel
+  const int KG = (dr_new(a.rows, b) + a.K - 1) * G, KGmax = a.rows_max * G, rb = dr_base(a.rows, b);
+  const bf16* kc = static_cast<const bf16*>(a.kcache);
+  const bf16* vc = static_cast<const bf16*>(a.vcache);
+  const bf16* Q = static_cast<const bf16*>(a.Q);
+
+  // this warp's tiles: i-th = chunk tile w + i * NW
+  const int my_tiles = ntiles > w ? (ntiles - w + NW - 1) / NW : 0;
+  uint8_t* wring = ring + (size_t)w * NS * C::STAGE;
+  auto load_tile = [&](int i) {
+    const int t = w + i * NW;
+    bf16* sk = reinterpret_cast<bf16*>(wring + (i % NS) * C::STAGE);
+    bf16* sv = sk + TK * HD;
+    const int base = k0 + t * TK;
+#pragma unroll
+    for (int e = lane; e < TK * (HD / 8); e += 32) {
+      const int kr = e / (HD / 8), c8 = e % (HD / 8);
+      const int key = base + kr;
+      const bool in = key < k1;
+      const size_t src = ((size_t)(off + (in ? key : k0)) * a.nkv + g) * HD + c8 * 8;
+      mm::cp16(mm::sa(sk + kv_sw<HD>(kr, c8)), kc + src, in ? 16 : 0);
+      mm::cp16(mm::sa(sv + kv_sw<HD>(kr, c8)), vc + src, in ? 16 : 0);
+    }
+  };
+  // the first tiles stream while the queries are staged
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) {
+    if (i < my_tiles) load_tile(i);
+    mm::cp_commit();
+  }
+  for (int e = tid; e < QR * (HD / 8); e += C::THREADS) {
+    const int qi = e / (HD / 8), c8 = e % (HD / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (qi < KG) {
+      const int r = rb + qi / G, h = g * G + qi % G;
+      v = *reinterpret_cast<const uint4*>(Q + ((size_t)r * a.nq + h) * HD + c8 * 8);
+    }
+    *reinterpret_cast<uint4*>(sQ + qi * LDS + c8 * 8) = v;
+  }
+  __syncthreads();
+
+  const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
+  constexpr float kRaise = 8.f;                        // log2 headroom of the reference maximum
+  float m_ref[MT][2], l_part[MT][2];
+  float O[MT][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    m_ref[mt][0] = m_ref[mt][1] = -INFINITY;
+    l_part[mt][0] = l_part[mt][1] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
+  }
+
+  for (int i = 0; i < my_tiles; ++i) {
+    if (i + NS - 1 < my_tiles) load_tile(i + NS - 1);
+    mm::cp_commit();
+    mm::cp_wait<NS - 1>();
+    __syncwarp();
+    const bf16* tK = reinterpret_cast<const bf16*>(wring + (i % NS) * C::STAGE);
+    const bf16* tV = tK + TK * HD;
+    // ---- S = Q K^T over this tile's 16 keys
+    float S[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      uint32_t bk[4];   // keys (2 x 8) x 16 dims
+      mm::ldsm4(bk, mm::sa(tK + kv_sw<HD>((lane >> 4) * 8 + (lane & 7), ks * 2 + ((lane >> 3) & 1))));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t aq[4];
+        mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+        mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
+        mm::mma16816(S[mt][1], aq, bk[2], bk[3]);
+      }
+    }
+    // ---- mask the tail, tile maxima per row (the quad of lanes holding it)
+    const int kbase = k0 + (w + i * NW) * TK + (lane & 3) * 2;
+    bool raise_any = false;
+    float tmax[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float v = S[mt][nt][hf * 2 + c] * sl2;
+            v = (kbase + nt * 8 + c < k1) ? v : -INFINITY;
+            S[mt][nt][hf * 2 + c] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        tmax[mt][hf] = mx;
+        raise_any |= mx > m_ref[mt][hf] + kRaise;
+      }
+    // ---- raise a row's reference maximum (and rescale its O) only when
+    // the tile exceeds it by more than 2^8; a warp-uniform branch
+    if (__any_sync(0xffffffffu, raise_any)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const bool up = tmax[mt][hf] > m_ref[mt][hf] + kRaise;
+          const float corr = !up ? 1.f : (m_ref[mt][hf] == -INFINITY ? 0.f : exp2f(m_ref[mt][hf] - tmax[mt][hf]));
+          if (up) m_ref[mt][hf] = tmax[mt][hf];
+          l_part[mt][hf] *= corr;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            O[mt][nt][hf * 2] *= corr;
+            O[mt][nt][hf * 2 + 1] *= corr;
+          }
+        }
+    }
+    // ---- probabilities (bf16 A fragments straight from the scores)
+    uint32_t ap[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float mr = m_ref[mt][c >> 1];
+          p[nt][c] = (mr == -INFINITY) ? 0.f : exp2f(S[mt][nt][c] - mr);
+        }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        l_part[mt][hf] += (p[0][hf * 2] + p[0][hf * 2 + 1]) + (p[1][hf * 2] + p[1][hf * 2 + 1]);
+      ap[mt][0] = pack_bf16(p[0][0], p[0][1]);
+      ap[mt][1] = pack_bf16(p[0][2], p[0][3]);
+      ap[mt][2] = pack_bf16(p[1][0], p[1][1]);
+      ap[mt][3] = pack_bf16(p[1][2], p[1][3]);
+    }
+    // ---- O += P V
+#pragma unroll
+    for (int np = 0; np < HD / 16; ++np) {
+      uint32_t bv[4];
+      mm::ldsm4t(bv, mm::sa(tV + kv_sw<HD>((lane & 7) + ((lane >> 3) & 1) * 8, np * 2 + (lane >> 4))));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mm::mma16816(O[mt][2 * np], ap[mt], bv[0], bv[1]);
+        mm::mma16816(O[mt][2 * np + 1], ap[mt], bv[2], bv[3]);
+      }
+    }
+    __syncwarp();
+  }
+  mm::cp_wait<0>();
+  // ---- the warps meet once: (m, l, O) of each warp, merged per row
+  __syncthreads();   // every warp is done with its ring, which now holds the merge
+  float* sO = reinterpret_cast<float*>(ring);                 // [NW][QR][HD]
+  float* sM = sO + (size_t)NW * QR * HD;                      // [NW][QR]
+  float* sL = sM + NW * QR;                                   // [NW][QR]
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int row = mt * 16 + hf * 8 + (lane >> 2);
+      float l = l_part[mt][hf];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      float* orow = sO + ((size_t)w * QR + row) * HD + (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        *reinterpret_cast<float2*>(orow + nt * 8) = make_float2(O[mt][nt][hf * 2], O[mt][nt][hf * 2 + 1]);
+      if ((lane & 3) == 0) {
+        sM[w * QR + row] = m_ref[mt][hf];
+        sL[w * QR + row] = l;
+      }
+    }
+  __syncthreads();
+  const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KGmax;
+  for (int e = tid; e < KG * (HD / 4); e += C::THREADS) {
+    const int row = e / (HD / 4), c4 = (e % (HD / 4)) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) M = fmaxf(M, sM[q * QR + row]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const float mq = sM[q * QR + row];
+      const float f = (mq == -INFINITY) ? 0.f : exp2f(mq - M);
+      const float4 o = *reinterpret_cast<const float4*>(sO + ((size_t)q * QR + row) * HD + c4);
+      acc.x += o.x * f;
+      acc.y += o.y * f;
+      acc.z += o.z * f;
+      acc.w += o.w * f;
+      l += sL[q * QR + row] * f;
+    }
+    *reinterpret_cast<float4*>(a.part_o + (prow + row) * HD + c4) = acc;
+    if (c4 == 0) {
+      a.part_ml[(prow + row) * 2 + 0] = M * 0.6931471805599453f;
+      a.part_ml[(prow + row) * 2 + 1] = l;
+    }
+  }
+}
+
+template <int MT, int HD, int NW, int NS>
+static cudaError_t launch_warp_mma(const DecodeAttnArgs& a, cudaStream_t st) {
+  using C = WarpAttnCfg<MT, HD, NW, NS>;
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(decode_warp_mma<MT, HD, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM);
+  });
+  if (e != cudaSuccess) return e;
+  launch_pdl(decode_warp_mma<MT, HD, NW, NS>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
+  return cudaGetLastError();
+}
+
 template <int MT, int HD, int NW = 4, int NS = 2>
 static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
   using C = MmaAttnCfg<MT, HD, NW, NS>;
@@ -550,8 +818,10 @@ static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
 template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
   const int KG = a.rows_max * (a.nq / a.nkv);
-  if (KG <= 16) return launch_split_mma<1, HD, HD / 16, 3>(a, st);
-  if (KG <= 32) return launch_split_mma<2, HD, 4, 3>(a, st);
+  // up to 32 query rows per KV head: warp-independent key slices; more rows
+  // (multi-row steps) share each K/V tile across the block
+  if (KG <= 16) return launch_warp_mma<1, HD, 4, 3>(a, st);
+  if (KG <= 32) return launch_warp_mma<2, HD, 4, 3>(a, st);
   if (KG <= 64) return launch_split_mma<4, HD>(a, st);
   return launch_split_mma<8, HD>(a, st);
 }
@@ -653,10 +923,6 @@ struct TrainMmaCfg {
   static constexpr int SMEM = (TQ * LDS + 4 * TK * LDS) * 2 + 2 * TK * 4;
 };
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 template <int HD>
 __global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTileArgs tt) {
