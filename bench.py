@@ -51,7 +51,19 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe-steps", type=int, default=None,
+                    help="steps of each per-op timing pass (default: --steps, at least 300, at most 2000)")
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="steps of the end-to-end pass (default: as --probe-steps)")
     return ap.parse_args()
+
+
+def pass_steps(args):
+    """(per-op probe steps, end-to-end steps): long enough for several clock
+    samples under load unless given explicitly (short runs under a profiler)."""
+    probe = args.probe_steps if args.probe_steps else min(max(args.steps, 300), 2000)
+    e2e = args.e2e_steps if args.e2e_steps else probe
+    return max(1, probe), max(1, e2e)
 
 
 # ----------------------------------------------------------------- helpers
@@ -612,7 +624,7 @@ def main():
     # ---- per-op time: CUDA events around every launch of one op class
     # (the contraction's kernel, or the attention's split kernel) on its own
     # launch stream, one class at a time
-    probe_steps = min(max(args.steps, 300), 2000)
+    probe_steps, e_steps = pass_steps(args)
     per_op_ms = {}
     for name, op in OP_IDS.items():
         cap = probe_steps * wl.num_layers + 8
@@ -680,7 +692,6 @@ def main():
 
     h2d = int(h_stage.numel())
     d2h = int(h_out.numel() * h_out.element_size())
-    e_steps = min(max(args.steps, 300), 2000)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
