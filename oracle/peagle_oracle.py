@@ -755,6 +755,108 @@ def loss_from_depth_sums(sums, decay=0.8):
             "loss": loss}
 
 
+# --------------------------------------------------------------------------
+# Gradients of the training loss  [PR: description and Changelog -- the
+# trainer runs the parallel masked-depth loss; "loss decreases" test]
+# The loss of parallel_forward written once more with float64 torch tensors,
+# and differentiated by autograd. The embedding is frozen (the draft reuses
+# the target's token embedding); every other weight gets a gradient:
+# fc_w, fc_norm_w, mask_hidden, final_norm_w, lm_head_w and every layer's
+# weights. All rows attend under one dense mask (train_allowed), so this is
+# for small inputs.
+# --------------------------------------------------------------------------
+GRAD_KEYS = ("fc_w", "fc_norm_w", "mask_hidden", "final_norm_w", "lm_head_w")
+LAYER_GRAD_KEYS = ("in_norm_w", "hidden_norm_w", "qkv_w", "o_w", "post_norm_w", "gate_up_w", "down_w")
+
+
+def parallel_loss_torch(model: DraftModel, aux, input_ids, position_ids, cu_seqlens, labels, loss_mask,
+                        K, r, r_min, seed, depth_decay=0.8, params=None):
+    """Returns (loss, params): loss a float64 torch scalar, params the dict of
+    leaf tensors (requires_grad) it was computed from, named like the weights
+    (params["layers"][l][key])."""
+    import torch
+    t = lambda a: torch.tensor(np.asarray(a, dtype=np.float64))
+    c = model.cfg
+    if params is None:
+        params = {k: t(getattr(model, k)).requires_grad_() for k in GRAD_KEYS}
+        params["layers"] = [{k: t(L[k]).requires_grad_() for k in LAYER_GRAD_KEYS if L.get(k) is not None}
+                            for L in model.layers]
+    eps = c["rms_eps"]
+    nq, nkv, hd, I = c["num_q_heads"], c["num_kv_heads"], c["head_dim"], c["intermediate"]
+    n = len(input_ids)
+    counts, sets = cod_select(n, K, r, r_min, seed)
+    anchor, depth = train_rows(n, counts, sets)
+    R = len(anchor)
+    _, start, end = conversation_bounds(cu_seqlens, n)
+
+    def norm(x, g):
+        return x / torch.sqrt(torch.mean(x * x, dim=-1, keepdim=True) + eps) * g
+
+    def project(a):
+        return norm(a @ params["fc_w"].T, params["fc_norm_w"])
+
+    def rope(x, pos):
+        half = hd // 2
+        inv = c["rope_theta"] ** (-(2.0 * np.arange(half)) / hd)
+        ang = torch.tensor(np.asarray(pos, dtype=np.float64)[:, None] * inv[None, :])
+        cs, sn = torch.cos(ang)[:, None, :], torch.sin(ang)[:, None, :]
+        x1, x2 = x[..., :half], x[..., half:]
+        return torch.cat([x1 * cs - x2 * sn, x2 * cs + x1 * sn], dim=-1)
+
+    d0 = torch.tensor(depth == 0)
+    hid = torch.where(d0[:, None], project(t(np.asarray(aux)[anchor])),
+                      project(params["mask_hidden"].reshape(1, -1)).expand(R, -1))
+    toks = np.where(depth == 0, np.asarray(input_ids)[anchor], c["ptd_token_id"])
+    emb = t(model.embed[toks])
+    pos = np.asarray(position_ids)[anchor] + depth
+    allowed = torch.tensor(train_allowed(anchor, depth, start))
+    scale = 1.0 / math.sqrt(hd)
+    h = hid
+    for l, L in enumerate(params["layers"]):
+        if l == 0:
+            hn = norm(hid, L["hidden_norm_w"])
+            x = torch.cat([norm(emb, L["in_norm_w"]), hn], dim=-1)
+            resid = hn if c["norm_before_residual"] else hid
+        else:
+            x = norm(h, L["in_norm_w"])
+            resid = h
+        qkv = x @ L["qkv_w"].T
+        q = rope(qkv[:, :nq * hd].reshape(R, nq, hd), pos)
+        k = rope(qkv[:, nq * hd:(nq + nkv) * hd].reshape(R, nkv, hd), pos)
+        v = qkv[:, (nq + nkv) * hd:].reshape(R, nkv, hd)
+        g = nq // nkv
+        kk = k.repeat_interleave(g, dim=1)
+        vv = v.repeat_interleave(g, dim=1)
+        sc = torch.einsum("rhd,khd->hrk", q, kk) * scale
+        sc = sc.masked_fill(~allowed[None], float("-inf"))
+        o = torch.einsum("hrk,khd->rhd", torch.softmax(sc, dim=-1), vv).reshape(R, nq * hd)
+        h1 = resid + o @ L["o_w"].T
+        y = norm(h1, L["post_norm_w"])
+        gu = y @ L["gate_up_w"].T
+        a = torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]
+        h = h1 + a @ L["down_w"].T
+    logits = norm(h, params["final_norm_w"]) @ params["lm_head_w"].T
+    lab, _ = row_labels(n, K, r, r_min, seed, cu_seqlens, labels, loss_mask, model.t2d)
+    lse = torch.logsumexp(logits, dim=-1)
+    loss = torch.zeros((), dtype=torch.float64)
+    for d in range(K):
+        m = np.flatnonzero((depth == d) & (lab >= 0))
+        if m.size:
+            ce = lse[m] - logits[m, lab[m]]
+            loss = loss + depth_decay ** d * ce.mean()
+    return loss, params
+
+
+def parallel_grads(model: DraftModel, **kw):
+    """(loss, gradients) of parallel_loss_torch as float64 numpy arrays,
+    named like the weights (grads["layers"][l][key])."""
+    loss, params = parallel_loss_torch(model, **kw)
+    loss.backward()
+    grads = {k: params[k].grad.numpy() for k in GRAD_KEYS}
+    grads["layers"] = [{k: v.grad.numpy() for k, v in L.items()} for L in params["layers"]]
+    return float(loss.detach()), grads
+
+
 def model_config(wl, norm_before_residual=True) -> dict:
     """Config dict for a synthetic workload description (attribute access)."""
     return {

@@ -800,3 +800,63 @@ def test_next_context_hand_worked():
     drafts = np.array([[5, 6, 7], [8, 9, 1]])
     toks, pos = O.next_context(drafts, np.array([2, 0]), np.array([40, 41]), np.array([10, 20]))
     assert toks == [[5, 6, 40], [41]] and pos == [[11, 12, 13], [21]]
+
+
+# ------------------------------------------------------------------- gradients
+def _grad_case(nbr=True, **kw):
+    wl, model, W, inp = tiny_train(**kw)
+    if not nbr:
+        model = O.DraftModel(dict(model.cfg, norm_before_residual=False), W)
+    return wl, model, W, inp
+
+
+@pytest.mark.parametrize("nbr", [True, False])
+def test_autograd_loss_is_the_forward_loss(nbr):
+    wl, model, W, inp = _grad_case(nbr)
+    res = O.parallel_forward(model, **inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    loss, _ = O.parallel_loss_torch(model, **inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    assert abs(float(loss.detach()) - res["loss"]) < 1e-12
+
+
+@pytest.mark.parametrize("nbr", [True, False])
+def test_gradients_match_central_differences(nbr):
+    # central differences of the (pinned) forward loss, in float64, on a few
+    # coordinates of every weight that has a gradient
+    wl, model, W, inp = _grad_case(nbr)
+    kw = dict(**inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    _, grads = O.parallel_grads(model, **kw)
+    rng = np.random.default_rng(3)
+    h = 1e-6
+
+    def loss_with(path, idx, delta):
+        W2 = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in W.items()}
+        W2["layers"] = [{k: (None if v is None else np.asarray(v, dtype=np.float64).copy()) for k, v in L.items()}
+                        for L in W["layers"]]
+        for k in ("fc_w", "fc_norm_w", "mask_hidden", "final_norm_w", "lm_head_w"):
+            W2[k] = np.asarray(W2[k], dtype=np.float64)
+        arr = W2[path[0]] if len(path) == 1 else W2["layers"][path[0]][path[1]]
+        arr[idx] += delta
+        return O.parallel_forward(O.DraftModel(model.cfg, W2), **kw)["loss"]
+
+    paths = [(k,) for k in O.GRAD_KEYS] + [(l, k) for l in range(wl.num_layers) for k in O.LAYER_GRAD_KEYS
+                                           if W["layers"][l].get(k) is not None]
+    for path in paths:
+        g = grads[path[0]] if len(path) == 1 else grads["layers"][path[0]][path[1]]
+        for _ in range(3):
+            idx = tuple(int(rng.integers(0, s)) for s in g.shape)
+            fd = (loss_with(path, idx, h) - loss_with(path, idx, -h)) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g).max()), (path, idx, fd, g[idx])
+
+
+def test_loss_decreases_along_the_negative_gradient():
+    wl, model, W, inp = _grad_case()
+    kw = dict(**inp, K=wl.K, r=0.7, r_min=0.2, seed=9)
+    loss0, grads = O.parallel_grads(model, **kw)
+    W2 = dict(W)
+    lr = 0.05
+    for k in O.GRAD_KEYS:
+        W2[k] = np.asarray(W[k], dtype=np.float64) - lr * grads[k].reshape(np.shape(W[k]))
+    W2["layers"] = [{k: (None if v is None else np.asarray(v, dtype=np.float64) - lr * grads["layers"][l][k])
+                     if k in grads["layers"][l] else v for k, v in L.items()} for l, L in enumerate(W["layers"])]
+    loss1 = O.parallel_forward(O.DraftModel(model.cfg, W2), **kw)["loss"]
+    assert loss1 < loss0 - 1e-4, (loss0, loss1)
