@@ -107,6 +107,11 @@ _sig("peagle_parallel_forward", c_int32, c_void_p, c_int32, c_void_p, c_void_p, 
      c_int32, c_void_p, c_void_p, c_int32, c_double, c_double, ctypes.c_uint64, c_double,
      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
      c_size_t, c_void_p)
+_sig("peagle_parallel_backward_workspace_size", c_int32, c_void_p, c_int32, c_int32, c_double, c_double,
+     ctypes.POINTER(c_size_t))
+_sig("peagle_parallel_backward", c_int32, c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+     c_void_p, c_void_p, c_int32, c_double, c_double, ctypes.c_uint64, c_double, c_void_p,
+     ctypes.POINTER(peagle_weights), c_void_p, c_size_t, c_void_p)
 _sig("peagle_combine_depth_sums", c_int32, c_int32, c_double, c_void_p, c_void_p, c_void_p, c_void_p,
      c_void_p, c_void_p)
 _sig("peagle_gemm_workspace_size", c_int32, c_int32, c_int32, c_int32, c_int32,
@@ -291,6 +296,21 @@ def peagle_parallel_forward(model, n, aux, input_ids, position_ids, cu_seqlens, 
         ptr(per_depth_loss), ptr(per_depth_acc), ptr(per_depth_valid), ptr(loss), ptr(row_argmax),
         ptr(row_ce), ptr(logits), ptr(depth_sums), ptr(workspace), workspace_bytes, _stream(stream)),
         "peagle_parallel_forward")
+
+
+def peagle_parallel_backward_workspace_size(model, n, K, r, r_min):
+    s = c_size_t()
+    _check(_lib.peagle_parallel_backward_workspace_size(model, n, K, r, r_min, ctypes.byref(s)),
+           "peagle_parallel_backward_workspace_size")
+    return s.value
+
+
+def peagle_parallel_backward(model, n, aux, input_ids, position_ids, cu_seqlens, num_seqs, labels, loss_mask, K,
+                             r, r_min, seed, depth_decay, loss, grads, workspace, workspace_bytes, stream=None):
+    _check(_lib.peagle_parallel_backward(
+        model, n, ptr(aux), ptr(input_ids), ptr(position_ids), ptr(cu_seqlens), num_seqs, ptr(labels),
+        ptr(loss_mask), K, r, r_min, seed & ((1 << 64) - 1), depth_decay, ptr(loss), ctypes.byref(grads),
+        ptr(workspace), workspace_bytes, _stream(stream)), "peagle_parallel_backward")
 
 
 def peagle_combine_depth_sums(K, depth_decay, depth_sums, per_depth_loss, per_depth_acc, per_depth_valid,

@@ -1168,6 +1168,491 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
   return PEAGLE_OK;
 }
 
+// ================================================================ backward
+// Gradients of the training loss (sum_d decay^d * mean_d CE) with respect to
+// every weight but the (frozen) embedding. The call runs the forward once
+// more, keeping each layer's activations, then goes backward: cross-entropy
+// -> head -> layers (MLP, post-norm, O, attention, RoPE, QKV, input norm) ->
+// layer-0 inputs -> fc_norm / fc and mask_hidden. Contractions run on the
+// library's GEMM over transposed copies: dX = dY W as dY (W^T)^T, dW = dY^T X
+// as (dY^T)(X^T)^T with the rows padded to a multiple of 64.
+struct BwdWs {
+  int* sem;
+  int *indices, *row_of, *anchor, *depth, *pos, *start, *end, *label;
+  int Rp, np1p, Vp;
+  void *x0src, *x0full, *z, *dlog, *ta, *tb, *gcast, *dgu, *dqkv, *auxm;
+  float *U, *Um, *hidsrc, *residsrc, *hidfull, *residfull, *hL, *logits, *part, *rce;
+  int* ram;
+  float *loss_d, *acc_d;
+  int* valid_d;
+  float *dh, *dh2, *dhid, *dbig, *dQ, *dK, *dV, *lse, *Dv, *rrow, *rrow2, *du, *dmask;
+  std::vector<void*> xin, q, k, v, o, y, act, wT_qkv, wT_o, wT_gu, wT_down;
+  std::vector<float*> hin, hmid, gu;
+  void *wT_lm, *wT_fc;
+};
+
+// a gradient buffer of the caller's peagle_weights (declared const there)
+static float* gout(const void* p) { return const_cast<float*>(static_cast<const float*>(p)); }
+
+static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, BwdWs& ws) {
+  const size_t es = esize(c);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), AHt = c.num_aux * c.target_hidden;
+  const int nqhd = c.num_q_heads * c.head_dim, nkvhd = c.num_kv_heads * c.head_dim, V = c.draft_vocab, L = c.num_layers;
+  const int dt = c.dtype;
+  ws.Rp = (R + 63) / 64 * 64;
+  ws.np1p = (n + 1 + 63) / 64 * 64;
+  ws.Vp = (V + 7) / 8 * 8;
+  const int Rp = ws.Rp, Vp = ws.Vp;
+  ws.sem = bp.take<int>(kGemmSemCount);
+  ws.indices = bp.take<int>(R);
+  ws.row_of = bp.take<int>((size_t)K * n);
+  ws.anchor = bp.take<int>(R);
+  ws.depth = bp.take<int>(R);
+  ws.pos = bp.take<int>(R);
+  ws.start = bp.take<int>(R);
+  ws.end = bp.take<int>(R);
+  ws.label = bp.take<int>(R);
+  ws.U = bp.take<float>(gemm_out_floats(dt, std::max(n, 1), H, AHt));
+  ws.Um = bp.take<float>(gemm_out_floats(dt, 1, H, AHt));
+  ws.x0src = bp.take_bytes((size_t)(n + 1) * 2 * H * es);
+  ws.hidsrc = bp.take<float>((size_t)(n + 1) * H);
+  ws.residsrc = bp.take<float>((size_t)(n + 1) * H);
+  ws.x0full = bp.take_bytes((size_t)R * 2 * H * es);
+  ws.hidfull = bp.take<float>((size_t)R * H);
+  ws.residfull = bp.take<float>((size_t)R * H);
+  ws.xin.assign(L, nullptr);
+  ws.q.assign(L, nullptr);
+  ws.k.assign(L, nullptr);
+  ws.v.assign(L, nullptr);
+  ws.o.assign(L, nullptr);
+  ws.y.assign(L, nullptr);
+  ws.act.assign(L, nullptr);
+  ws.wT_qkv.assign(L, nullptr);
+  ws.wT_o.assign(L, nullptr);
+  ws.wT_gu.assign(L, nullptr);
+  ws.wT_down.assign(L, nullptr);
+  ws.hin.assign(L, nullptr);
+  ws.hmid.assign(L, nullptr);
+  ws.gu.assign(L, nullptr);
+  for (int l = 0; l < L; ++l) {
+    const int in = l == 0 ? 2 * H : H;
+    ws.xin[l] = l == 0 ? ws.x0full : bp.take_bytes((size_t)R * H * es);
+    ws.hin[l] = bp.take<float>((size_t)R * H);
+    ws.q[l] = bp.take_bytes((size_t)R * nqhd * es);
+    ws.k[l] = bp.take_bytes((size_t)R * nkvhd * es);
+    ws.v[l] = bp.take_bytes((size_t)R * nkvhd * es);
+    ws.o[l] = bp.take_bytes((size_t)R * nqhd * es);
+    ws.hmid[l] = bp.take<float>((size_t)R * H);
+    ws.y[l] = bp.take_bytes((size_t)R * H * es);
+    ws.gu[l] = bp.take<float>((size_t)R * 2 * I);
+    ws.act[l] = bp.take_bytes((size_t)R * I * es);
+    ws.wT_qkv[l] = bp.take_bytes((size_t)in * QKV * es);
+    ws.wT_o[l] = bp.take_bytes((size_t)nqhd * H * es);
+    ws.wT_gu[l] = bp.take_bytes((size_t)H * 2 * I * es);
+    ws.wT_down[l] = bp.take_bytes((size_t)I * H * es);
+  }
+  ws.hL = bp.take<float>((size_t)R * H);
+  ws.z = bp.take_bytes((size_t)R * H * es);
+  ws.wT_lm = bp.take_bytes((size_t)H * Vp * es);
+  ws.wT_fc = bp.take_bytes((size_t)AHt * H * es);
+  ws.logits = bp.take<float>((size_t)R * V);
+  ws.rce = bp.take<float>(R);
+  ws.ram = bp.take<int>(R);
+  ws.loss_d = bp.take<float>(K);
+  ws.acc_d = bp.take<float>(K);
+  ws.valid_d = bp.take<int>(K);
+  ws.dlog = bp.take_bytes((size_t)R * Vp * es);
+  // partial slabs of every contraction of the pass
+  const int widths[] = {H, I, 2 * I, QKV, nqhd, 2 * H, V, Vp, AHt};
+  size_t pf = 0;
+  for (int N : widths)
+    for (int Kd : widths) pf = std::max(pf, gemm_out_floats(dt, R, N, Kd));
+  pf = std::max(pf, gemm_out_floats(dt, R, V, H));
+  const int outs[] = {V, Vp, H, 2 * I, QKV, nqhd, I};
+  const int ins[] = {H, I, 2 * H, nqhd, AHt};
+  for (int M : outs)
+    for (int N : ins) pf = std::max(pf, gemm_out_floats(dt, M, N, Rp));
+  pf = std::max(pf, gemm_out_floats(dt, H, AHt, ws.np1p));
+  pf = std::max(pf, gemm_out_floats(dt, 1, AHt, H));
+  ws.part = bp.take<float>(pf);
+  const int tw = std::max(std::max(std::max(Vp, 2 * I), std::max(QKV, 2 * H)), std::max(AHt, nqhd));
+  const int tr = std::max(Rp, ws.np1p);
+  ws.ta = bp.take_bytes((size_t)tw * tr * es);
+  ws.tb = bp.take_bytes((size_t)tw * tr * es);
+  const int gw = std::max(std::max(std::max(H, I), std::max(2 * I, QKV)), std::max(nqhd, 2 * H));
+  ws.gcast = bp.take_bytes((size_t)R * gw * es);
+  ws.dgu = bp.take_bytes((size_t)R * 2 * I * es);
+  ws.dqkv = bp.take_bytes((size_t)R * QKV * es);
+  ws.dh = bp.take<float>((size_t)R * H);
+  ws.dh2 = bp.take<float>((size_t)R * H);
+  ws.dhid = bp.take<float>((size_t)R * H);
+  ws.dbig = bp.take<float>((size_t)R * gw);
+  ws.dQ = bp.take<float>((size_t)R * nqhd);
+  ws.dK = bp.take<float>((size_t)R * nkvhd);
+  ws.dV = bp.take<float>((size_t)R * nkvhd);
+  ws.lse = bp.take<float>((size_t)R * c.num_q_heads);
+  ws.Dv = bp.take<float>((size_t)R * c.num_q_heads);
+  ws.rrow = bp.take<float>(std::max(R, n + 1));
+  ws.rrow2 = bp.take<float>(std::max(R, n + 1));
+  ws.du = bp.take<float>((size_t)(n + 1) * H);
+  ws.dmask = bp.take<float>(H);
+  ws.auxm = bp.take_bytes((size_t)(n + 1) * AHt * es);
+}
+
+peagle_status peagle_parallel_backward_workspace_size(const peagle_model* m, int32_t n, int32_t K, double r, double r_min,
+                                                      size_t* bytes) {
+  if (!m || !bytes) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward_workspace_size: NULL argument");
+  int32_t counts[16];
+  peagle_status st = peagle_cod_counts(n, K, r, r_min, counts);
+  if (st) return st;
+  int R = 0;
+  for (int d = 0; d < K; ++d) R += counts[d];
+  Bump bp(nullptr);
+  BwdWs ws;
+  bwd_layout(m->cfg, n, K, R, bp, ws);
+  *bytes = bp.off;
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const void* aux, const int32_t* input_ids,
+                                       const int32_t* position_ids, const int32_t* cu_seqlens, int32_t num_seqs,
+                                       const int32_t* labels, const uint8_t* loss_mask, int32_t K, double r,
+                                       double r_min, uint64_t seed, double depth_decay, float* loss,
+                                       const peagle_weights* grads, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (!m) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: model is NULL");
+  const peagle_config& c = m->cfg;
+  int32_t counts[16];
+  peagle_status st = peagle_cod_counts(n, K, r, r_min, counts);
+  if (st) return st;
+  if (!isfinite(depth_decay)) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: depth_decay not finite");
+  if (n < 1 || !aux || !input_ids || !position_ids || !cu_seqlens || !labels || num_seqs < 1 || num_seqs > n || !loss)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: a required input is NULL, n < 1 or num_seqs=%d out of [1, n]",
+         num_seqs);
+  if (!grads || !grads->fc_w || !grads->fc_norm_w || !grads->mask_hidden || !grads->final_norm_w || !grads->lm_head_w ||
+      !grads->layers)
+    FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: a gradient buffer is NULL");
+  for (int l = 0; l < c.num_layers; ++l) {
+    const peagle_layer_weights& G = grads->layers[l];
+    if (!G.in_norm_w || !G.qkv_w || !G.o_w || !G.post_norm_w || !G.gate_up_w || !G.down_w || (l == 0 && !G.hidden_norm_w))
+      FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: a gradient buffer of layer %d is NULL", l);
+  }
+  if (c.dtype == PEAGLE_BF16 && !aligned16(aux)) FAIL(PEAGLE_ERR_INVALID_ARG, "parallel_backward: aux not 16-byte aligned");
+  int off[17];
+  off[0] = 0;
+  for (int d = 0; d < K; ++d) off[d + 1] = off[d] + counts[d];
+  const int R = off[K];
+  size_t need = 0;
+  peagle_parallel_backward_workspace_size(m, n, K, r, r_min, &need);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    FAIL(PEAGLE_ERR_WORKSPACE, "parallel_backward: workspace %zu bytes at %p, need %zu (256-byte aligned)",
+         workspace_bytes, workspace, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Bump bp(workspace);
+  BwdWs ws;
+  bwd_layout(c, n, K, R, bp, ws);
+  const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), L = c.num_layers, V = c.draft_vocab;
+  const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
+  const int nqhd = nq * hd, nkvhd = nkv * hd;
+  const int dt = c.dtype, es = (int)esize(c), gbf = dt == PEAGLE_BF16 ? 1 : 0;
+  const int Rp = ws.Rp, Vp = ws.Vp;
+  const float eps = (float)c.rms_eps;
+  auto at = [es](const void* base, size_t elems) { return static_cast<char*>(const_cast<void*>(base)) + elems * es; };
+  GemmOut go;
+  // D = X W^T into the partial slabs; the result is ws.part (row stride N).
+  // Only a model weight (w_early) may be read before the kernel waits for
+  // its predecessor: the transposed copies of this pass are written by
+  // kernels of the same launch chain.
+  auto mm = [&](const void* X, int ldx, const void* W, int M, int N, int Kd, bool w_early = false) {
+    return gemm_launch(dt, X, ldx, W, M, N, Kd, ws.part, &go, ws.sem, m->status, -1, s, w_early);
+  };
+  auto copy_out = [&](int M, int N, float* dst) { return launch_sum_splits(go, M, N, dst, s); };
+
+  CUDA_TRY(cudaMemsetAsync(ws.sem, 0, kGemmSemCount * sizeof(int), s));
+  // ---- rows and their metadata (the forward's)
+  st = cod_enqueue(n, K, seed, counts, ws.indices, ws.row_of, s);
+  if (st) return st;
+  TrainMetaArgs ta{};
+  ta.n = n;
+  ta.R = R;
+  ta.K = K;
+  ta.S = num_seqs;
+  ta.Vt = c.target_vocab;
+  ta.Vd = V;
+  ta.max_pos = c.max_position;
+  memcpy(ta.off, off, sizeof off);
+  ta.indices = ws.indices;
+  ta.position_ids = position_ids;
+  ta.cu = cu_seqlens;
+  ta.labels = labels;
+  ta.loss_mask = loss_mask;
+  ta.t2d = m->w.t2d;
+  ta.row_anchor = ws.anchor;
+  ta.row_depth = ws.depth;
+  ta.row_pos = ws.pos;
+  ta.row_start = ws.start;
+  ta.row_end = ws.end;
+  ta.row_label = ws.label;
+  ta.status = m->status;
+  CUDA_TRY(launch_train_meta(ta, s));
+
+  // ---- forward, keeping activations. fc over the n aux rows and the
+  // mask_hidden row (source row n)
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, n, H, AHt, ws.U, &go, ws.sem, m->status, -1, s));
+  FcFinishArgs fa{};
+  fa.u = go;
+  fa.H = H;
+  fa.Vt = c.target_vocab;
+  fa.tok = input_ids;
+  fa.embed = m->w.embed;
+  fa.g_fc = m->w.fc_norm_w;
+  fa.g_in = m->layers[0].in_norm_w;
+  fa.g_h = m->layers[0].hidden_norm_w;
+  fa.eps = eps;
+  fa.nbr = c.norm_before_residual;
+  fa.x0 = ws.x0src;
+  fa.resid = ws.residsrc;
+  fa.hid = ws.hidsrc;
+  fa.status = m->status;
+  CUDA_TRY(launch_fc_finish(dt, n, fa, s));
+  CUDA_TRY(gemm_launch(dt, m->w.mask_hidden, AHt, m->w.fc_w, 1, H, AHt, ws.Um, &go, ws.sem, m->status, -1, s));
+  fa.u = go;
+  fa.tok = nullptr;
+  fa.tok_const = c.ptd_token_id;
+  fa.x0 = at(ws.x0src, (size_t)n * 2 * H);
+  fa.resid = ws.residsrc + (size_t)n * H;
+  fa.hid = ws.hidsrc + (size_t)n * H;
+  CUDA_TRY(launch_fc_finish(dt, 1, fa, s));
+  CUDA_TRY(launch_gather_masked(es, ws.x0src, n, R, 2 * H, ws.x0full, s));
+  CUDA_TRY(launch_gather_masked(4, ws.hidsrc, n, R, H, ws.hidfull, s));
+  CUDA_TRY(launch_gather_masked(4, ws.residsrc, n, R, H, ws.residfull, s));
+
+  for (int l = 0; l < L; ++l) {
+    const peagle_layer_weights& W = m->layers[l];
+    const int in = l == 0 ? 2 * H : H;
+    float* hstream = ws.hmid[l];   // the residual stream while the layer runs
+    CUDA_TRY(mm(ws.xin[l], in, W.qkv_w, R, QKV, in, true));
+    QkvArgs qa{};
+    qa.in = go;
+    qa.nq = nq;
+    qa.nkv = nkv;
+    qa.hd = hd;
+    qa.H = H;
+    qa.K = K;
+    qa.mode = 0;
+    qa.row0 = 0;
+    qa.src0 = 0;
+    qa.rcos = m->rcos;
+    qa.rsin = m->rsin;
+    qa.max_pos = c.max_position;
+    qa.row_pos = ws.pos;
+    qa.Q = ws.q[l];
+    qa.Kout = ws.k[l];
+    qa.Vout = ws.v[l];
+    qa.status = m->status;
+    if (l == 0) {   // the layer-0 residual seeds the stream
+      qa.resid0 = ws.residfull;
+      qa.h = hstream;
+    }
+    CUDA_TRY(launch_qkv_finish(dt, R, qa, s));
+    if (l == 0) CUDA_TRY(cudaMemcpyAsync(ws.hin[0], hstream, (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
+    else CUDA_TRY(cudaMemcpyAsync(hstream, ws.hin[l], (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
+    TrainAttnArgs aa{};
+    aa.R = R;
+    aa.n = n;
+    aa.nq = nq;
+    aa.nkv = nkv;
+    aa.hd = hd;
+    aa.Q = ws.q[l];
+    aa.Kr = ws.k[l];
+    aa.Vr = ws.v[l];
+    aa.row_anchor = ws.anchor;
+    aa.row_depth = ws.depth;
+    aa.row_start = ws.start;
+    aa.row_of = ws.row_of;
+    aa.O = ws.o[l];
+    aa.scale = 1.0f / sqrtf((float)hd);
+    aa.status = m->status;   // no V^T scratch: the mma.sync / CUDA-core kernels
+    TrainTileArgs tt{};
+    tt.K = K;
+    for (int d = 0; d <= K; ++d) tt.row_off[d] = off[d];
+    CUDA_TRY(launch_train_attn(dt, aa, tt, -1, s));
+    CUDA_TRY(mm(ws.o[l], nqhd, W.o_w, R, H, nqhd, true));
+    ResidNormArgs ra{};
+    ra.in = go;
+    ra.H = H;
+    ra.row0 = 0;
+    ra.h = hstream;
+    ra.gain = W.post_norm_w;
+    ra.eps = eps;
+    ra.y = ws.y[l];
+    CUDA_TRY(launch_resid_norm(dt, R, ra, s));   // hstream = h_mid
+    CUDA_TRY(mm(ws.y[l], H, W.gate_up_w, R, 2 * I, H, true));
+    CUDA_TRY(copy_out(R, 2 * I, ws.gu[l]));
+    CUDA_TRY(launch_swiglu(dt, GemmOut{ws.gu[l], 2 * I, 1, 0}, R, I, ws.act[l], s));
+    CUDA_TRY(mm(ws.act[l], I, W.down_w, R, H, I, true));
+    // h_out = h_mid + down: into the next layer's input stream (or hL)
+    float* hnext = (l + 1 < L) ? ws.hin[l + 1] : ws.hL;
+    CUDA_TRY(cudaMemcpyAsync(hnext, hstream, (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
+    ra.in = go;
+    ra.h = hnext;
+    ra.gain = (l + 1 < L) ? m->layers[l + 1].in_norm_w : m->w.final_norm_w;
+    ra.y = (l + 1 < L) ? ws.xin[l + 1] : ws.z;
+    CUDA_TRY(launch_resid_norm(dt, R, ra, s));
+  }
+  // head: logits, per-row CE, the loss and its per-depth counts
+  CUDA_TRY(mm(ws.z, H, m->w.lm_head_w, R, V, H, true));
+  CUDA_TRY(copy_out(R, V, ws.logits));
+  CUDA_TRY(launch_ce_rows(GemmOut{ws.logits, V, 1, 0}, R, V, 0, ws.label, nullptr, ws.rce, ws.ram, s));
+  CeReduceArgs cr{};
+  cr.row_ce = ws.rce;
+  cr.row_am = ws.ram;
+  cr.row_label = ws.label;
+  memcpy(cr.off, off, sizeof off);
+  cr.K = K;
+  cr.decay = depth_decay;
+  cr.loss_d = ws.loss_d;
+  cr.acc_d = ws.acc_d;
+  cr.valid_d = ws.valid_d;
+  cr.loss = loss;
+  CUDA_TRY(launch_ce_reduce(cr, s));
+
+  // ---- backward. Weight transposes W^T [in, out] (lm_head padded to Vp)
+  CUDA_TRY(launch_transpose(dt, m->w.lm_head_w, V, H, H, ws.wT_lm, Vp, Vp, s));
+  CUDA_TRY(launch_transpose(dt, m->w.fc_w, H, AHt, AHt, ws.wT_fc, H, H, s));
+  for (int l = 0; l < L; ++l) {
+    const peagle_layer_weights& W = m->layers[l];
+    const int in = l == 0 ? 2 * H : H;
+    CUDA_TRY(launch_transpose(dt, W.qkv_w, QKV, in, in, ws.wT_qkv[l], QKV, QKV, s));
+    CUDA_TRY(launch_transpose(dt, W.o_w, H, nqhd, nqhd, ws.wT_o[l], H, H, s));
+    CUDA_TRY(launch_transpose(dt, W.gate_up_w, 2 * I, H, H, ws.wT_gu[l], 2 * I, 2 * I, s));
+    CUDA_TRY(launch_transpose(dt, W.down_w, H, I, I, ws.wT_down[l], H, H, s));
+  }
+  // gain gradients accumulate
+  CUDA_TRY(cudaMemsetAsync(gout(grads->fc_norm_w), 0, (size_t)H * 4, s));
+  CUDA_TRY(cudaMemsetAsync(gout(grads->final_norm_w), 0, (size_t)H * 4, s));
+  for (int l = 0; l < L; ++l) {
+    CUDA_TRY(cudaMemsetAsync(gout(grads->layers[l].in_norm_w), 0, (size_t)H * 4, s));
+    CUDA_TRY(cudaMemsetAsync(gout(grads->layers[l].post_norm_w), 0, (size_t)H * 4, s));
+    if (l == 0) CUDA_TRY(cudaMemsetAsync(gout(grads->layers[0].hidden_norm_w), 0, (size_t)H * 4, s));
+  }
+  // dW = dY^T X: both transposed ([out, Rp], [in, Rp]) then contracted over Rp
+  // (the first out_rows rows of the [out, in] result go to dW)
+  auto dweight = [&](const void* dY_es, int out, const void* X_es, int in, int rows, int rows_pad, float* dW,
+                     int out_rows) -> cudaError_t {
+    cudaError_t e = launch_transpose(dt, dY_es, rows, out, out, ws.ta, rows_pad, rows_pad, s);
+    if (e == cudaSuccess) e = launch_transpose(dt, X_es, rows, in, in, ws.tb, rows_pad, rows_pad, s);
+    if (e == cudaSuccess) e = mm(ws.ta, rows_pad, ws.tb, out, in, rows_pad);
+    if (e == cudaSuccess) e = copy_out(out_rows, in, dW);
+    return e;
+  };
+  // cross-entropy -> logits gradient (padded to Vp columns)
+  CUDA_TRY(cudaMemsetAsync(ws.dlog, 0, (size_t)R * Vp * es, s));   // the Vp - V pad columns stay 0
+  CUDA_TRY(launch_ce_bwd(dt, ws.logits, R, V, ws.label, ws.depth, ws.valid_d, depth_decay, ws.dlog, Vp, s));
+  // lm_head: dW_lm = dlogits^T z; dz = dlogits W_lm
+  CUDA_TRY(dweight(ws.dlog, Vp, ws.z, H, R, Rp, gout((grads->lm_head_w)), V));
+  CUDA_TRY(mm(ws.dlog, Vp, ws.wT_lm, R, H, Vp));
+  CUDA_TRY(copy_out(R, H, ws.dh2));
+  // final norm: dh = RMSNorm'(hL) dz
+  CUDA_TRY(launch_rms_bwd(4, ws.hL, H, m->w.final_norm_w, gbf, ws.dh2, H, nullptr, 0, ws.dh, H, ws.rrow, R, H, eps, s));
+  CUDA_TRY(launch_gain_grad(4, ws.hL, H, nullptr, 0, 0, ws.dh2, H, ws.rrow, R, H, const_cast<float*>(
+                            static_cast<const float*>(grads->final_norm_w)), s));
+
+  for (int l = L - 1; l >= 0; --l) {
+    const peagle_layer_weights& W = m->layers[l];
+    const peagle_layer_weights& G = grads->layers[l];
+    const int in = l == 0 ? 2 * H : H;
+    // MLP: dact = dh W_down; dW_down = dh^T act
+    CUDA_TRY(launch_cast(dt, ws.dh, ws.gcast, (long long)R * H, s));
+    CUDA_TRY(dweight(ws.gcast, H, ws.act[l], I, R, Rp, gout((G.down_w)), H));
+    CUDA_TRY(mm(ws.gcast, H, ws.wT_down[l], R, I, H));
+    CUDA_TRY(launch_swiglu_bwd(dt, ws.gu[l], ws.part, R, I, ws.dgu, s));
+    // dy = dgu W_gu; dW_gu = dgu^T y
+    CUDA_TRY(dweight(ws.dgu, 2 * I, ws.y[l], H, R, Rp, gout((G.gate_up_w)), 2 * I));
+    CUDA_TRY(mm(ws.dgu, 2 * I, ws.wT_gu[l], R, H, 2 * I));
+    // post-attention norm: dh_mid = dh + RMSNorm'(h_mid) dy
+    CUDA_TRY(copy_out(R, H, ws.dh2));
+    CUDA_TRY(launch_rms_bwd(4, ws.hmid[l], H, W.post_norm_w, gbf, ws.dh2, H, ws.dh, H, ws.dh, H, ws.rrow, R, H, eps, s));
+    CUDA_TRY(launch_gain_grad(4, ws.hmid[l], H, nullptr, 0, 0, ws.dh2, H, ws.rrow, R, H,
+                              gout((G.post_norm_w)), s));
+    // O projection: do = dh_mid W_o; dW_o = dh_mid^T o
+    CUDA_TRY(launch_cast(dt, ws.dh, ws.gcast, (long long)R * H, s));
+    CUDA_TRY(dweight(ws.gcast, H, ws.o[l], nqhd, R, Rp, gout((G.o_w)), H));
+    CUDA_TRY(mm(ws.gcast, H, ws.wT_o[l], R, nqhd, H));
+    CUDA_TRY(launch_cast(dt, ws.part, ws.gcast, (long long)R * nqhd, s));   // do, model dtype
+    // attention and RoPE
+    AttnBwdArgs ab{};
+    ab.R = R;
+    ab.n = n;
+    ab.K = K;
+    ab.nq = nq;
+    ab.nkv = nkv;
+    ab.hd = hd;
+    ab.Q = ws.q[l];
+    ab.Kr = ws.k[l];
+    ab.Vr = ws.v[l];
+    ab.O = ws.o[l];
+    ab.dO = ws.gcast;
+    ab.row_anchor = ws.anchor;
+    ab.row_depth = ws.depth;
+    ab.row_start = ws.start;
+    ab.row_end = ws.end;
+    ab.row_of = ws.row_of;
+    memcpy(ab.off, off, sizeof off);
+    ab.scale = 1.0f / sqrtf((float)hd);
+    ab.dQ = ws.dQ;
+    ab.dK = ws.dK;
+    ab.dV = ws.dV;
+    ab.lse = ws.lse;
+    ab.Dv = ws.Dv;
+    CUDA_TRY(launch_attn_bwd(dt, ab, s));
+    CUDA_TRY(launch_rope_bwd(dt, hd, ws.dQ, ws.dK, ws.dV, ws.pos, m->rcos, m->rsin, c.max_position, R, nq, nkv, ws.dqkv,
+                             s));
+    // QKV: dxin = dqkv W_qkv; dW_qkv = dqkv^T xin
+    CUDA_TRY(dweight(ws.dqkv, QKV, ws.xin[l], in, R, Rp, gout((G.qkv_w)), QKV));
+    CUDA_TRY(mm(ws.dqkv, QKV, ws.wT_qkv[l], R, in, QKV));
+    CUDA_TRY(copy_out(R, in, ws.dbig));
+    if (l > 0) {   // input norm: dh = dh_mid + RMSNorm'(h_in) dxin
+      CUDA_TRY(launch_rms_bwd(4, ws.hin[l], H, W.in_norm_w, gbf, ws.dbig, H, ws.dh, H, ws.dh, H, ws.rrow, R, H, eps, s));
+      CUDA_TRY(launch_gain_grad(4, ws.hin[l], H, nullptr, 0, 0, ws.dbig, H, ws.rrow, R, H,
+                                gout((G.in_norm_w)), s));
+    } else {
+      // layer-0 input [RMSNorm_in(E[tok]) ; RMSNorm_h(hid)], residual = the
+      // normed hidden (norm_before_residual) or hid itself
+      CUDA_TRY(launch_rms_of_rows(es, m->w.embed, H, input_ids, n, c.ptd_token_id, R, H, eps, ws.rrow2, s));
+      CUDA_TRY(launch_gain_grad(es, m->w.embed, H, input_ids, n, c.ptd_token_id, ws.dbig, 2 * H, ws.rrow2, R, H,
+                                gout((G.in_norm_w)), s));
+      const float* dhn = ws.dbig + H;   // row stride 2H
+      if (c.norm_before_residual)   // d(hn) total = dxin's hidden half + the residual's gradient
+        CUDA_TRY(launch_add_rows(dhn, 2 * H, ws.dh, H, ws.dh2, H, R, H, s));
+      const float* dtot = c.norm_before_residual ? ws.dh2 : dhn;
+      const int ldt = c.norm_before_residual ? H : 2 * H;
+      CUDA_TRY(launch_rms_bwd(4, ws.hidfull, H, W.hidden_norm_w, gbf, dtot, ldt, c.norm_before_residual ? nullptr : ws.dh,
+                              H, ws.dhid, H, ws.rrow, R, H, eps, s));
+      CUDA_TRY(launch_gain_grad(4, ws.hidfull, H, nullptr, 0, 0, dtot, ldt, ws.rrow, R, H,
+                                gout((G.hidden_norm_w)), s));
+    }
+  }
+  // fc_norm and fc: depth-0 rows take u = aux W_fc^T; the masked rows share
+  // u_mask = mask_hidden W_fc^T, so their hid gradients add up first
+  CUDA_TRY(launch_colsum(ws.dhid, H, n, R, H, ws.dmask, s));
+  CUDA_TRY(cudaMemcpyAsync(ws.dhid + (size_t)n * H, ws.dmask, (size_t)H * 4, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(ws.dbig, ws.U, (size_t)n * H * 4, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(ws.dbig + (size_t)n * H, ws.Um, (size_t)H * 4, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(launch_rms_bwd(4, ws.dbig, H, m->w.fc_norm_w, gbf, ws.dhid, H, nullptr, 0, ws.du, H, ws.rrow, n + 1, H, eps, s));
+  CUDA_TRY(launch_gain_grad(4, ws.dbig, H, nullptr, 0, 0, ws.dhid, H, ws.rrow, n + 1, H,
+                            gout((grads->fc_norm_w)), s));
+  // dW_fc = [du; du_m]^T [aux; mask_hidden]; d mask_hidden = du_m W_fc
+  CUDA_TRY(launch_cast(dt, ws.du, ws.gcast, (long long)(n + 1) * H, s));
+  CUDA_TRY(cudaMemcpyAsync(ws.auxm, aux, (size_t)n * AHt * es, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(at(ws.auxm, (size_t)n * AHt), m->w.mask_hidden, (size_t)AHt * es, cudaMemcpyDeviceToDevice, s));
+  CUDA_TRY(dweight(ws.gcast, H, ws.auxm, AHt, n + 1, ws.np1p, gout((grads->fc_w)),
+                   H));
+  CUDA_TRY(mm(at(ws.gcast, (size_t)n * H), H, ws.wT_fc, 1, AHt, H));
+  CUDA_TRY(copy_out(1, AHt, gout((grads->mask_hidden))));
+  return PEAGLE_OK;
+}
+
 peagle_status peagle_combine_depth_sums(int32_t K, double depth_decay, const double* depth_sums,
                                         float* per_depth_loss, float* per_depth_acc, int32_t* per_depth_valid,
                                         float* loss, void* stream) {

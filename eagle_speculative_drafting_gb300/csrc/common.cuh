@@ -145,9 +145,13 @@ size_t gemm_out_floats(int dtype, int M, int N, int K);
 constexpr int kGemmSemCount = 4096;
 // Runs D = X W^T into out (planning the split itself; fills *o). The K
 // slices are summed inside the kernel, so *o always describes one slab.
-// X [M, K] with row stride ldx elements, W [N, K] contiguous.
+// X [M, K] with row stride ldx elements, W [N, K] contiguous. With w_early
+// the first tiles of W load before the kernel waits for its predecessor
+// (programmatic dependent launch): only for W that no kernel of the chain
+// writes, such as model weights; pass false when W was just produced.
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
-                        float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s);
+                        float* out, GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s,
+                        bool w_early = true);
 
 // Fused head epilogue of a bf16 contraction: instead of (or besides) the
 // fp32 result, per (row, column tile) partials of the row's argmax (value,
@@ -178,6 +182,6 @@ void gemm_set_wait_limit(unsigned long long ns);
 int gemm_col_tiles(int M, int N, int K);
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K,
                             float* out, GemmOut* o, int* sem, int* dev_status, int probe_op,
-                            const GemmEpi* epi, cudaStream_t s);
+                            const GemmEpi* epi, cudaStream_t s, bool w_early = true);
 
 }  // namespace pe

@@ -49,6 +49,8 @@ struct TcArgs {
   int* sem;                // per-tile arrival counters (zero between launches)
   int* status;
   unsigned long long wait_ns;  // bound of every wait of the roles (0: one try)
+  int w_early;             // W is not written by the kernels just before: its first
+                           // tiles may load before the dependency wait
   // fused head epilogue (op != EPI_STORE): one partial per (row, column tile)
   int op;
   int part_ld;             // column tiles per row
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (!waited) {
           // the weight tiles of the first stages depend on no earlier kernel:
           // start streaming them before waiting for the activations
-          pre = min(ke - kb, C::STAGES);
+          pre = g.w_early ? min(ke - kb, C::STAGES) : 0;
           for (int q = 0; q < pre; ++q) {
             const int k = kb + q, nv = nsub(k);
             tc::mbar_expect_tx(&full[q], nv * (C::A_SUB + C::B_SUB));
@@ -1027,13 +1029,13 @@ int gemm_col_tiles(int M, int N, int K) {
 }
 
 cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
-                        GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s) {
-  return gemm_launch_epi(dtype, X, ldx, W, M, N, K, out, o, sem, dev_status, probe_op, nullptr, s);
+                        GemmOut* o, int* sem, int* dev_status, int probe_op, cudaStream_t s, bool w_early) {
+  return gemm_launch_epi(dtype, X, ldx, W, M, N, K, out, o, sem, dev_status, probe_op, nullptr, s, w_early);
 }
 
 cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, int M, int N, int K, float* out,
                             GemmOut* o, int* sem, int* dev_status, int probe_op, const GemmEpi* epi,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool w_early) {
   if (M <= 0 || N <= 0) {
     if (o) *o = GemmOut{out, N, 1, 0};
     return cudaSuccess;
@@ -1061,6 +1063,7 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.sem = sem;
   args.status = dev_status;
   args.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  args.w_early = w_early ? 1 : 0;
   args.op = EPI_STORE;
   args.gate_off = 0;
   if (epi && epi->op == GEMM_EPI_SWIGLU) {

@@ -127,6 +127,7 @@ __global__ void fc_finish_kernel(FcFinishArgs a) {
       x0[j] = from_f<T>(ev[i] * inv3 * gi[i]);
       x0[H + j] = from_f<T>(hn);
       if (a.resid) a.resid[(size_t)r * H + j] = a.nbr ? hn : h;
+      if (a.hid) a.hid[(size_t)r * H + j] = h;
     }
   }
 }
@@ -638,6 +639,7 @@ __global__ void train_meta_kernel(TrainMetaArgs a) {
   a.row_pos[r] = pos;
   a.row_start[r] = s;
   a.row_label[r] = lab;
+  if (a.row_end) a.row_end[r] = e;
 }
 
 // -------------------------------------------------------------------------

@@ -59,6 +59,7 @@ struct FcFinishArgs {
   int nbr;                // norm_before_residual
   void* x0;               // out [rows, 2H]
   float* resid;           // out [rows, H] or NULL
+  float* hid;             // out [rows, H] fc_norm output, or NULL
   int* status;
 };
 
@@ -120,6 +121,7 @@ struct TrainMetaArgs {
   const uint8_t* loss_mask;
   const int* t2d;
   int *row_anchor, *row_depth, *row_pos, *row_start, *row_label;
+  int* row_end;           // optional: end of the row's conversation
   int* status;
 };
 
@@ -216,6 +218,40 @@ struct TrainTileArgs {
   int row_off[17];   // depth d rows [row_off[d], row_off[d+1])
   int tile_off[17];  // depth d tiles [tile_off[d], tile_off[d+1]) (filled by the launcher)
 };
+// Backward of the depth-masked training attention: a query-major pass (dQ,
+// and each (row, head)'s log-sum-exp and D = dO . O) and a key-major pass
+// (dK, dV) over the rows that see each key.
+struct AttnBwdArgs {
+  int R, n, K, nq, nkv, hd;
+  const void *Q, *Kr, *Vr, *O, *dO;   // model dtype, [R, nq|nkv, hd]
+  const int *row_anchor, *row_depth, *row_start, *row_end, *row_of;
+  int off[17];                        // depth d rows [off[d], off[d+1])
+  float scale;
+  float *dQ, *dK, *dV;                // fp32 [R, nq|nkv, hd]
+  float *lse, *Dv;                    // fp32 [R, nq]
+};
+cudaError_t launch_attn_bwd(int dtype, const AttnBwdArgs& a, cudaStream_t st);
+cudaError_t launch_transpose(int dtype, const void* src, int rows, int cols, int lds, void* dst, int ldd, int rows_pad,
+                             cudaStream_t st);
+cudaError_t launch_cast(int dtype, const float* src, void* dst, long long count, cudaStream_t st);
+cudaError_t launch_gather_masked(int es, const void* src, int n, int rows, int cols, void* dst, cudaStream_t st);
+cudaError_t launch_colsum(const float* src, int ld, int r0, int r1, int cols, float* dst, cudaStream_t st);
+cudaError_t launch_ce_bwd(int dtype, const float* logits, int rows, int V, const int* row_label, const int* row_depth,
+                          const int* valid_d, double decay, void* dlogits, int ldd, cudaStream_t st);
+cudaError_t launch_add_rows(const float* a, int lda, const float* b, int ldb, float* out, int ldo, int rows, int cols,
+                            cudaStream_t st);
+cudaError_t launch_rms_bwd(int x_es, const void* x, int ldx, const void* gain, int gain_bf16, const float* dy, int ldy,
+                           const float* add, int ld_add, float* dx, int ldd, float* r_out, int rows, int H, float eps,
+                           cudaStream_t st);
+cudaError_t launch_gain_grad(int x_es, const void* x, int ldx, const int* map, int map_mod, int map_const, const float* dy,
+                             int ldy, const float* r, int rows, int H, float* dg, cudaStream_t st);
+cudaError_t launch_rms_of_rows(int x_es, const void* x, int ldx, const int* map, int map_mod, int map_const, int rows, int H,
+                               float eps, float* r_out, cudaStream_t st);
+cudaError_t launch_swiglu_bwd(int dtype, const float* gu, const float* dact, int rows, int I, void* dgu, cudaStream_t st);
+cudaError_t launch_rope_bwd(int dtype, int hd, const float* dq, const float* dk, const float* dv, const int* row_pos,
+                            const float* rcos, const float* rsin, int max_pos, int rows, int nq, int nkv, void* dqkv,
+                            cudaStream_t st);
+
 cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTileArgs& tt, int probe_op,
                               cudaStream_t st);
 // tcgen05 training attention (bf16, hd = 128); false when it does not apply

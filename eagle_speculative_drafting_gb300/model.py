@@ -32,7 +32,7 @@ def weights_struct(weights: dict):
         peagle_layer_weights(ptr(L["in_norm_w"]), ptr(L.get("hidden_norm_w")), ptr(L["qkv_w"]),
                              ptr(L["o_w"]), ptr(L["post_norm_w"]), ptr(L["gate_up_w"]),
                              ptr(L["down_w"])) for L in Ls])
-    w = peagle_weights(ptr(weights["embed"]), ptr(weights["fc_w"]), ptr(weights["fc_norm_w"]),
+    w = peagle_weights(ptr(weights.get("embed")), ptr(weights["fc_w"]), ptr(weights["fc_norm_w"]),
                        ptr(weights["mask_hidden"]), ptr(weights["final_norm_w"]),
                        ptr(weights["lm_head_w"]), ptr(weights.get("d2t")), ptr(weights.get("t2d")),
                        ctypes.cast(layers, ctypes.POINTER(peagle_layer_weights)))
@@ -128,6 +128,28 @@ class Model:
                                 out["per_depth_valid"], out["loss"], row_argmax, row_ce, logits,
                                 ws, nbytes, stream, depth_sums=depth_sums)
         return out
+
+    def parallel_backward(self, aux, input_ids, position_ids, cu_seqlens, labels, K, r, r_min, seed,
+                          depth_decay=0.8, loss_mask=None, stream=None):
+        """Loss and fp32 gradients of every trainable weight (dict named like
+        the weights; grads["layers"][l][key])."""
+        import torch
+        from . import peagle_parallel_backward, peagle_parallel_backward_workspace_size
+        n = input_ids.numel()
+        nbytes = peagle_parallel_backward_workspace_size(self.handle, n, K, r, r_min)
+        ws = self.workspace(("backward", n, K, r, r_min), nbytes)
+        shapes = weight_shapes(self.cfg)
+        f32 = dict(dtype=torch.float32, device="cuda")
+        grads = {k: torch.empty(shapes[k], **f32) for k in ("fc_w", "fc_norm_w", "mask_hidden", "final_norm_w",
+                                                               "lm_head_w")}
+        grads["embed"] = None
+        grads["layers"] = [{k: (None if sh is None else torch.empty(sh, **f32)) for k, sh in L.items()}
+                           for L in shapes["layers"]]
+        gw, keep = weights_struct(grads)
+        loss = torch.empty(1, **f32)
+        peagle_parallel_backward(self.handle, n, aux, input_ids, position_ids, cu_seqlens, cu_seqlens.numel() - 1,
+                                 labels, loss_mask, K, r, r_min, seed, depth_decay, loss, gw, ws, nbytes, stream)
+        return loss, grads
 
     def save_checkpoint(self, directory, stream=None):
         """Writes the model's weights as a vLLM-loadable P-EAGLE checkpoint."""

@@ -352,6 +352,37 @@ peagle_status peagle_parallel_forward(const peagle_model* model, int32_t n, cons
  * per-depth means, counts and the loss sum_d depth_decay^d * mean_d, with
  * the arithmetic of the single-sequence reduction (a depth without labelled
  * rows contributes 0). All pointers device. K in [1, 16]. */
+/* ---- backward of the training-shaped forward ----------------------------- */
+peagle_status peagle_parallel_backward_workspace_size(const peagle_model* model, int32_t n, int32_t K,
+                                                      double r, double r_min, size_t* bytes);
+/* Gradients of the training loss sum_d depth_decay^d * mean_d CE (the loss
+ * of peagle_parallel_forward on the same arguments; #2376, PR description
+ * and Changelog: the trainer runs the parallel masked-depth loss) with
+ * respect to every weight except the token embedding (frozen: the draft
+ * shares the target's). The call runs the forward again, keeping every
+ * layer's activations in the workspace, then the backward: cross-entropy,
+ * lm_head, final norm, each layer (MLP, post-attention norm, O projection,
+ * depth-masked attention, RoPE, QKV, input norm), the layer-0 inputs, then
+ * fc_norm / fc over the depth-0 rows and the shared masked row, which gives
+ * mask_hidden its gradient.
+ *   inputs        as peagle_parallel_forward (n >= 1)
+ *   loss          device float [1] out: the loss
+ *   grads         HOST struct of device float (fp32) buffers shaped like the
+ *                 weights, written (not accumulated): fc_w, fc_norm_w,
+ *                 mask_hidden, final_norm_w, lm_head_w and every layer's
+ *                 fields (hidden_norm_w for layer 0 only); embed, d2t, t2d
+ *                 are ignored and may be NULL
+ * The contractions run on the library's GEMM over transposed copies; the
+ * workspace holds the activations of every layer (about R * (10 H + 3 I)
+ * elements per layer, plus R * Vd floats of logits). */
+peagle_status peagle_parallel_backward(const peagle_model* model, int32_t n, const void* aux,
+                                       const int32_t* input_ids, const int32_t* position_ids,
+                                       const int32_t* cu_seqlens, int32_t num_seqs,
+                                       const int32_t* labels, const uint8_t* loss_mask, int32_t K,
+                                       double r, double r_min, uint64_t seed, double depth_decay,
+                                       float* loss, const peagle_weights* grads, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
 peagle_status peagle_combine_depth_sums(int32_t K, double depth_decay, const double* depth_sums,
                                         float* per_depth_loss, float* per_depth_acc,
                                         int32_t* per_depth_valid, float* loss, void* stream);

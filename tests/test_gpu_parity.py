@@ -640,3 +640,77 @@ def test_closed_draft_verify_loop_matches_the_oracle():
             o = int(inp["kv_offsets"][b])
             assert H().max_abs_rel(g[o:o + lens[b]], kc[l][o:o + lens[b]]) <= F32_TOL
     assert pe().peagle_get_device_status(model.handle) == 0
+
+
+# ------------------------------------------------------------------ backward
+def _grad_pairs(got, ref):
+    for k in O.GRAD_KEYS:
+        yield k, got[k], ref[k]
+    for l, (gl, rl) in enumerate(zip(got["layers"], ref["layers"])):
+        for k, v in rl.items():
+            yield f"layers.{l}.{k}", gl[k], v
+
+
+def check_backward(wl, inp, K, r, rmin, seed, tol, W=None, nbr=True):
+    W = synth.make_weights(wl) if W is None else W
+    model = H().make_model(wl, W, norm_before_residual=int(nbr))
+    d = H().upload_train(wl, inp)
+    loss, g = model.parallel_backward(d["aux"], d["input_ids"], d["position_ids"], d["cu_seqlens"], d["labels"],
+                                      K, r, rmin, seed, loss_mask=d["loss_mask"])
+    torch.cuda.synchronize()
+    got = {k: (v.cpu().numpy() if v is not None else None) for k, v in g.items() if k != "layers"}
+    got["layers"] = [{k: (v.cpu().numpy() if v is not None else None) for k, v in L.items()} for L in g["layers"]]
+    om = H().oracle_model(wl, W, nbr)
+    ref_loss, ref = O.parallel_grads(om, **{k: inp[k] for k in ("aux", "input_ids", "position_ids", "cu_seqlens",
+                                                                "labels", "loss_mask")}, K=K, r=r, r_min=rmin,
+                                     seed=seed)
+    assert abs(float(loss.item()) - ref_loss) <= tol * max(1.0, abs(ref_loss))
+    worst = {}
+    for name, a, b in _grad_pairs(got, ref):
+        err = H().max_abs_rel(np.asarray(a).reshape(np.shape(b)), b)
+        worst[name] = err
+    assert max(worst.values()) <= tol, sorted(worst.items(), key=lambda kv: -kv[1])[:5]
+    assert pe().peagle_get_device_status(model.handle) == 0
+    return model, d, g, loss
+
+
+@pytest.mark.parametrize("nbr", [True, False])
+def test_backward_f32_matches_autograd(nbr):
+    wl, inp = small_train()
+    check_backward(wl, inp, 4, 0.7, 0.2, 11, F32_TOL, nbr=nbr)
+
+
+def test_backward_bf16_matches_autograd():
+    wl, inp = small_train(dtype="bf16", n=300, lens=(120, 7, 100, 73), K=4)
+    check_backward(wl, inp, 4, 0.7, 0.2, 99, BF16_TOL)
+
+
+def test_backward_f32_draft_vocab_and_loss_mask():
+    # a 600-id draft vocab (t2d = -1 labels carry no loss), a loss mask, and a
+    # vocabulary width that is not a multiple of 8
+    wl, inp = small_train(n=50, lens=(30, 20), K=3)
+    W = synth.make_weights(wl)
+    d2t, t2d = draft_vocab_maps(wl.vocab, 606, 8)
+    W = dict(W, lm_head_w=W["lm_head_w"][:606].copy(), d2t=d2t, t2d=t2d)
+    inp["loss_mask"] = (np.arange(50) % 4 != 1).astype(np.uint8)
+    check_backward(wl, inp, 3, 0.7, 0.2, 5, F32_TOL, W=W)
+
+
+def test_backward_step_lowers_the_loss():
+    # one plain gradient step on the device weights lowers the forward loss
+    wl, inp = small_train(dtype="bf16", n=300, lens=(120, 7, 100, 73), K=4)
+    W = synth.make_weights(wl)
+    model, d, g, loss0 = check_backward(wl, inp, 4, 0.7, 0.2, 3, BF16_TOL, W=W)
+    lr = 0.5
+    with torch.no_grad():
+        for k in O.GRAD_KEYS:
+            w = model._keep[k]
+            w.copy_((w.float() - lr * g[k].reshape(w.shape)).to(w.dtype))
+        for L, G in zip(model._keep["layers"], g["layers"]):
+            for k, gv in G.items():
+                if gv is not None and L.get(k) is not None:
+                    L[k].copy_((L[k].float() - lr * gv).to(L[k].dtype))
+    model2 = pe().Model(model.cfg, model._keep)   # the masked-row constants follow the new weights
+    out = model2.parallel_forward(d["aux"], d["input_ids"], d["position_ids"], d["cu_seqlens"], d["labels"], 4, 0.7,
+                                  0.2, 3)
+    assert float(out["loss"].item()) < float(loss0.item()) - 1e-3
