@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="bound on the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="training workloads: time the forward + backward (gradients of every weight)")
     ap.add_argument("--probe-steps", type=int, default=None,
                     help="steps of each per-op timing pass (default: --steps, at least 300, at most 2000)")
     ap.add_argument("--e2e-steps", type=int, default=None,
@@ -556,6 +558,69 @@ def run_train(args, wl):
         dist.destroy_process_group()
 
 
+def run_backward(args, wl):
+    """Forward + backward of the training-shaped pass on one GPU: the loss
+    and the gradients of every weight but the embedding, per packed
+    sequence. Metric: training rows (all depths) per second."""
+    import torch
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import eagle_speculative_drafting_gb300 as pe
+    import synth
+    from eagle_speculative_drafting_gb300 import marshal
+    from eagle_speculative_drafting_gb300.model import weight_shapes, weights_struct
+
+    W = synth.make_weights(wl)
+    inp = synth.make_train_inputs(wl)
+    model = marshal.make_model(wl, W)
+    d = marshal.upload_train(wl, inp)
+    n, K, r, rmin, seed = wl.n_tokens, inp["K"], inp["r"], inp["r_min"], inp["seed"]
+    R = sum(pe.peagle_cod_counts(n, K, r, rmin))
+    nbytes = pe.peagle_parallel_backward_workspace_size(model.handle, n, K, r, rmin)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    shapes = weight_shapes(model.cfg)
+    f32 = dict(dtype=torch.float32, device="cuda")
+    grads = {k: torch.empty(shapes[k], **f32) for k in ("fc_w", "fc_norm_w", "mask_hidden", "final_norm_w",
+                                                           "lm_head_w")}
+    grads["layers"] = [{k: (None if sh is None else torch.empty(sh, **f32)) for k, sh in L.items()}
+                       for L in shapes["layers"]]
+    gw, keep = weights_struct(grads)
+    loss = torch.empty(1, **f32)
+    S = len(inp["cu_seqlens"]) - 1
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pe.peagle_parallel_backward(model.handle, n, d["aux"], d["input_ids"], d["position_ids"], d["cu_seqlens"],
+                                    S, d["labels"], None, K, r, rmin, seed, inp["depth_decay"], loss, gw, ws,
+                                    nbytes, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local).__enter__()
+    launches0 = pe.peagle_kernel_launches()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
+    ms = e0.elapsed_time(e1) / args.steps
+    line = {"metric": "training rows/s per P-EAGLE forward + backward", "value": R / (ms / 1000.0),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic", "config": {"workload": wl.name, "n_tokens": n, "K": K, "rows": R,
+                                            "pass": "forward + backward, gradients of every weight"},
+            "gpu_launches": int(pe.peagle_kernel_launches() - launches0), "loss": float(loss.item()),
+            "workspace_bytes": int(nbytes), "device_status": pe.peagle_get_device_status(model.handle),
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 # ------------------------------------------------------------------- ours
 def main():
     args = parse_args()
@@ -564,7 +629,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args, wl)
     if wl.kind == "train":
-        return run_train(args, wl)
+        return run_backward(args, wl) if args.backward else run_train(args, wl)
 
     import torch
     rank, world, local = dist_env()
