@@ -1187,7 +1187,7 @@ struct BwdWs {
   int* valid_d;
   float *dh, *dh2, *dhid, *dbig, *dQ, *dK, *dV, *lse, *Dv, *rrow, *rrow2, *du, *dmask;
   std::vector<void*> xin, q, k, v, o, y, act, wT_qkv, wT_o, wT_gu, wT_down;
-  std::vector<float*> hin, hmid, gu;
+  std::vector<float*> hin, hmid, gu, lse2;   // lse2: each layer's base-2 log-sum-exp (bf16 path)
   void *wT_lm, *wT_fc;
 };
 
@@ -1234,6 +1234,7 @@ static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, Bw
   ws.hin.assign(L, nullptr);
   ws.hmid.assign(L, nullptr);
   ws.gu.assign(L, nullptr);
+  ws.lse2.assign(L, nullptr);
   for (int l = 0; l < L; ++l) {
     const int in = l == 0 ? 2 * H : H;
     ws.xin[l] = l == 0 ? ws.x0full : bp.take_bytes((size_t)R * H * es);
@@ -1246,6 +1247,7 @@ static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, Bw
     ws.y[l] = bp.take_bytes((size_t)R * H * es);
     ws.gu[l] = bp.take<float>((size_t)R * 2 * I);
     ws.act[l] = bp.take_bytes((size_t)R * I * es);
+    ws.lse2[l] = bp.take<float>((size_t)R * c.num_q_heads);
     ws.wT_qkv[l] = bp.take_bytes((size_t)in * QKV * es);
     ws.wT_o[l] = bp.take_bytes((size_t)nqhd * H * es);
     ws.wT_gu[l] = bp.take_bytes((size_t)H * 2 * I * es);
@@ -1473,6 +1475,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     aa.O = ws.o[l];
     aa.scale = 1.0f / sqrtf((float)hd);
     aa.status = m->status;   // no V^T scratch: the mma.sync / CUDA-core kernels
+    aa.lse2 = dt == PEAGLE_BF16 ? ws.lse2[l] : nullptr;   // the tensor-core backward rebuilds P from it
     TrainTileArgs tt{};
     tt.K = K;
     for (int d = 0; d <= K; ++d) tt.row_off[d] = off[d];
@@ -1605,6 +1608,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     ab.dV = ws.dV;
     ab.lse = ws.lse;
     ab.Dv = ws.Dv;
+    ab.lse2 = dt == PEAGLE_BF16 ? ws.lse2[l] : nullptr;
     CUDA_TRY(launch_attn_bwd(dt, ab, s));
     CUDA_TRY(launch_rope_bwd(dt, hd, ws.dQ, ws.dK, ws.dV, ws.pos, m->rcos, m->rsin, c.max_position, R, nq, nkv, ws.dqkv,
                              s));

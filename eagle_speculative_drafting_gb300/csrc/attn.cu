@@ -17,6 +17,7 @@
 // (i, 1..d).
 #include <math.h>
 
+#include "mma.cuh"
 #include "rows.cuh"
 
 namespace pe {
@@ -225,37 +226,6 @@ __global__ void decode_combine(DecodeAttnArgs a) {
 //   softmax     row maxima/sums meet in shared memory, P goes to smem (bf16);
 //   O += P V    warp w owns head dims [w*hd/4, (w+1)*hd/4).
 // Rows are the K*G queries reading this KV head, padded to 16*MT.
-namespace mm {
-__device__ __forceinline__ uint32_t sa(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
-      " {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src, int bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-}  // namespace mm
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // NW warps: warp w scores keys [w*KW, (w+1)*KW) of each 64-key tile for
 // every row and owns head dims [w*DW, (w+1)*DW) of the P V product. This
@@ -1095,6 +1065,7 @@ __global__ void __launch_bounds__(128) train_attn_mma(TrainAttnArgs a, TrainTile
   for (int hf = 0; hf < 2; ++hf) {
     const int q = 16 * w + hf * 8 + (lane >> 2);
     if (q >= nrows) continue;
+    if (a.lse2 && (lane & 3) == 0) a.lse2[(size_t)(row0 + q) * a.nq + h] = m_run[hf] + log2f(l_run[hf]);
     const float inv = l_run[hf] > 0.f ? 1.f / l_run[hf] : 0.f;
     bf16* dst = Og + ((size_t)(row0 + q) * a.nq + h) * HD + (lane & 3) * 2;
 #pragma unroll

@@ -544,6 +544,7 @@ cudaError_t launch_rope_bwd(int dtype, int hd, const float* dq, const float* dk,
 
 cudaError_t launch_attn_bwd(int dtype, const AttnBwdArgs& a, cudaStream_t st) {
   if (a.R <= 0) return cudaSuccess;
+  if (attn_bwd_mma_supported(dtype, a)) return launch_attn_bwd_mma(a, st);
   const dim3 gq(a.R, (a.nq + 3) / 4), gkv(a.R, (a.nkv + 3) / 4);
   if (dtype == PEAGLE_BF16) {
     if (a.hd == 128) {

@@ -164,6 +164,8 @@ struct TrainAttnArgs {
   void* Vt;                  // bf16 scratch [nkv*hd, Rp] for V transposed (tensor-core path) or NULL
   int Rp;                    // row stride of Vt: R rounded up to 64
   int* status;
+  float* lse2;               // fp32 [R, nq] or NULL: log2 of each row's softmax sum of 2^(s * scale * log2 e),
+                             // i.e. the log-sum-exp in base-2 units of the scaled scores (the backward's input)
 };
 
 cudaError_t launch_rope_table(float* c, float* s, int max_pos, int hd, double theta, cudaStream_t st);
@@ -228,9 +230,13 @@ struct AttnBwdArgs {
   int off[17];                        // depth d rows [off[d], off[d+1])
   float scale;
   float *dQ, *dK, *dV;                // fp32 [R, nq|nkv, hd]
-  float *lse, *Dv;                    // fp32 [R, nq]
+  float *lse, *Dv;                    // fp32 [R, nq]: log-sum-exp (natural units) and dO . O
+  const float* lse2;                  // bf16 tensor-core path: the forward's base-2 log-sum-exp [R, nq], else NULL
 };
 cudaError_t launch_attn_bwd(int dtype, const AttnBwdArgs& a, cudaStream_t st);
+// bf16 tensor-core form (needs lse2 from the forward; hd 64 or 128)
+bool attn_bwd_mma_supported(int dtype, const AttnBwdArgs& a);
+cudaError_t launch_attn_bwd_mma(const AttnBwdArgs& a, cudaStream_t st);
 cudaError_t launch_transpose(int dtype, const void* src, int rows, int cols, int lds, void* dst, int ldd, int rows_pad,
                              cudaStream_t st);
 cudaError_t launch_cast(int dtype, const float* src, void* dst, long long count, cudaStream_t st);

@@ -685,6 +685,14 @@ def test_backward_bf16_matches_autograd():
     check_backward(wl, inp, 4, 0.7, 0.2, 99, BF16_TOL)
 
 
+def test_backward_bf16_hd128_gqa_long_conversations():
+    # head dim 128, three query heads per KV head, K = 6: conversations span
+    # several 64-key tiles of the tensor-core backward, with ragged tails
+    wl, inp = small_train(dtype="bf16", n=700, lens=(300, 5, 129, 200, 66), K=6, hidden=384, num_q_heads=6,
+                          num_kv_heads=2, head_dim=128)
+    check_backward(wl, inp, 6, 0.7, 0.2, 21, BF16_TOL)
+
+
 def test_backward_f32_draft_vocab_and_loss_mask():
     # a 600-id draft vocab (t2d = -1 labels carry no loss), a loss mask, and a
     # vocabulary width that is not a multiple of 8
