@@ -112,7 +112,9 @@ cudaError_t library_status_word(int** out);
 // Runs fn() on the current device once: `done` holds one bit per device,
 // set after fn() succeeded there. Launch attributes such as the dynamic
 // shared-memory limit apply to the device current when they are set, so
-// every device a kernel runs on needs its own set-up. Safe across threads.
+// every device a kernel runs on needs its own set-up. Safe across threads;
+// fn() must not call once_per_device itself (the set-up lock is not
+// recursive).
 template <typename F>
 inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& fn) {
   const int dev = current_device();

@@ -311,11 +311,18 @@ __device__ void swiglu_finish_rows(const TcArgs& g, int m_begin, int m_end, int 
   }
 }
 
-template <int BN, bool SWAP>
+// CM = 2: two CTAs of a cluster take the two A tiles (row blocks 2p, 2p+1) of
+// the same weight tile; each loads its half of the weight rows and
+// multicasts it into both CTAs' ring stage, so every SM fetches half the
+// weight bytes per product. A stage is free again once both CTAs' products
+// have read it (each commit arrives on both CTAs' empty barrier).
+template <int BN, bool SWAP, int CM>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcArgs g) {
+  static_assert(CM == 1 || (CM == 2 && !SWAP), "clusters pair wide (unswapped) tiles only");
   using C = TcCfg<BN, SWAP>;
+  constexpr uint16_t kPeers = (uint16_t)((1u << CM) - 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -334,7 +341,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], CM);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
@@ -348,7 +355,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
   if (warp == 1) tc::tmem_alloc(tslot, C::TMEM_COLS);
   tc::fence_before();
-  __syncthreads();
+  if constexpr (CM > 1) tc::cluster_sync();   // the peer's barriers exist before any multicast
+  else __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
   pdl_trigger();   // the next kernel may launch now and wait for this one
@@ -356,8 +364,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int tilesA = (g.rowsA + 127) / 128;
   const int tilesB = (g.rowsB + BN - 1) / BN;
   const int ktiles = (g.K + C::KT - 1) / C::KT;
+  // work items are cluster tiles: CM consecutive A tiles of one weight tile
+  // (the host pairs tiles only when tilesA is a multiple of CM)
+  const int cr = CM > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int tilesAg = tilesA / CM;
+  auto tile_of = [&](int t, int& ta, int& tb) {
+    ta = (t % tilesAg) * CM + cr;
+    tb = t / tilesAg;
+  };
+  // k-tile j of a work item: wide tiles start their K walk at an offset
+  // that depends on the weight tile, so the CTAs running at once read
+  // different column ranges of the weights (a lockstep walk sends every
+  // request to the same column slice of thousands of rows)
+  auto k_at = [&](int tb, int kb, int ke, int j) {
+    if (SWAP) return kb + j;
+    const int n = ke - kb;
+    int q = j + (int)(((long long)tb * n) / tilesB);
+    if (q >= n) q -= n;
+    return kb + q;
+  };
   Sched sc;
-  sc.init(tilesA * tilesB, ktiles, g.splits, g.streamk, gridDim.x, blockIdx.x);
+  sc.init(tilesAg * tilesB, ktiles, g.splits, g.streamk, gridDim.x / CM, blockIdx.x / CM);
   Seg sg;
   int p_issued = 0;   // ring iterations whose TMA copies the producer issued
   // boxes of 64 K-columns that exist in k-tile k (the last one may be short)
@@ -377,7 +404,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc::tma_load_2d(dst, &tmA, x, t * 128, bar);
           }
         } else {
-          if (g.gate_off) {
+          if constexpr (CM > 1) {
+            // this CTA's half: the gate rows (rank 0) or the up rows (rank 1)
+            // of a gated tile, else rows [cr * BN/2, (cr + 1) * BN/2)
+            const int y = g.gate_off ? (cr == 0 ? t * (BN / 2) : g.gate_off + t * (BN / 2)) : t * BN + cr * (BN / 2);
+            tc::tma_load_2d_mc(dst + cr * (BN / 2) * 128, &tmB, x, y, bar, kPeers);
+          } else if (g.gate_off) {
             tc::tma_load_2d(dst, &tmB, x, t * (BN / 2), bar);
             tc::tma_load_2d(dst + (BN / 2) * 128, &tmB, x, g.gate_off + t * (BN / 2), bar);
           } else {
@@ -388,14 +420,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int it = 0, pre = 0;
       bool waited = false;
       while (!*abort_flag && sc.next(sg)) {
-        const int ta = sg.tile % tilesA, tb = sg.tile / tilesA;
+        int ta, tb;
+        tile_of(sg.tile, ta, tb);
         const int kb = sg.kb, ke = sg.ke;
         if (!waited) {
           // the weight tiles of the first stages depend on no earlier kernel:
           // start streaming them before waiting for the activations
           pre = g.w_early ? min(ke - kb, C::STAGES) : 0;
           for (int q = 0; q < pre; ++q) {
-            const int k = kb + q, nv = nsub(k);
+            const int k = k_at(tb, kb, ke, q), nv = nsub(k);
             tc::mbar_expect_tx(&full[q], nv * (C::A_SUB + C::B_SUB));
             for (int i = 0; i < nv; ++i) {
               if (SWAP) load_w(sA + q * C::A_BYTES + i * C::A_SUB, k * C::KT + i * 64, ta, &full[q]);
@@ -405,7 +438,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           pdl_wait();
           waited = true;
         }
-        for (int k = kb; k < ke; ++k, ++it) {
+        for (int j = 0; j < ke - kb; ++j, ++it) {
+          const int k = k_at(tb, kb, ke, j);
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           const int nv = nsub(k);
@@ -435,6 +469,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       if (!waited) pdl_wait();
       p_issued = max(it, pre);
+      if constexpr (CM > 1) {
+        // the peer's products arrive on this CTA's empty barriers: wait for
+        // the release of the last stages before the CTA may go
+        for (int q = max(0, it - C::STAGES); q < it && !*abort_flag; ++q) {
+          if (!tc::mbar_wait_for(&empty[q % C::STAGES], (q / C::STAGES) & 1, g.wait_ns)) {
+            *abort_flag = 1;
+            set_status(g.status, PEAGLE_DEV_TIMEOUT);
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -442,6 +486,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int it = 0, j = 0;
       for (; !*abort_flag && sc.next(sg); ++j) {
         const int kb = sg.kb, ke = sg.ke;
+        int ta, tb;
+        tile_of(sg.tile, ta, tb);
         const int buf = j & 1;
         const uint32_t use = j >> 1;
         if (!tc::mbar_wait_for(&tempty[buf], (use & 1) ^ 1, g.wait_ns)) {
@@ -452,7 +498,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc::fence_after();
         const uint32_t dcol = tbase + buf * BN;
         bool ok = true;
-        for (int k = kb; k < ke; ++k, ++it) {
+        for (int jk = 0; jk < ke - kb; ++jk, ++it) {
+          const int k = k_at(tb, kb, ke, jk);
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
           if (!tc::mbar_wait_for(&full[s], ph, g.wait_ns)) {
@@ -467,10 +514,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               tc::mma_bf16(dcol, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
-                           (k > kb || i > 0 || kk > 0) ? 1u : 0u);
+                           (jk > 0 || i > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          tc::mma_commit(&empty[s]);
+          if constexpr (CM > 1) tc::mma_commit_mc(&empty[s], kPeers);
+          else tc::mma_commit(&empty[s]);
         }
         if (!ok) {
           *abort_flag = 1;
@@ -487,8 +535,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int quad = warp & 3;
     int j = 0;
     for (; sc.next(sg); ++j) {
-      const int tile = sg.tile, sp = sg.slab;
-      const int ta = tile % tilesA, tb = tile / tilesA;
+      int ta, tb;
+      tile_of(sg.tile, ta, tb);
+      const int tile = tb * tilesA + ta, sp = sg.slab;
       const int buf = j & 1;
       const uint32_t use = j >> 1;
       // Whether to go on is decided by the four epilogue warps together (an
@@ -829,6 +878,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc::fence_before();
     __syncthreads();
   }
+  if constexpr (CM > 1) tc::cluster_sync();   // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     tc::fence_after();
     tc::tmem_dealloc(tbase, C::TMEM_COLS);
@@ -926,6 +976,7 @@ static int swap_bn(int M) {
 struct Plan {
   bool swap;
   int bn;
+  int cm;       // CTAs per cluster sharing a weight tile (1 or 2)
   int splits;   // partial slabs per tile (the most any tile needs)
   int tiles;
   int ktiles;
@@ -934,6 +985,7 @@ struct Plan {
 };
 
 static int sub_boxes(int bn) { return bn == 16 ? 4 : (bn <= 64 ? 2 : 1); }
+static int cluster_slots(int bn);
 
 // Few activation rows (swap): stream-K over all (tile, k-tile) units, one
 // persistent CTA per SM. Wide tiles: items (tile, K slice), choosing the
@@ -953,10 +1005,13 @@ static Plan plan_gemm(int M, int N, int K) {
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
+  // wide tiles in pairs of A tiles that share each weight tile (multicast)
+  p.cm = (!p.swap && tilesA % 2 == 0) ? 2 : 1;
   const int kt_elems = 64 * (p.swap ? sub_boxes(p.bn) : 1);
   p.ktiles = (K + kt_elems - 1) / kt_elems;
   const int sms = num_sms();
   if (p.swap && p.tiles <= kGemmSemCount) {
+    p.cm = 1;
     p.streamk = 1;
     const long long U = (long long)p.tiles * p.ktiles;
     p.grid = (int)std::min<long long>(U, sms);
@@ -976,19 +1031,23 @@ static Plan plan_gemm(int M, int N, int K) {
     return p;
   }
   p.streamk = 0;
-  const int smax = (2 * p.tiles >= sms) ? 1 : std::max(1, std::min(4, p.ktiles / 2));
+  p.cm = p.cm > 1 && cluster_slots(p.bn) > 0 ? p.cm : 1;
+  // items and CTA slots counted in clusters
+  const int slots = p.cm > 1 ? cluster_slots(p.bn) : sms;
+  const int tiles = p.tiles / p.cm;
+  const int smax = (2 * tiles >= slots) ? 1 : std::max(1, std::min(4, p.ktiles / 2));
   double best = -1.0;
   p.splits = 1;
   for (int s = 1; s <= smax && (s == 1 || p.tiles <= kGemmSemCount); ++s) {
-    const long long items = (long long)p.tiles * s;
-    const long long rounds = (items + sms - 1) / sms;
-    const double eff = (double)items / (double)(rounds * sms);
+    const long long items = (long long)tiles * s;
+    const long long rounds = (items + slots - 1) / slots;
+    const double eff = (double)items / (double)(rounds * slots);
     if (eff > best + 0.02) {
       best = eff;
       p.splits = s;
     }
   }
-  p.grid = (int)std::min<long long>((long long)p.tiles * p.splits, sms);
+  p.grid = (int)std::min<long long>((long long)tiles * p.splits, slots) * p.cm;
   return p;
 }
 
@@ -999,29 +1058,78 @@ size_t gemm_out_floats(int dtype, int M, int N, int K) {
   return (size_t)plan_gemm(M, N, K).splits * M * N;
 }
 
-template <int BN, bool SWAP>
+template <int BN, bool SWAP, int CM>
+static cudaError_t set_smem_attr() {
+  using C = TcCfg<BN, SWAP>;
+  static std::atomic<unsigned long long> attr_done{0};
+  return once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+}
+
+template <int BN, bool SWAP, int CM>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
                              cudaStream_t s) {
   using C = TcCfg<BN, SWAP>;
-  static std::atomic<unsigned long long> attr_done{0};
-  cudaError_t e0 = once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  });
+  cudaError_t e0 = set_smem_attr<BN, SWAP, CM>();
   if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CM;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP>, a, b, args);
+  cfg.numAttrs = CM > 1 ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP, CM>, a, b, args);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+// Clusters of two wide-tile CTAs that fit on the current device at once (one
+// CTA per SM; a pair needs two SMs of one GPC), or 0 if none.
+template <int BN>
+static int cluster_slots_bn() {
+  static std::atomic<int> slots[kMaxDevices];
+  static std::atomic<unsigned long long> done{0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  // the shared-memory limit first: set-up calls do not nest (one lock)
+  if (set_smem_attr<BN, false, 2>() != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaError_t e = once_per_device(done, [dev] {
+    int n = 0;
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = TcCfg<BN, false>::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, false, 2>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();   // a refused query leaves no sticky error
+    slots[dev].store(n);
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return 0;
+  return slots[dev].load();
+}
+
+static int cluster_slots(int bn) { return bn == 128 ? cluster_slots_bn<128>() : cluster_slots_bn<256>(); }
 
 int gemm_col_tiles(int M, int N, int K) {
   const Plan p = plan_gemm(M, N, K);
@@ -1097,7 +1205,8 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   } else {
     args.rowsA = M;
     args.rowsB = N;
-    ok = make_map(&ma, X, M, K, ldx, 128) && make_map(&mb, W, N, K, K, p.bn / wdiv);
+    // a paired CTA loads half of each weight tile (one half-height box)
+    ok = make_map(&ma, X, M, K, ldx, 128) && make_map(&mb, W, N, K, K, p.bn / (p.cm > 1 ? 2 : wdiv));
   }
   if (!ok) {
     set_error("cuTensorMapEncodeTiled failed (M=%d N=%d K=%d)", M, N, K);
@@ -1110,15 +1219,18 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   probe_start(probe_op, s);
   if (p.swap) {
     switch (p.bn) {
-      case 16: e = launch_tc<16, true>(ma, mb, args, items, s); break;
-      case 32: e = launch_tc<32, true>(ma, mb, args, items, s); break;
-      case 64: e = launch_tc<64, true>(ma, mb, args, items, s); break;
-      case 128: e = launch_tc<128, true>(ma, mb, args, items, s); break;
-      default: e = launch_tc<256, true>(ma, mb, args, items, s); break;
+      case 16: e = launch_tc<16, true, 1>(ma, mb, args, items, s); break;
+      case 32: e = launch_tc<32, true, 1>(ma, mb, args, items, s); break;
+      case 64: e = launch_tc<64, true, 1>(ma, mb, args, items, s); break;
+      case 128: e = launch_tc<128, true, 1>(ma, mb, args, items, s); break;
+      default: e = launch_tc<256, true, 1>(ma, mb, args, items, s); break;
     }
+  } else if (p.cm == 2) {
+    e = (p.bn == 128) ? launch_tc<128, false, 2>(ma, mb, args, items, s)
+                      : launch_tc<256, false, 2>(ma, mb, args, items, s);
   } else {
-    e = (p.bn == 128) ? launch_tc<128, false>(ma, mb, args, items, s)
-                      : launch_tc<256, false>(ma, mb, args, items, s);
+    e = (p.bn == 128) ? launch_tc<128, false, 1>(ma, mb, args, items, s)
+                      : launch_tc<256, false, 1>(ma, mb, args, items, s);
   }
   probe_stop(probe_op, s);
   return e;

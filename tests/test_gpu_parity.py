@@ -49,7 +49,11 @@ GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17,
                # wide tiles, ragged in every dimension, several rounds
                (300, 40000, 320), (512, 32000, 512),
                # few wide tiles with a long K: 256-wide tiles in four K slices
-               (300, 1024, 9000)]
+               (300, 1024, 9000),
+               # pairs of row tiles sharing each weight tile (multicast): the
+               # batched-decode O and down projections (the latter in K slices)
+               # and a ragged width
+               (512, 4096, 4096), (512, 4096, 14336), (768, 1300, 600)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
