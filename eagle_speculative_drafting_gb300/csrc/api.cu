@@ -1355,7 +1355,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   bwd_layout(c, n, K, R, bp, ws);
   const int H = c.hidden, I = c.intermediate, QKV = qkv_out(c), L = c.num_layers, V = c.draft_vocab;
   const int nq = c.num_q_heads, nkv = c.num_kv_heads, hd = c.head_dim, AHt = c.num_aux * c.target_hidden;
-  const int nqhd = nq * hd, nkvhd = nkv * hd;
+  const int nqhd = nq * hd;
   const int dt = c.dtype, es = (int)esize(c), gbf = dt == PEAGLE_BF16 ? 1 : 0;
   const int Rp = ws.Rp, Vp = ws.Vp;
   const float eps = (float)c.rms_eps;
@@ -1369,6 +1369,16 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     return gemm_launch(dt, X, ldx, W, M, N, Kd, ws.part, &go, ws.sem, m->status, -1, s, w_early);
   };
   auto copy_out = [&](int M, int N, float* dst) { return launch_sum_splits(go, M, N, dst, s); };
+  // D = X W^T into dst [M, N]: straight there when the contraction needs one
+  // slab (the kernel leaves the finished tile in slab 0), else through the
+  // partial slabs and a copy
+  auto mm_into = [&](float* dst, const void* X, int ldx, const void* W, int M, int N, int Kd,
+                     bool w_early = false) -> cudaError_t {
+    if (gemm_out_floats(dt, M, N, Kd) == (size_t)M * N)
+      return gemm_launch(dt, X, ldx, W, M, N, Kd, dst, &go, ws.sem, m->status, -1, s, w_early);
+    cudaError_t e = mm(X, ldx, W, M, N, Kd, w_early);
+    return e == cudaSuccess ? copy_out(M, N, dst) : e;
+  };
 
   CUDA_TRY(cudaMemsetAsync(ws.sem, 0, kGemmSemCount * sizeof(int), s));
   // ---- rows and their metadata (the forward's)
@@ -1490,8 +1500,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     ra.eps = eps;
     ra.y = ws.y[l];
     CUDA_TRY(launch_resid_norm(dt, R, ra, s));   // hstream = h_mid
-    CUDA_TRY(mm(ws.y[l], H, W.gate_up_w, R, 2 * I, H, true));
-    CUDA_TRY(copy_out(R, 2 * I, ws.gu[l]));
+    CUDA_TRY(mm_into(ws.gu[l], ws.y[l], H, W.gate_up_w, R, 2 * I, H, true));
     CUDA_TRY(launch_swiglu(dt, GemmOut{ws.gu[l], 2 * I, 1, 0}, R, I, ws.act[l], s));
     CUDA_TRY(mm(ws.act[l], I, W.down_w, R, H, I, true));
     // h_out = h_mid + down: into the next layer's input stream (or hL)
@@ -1504,8 +1513,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     CUDA_TRY(launch_resid_norm(dt, R, ra, s));
   }
   // head: logits, per-row CE, the loss and its per-depth counts
-  CUDA_TRY(mm(ws.z, H, m->w.lm_head_w, R, V, H, true));
-  CUDA_TRY(copy_out(R, V, ws.logits));
+  CUDA_TRY(mm_into(ws.logits, ws.z, H, m->w.lm_head_w, R, V, H, true));
   CUDA_TRY(launch_ce_rows(GemmOut{ws.logits, V, 1, 0}, R, V, 0, ws.label, nullptr, ws.rce, ws.ram, s));
   CeReduceArgs cr{};
   cr.row_ce = ws.rce;
@@ -1545,8 +1553,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
                      int out_rows) -> cudaError_t {
     cudaError_t e = launch_transpose(dt, dY_es, rows, out, out, ws.ta, rows_pad, rows_pad, s);
     if (e == cudaSuccess) e = launch_transpose(dt, X_es, rows, in, in, ws.tb, rows_pad, rows_pad, s);
-    if (e == cudaSuccess) e = mm(ws.ta, rows_pad, ws.tb, out, in, rows_pad);
-    if (e == cudaSuccess) e = copy_out(out_rows, in, dW);
+    if (e == cudaSuccess) e = mm_into(dW, ws.ta, rows_pad, ws.tb, out_rows, in, rows_pad);
     return e;
   };
   // cross-entropy -> logits gradient (padded to Vp columns)
@@ -1554,8 +1561,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   CUDA_TRY(launch_ce_bwd(dt, ws.logits, R, V, ws.label, ws.depth, ws.valid_d, depth_decay, ws.dlog, Vp, s));
   // lm_head: dW_lm = dlogits^T z; dz = dlogits W_lm
   CUDA_TRY(dweight(ws.dlog, Vp, ws.z, H, R, Rp, gout((grads->lm_head_w)), V));
-  CUDA_TRY(mm(ws.dlog, Vp, ws.wT_lm, R, H, Vp));
-  CUDA_TRY(copy_out(R, H, ws.dh2));
+  CUDA_TRY(mm_into(ws.dh2, ws.dlog, Vp, ws.wT_lm, R, H, Vp));
   // final norm: dh = RMSNorm'(hL) dz
   CUDA_TRY(launch_rms_bwd(4, ws.hL, H, m->w.final_norm_w, gbf, ws.dh2, H, nullptr, 0, ws.dh, H, ws.rrow, R, H, eps, s));
   CUDA_TRY(launch_gain_grad(4, ws.hL, H, nullptr, 0, 0, ws.dh2, H, ws.rrow, R, H, const_cast<float*>(
@@ -1572,9 +1578,8 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     CUDA_TRY(launch_swiglu_bwd(dt, ws.gu[l], ws.part, R, I, ws.dgu, s));
     // dy = dgu W_gu; dW_gu = dgu^T y
     CUDA_TRY(dweight(ws.dgu, 2 * I, ws.y[l], H, R, Rp, gout((G.gate_up_w)), 2 * I));
-    CUDA_TRY(mm(ws.dgu, 2 * I, ws.wT_gu[l], R, H, 2 * I));
+    CUDA_TRY(mm_into(ws.dh2, ws.dgu, 2 * I, ws.wT_gu[l], R, H, 2 * I));
     // post-attention norm: dh_mid = dh + RMSNorm'(h_mid) dy
-    CUDA_TRY(copy_out(R, H, ws.dh2));
     CUDA_TRY(launch_rms_bwd(4, ws.hmid[l], H, W.post_norm_w, gbf, ws.dh2, H, ws.dh, H, ws.dh, H, ws.rrow, R, H, eps, s));
     CUDA_TRY(launch_gain_grad(4, ws.hmid[l], H, nullptr, 0, 0, ws.dh2, H, ws.rrow, R, H,
                               gout((G.post_norm_w)), s));
@@ -1614,8 +1619,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
                              s));
     // QKV: dxin = dqkv W_qkv; dW_qkv = dqkv^T xin
     CUDA_TRY(dweight(ws.dqkv, QKV, ws.xin[l], in, R, Rp, gout((G.qkv_w)), QKV));
-    CUDA_TRY(mm(ws.dqkv, QKV, ws.wT_qkv[l], R, in, QKV));
-    CUDA_TRY(copy_out(R, in, ws.dbig));
+    CUDA_TRY(mm_into(ws.dbig, ws.dqkv, QKV, ws.wT_qkv[l], R, in, QKV));
     if (l > 0) {   // input norm: dh = dh_mid + RMSNorm'(h_in) dxin
       CUDA_TRY(launch_rms_bwd(4, ws.hin[l], H, W.in_norm_w, gbf, ws.dbig, H, ws.dh, H, ws.dh, H, ws.rrow, R, H, eps, s));
       CUDA_TRY(launch_gain_grad(4, ws.hin[l], H, nullptr, 0, 0, ws.dbig, H, ws.rrow, R, H,
@@ -1652,8 +1656,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   CUDA_TRY(cudaMemcpyAsync(at(ws.auxm, (size_t)n * AHt), m->w.mask_hidden, (size_t)AHt * es, cudaMemcpyDeviceToDevice, s));
   CUDA_TRY(dweight(ws.gcast, H, ws.auxm, AHt, n + 1, ws.np1p, gout((grads->fc_w)),
                    H));
-  CUDA_TRY(mm(at(ws.gcast, (size_t)n * H), H, ws.wT_fc, 1, AHt, H));
-  CUDA_TRY(copy_out(1, AHt, gout((grads->mask_hidden))));
+  CUDA_TRY(mm_into(gout(grads->mask_hidden), at(ws.gcast, (size_t)n * H), H, ws.wT_fc, 1, AHt, H));
   return PEAGLE_OK;
 }
 
