@@ -4,26 +4,32 @@
 // conversation up to its anchor plus its own chain rows (anchor, 1..d);
 // "P_Eagle" README: packed conversations isolated by cu_seqlens).
 //
-// One CTA = 128 consecutive rows of one depth (anchors ascending) x one
-// query head, 192 threads:
-//   warp 0     one thread loads Q once and streams 128-key tiles of K and
-//              of V transposed (V^T, so both products take K-major
-//              operands) with TMA: K into a 3-stage ring released by the
-//              score product, V^T into a 2-stage ring released by P V;
+// One CTA = 128 consecutive rows of one depth (anchors ascending) x one query
+// head, 480 threads:
+//   warp 0     one thread loads Q once and streams 128-key tiles of K with
+//              TMA into a 3-stage ring released by the score product;
+//   warp 14    one thread streams the tiles of V transposed (V^T, so both
+//              products take K-major operands) into a 2-stage ring
+//              released by P V (two producers: a K load never waits for a
+//              V slot);
 //   warp 1     one thread issues tcgen05.mma: S = Q K^T (M = 128 rows,
-//              N = 128 keys, K = hd) into one of two TMEM score buffers,
-//              and O += P V (N = hd, K = 128 keys) into a TMEM accumulator;
+//              N = 128 keys, K = hd) into one of two TMEM buffers, and
+//              O += P V (N = hd, K = 128 keys) into a TMEM accumulator with
+//              P read from TMEM;
 //   warps 2-9  two threads per row (64 columns each): read the scores from
 //              TMEM, mask (start(i) <= key <= anchor(i)), online softmax in
-//              exp2 units (the halves meet in shared memory for the row
-//              maximum), write P (bf16) into shared memory in the
-//              128B-swizzled K-major layout the second product reads;
+//              exp2 units (the two halves of a row meet in shared memory
+//              behind a named barrier of their two warps), write P (bf16,
+//              two per 32-bit column) back over the first 32 of the thread's
+//              own 64 score columns; the buffer is free again once P V has
+//              read it;
 //   warps 10-13 meanwhile, one thread per row: the <= d chain keys of the
 //              row on the CUDA cores (their maximum, sum and weighted value
 //              sum, the latter in spare TMEM columns), merged at the end.
 // The reference maximum of a row is only raised when the tile maximum
-// exceeds it by more than 2^8 (then O is rescaled in TMEM); in between,
-// probabilities relative to the older maximum stay below 256.
+// exceeds it by more than 2^8 (then O is rescaled in TMEM, after the
+// previous P V has landed); in between, probabilities relative to the older
+// maximum stay below 256.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel sets
 // PEAGLE_DEV_TIMEOUT and stops, after waiting (again bounded) for the TMA
 // copies and tensor-core products it has already issued.
@@ -33,15 +39,20 @@
 namespace pe {
 
 namespace ta {
-constexpr int TQ = 128, TK = 128, HD = 128, NK = 2, NV = 2, THREADS = 448;
+constexpr int TQ = 128, TK = 128, HD = 128, NK = 3, NV = 2, THREADS = 480;
 constexpr int QB = TQ * HD * 2;    // Q tile (two 64-column boxes)
 constexpr int KB = TK * HD * 2;    // K tile
 constexpr int VB = HD * TK * 2;    // V^T tile
-constexpr int PB = TQ * TK * 2;    // P tile
 constexpr int BOX = 128 * 128;     // one 64-column x 128-row box
-constexpr int SMEM = 1024 + QB + NK * KB + NV * VB + PB + 8 * TQ * 4 + 256;
+constexpr int SMEM = 1024 + QB + NK * KB + NV * VB + 8 * TQ * 4 + 256;
 constexpr float kRescale = 8.f;    // log2 headroom before the reference max moves
+constexpr int kWarpV = 14;         // the V producer
 }  // namespace ta
+
+// named barrier of the two softmax warps that hold rows quad*32 .. +31
+__device__ __forceinline__ void pair_sync(int quad) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + quad) : "memory");
+}
 
 __global__ void __launch_bounds__(ta::THREADS, 1)
     train_attn_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -52,25 +63,24 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + QB;              // [NK][KB]
   uint8_t* sV = sK + NK * KB;         // [NV][VB]
-  uint8_t* sP = sV + NV * VB;
-  float* sCm = reinterpret_cast<float*>(sP + PB);   // [TQ] chain maximum per row
-  float* sCl = sCm + TQ;                            // [TQ] chain sum per row
-  float* sX = sCl + TQ;                             // [2 tiles][2 halves][TQ] partial row maxima, then sums
-  uint64_t* qfull = reinterpret_cast<uint64_t*>(sX + 4 * TQ);
+  float* sX = reinterpret_cast<float*>(sV + NV * VB);   // [2 tiles][2 halves][TQ] partial row maxima
+  float* sCm = sX + 4 * TQ;                            // [TQ] chain maximum per row
+  float* sCl = sCm + TQ;                               // [TQ] chain sum per row
+  float* sL = sCl + TQ;                                // [2 halves][TQ] partial row sums
+  uint64_t* qfull = reinterpret_cast<uint64_t*>(sL + 2 * TQ);
   uint64_t* kfull = qfull + 1;        // [NK]
   uint64_t* kempty = kfull + NK;      // [NK]
   uint64_t* vfull = kempty + NK;      // [NV]
   uint64_t* vempty = vfull + NV;      // [NV]
-  uint64_t* sfull = vempty + NV;      // [2]
-  uint64_t* sfree = sfull + 2;        // [2]
-  uint64_t* pfull = sfree + 2;
+  uint64_t* sfull = vempty + NV;      // [2] scores of a tile are in TMEM buffer b
+  uint64_t* sfree = sfull + 2;        // [2] buffer b's P has been read by P V
+  uint64_t* pfull = sfree + 2;        // P of a tile is in TMEM and O is rescaled (both halves)
   uint64_t* pfree = pfull + 1;        // one completion per P V product
   uint64_t* chfull = pfree + 1;       // chain results of every row
-  uint64_t* xfull = chfull + 1;       // [2] both halves' partial maxima of a tile (by parity)
-  uint64_t* lfull = xfull + 2;        // both halves' partial sums
-  uint64_t* drain = lfull + 1;        // completion of every product issued, on abort
+  uint64_t* drain = chfull + 1;       // completion of every product issued, on abort
   uint32_t* tslot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  volatile int* v_issued_s = abort_flag + 1;   // V^T tiles whose copies the V producer issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -85,16 +95,14 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&sfull[b], 1);
-      tc::mbar_init(&sfree[b], 256);
+      tc::mbar_init(&sfree[b], 1);
     }
     tc::mbar_init(pfull, 256);
     tc::mbar_init(pfree, 1);
     tc::mbar_init(chfull, 128);
-    tc::mbar_init(&xfull[0], 256);
-    tc::mbar_init(&xfull[1], 256);
-    tc::mbar_init(lfull, 256);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
+    *v_issued_s = 0;
     tc::fence_mbar_init();
     tc::prefetch_map(&tmQ);
     tc::prefetch_map(&tmK);
@@ -123,7 +131,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
   const int ntiles = (kend - kbeg) / TK + 1;
   const float sl2 = a.scale * 1.4426950408889634f;
   constexpr uint32_t idesc = tc::idesc_bf16(128, 128);
-  int k_issued = 0, v_issued = 0;   // K and V^T tiles whose copies warp 0 issued
+  int k_issued = 0;   // K tiles whose copies warp 0 issued
 
   if (warp == 0) {
     if (lane == 0) {
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
       tc::tma_load_2d(sQ, &tmQ, h * HD, row0, qfull);
       tc::tma_load_2d(sQ + BOX, &tmQ, h * HD + 64, row0, qfull);
       for (int t = 0; t < ntiles && !*abort_flag; ++t) {
-        const int sk = t % NK, sv = t % NV;
+        const int sk = t % NK;
         const int key0 = kbeg + t * TK;
         if (!tc::mbar_wait(&kempty[sk], ((t / NK) & 1) ^ 1)) {
           *abort_flag = 1;
@@ -142,6 +150,14 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         tc::tma_load_2d(sK + sk * KB, &tmK, g * HD, key0, &kfull[sk]);
         tc::tma_load_2d(sK + sk * KB + BOX, &tmK, g * HD + 64, key0, &kfull[sk]);
         k_issued = t + 1;
+      }
+    }
+  } else if (warp == kWarpV) {
+    if (lane == 0) {
+      int v_issued = 0;
+      for (int t = 0; t < ntiles && !*abort_flag; ++t) {
+        const int sv = t % NV;
+        const int key0 = kbeg + t * TK;
         if (!tc::mbar_wait(&vempty[sv], ((t / NV) & 1) ^ 1)) {
           *abort_flag = 1;
           set_status(a.status, PEAGLE_DEV_TIMEOUT);
@@ -152,25 +168,30 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         tc::tma_load_2d(sV + sv * VB + BOX, &tmV, key0 + 64, g * HD, &vfull[sv]);
         v_issued = t + 1;
       }
+      *v_issued_s = v_issued;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t tO = tbase + 256;
-      // O += P_u V_u, then release the P buffer and the tile's stage
+      // O += P_u V_u, P_u from TMEM buffer u & 1 (keys 64i .. 64i+63 in
+      // columns 64i .. 64i+31); then release the V^T stage, the buffer and O
       auto pv = [&](int u) -> bool {
-        const int su = u % NV;
-        if (!tc::mbar_wait(pfull, u & 1) || !tc::mbar_wait(&vfull[su], (u / NV) & 1)) return false;
+        const int su = u % NV, b = u & 1;
+        // every softmax thread has written its P and rescaled its O columns
+        // (each product of the tile adds into all of O)
+        if (!tc::mbar_wait(&vfull[su], (u / NV) & 1) || !tc::mbar_wait(pfull, u & 1)) return false;
         tc::fence_after();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          const uint32_t a0 = tc::smem_u32(sP + i * BOX), b0 = tc::smem_u32(sV + su * VB + i * BOX);
+          const uint32_t b0 = tc::smem_u32(sV + su * VB + i * BOX);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tO, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
-                         (u > 0 || i > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_bf16_tmem_a(tO, tbase + b * 128 + i * 64 + kk * 8, tc::sw128_desc(b0 + kk * 32), idesc,
+                                (u > 0 || i > 0 || kk > 0) ? 1u : 0u);
         }
         tc::mma_commit(pfree);
         tc::mma_commit(&vempty[su]);
+        tc::mma_commit(&sfree[b]);
         return true;
       };
       bool ok = tc::mbar_wait(qfull, 0);
@@ -211,13 +232,28 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     constexpr int HC = TK / 2;   // columns per thread
     float m_ref = -INFINITY, l = 0.f;
     // every wait is skipped once the kernel has aborted, so a timeout never
-    // leaves the other threads waiting on this one
+    // leaves the other threads waiting on this one; the loop itself (and
+    // its pair barriers) always runs to the end
     auto wait = [&](uint64_t* bar, uint32_t par) -> bool {
       bool ok = !*abort_flag && tc::mbar_wait(bar, par);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0 && !*abort_flag) {
         *abort_flag = 1;
         set_status(a.status, PEAGLE_DEV_TIMEOUT);
+      }
+      return ok;
+    };
+    // P V completions are observed strictly in order (one pfree phase at a
+    // time): a parity wait is only unambiguous while the barrier is at most
+    // one phase ahead of the phase waited for. The warp catches up on
+    // product t-1 before it signals P of tile t: product t cannot start
+    // before that signal, so the barrier is never two phases ahead.
+    int pv_seen = 0;
+    auto wait_pv = [&](int u) -> bool {   // until product u has completed
+      bool ok = true;
+      while (pv_seen <= u) {
+        ok = wait(pfree, pv_seen & 1) && ok;
+        ++pv_seen;
       }
       return ok;
     };
@@ -240,8 +276,6 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < HC; ++c) sv[c] = -INFINITY;
       }
-      tc::fence_before();
-      tc::mbar_arrive(&sfree[b]);   // the score buffer may be rewritten
       // mask to the row's visible columns [lo, hi] of this half tile and take
       // the row maximum of the raw scores (the scale is positive, so it is
       // applied to the maximum and folded into the exponent below); eight
@@ -265,29 +299,24 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         }
       }
       // the row maximum from both halves (slots alternate by tile parity, so
-      // a slot is rewritten only after both halves have passed the next tile)
+      // a slot is rewritten only after the partner has passed the next
+      // tile's barrier, i.e. read this one)
       float* xs = sX + b * 2 * TQ;
       xs[hf * TQ + row] = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                 fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-      tc::mbar_arrive(&xfull[b]);
-      wait(&xfull[b], (t >> 1) & 1);
+      pair_sync(quad);
       const float mraw = fmaxf(xs[row], xs[TQ + row]);
       const float mx = mraw == -INFINITY ? -INFINITY : mraw * sl2;
-      // the previous P V product must be done before P is overwritten or O
-      // rescaled
-      if (t >= 1) {
-        wait(pfree, (t - 1) & 1);
-        tc::fence_after();
-      }
       // a row raises its reference maximum when the tile exceeds it by more
       // than 2^8 (both halves decide alike); O holds earlier tiles' products
       // only from tile 1 on, and a row whose reference was still -inf
-      // contributed zeros, so only the others rescale (TMEM accesses are
-      // warp-wide)
+      // contributed zeros, so only the others rescale, after the previous
+      // P V product has landed (TMEM accesses are warp-wide)
       const bool raise = mx > m_ref + kRescale;
       const float corr = !raise ? 1.f : (m_ref == -INFINITY ? 0.f : tc::ex2_approx(m_ref - mx));
       const bool rescale = raise && t >= 1 && m_ref != -INFINITY;
-      if (__any_sync(0xffffffffu, rescale) && !*abort_flag) {
+      if (__any_sync(0xffffffffu, rescale) && wait_pv(t - 1)) {
+        tc::fence_after();
 #pragma unroll 1
         for (int c = 0; c < HC / 16; ++c) {
           uint32_t r[16];
@@ -303,42 +332,48 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
         l *= corr;
         m_ref = mx;
       }
-      // probabilities (bf16) into this half's box of the swizzled P rows,
+      // probabilities, two bf16 per 32-bit column, over the first 32 of this
+      // thread's 64 score columns (written 16 columns at a time, one wait);
       // eight partial sums; a quarter of the exponentials run on the FMA pipe
       float ps[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ps[k] = 0.f;
       const float nref = m_ref == -INFINITY ? -INFINITY : -m_ref;   // -inf rows: every p = 0
-      uint8_t* prow = sP + hf * BOX + row * 128;
+      const uint32_t tP = tbase + tl + b * 128 + hf * HC;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint32_t w[4];
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = q * 8 + e * 2;
-          const float x0 = fmaf(sv[c], sl2, nref), x1 = fmaf(sv[c + 1], sl2, nref);
-          const bool poly = (q & 3) == 3;
-          const float p0 = poly ? tc::ex2_poly(x0) : tc::ex2_approx(x0);
-          const float p1 = poly ? tc::ex2_poly(x1) : tc::ex2_approx(x1);
-          ps[q] += p0 + p1;
-          const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-          w[e] = *reinterpret_cast<const uint32_t*>(&pp);
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = hc * 4 + qq;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = q * 8 + e * 2;
+            const float x0 = fmaf(sv[c], sl2, nref), x1 = fmaf(sv[c + 1], sl2, nref);
+            const bool poly = (q & 3) == 3;
+            const float p0 = poly ? tc::ex2_poly(x0) : tc::ex2_approx(x0);
+            const float p1 = poly ? tc::ex2_poly(x1) : tc::ex2_approx(x1);
+            ps[q] += p0 + p1;
+            const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+            w[qq * 4 + e] = *reinterpret_cast<const uint32_t*>(&pp);
+          }
         }
-        *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (have) tc::tmem_st16_nowait(tP + hc * 16, w);
       }
+      tc::tmem_st_wait();
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      tc::fence_proxy_async();
+      if (t >= 1) wait_pv(t - 1);   // issued a tile ago, long done: keeps the count in step
       tc::fence_before();
       tc::mbar_arrive(pfull);
     }
     // ---- the row sum from both halves, the chain keys, then the output
-    const bool done = wait(pfree, (ntiles - 1) & 1);
+    const bool done = wait_pv(ntiles - 1);
     tc::fence_after();
-    sX[hf * TQ + row] = l;   // tile slots are free: every tile's maxima were read
-    tc::mbar_arrive(lfull);
-    const bool summed = wait(lfull, 0) && wait(chfull, 0);
+    sL[hf * TQ + row] = l;
+    pair_sync(quad);
+    const bool summed = wait(chfull, 0);
     if (done && summed) {
-      const float lt = sX[row] + sX[TQ + row];
+      const float lt = sL[row] + sL[TQ + row];
       const float m_c = sCm[row], l_c = sCl[row];
       const float m_f = fmaxf(m_ref, m_c);
       const float so = (m_ref == -INFINITY) ? 0.f : tc::ex2_approx(m_ref - m_f);
@@ -366,21 +401,21 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
       if (live) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t w[8];
+          uint32_t wo[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float x0 = (__uint_as_float(ro[c][2 * k]) * so + __uint_as_float(ra[c][2 * k]) * sc) * inv;
             const float x1 =
                 (__uint_as_float(ro[c][2 * k + 1]) * so + __uint_as_float(ra[c][2 * k + 1]) * sc) * inv;
             const __nv_bfloat162 pp = __floats2bfloat162_rn(x0, x1);
-            w[k] = *reinterpret_cast<const uint32_t*>(&pp);
+            wo[k] = *reinterpret_cast<const uint32_t*>(&pp);
           }
-          Og[c * 2] = make_uint4(w[0], w[1], w[2], w[3]);
-          Og[c * 2 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          Og[c * 2] = make_uint4(wo[0], wo[1], wo[2], wo[3]);
+          Og[c * 2 + 1] = make_uint4(wo[4], wo[5], wo[6], wo[7]);
         }
       }
     }
-  } else {
+  } else if (warp < kWarpV) {
     // ---- chain keys (anchor, 1..d) of row quad*32 + lane, while the tiles
     // run: their maximum m_c, sum l_c and value sum relative to m_c (in TMEM
     // columns 384..511 of the row's lane)
@@ -485,6 +520,7 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
     // an aborted CTA drains what it issued before its shared memory and TMEM
     // go: Q, the last phase of every K and V^T stage, then every product
     if (warp == 0 && lane == 0) {
+      const int v_issued = *v_issued_s;
       tc::mbar_wait(qfull, 0);
       for (int t = max(0, k_issued - NK); t < k_issued; ++t) tc::mbar_wait(&kfull[t % NK], (t / NK) & 1);
       for (int t = max(0, v_issued - NV); t < v_issued; ++t) tc::mbar_wait(&vfull[t % NV], (t / NV) & 1);
