@@ -198,19 +198,23 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x for x <= 8 on the FMA pipe, to share the exponentials of a softmax
-// with the special-function unit: x = j + f with j = floor(x), 2^f from a
-// cubic in f whose coefficients were fitted to 2^f on [0, 1] for relative
-// error (8.6e-5 at most; the values are rounded to bf16 afterwards), 2^j
-// added to the exponent field. Results below 2^-126 are 0.
+// 2^x for x <= 8 on the FMA and integer pipes only, to share the
+// exponentials of a softmax with the special-function unit (rounding by
+// floorf or a float-to-int conversion would run on that same unit): adding
+// 1.5 * 2^23 leaves j = round(x) in the low mantissa bits of t, 2^f for
+// f = x - j in [-1/2, 1/2] comes from a cubic whose coefficients were fitted
+// to 2^f on that interval for relative error (2.2e-4 at most; the values
+// are rounded to bf16 afterwards), and j is added to the exponent field.
+// Results below 2^-126 are 0.
 __device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -127.f);
-  const float j = floorf(x);
-  const float f = x - j;
-  float p = fmaf(f, 0.0770665630698204f, 0.2276456654071808f);
-  p = fmaf(p, f, 0.6951165795326233f);
-  p = fmaf(p, f, 1.0f);
-  const float r = __int_as_float(__float_as_int(p) + (static_cast<int>(j) << 23));
+  const float xc = fmaxf(x, -126.f);
+  const float t = __fadd_rn(xc, 12582912.f);
+  const float f = __fsub_rn(xc, __fsub_rn(t, 12582912.f));
+  float p = fmaf(f, 0.05286737531423569f, 0.24215202033519745f);
+  p = fmaf(p, f, 0.6935867667198181f);
+  p = fmaf(p, f, 0.9999627470970154f);
+  const uint32_t j = static_cast<uint32_t>(__float_as_int(t) - 0x4B400000);
+  const float r = __int_as_float(static_cast<int>(static_cast<uint32_t>(__float_as_int(p)) + (j << 23)));
   return x < -126.f ? 0.f : r;
 }
 // thread i stores 16 columns of 32-bit values to lane (base + i); the wait
