@@ -1558,7 +1558,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   };
   // cross-entropy -> logits gradient (padded to Vp columns)
   CUDA_TRY(cudaMemsetAsync(ws.dlog, 0, (size_t)R * Vp * es, s));   // the Vp - V pad columns stay 0
-  CUDA_TRY(launch_ce_bwd(dt, ws.logits, R, V, ws.label, ws.depth, ws.valid_d, depth_decay, ws.dlog, Vp, s));
+  CUDA_TRY(launch_ce_bwd(dt, ws.logits, R, V, ws.label, ws.depth, ws.valid_d, ws.rce, depth_decay, ws.dlog, Vp, s));
   // lm_head: dW_lm = dlogits^T z; dz = dlogits W_lm
   CUDA_TRY(dweight(ws.dlog, Vp, ws.z, H, R, Rp, gout((grads->lm_head_w)), V));
   CUDA_TRY(mm_into(ws.dh2, ws.dlog, Vp, ws.wT_lm, R, H, Vp));

@@ -39,6 +39,33 @@ __global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ sr
   }
 }
 
+// bf16 with even widths and strides: 64 x 64 tiles moved as bf16 pairs, so
+// every warp access is one 128-byte row
+__global__ void __launch_bounds__(256) transpose_bf16x2_kernel(const bf16* __restrict__ src, int rows, int cols,
+                                                               int lds, bf16* __restrict__ dst, int ldd, int rows_pad) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float tile[64][65];
+  const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int k = 0; k < 64; k += 8) {
+    const int r = r0 + ty + k, c = c0 + 2 * tx;
+    float2 v = make_float2(0.f, 0.f);
+    if (r < rows && c < cols) v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + (size_t)r * lds + c));
+    tile[ty + k][2 * tx] = v.x;
+    tile[ty + k][2 * tx + 1] = v.y;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 64; k += 8) {
+    const int c = c0 + ty + k, r = r0 + 2 * tx;
+    if (c < cols && r < rows_pad)
+      *reinterpret_cast<__nv_bfloat162*>(dst + (size_t)c * ldd + r) =
+          __floats2bfloat162_rn(tile[2 * tx][ty + k], tile[2 * tx + 1][ty + k]);
+  }
+}
+
 template <typename T>
 __global__ void cast_kernel(const float* __restrict__ src, T* __restrict__ dst, long long count) {
   pdl_trigger();
@@ -86,38 +113,36 @@ __global__ void colsum_kernel(const float* __restrict__ src, int ld, int r0, int
 // -------------------------------------------------------- cross-entropy
 // Gradient of sum_d decay^d * mean_d CE with respect to the logits of row r:
 // w_r * (softmax(logits_r) - onehot(label_r)), w_r = decay^depth / (labelled
-// rows of that depth); rows without a label get zeros.
+// rows of that depth); rows without a label get zeros. The forward's row CE
+// gives the log-sum-exp (CE + the label's logit), so the row is read once.
 template <typename T>
 __global__ void __launch_bounds__(256) ce_bwd_kernel(const float* __restrict__ logits, int V, const int* row_label,
-                                                     const int* row_depth, const int* valid_d, double decay,
-                                                     T* __restrict__ dlogits, int ldd) {
+                                                     const int* row_depth, const int* valid_d, const float* row_ce,
+                                                     double decay, T* __restrict__ dlogits, int ldd) {
   pdl_trigger();
   pdl_wait();
-  __shared__ float red[32];
   const int r = blockIdx.x;
   const float* x = logits + (size_t)r * V;
   T* out = dlogits + (size_t)r * ldd;
   const int lab = row_label[r];
   const int cnt = lab >= 0 ? valid_d[row_depth[r]] : 0;
+  const bool vec = (V & 3) == 0 && (ldd & 3) == 0;
   if (lab < 0 || cnt <= 0) {
     for (int v = threadIdx.x; v < V; v += blockDim.x) out[v] = from_f<T>(0.f);
     return;
   }
   const float w = (float)(pow(decay, (double)row_depth[r]) / cnt);
-  float m = -INFINITY;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, x[v]);
-  m = warp_max(m);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  m = -INFINITY;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-  float s = 0.f;
-  for (int v = threadIdx.x; v < V; v += blockDim.x) s += __expf(x[v] - m);
-  s = block_sum(s, red);
-  const float inv = 1.f / s;
-  for (int v = threadIdx.x; v < V; v += blockDim.x)
-    out[v] = from_f<T>(w * (__expf(x[v] - m) * inv - (v == lab ? 1.f : 0.f)));
+  const float lse = row_ce[r] + x[lab];
+  if (vec) {
+    for (int v = threadIdx.x * 4; v < V; v += blockDim.x * 4) {
+      const float4 xv = *reinterpret_cast<const float4*>(x + v);
+      float g[4] = {w * __expf(xv.x - lse), w * __expf(xv.y - lse), w * __expf(xv.z - lse), w * __expf(xv.w - lse)};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) out[v + e] = from_f<T>(v + e == lab ? g[e] - w : g[e]);
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += blockDim.x) out[v] = from_f<T>(w * (__expf(x[v] - lse) - (v == lab ? 1.f : 0.f)));
+  }
 }
 
 // ---------------------------------------------------------------- RMSNorm
@@ -202,14 +227,14 @@ __global__ void swiglu_bwd_kernel(const float* __restrict__ gu, const float* __r
                                   T* __restrict__ dgu) {
   pdl_trigger();
   pdl_wait();
-  const long long total = (long long)rows * I;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(e / I), j = (int)(e % I);
-    const float g = gu[(size_t)r * 2 * I + j], u = gu[(size_t)r * 2 * I + I + j], da = dact[e];
-    const float s = 1.f / (1.f + __expf(-g));
-    dgu[(size_t)r * 2 * I + j] = from_f<T>(da * u * s * (1.f + g * (1.f - s)));
-    dgu[(size_t)r * 2 * I + I + j] = from_f<T>(da * g * s);
-  }
+  // rows over blocks, columns over threads: coalesced, no index division
+  for (int r = blockIdx.x; r < rows; r += gridDim.x)
+    for (int j = threadIdx.x; j < I; j += blockDim.x) {
+      const float g = gu[(size_t)r * 2 * I + j], u = gu[(size_t)r * 2 * I + I + j], da = dact[(size_t)r * I + j];
+      const float s = 1.f / (1.f + __expf(-g));
+      dgu[(size_t)r * 2 * I + j] = from_f<T>(da * u * s * (1.f + g * (1.f - s)));
+      dgu[(size_t)r * 2 * I + I + j] = from_f<T>(da * g * s);
+    }
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -418,6 +443,12 @@ int grid1(long long total, int threads) {
 cudaError_t launch_transpose(int dtype, const void* src, int rows, int cols, int lds, void* dst, int ldd, int rows_pad,
                              cudaStream_t st) {
   if (rows_pad <= 0 || cols <= 0) return cudaSuccess;
+  if (dtype == PEAGLE_BF16 && (cols & 1) == 0 && (lds & 1) == 0 && (ldd & 1) == 0 && (rows_pad & 1) == 0 &&
+      (reinterpret_cast<uintptr_t>(src) & 3) == 0 && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+    launch_pdl(transpose_bf16x2_kernel, dim3((rows_pad + 63) / 64, (cols + 63) / 64), 256, 0, st,
+               static_cast<const bf16*>(src), rows, cols, lds, static_cast<bf16*>(dst), ldd, rows_pad);
+    BW_END();
+  }
   const dim3 grid((rows_pad + 31) / 32, (cols + 31) / 32);
   if (dtype == PEAGLE_BF16)
     launch_pdl(transpose_kernel<bf16>, grid, 256, 0, st, static_cast<const bf16*>(src), rows, cols, lds,
@@ -453,13 +484,14 @@ cudaError_t launch_colsum(const float* src, int ld, int r0, int r1, int cols, fl
 }
 
 cudaError_t launch_ce_bwd(int dtype, const float* logits, int rows, int V, const int* row_label, const int* row_depth,
-                          const int* valid_d, double decay, void* dlogits, int ldd, cudaStream_t st) {
+                          const int* valid_d, const float* row_ce, double decay, void* dlogits, int ldd,
+                          cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   if (dtype == PEAGLE_BF16)
-    launch_pdl(ce_bwd_kernel<bf16>, rows, 256, 0, st, logits, V, row_label, row_depth, valid_d, decay,
+    launch_pdl(ce_bwd_kernel<bf16>, rows, 256, 0, st, logits, V, row_label, row_depth, valid_d, row_ce, decay,
                static_cast<bf16*>(dlogits), ldd);
   else
-    launch_pdl(ce_bwd_kernel<float>, rows, 256, 0, st, logits, V, row_label, row_depth, valid_d, decay,
+    launch_pdl(ce_bwd_kernel<float>, rows, 256, 0, st, logits, V, row_label, row_depth, valid_d, row_ce, decay,
                static_cast<float*>(dlogits), ldd);
   BW_END();
 }
@@ -511,12 +543,12 @@ cudaError_t launch_rms_of_rows(int x_es, const void* x, int ldx, const int* map,
 }
 
 cudaError_t launch_swiglu_bwd(int dtype, const float* gu, const float* dact, int rows, int I, void* dgu, cudaStream_t st) {
-  const long long total = (long long)rows * I;
-  if (total <= 0) return cudaSuccess;
+  if (rows <= 0 || I <= 0) return cudaSuccess;
+  const int grid = std::min(rows, num_sms() * 8);
   if (dtype == PEAGLE_BF16)
-    launch_pdl(swiglu_bwd_kernel<bf16>, grid1(total, 256), 256, 0, st, gu, dact, rows, I, static_cast<bf16*>(dgu));
+    launch_pdl(swiglu_bwd_kernel<bf16>, grid, 256, 0, st, gu, dact, rows, I, static_cast<bf16*>(dgu));
   else
-    launch_pdl(swiglu_bwd_kernel<float>, grid1(total, 256), 256, 0, st, gu, dact, rows, I, static_cast<float*>(dgu));
+    launch_pdl(swiglu_bwd_kernel<float>, grid, 256, 0, st, gu, dact, rows, I, static_cast<float*>(dgu));
   BW_END();
 }
 

@@ -314,14 +314,13 @@ __global__ void swiglu_kernel(GemmOut in, int rows, int I, void* act_) {
   pdl_trigger();
   pdl_wait();
   T* act = static_cast<T*>(act_);
-  const long long total = (long long)rows * I;
-  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(e / I), j = (int)(e % I);
-    const float gt = sum_parts(in, (size_t)r * in.ldo + j);
-    const float up = sum_parts(in, (size_t)r * in.ldo + I + j);
-    act[e] = from_f<T>(gt / (1.f + expf(-gt)) * up);
-  }
+  // rows over blocks, columns over threads: coalesced, no index division
+  for (int r = blockIdx.x; r < rows; r += gridDim.x)
+    for (int j = threadIdx.x; j < I; j += blockDim.x) {
+      const float gt = sum_parts(in, (size_t)r * in.ldo + j);
+      const float up = sum_parts(in, (size_t)r * in.ldo + I + j);
+      act[(size_t)r * I + j] = from_f<T>(gt / (1.f + expf(-gt)) * up);
+    }
 }
 
 // -------------------------------------------------------------------------
@@ -858,9 +857,9 @@ cudaError_t launch_resid_norm(int dtype, int rows, const ResidNormArgs& a, cudaS
 
 cudaError_t launch_swiglu(int dtype, const GemmOut& in, int rows, int I, void* act, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
-  const long long total = (long long)rows * I;
-  if (dtype == PEAGLE_BF16) launch_pdl(swiglu_kernel<bf16>, grid_for(total, 256), 256, 0, st, in, rows, I, act);
-  else launch_pdl(swiglu_kernel<float>, grid_for(total, 256), 256, 0, st, in, rows, I, act);
+  const int grid = std::min(rows, num_sms() * 8);
+  if (dtype == PEAGLE_BF16) launch_pdl(swiglu_kernel<bf16>, grid, 256, 0, st, in, rows, I, act);
+  else launch_pdl(swiglu_kernel<float>, grid, 256, 0, st, in, rows, I, act);
   PE_LAUNCH_END();
 }
 

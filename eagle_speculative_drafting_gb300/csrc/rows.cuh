@@ -243,7 +243,8 @@ cudaError_t launch_cast(int dtype, const float* src, void* dst, long long count,
 cudaError_t launch_gather_masked(int es, const void* src, int n, int rows, int cols, void* dst, cudaStream_t st);
 cudaError_t launch_colsum(const float* src, int ld, int r0, int r1, int cols, float* dst, cudaStream_t st);
 cudaError_t launch_ce_bwd(int dtype, const float* logits, int rows, int V, const int* row_label, const int* row_depth,
-                          const int* valid_d, double decay, void* dlogits, int ldd, cudaStream_t st);
+                          const int* valid_d, const float* row_ce, double decay, void* dlogits, int ldd,
+                          cudaStream_t st);
 cudaError_t launch_add_rows(const float* a, int lda, const float* b, int ldb, float* out, int ldo, int rows, int cols,
                             cudaStream_t st);
 cudaError_t launch_rms_bwd(int x_es, const void* x, int ldx, const void* gain, int gain_bf16, const float* dy, int ldy,
