@@ -1181,6 +1181,7 @@ struct BwdWs {
   int *indices, *row_of, *anchor, *depth, *pos, *start, *end, *label;
   int Rp, np1p, Vp;
   void *x0src, *x0full, *z, *dlog, *ta, *tb, *gcast, *dgu, *dqkv, *auxm;
+  void* vt;   // V transposed [nkv*hd, Rp] for the tensor-core forward attention, or NULL
   float *U, *Um, *hidsrc, *residsrc, *hidfull, *residfull, *hL, *logits, *part, *rce;
   int* ram;
   float *loss_d, *acc_d;
@@ -1299,6 +1300,8 @@ static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, Bw
   ws.du = bp.take<float>((size_t)(n + 1) * H);
   ws.dmask = bp.take<float>(H);
   ws.auxm = bp.take_bytes((size_t)(n + 1) * AHt * es);
+  ws.vt = (dt == PEAGLE_BF16 && c.head_dim == 128) ? bp.take_bytes((size_t)c.num_kv_heads * c.head_dim * Rp * es)
+                                                     : nullptr;
 }
 
 peagle_status peagle_parallel_backward_workspace_size(const peagle_model* m, int32_t n, int32_t K, double r, double r_min,
@@ -1484,7 +1487,9 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     aa.row_of = ws.row_of;
     aa.O = ws.o[l];
     aa.scale = 1.0f / sqrtf((float)hd);
-    aa.status = m->status;   // no V^T scratch: the mma.sync / CUDA-core kernels
+    aa.status = m->status;
+    aa.Vt = ws.vt;   // bf16, hd 128: the tcgen05 kernel; else mma.sync / CUDA cores
+    aa.Rp = Rp;
     aa.lse2 = dt == PEAGLE_BF16 ? ws.lse2[l] : nullptr;   // the tensor-core backward rebuilds P from it
     TrainTileArgs tt{};
     tt.K = K;

@@ -29,7 +29,8 @@
 // The reference maximum of a row is only raised when the tile maximum
 // exceeds it by more than 2^8 (then O is rescaled in TMEM, after the
 // previous P V has landed); in between, probabilities relative to the older
-// maximum stay below 256.
+// maximum stay below 256. With lse2 given, each row's base-2 log-sum-exp of
+// its scaled scores is written too.
 // Every mbarrier wait is bounded (1 s); on expiry the kernel sets
 // PEAGLE_DEV_TIMEOUT and stops, after waiting (again bounded) for the TMA
 // copies and tensor-core products it has already issued.
@@ -380,6 +381,8 @@ __global__ void __launch_bounds__(ta::THREADS, 1)
       const float sc = (m_c == -INFINITY) ? 0.f : tc::ex2_approx(m_c - m_f);
       const float lf = lt * so + l_c * sc;
       const float inv = lf > 0.f ? 1.f / lf : 0.f;
+      // the base-2 log-sum-exp of the row's scaled scores (all its keys), for the backward
+      if (a.lse2 && live && hf == 0) a.lse2[(size_t)(row0 + row) * a.nq + h] = m_f + __log2f(lf);
       const uint32_t tA = tbase + 384 + tl + hf * 64;
       uint4* Og = reinterpret_cast<uint4*>(static_cast<bf16*>(a.O) + ((size_t)(row0 + row) * a.nq + h) * HD + hf * 64);
       uint32_t ro[4][16], ra[4][16];
