@@ -1005,8 +1005,10 @@ static Plan plan_gemm(int M, int N, int K) {
   const int tilesA = p.swap ? (N + 127) / 128 : (M + 127) / 128;
   const int tilesB = p.swap ? (M + p.bn - 1) / p.bn : (N + p.bn - 1) / p.bn;
   p.tiles = tilesA * tilesB;
-  // wide tiles in pairs of A tiles that share each weight tile (multicast)
-  p.cm = (!p.swap && tilesA % 2 == 0) ? 2 : 1;
+  // wide tiles in pairs of A tiles that share each weight tile (multicast):
+  // measured to pay on long row counts (training) and to cost a little on
+  // the 512-row batched decode contractions (gate/up +1.5 us, head +2.4 us)
+  p.cm = (!p.swap && tilesA % 2 == 0 && tilesA >= 8) ? 2 : 1;
   const int kt_elems = 64 * (p.swap ? sub_boxes(p.bn) : 1);
   p.ktiles = (K + kt_elems - 1) / kt_elems;
   const int sms = num_sms();
