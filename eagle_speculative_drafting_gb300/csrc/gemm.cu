@@ -688,14 +688,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                            (reinterpret_cast<uintptr_t>(g.out) & 15) == 0;
           if (SWAP && al4) {
             // warp w of the epilogue sums rows w, w + 4, ... of the tile;
-            // lanes take 4 consecutive columns each (float4). Four rows of
-            // four slabs are in flight per thread before any of their sums
-            // is stored (slab 0 is read and rewritten by the same thread).
+            // lanes take 4 consecutive columns each (float4). Up to eight
+            // rows of four slabs are in flight per thread before any of their
+            // sums is stored (slab 0 is read and rewritten by the same
+            // thread): the finishing CTA's sum is the kernel's tail.
             const int m0 = tb * BN, mc = min(BN, g.M - m0);
             const int et = threadIdx.x - 64, rg = et >> 5;
             const int n0 = ta * 128 + (et & 31) * 4;
             if (n0 < g.N) {
-              constexpr int RB = 4;
+              constexpr int RB = BN / 4 < 8 ? BN / 4 : 8;
               for (int r0 = rg; r0 < mc; r0 += 4 * RB) {
                 float4 acc[RB];
 #pragma unroll
