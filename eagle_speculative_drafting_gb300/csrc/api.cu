@@ -1058,12 +1058,32 @@ peagle_status peagle_parallel_forward(const peagle_model* m, int32_t n, const vo
       const int src_rows = (l == 0) ? n : R;
       for (int c0 = 0; c0 < src_rows; c0 += rc) {
         const int mr = std::min(rc, src_rows - c0);
-        if (l == 0)
-          CUDA_TRY(gemm_launch(dt, atc(ws.x0, (size_t)c0 * 2 * H), 2 * H, W.qkv_w, mr, QKV, 2 * H, ws.part, &go,
-                               ws.sem, m->status, PEAGLE_OP_QKV, s));
-        else
-          CUDA_TRY(gemm_launch(dt, atc(ws.xin, (size_t)c0 * H), H, W.qkv_w, mr, QKV, H, ws.part, &go, ws.sem, m->status,
-                               PEAGLE_OP_QKV, s));
+        const int kin = (l == 0) ? 2 * H : H;
+        const void* X = (l == 0) ? atc(ws.x0, (size_t)c0 * 2 * H) : atc(ws.xin, (size_t)c0 * H);
+        if (hd == 128 && gemm_qkv_fusable(dt, mr, QKV, kin)) {
+          // rotary and the bf16 q/k/v in the contraction's epilogue; the
+          // layer-0 residual seed is a copy
+          GemmEpi ep{};
+          ep.op = GEMM_EPI_QKV;
+          ep.nq = nq;
+          ep.nkv = nkv;
+          ep.max_pos = c.max_position;
+          ep.row_base = c0;
+          ep.rcos = m->rcos;
+          ep.rsin = m->rsin;
+          ep.row_pos = ws.pos;
+          ep.q = ws.q;
+          ep.k = ws.kr;
+          ep.v = ws.vr;
+          CUDA_TRY(gemm_launch_epi(dt, X, kin, W.qkv_w, mr, QKV, kin, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV,
+                                   &ep, s));
+          qa.in = go;   // (unread by the masked-row finish below, which takes mask_qkv)
+          if (l == 0)
+            CUDA_TRY(cudaMemcpyAsync(ws.h + (size_t)c0 * H, ws.resid0 + (size_t)c0 * H, (size_t)mr * H * 4,
+                                     cudaMemcpyDeviceToDevice, s));
+          continue;
+        }
+        CUDA_TRY(gemm_launch(dt, X, kin, W.qkv_w, mr, QKV, kin, ws.part, &go, ws.sem, m->status, PEAGLE_OP_QKV, s));
         qa.in = go;
         qa.mode = 0;
         qa.row0 = c0;
@@ -1446,7 +1466,27 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     const peagle_layer_weights& W = m->layers[l];
     const int in = l == 0 ? 2 * H : H;
     float* hstream = ws.hmid[l];   // the residual stream while the layer runs
-    CUDA_TRY(mm(ws.xin[l], in, W.qkv_w, R, QKV, in, true));
+    const bool fuse_qkv = hd == 128 && gemm_qkv_fusable(dt, R, QKV, in);
+    if (fuse_qkv) {   // rotary and the bf16 q/k/v in the contraction's epilogue
+      GemmEpi ep{};
+      ep.op = GEMM_EPI_QKV;
+      ep.nq = nq;
+      ep.nkv = nkv;
+      ep.max_pos = c.max_position;
+      ep.row_base = 0;
+      ep.rcos = m->rcos;
+      ep.rsin = m->rsin;
+      ep.row_pos = ws.pos;
+      ep.q = ws.q[l];
+      ep.k = ws.k[l];
+      ep.v = ws.v[l];
+      CUDA_TRY(gemm_launch_epi(dt, ws.xin[l], in, W.qkv_w, R, QKV, in, ws.part, &go, ws.sem, m->status, -1, &ep, s,
+                               true));
+      if (l == 0)
+        CUDA_TRY(cudaMemcpyAsync(hstream, ws.residfull, (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
+    } else {
+      CUDA_TRY(mm(ws.xin[l], in, W.qkv_w, R, QKV, in, true));
+    }
     QkvArgs qa{};
     qa.in = go;
     qa.nq = nq;
@@ -1469,7 +1509,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
       qa.resid0 = ws.residfull;
       qa.h = hstream;
     }
-    CUDA_TRY(launch_qkv_finish(dt, R, qa, s));
+    if (!fuse_qkv) CUDA_TRY(launch_qkv_finish(dt, R, qa, s));
     if (l == 0) CUDA_TRY(cudaMemcpyAsync(ws.hin[0], hstream, (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
     else CUDA_TRY(cudaMemcpyAsync(hstream, ws.hin[l], (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));
     TrainAttnArgs aa{};

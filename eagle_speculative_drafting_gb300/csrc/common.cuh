@@ -162,7 +162,12 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
 // GEMM_EPI_SWIGLU: W is a [2I, K] gate/up weight (gate rows first); the
 // result silu(gate) * up [M, I] is written as bf16 to act (row stride
 // act_ld). Needs 2I % 256 == 0.
-enum { GEMM_EPI_ARGMAX = 1, GEMM_EPI_CE = 2, GEMM_EPI_SWIGLU = 3 };
+// GEMM_EPI_QKV: D's columns are [q heads | k heads | v heads], head dim
+// 128; q and k are rotated by the position of their row (pairs j, j + 64,
+// cos/sin tables [max_pos][64]) and q, k, v are written as bf16 to
+// q [rows, nq*128] and k, v [rows, nkv*128] at row row_base + GEMM row.
+// Only where gemm_qkv_fusable() holds (one partial slab, wide tiles).
+enum { GEMM_EPI_ARGMAX = 1, GEMM_EPI_CE = 2, GEMM_EPI_SWIGLU = 3, GEMM_EPI_QKV = 4 };
 struct GemmEpi {
   int op;
   void* act;
@@ -172,7 +177,15 @@ struct GemmEpi {
   float *p_max, *p_sum, *p_lab;   // [M, gemm_col_tiles]
   int* p_idx;
   const int* labels;    // GEMM_EPI_CE: label per row, -1 = none
+  // GEMM_EPI_QKV
+  int nq, nkv, max_pos, row_base;
+  const float *rcos, *rsin;
+  const int* row_pos;
+  void *q, *k, *v;
 };
+// Whether D = X W^T [M, N] (bf16) can take the q/k/v epilogue: unswapped
+// tiles, one partial slab, whole 128-column heads.
+bool gemm_qkv_fusable(int dtype, int M, int N, int K);
 // 2-D bf16 tensor map over a [rows, cols] matrix (row stride ld elements),
 // box = 64 columns x box_rows rows, 128-byte swizzle. False if the driver
 // rejects it.

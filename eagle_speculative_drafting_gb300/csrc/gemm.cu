@@ -36,7 +36,7 @@ namespace pe {
 // =========================================================================
 // The tcgen05 kernel
 // =========================================================================
-enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_CE = 2, EPI_SWIGLU = 3 };
+enum { EPI_STORE = 0, EPI_ARGMAX = 1, EPI_CE = 2, EPI_SWIGLU = 3, EPI_QKV = 4 };
 
 struct TcArgs {
   int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
@@ -64,6 +64,11 @@ struct TcArgs {
   int gate_off;
   void* act;
   int act_ld;
+  // EPI_QKV: rotate q/k by position, write q/k/v as bf16 (head dim 128)
+  int nq, nkv, max_pos, row_base;
+  const float *rcos, *rsin;
+  const int* row_pos;
+  void *q_out, *k_out, *v_out;
 };
 
 // Running head statistics of one row over some columns: argmax (lowest
@@ -576,7 +581,79 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         float* stg = staging + (warp - 2) * 32 * C::STG_LD;
         const int m0 = ta * 128 + quad * 32;
         const bool head = g.op == EPI_ARGMAX || g.op == EPI_CE;
-        if (g.op == EPI_SWIGLU && sg.nslab == 1) {
+        if (g.op == EPI_QKV) {
+          // columns [q heads | k heads | v heads] of 128: q and k rotated by
+          // the row's position (pairs j, j + 64), all three written as bf16
+          // (the host only asks for this on unsplit tiles)
+          const int my_m = m0 + lane;
+          int pos = 0;
+          if (my_m < g.M) {
+            pos = g.row_pos[g.row_base + my_m];
+            if (pos < 0 || pos >= g.max_pos) {
+              set_status(g.status, PEAGLE_DEV_BOUNDS);
+              pos = pos < 0 ? 0 : g.max_pos - 1;
+            }
+          }
+          const float4* cs = reinterpret_cast<const float4*>(g.rcos + (size_t)pos * 64);
+          const float4* sn = reinterpret_cast<const float4*>(g.rsin + (size_t)pos * 64);
+          const int qcols = g.nq * 128, kcols = g.nkv * 128;
+#pragma unroll 1
+          for (int hh = 0; hh < BN / 128; ++hh) {
+            const int nh = tb * BN + hh * 128;   // the head's first column
+            if (nh >= g.N) break;
+            const bool rot = nh < qcols + kcols;
+            bf16* dst;
+            int ld;
+            if (nh < qcols) {
+              dst = static_cast<bf16*>(g.q_out) + nh;
+              ld = qcols;
+            } else if (nh < qcols + kcols) {
+              dst = static_cast<bf16*>(g.k_out) + (nh - qcols);
+              ld = kcols;
+            } else {
+              dst = static_cast<bf16*>(g.v_out) + (nh - qcols - kcols);
+              ld = kcols;
+            }
+#pragma unroll 1
+            for (int j0 = 0; j0 < 64; j0 += 16) {
+              uint32_t rl[16], rh[16];
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + hh * 128 + j0, rl);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + hh * 128 + 64 + j0, rh);
+              float c[16], sv[16];
+              if (rot) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const float4 cv = cs[j0 / 4 + q4], s4 = sn[j0 / 4 + q4];
+                  c[q4 * 4] = cv.x, c[q4 * 4 + 1] = cv.y, c[q4 * 4 + 2] = cv.z, c[q4 * 4 + 3] = cv.w;
+                  sv[q4 * 4] = s4.x, sv[q4 * 4 + 1] = s4.y, sv[q4 * 4 + 2] = s4.z, sv[q4 * 4 + 3] = s4.w;
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const float x = __uint_as_float(rl[k]), y = __uint_as_float(rh[k]);
+                stg[lane * C::STG_LD + k] = rot ? x * c[k] - y * sv[k] : x;
+                stg[lane * C::STG_LD + 16 + k] = rot ? y * c[k] + x * sv[k] : y;
+              }
+              __syncwarp();
+              // 32 rows x (16 + 16) bf16: lane & 7 takes two columns of a row,
+              // four rows per pass
+              const int cc = (lane & 7) * 2;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int rr = i * 4 + (lane >> 3);
+                const int m = m0 + rr;
+                if (m < g.M) {
+                  const float* srow = stg + rr * C::STG_LD;
+                  bf16* drow = dst + (size_t)(g.row_base + m) * ld;
+                  *reinterpret_cast<__nv_bfloat162*>(drow + j0 + cc) = __floats2bfloat162_rn(srow[cc], srow[cc + 1]);
+                  *reinterpret_cast<__nv_bfloat162*>(drow + 64 + j0 + cc) =
+                      __floats2bfloat162_rn(srow[16 + cc], srow[16 + cc + 1]);
+                }
+              }
+              __syncwarp();
+            }
+          }
+        } else if (g.op == EPI_SWIGLU && sg.nslab == 1) {
           // columns c and BN/2 + c are gate and up of output column
           // tb * BN/2 + c: write silu(gate) * up as bf16, coalesced
           constexpr int HALF = BN / 2;
@@ -1056,6 +1133,12 @@ static Plan plan_gemm(int M, int N, int K) {
 
 int gemm_splits(int M, int N, int K) { return plan_gemm(M, N, K).splits; }
 
+bool gemm_qkv_fusable(int dtype, int M, int N, int K) {
+  if (dtype != PEAGLE_BF16 || M <= 0 || N % 128 != 0) return false;
+  const Plan p = plan_gemm(M, N, K);
+  return !p.swap && p.splits == 1;
+}
+
 size_t gemm_out_floats(int dtype, int M, int N, int K) {
   if (dtype != PEAGLE_BF16) return (size_t)M * N;
   return (size_t)plan_gemm(M, N, K).splits * M * N;
@@ -1177,7 +1260,23 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.w_early = w_early ? 1 : 0;
   args.op = EPI_STORE;
   args.gate_off = 0;
-  if (epi && epi->op == GEMM_EPI_SWIGLU) {
+  if (epi && epi->op == GEMM_EPI_QKV) {
+    if (p.swap || p.splits != 1 || N % 128 != 0) {
+      set_error("q/k/v epilogue needs wide unsplit tiles (M=%d N=%d K=%d)", M, N, K);
+      return cudaErrorInvalidValue;
+    }
+    args.op = EPI_QKV;
+    args.nq = epi->nq;
+    args.nkv = epi->nkv;
+    args.max_pos = epi->max_pos;
+    args.row_base = epi->row_base;
+    args.rcos = epi->rcos;
+    args.rsin = epi->rsin;
+    args.row_pos = epi->row_pos;
+    args.q_out = epi->q;
+    args.k_out = epi->k;
+    args.v_out = epi->v;
+  } else if (epi && epi->op == GEMM_EPI_SWIGLU) {
     if (N % 256 != 0) {
       set_error("fused SwiGLU needs the gate/up width %d to be a multiple of 256", N);
       return cudaErrorInvalidValue;
