@@ -192,6 +192,37 @@ def source_digest(root=None):
     return h.hexdigest()[:16]
 
 
+def graph_replay(step, d, targets, steps, dist):
+    """Times `steps` replays of one draft step + verify captured as a CUDA
+    graph; None without a GPU, or {"error": ...} if the capture failed."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step(d, targets, torch.cuda.current_stream())   # warm the side stream once
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            step(d, targets, torch.cuda.current_stream())
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda") / steps
+        return {"ms_per_step": ms, "replays": steps}
+    except Exception as exc:   # reported in the JSON line, never fatal
+        torch.cuda.synchronize()
+        return {"error": str(exc).splitlines()[0][:200]}
+
+
 def recorded_traffic(op, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources; else None."""
@@ -661,11 +692,12 @@ def main():
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step(dd, targets):
+    def step(dd, targets, on=None):
+        st = stream if on is None else on
         pe.peagle_draft_step(model.handle, B, K, dd["aux"], dd["anchor_tokens"], dd["anchor_pos"],
                              dd["k_cache"], dd["v_cache"], dd["kv_offsets"], dd["kv_lens"], kv_cap,
-                             max_kv, 0, drafts, None, ws, ws_bytes, stream)
-        pe.peagle_verify_accept(B, K, drafts, targets, acc, nxt, stream)
+                             max_kv, 0, drafts, None, ws, ws_bytes, st)
+        pe.peagle_verify_accept(B, K, drafts, targets, acc, nxt, st)
 
     # targets whose agreement with the drafts has geometric(0.7) length
     step(d, torch.zeros((B, K + 1), dtype=torch.int32, device="cuda"))
@@ -722,6 +754,13 @@ def main():
     ms_total = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     ms_step = ms_total / args.steps
     value = job_throughput(world, B, K, ms_step)
+
+    # ---- the same step captured once as a CUDA graph and replayed (the
+    # launches are recorded with their programmatic dependencies)
+    graph = graph_replay(step, d, targets, args.steps, dist)
+    if graph is not None and "ms_per_step" in graph:
+        graph["value"] = job_throughput(world, B, K, graph["ms_per_step"])
+        graph["unit"] = UNIT
 
     # ---- end to end through the public API with host buffers: each step's
     # inputs leave one pinned host buffer in one copy (16-byte aligned
@@ -815,6 +854,7 @@ def main():
                      "timing": f"CUDA events around each launch on its stream, {probe_steps} steps "
                                f"in a probe pass before the timed region"},
         "ops": ops,
+        "graph_replay": graph,
         "tc_peak_tflops": tc_peak,
         "device_status": status,
     }
