@@ -309,6 +309,77 @@ def test_decode_flags_out_of_range_token():
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
+@pytest.mark.parametrize("kw", [dict(),
+                                # tcgen05 contractions, 2-CTA multicast pairs, chunked attention
+                                dict(head_dim=128, num_q_heads=8, num_kv_heads=2, hidden=1024, batch=40,
+                                     K=8, vocab=40000, kv_len_range=(0, 4000), max_position=8192)])
+def test_decode_step_replays_as_cuda_graph(kw):
+    # the draft step + verify, captured once as a CUDA graph: replays give
+    # the eager step's tokens and logits bit for bit, and read the inputs'
+    # current contents (nothing host-side is frozen into the graph but
+    # pointers and sizes)
+    import torch
+    wl = small_bf16_decode(**kw)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    d = H().upload_decode(wl, inp)
+    B, K, Vd = wl.batch, wl.K, model.cfg.draft_vocab
+    max_kv = int(np.max(inp["kv_lens"]))
+    cap = int(inp["kv_capacity"])
+    rng = np.random.default_rng(77)
+    targets = torch.from_numpy(rng.integers(0, wl.vocab, (B, K)).astype(np.int32)).cuda()
+    dev = dict(device="cuda")
+
+    def step(toks, logits, acc, nxt, stream=None):
+        model.draft_step(K, d["aux"], d["anchor_tokens"], d["anchor_pos"], d["k_cache"], d["v_cache"],
+                         d["kv_offsets"], d["kv_lens"], cap, max_kv, False, draft_tokens=toks,
+                         logits=logits, stream=stream)
+        pe().peagle_verify_accept(B, K, toks, targets, acc, nxt, stream=stream)
+
+    def bufs():
+        return (torch.empty((B, K), dtype=torch.int32, **dev), torch.empty((B, K, Vd), dtype=torch.float32, **dev),
+                torch.empty(B, dtype=torch.int32, **dev), torch.empty(B, dtype=torch.int32, **dev))
+
+    def host(b):
+        return [x.cpu().numpy() for x in b]
+
+    eager = bufs()
+    step(*eager)
+    torch.cuda.synchronize()
+    want = host(eager)
+
+    g = torch.cuda.CUDAGraph()
+    gb = bufs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(*gb, stream=torch.cuda.current_stream())
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for x in gb:
+        x.fill_(-7)
+    with torch.cuda.graph(g):
+        step(*gb, stream=torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(host(gb), want):
+        assert np.array_equal(a, b)
+
+    # new anchors and aux rows in place: the replay follows them
+    d["anchor_tokens"].copy_(torch.from_numpy(rng.integers(0, wl.vocab, B).astype(np.int32)))
+    d["aux"].mul_(-0.5)
+    g.replay()
+    step(*eager)
+    torch.cuda.synchronize()
+    got, want2 = host(gb), host(eager)
+    for a, b in zip(got, want2):
+        assert np.array_equal(a, b)
+    assert not np.array_equal(got[1], want[1])
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
 # -------------------------------------------------------------- training
 def small_train(dtype="f32", n=64, lens=(20, 1, 30, 13), K=4, **kw):
     wl = small_bf16_decode(dtype=dtype, kind="train", n_tokens=n, K=K, **kw)
