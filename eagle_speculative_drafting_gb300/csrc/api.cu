@@ -1308,8 +1308,10 @@ static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, Bw
   ws.dqkv = bp.take_bytes((size_t)R * QKV * es);
   ws.dh = bp.take<float>((size_t)R * H);
   ws.dh2 = bp.take<float>((size_t)R * H);
-  ws.dhid = bp.take<float>((size_t)R * H);
-  ws.dbig = bp.take<float>((size_t)R * gw);
+  // the n depth-0 rows and, in row n, the masked rows' summed gradient (with
+  // K = 1 there are no masked rows and R = n)
+  ws.dhid = bp.take<float>((size_t)std::max(R, n + 1) * H);
+  ws.dbig = bp.take<float>((size_t)std::max(R, n + 1) * gw);
   ws.dQ = bp.take<float>((size_t)R * nqhd);
   ws.dK = bp.take<float>((size_t)R * nkvhd);
   ws.dV = bp.take<float>((size_t)R * nkvhd);

@@ -42,6 +42,7 @@ struct TcArgs {
   int rowsA, rowsB, K;     // A role has rowsA rows, B role rowsB rows, both K wide
   int splits;              // K slices per output tile (split mode)
   int streamk;             // 1: stream-K schedule (see Sched)
+  int coop;                // 1: every split item runs in the first round (see the epilogue)
   float* out;              // fp32 partial slabs
   int ldo;                 // row stride of a slab (elements)
   size_t split_stride;     // elements between slabs
@@ -272,14 +273,23 @@ struct Sched {
 constexpr int TC_THREADS = 192;
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block
 
-template <int BN, bool SWAP>
+constexpr int pow2_at_least(int v, int p = 32) { return p >= v ? p : pow2_at_least(v, 2 * p); }
+
+// MA = 2: the A role tile is two 128-row blocks that share every weight
+// stage (two M = 128 products per K step into two accumulators): 256-row
+// items, fewer of them, for contractions whose 128-row items would leave
+// the last round of CTAs mostly empty. (Per byte received it does 1.3-1.5x
+// the tensor work of a 128 x 256 tile, but only three of its stages fit,
+// and with the ring latency-bound a K step then takes about as long per
+// flop as with four 128 x 256 stages.)
+template <int BN, bool SWAP, int MA = 1>
 struct TcCfg {
   // Narrow (swapped) tiles read several 64-wide boxes per stage, so each
   // weight row is fetched in 256-512 byte runs rather than 128-byte pieces.
   static constexpr int SUB = (SWAP && BN == 16) ? 4 : ((SWAP && BN <= 64) ? 2 : 1);
   static constexpr int A_SUB = 128 * 128;               // 128 rows x 64 bf16
   static constexpr int B_SUB = BN * 128;                // BN rows x 64 bf16
-  static constexpr int A_BYTES = SUB * A_SUB;
+  static constexpr int A_BYTES = MA * SUB * A_SUB;
   static constexpr int B_BYTES = SUB * B_SUB;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int KT = 64 * SUB;                   // K elements per stage
@@ -289,7 +299,14 @@ struct TcCfg {
   static constexpr int STAGING = SWAP ? 0 : 4 * 32 * STG_LD * 4;
   static constexpr int STAGES = std::min(12, (kSmemLimit - 1024 - 256 - STAGING) / STAGE);
   static constexpr int SMEM = 1024 + STAGES * STAGE + 256 + STAGING;
-  static constexpr int TMEM_COLS = (2 * BN < 32) ? 32 : 2 * BN;
+  // TMEM columns of one work item's accumulators; two sets (the next item
+  // accumulates while the last drains) when both fit in the 512 columns
+  static constexpr int ACC = MA * BN;
+  static constexpr int NBUF = 2 * ACC <= 512 ? 2 : 1;
+  static constexpr int TMEM_COLS = pow2_at_least(NBUF * ACC);
+  static_assert(MA == 1 || (!SWAP && SUB == 1), "two row blocks only on wide tiles");
+  static_assert(ACC <= 512 && BN % 16 == 0 && BN <= 256, "tile does not fit one CTA's TMEM");
+  static_assert(STAGES >= 2, "ring too shallow");
 };
 
 // silu(gate) * up of finished rows read back from slab 0, where a tile's
@@ -316,17 +333,116 @@ __device__ void swiglu_finish_rows(const TcArgs& g, int m_begin, int m_end, int 
   }
 }
 
+// Waits (bounded by limit_ns) until a global counter reaches target; the
+// load is an acquire, so the writes released before the increments that
+// brought it there are visible afterwards.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+    __nanosleep(100);
+  }
+}
+
+// Sum of a split tile's slabs for rows [mlo, mhi) and columns [n0, n0 + BN)
+// into slab 0, in slab order: warp ew of the four epilogue warps takes rows
+// in blocks of four, lanes take float4 columns (lane * 4 + 128 j). All loads
+// of two slabs x four rows are in flight before their sums.
+template <int BN>
+__device__ void coop_sum_rows(const TcArgs& g, int mlo, int mhi, int n0, int nslab, int ew, int lane) {
+  const int ncol = min(g.N, n0 + BN);
+  const bool al4 = (g.N & 3) == 0 && (g.ldo & 3) == 0 && (g.split_stride & 3) == 0 &&
+                   (reinterpret_cast<uintptr_t>(g.out) & 15) == 0;
+  if (al4) {
+    constexpr int NV = (BN + 127) / 128;
+    constexpr int RB = 4;
+    for (int mb = mlo + ew * RB; mb < mhi; mb += 4 * RB) {
+      float4 acc[RB][NV];
+#pragma unroll
+      for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int jv = 0; jv < NV; ++jv) acc[i][jv] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q0 = 0; q0 < nslab; q0 += 2) {
+        float4 t[2][RB][NV];
+#pragma unroll
+        for (int qi = 0; qi < 2; ++qi)
+#pragma unroll
+          for (int i = 0; i < RB; ++i)
+#pragma unroll
+            for (int jv = 0; jv < NV; ++jv) {
+              const int m = mb + i, n = n0 + jv * 128 + lane * 4;
+              t[qi][i][jv] = (q0 + qi < nslab && m < mhi && n < ncol)
+                                 ? __ldcg(reinterpret_cast<const float4*>(g.out + (size_t)(q0 + qi) * g.split_stride +
+                                                                          (size_t)m * g.ldo + n))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int qi = 0; qi < 2; ++qi)
+#pragma unroll
+          for (int i = 0; i < RB; ++i)
+#pragma unroll
+            for (int jv = 0; jv < NV; ++jv)
+              if (q0 + qi < nslab) {
+                acc[i][jv].x += t[qi][i][jv].x;
+                acc[i][jv].y += t[qi][i][jv].y;
+                acc[i][jv].z += t[qi][i][jv].z;
+                acc[i][jv].w += t[qi][i][jv].w;
+              }
+      }
+#pragma unroll
+      for (int i = 0; i < RB; ++i)
+#pragma unroll
+        for (int jv = 0; jv < NV; ++jv) {
+          const int m = mb + i, n = n0 + jv * 128 + lane * 4;
+          if (m < mhi && n < ncol) *reinterpret_cast<float4*>(g.out + (size_t)m * g.ldo + n) = acc[i][jv];
+        }
+    }
+  } else {
+    constexpr int NC = BN >= 32 ? BN / 32 : 1;
+    for (int m = mlo + ew; m < mhi; m += 4) {
+      const size_t base = (size_t)m * g.ldo + n0 + lane;
+      float acc[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+      for (int q0 = 0; q0 < nslab; q0 += 4) {
+        float t[4][NC];
+#pragma unroll
+        for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            t[qi][c] = (q0 + qi < nslab && n0 + c * 32 + lane < ncol)
+                           ? __ldcg(g.out + (size_t)(q0 + qi) * g.split_stride + base + c * 32)
+                           : 0.f;
+#pragma unroll
+        for (int qi = 0; qi < 4; ++qi)
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            if (q0 + qi < nslab) acc[c] += t[qi][c];
+      }
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        if (n0 + c * 32 + lane < ncol) g.out[base + c * 32] = acc[c];
+    }
+  }
+}
+
 // CM = 2: two CTAs of a cluster take the two A tiles (row blocks 2p, 2p+1) of
 // the same weight tile; each loads its half of the weight rows and
 // multicasts it into both CTAs' ring stage, so every SM fetches half the
 // weight bytes per product. A stage is free again once both CTAs' products
 // have read it (each commit arrives on both CTAs' empty barrier).
-template <int BN, bool SWAP, int CM>
+// MA = 2: a work item covers 256 activation rows (row blocks 2t, 2t+1) in
+// one CTA; both 128-row blocks and the weight tile share a ring stage.
+template <int BN, bool SWAP, int CM, int MA>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcArgs g) {
   static_assert(CM == 1 || (CM == 2 && !SWAP), "clusters pair wide (unswapped) tiles only");
-  using C = TcCfg<BN, SWAP>;
+  static_assert(MA == 1 || CM == 1, "one pairing at a time");
+  using C = TcCfg<BN, SWAP, MA>;
   constexpr uint16_t kPeers = (uint16_t)((1u << CM) - 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -366,7 +482,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tbase = *tslot;
   pdl_trigger();   // the next kernel may launch now and wait for this one
 
-  const int tilesA = (g.rowsA + 127) / 128;
+  const int tilesA = (g.rowsA + 128 * MA - 1) / (128 * MA);
   const int tilesB = (g.rowsB + BN - 1) / BN;
   const int ktiles = (g.K + C::KT - 1) / C::KT;
   // work items are cluster tiles: CM consecutive A tiles of one weight tile
@@ -434,7 +550,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           pre = g.w_early ? min(ke - kb, C::STAGES) : 0;
           for (int q = 0; q < pre; ++q) {
             const int k = k_at(tb, kb, ke, q), nv = nsub(k);
-            tc::mbar_expect_tx(&full[q], nv * (C::A_SUB + C::B_SUB));
+            tc::mbar_expect_tx(&full[q], nv * (MA * C::A_SUB + C::B_SUB));
             for (int i = 0; i < nv; ++i) {
               if (SWAP) load_w(sA + q * C::A_BYTES + i * C::A_SUB, k * C::KT + i * 64, ta, &full[q]);
               else load_w(sB + q * C::B_BYTES + i * C::B_SUB, k * C::KT + i * 64, tb, &full[q]);
@@ -451,7 +567,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (it < pre) {   // weight half already in flight
             for (int i = 0; i < nv; ++i) {
               if (SWAP) tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
-              else tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
+              else
+                for (int h = 0; h < MA; ++h)
+                  tc::tma_load_2d(sA + s * C::A_BYTES + (h + i) * C::A_SUB, &tmA, k * C::KT + i * 64,
+                                  (ta * MA + h) * 128, &full[s]);
             }
             continue;
           }
@@ -460,13 +579,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             set_status(g.status, PEAGLE_DEV_TIMEOUT);
             break;
           }
-          tc::mbar_expect_tx(&full[s], nv * (C::A_SUB + C::B_SUB));
+          tc::mbar_expect_tx(&full[s], nv * (MA * C::A_SUB + C::B_SUB));
           for (int i = 0; i < nv; ++i) {
             if (SWAP) {
               load_w(sA + s * C::A_BYTES + i * C::A_SUB, k * C::KT + i * 64, ta, &full[s]);
               tc::tma_load_2d(sB + s * C::B_BYTES + i * C::B_SUB, &tmB, k * C::KT + i * 64, tb * BN, &full[s]);
             } else {
-              tc::tma_load_2d(sA + s * C::A_BYTES + i * C::A_SUB, &tmA, k * C::KT + i * 64, ta * 128, &full[s]);
+              // (wide tiles have one box per stage: i = 0, block h at h * A_SUB)
+              for (int h = 0; h < MA; ++h)
+                tc::tma_load_2d(sA + s * C::A_BYTES + (h + i) * C::A_SUB, &tmA, k * C::KT + i * 64,
+                                (ta * MA + h) * 128, &full[s]);
               load_w(sB + s * C::B_BYTES + i * C::B_SUB, k * C::KT + i * 64, tb, &full[s]);
             }
           }
@@ -493,15 +615,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int kb = sg.kb, ke = sg.ke;
         int ta, tb;
         tile_of(sg.tile, ta, tb);
-        const int buf = j & 1;
-        const uint32_t use = j >> 1;
+        const int buf = j % C::NBUF;
+        const uint32_t use = j / C::NBUF;
         if (!tc::mbar_wait_for(&tempty[buf], (use & 1) ^ 1, g.wait_ns)) {
           *abort_flag = 1;
           set_status(g.status, PEAGLE_DEV_TIMEOUT);
           break;
         }
         tc::fence_after();
-        const uint32_t dcol = tbase + buf * BN;
+        const uint32_t dcol = tbase + buf * C::ACC;
         bool ok = true;
         for (int jk = 0; jk < ke - kb; ++jk, ++it) {
           const int k = k_at(tb, kb, ke, jk);
@@ -518,8 +640,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t b0 = tc::smem_u32(sB + s * C::B_BYTES + i * C::B_SUB);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              tc::mma_bf16(dcol, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32), idesc,
-                           (jk > 0 || i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int h = 0; h < MA; ++h)
+                tc::mma_bf16(dcol + h * BN, tc::sw128_desc(a0 + h * C::A_SUB + kk * 32), tc::sw128_desc(b0 + kk * 32),
+                             idesc, (jk > 0 || i > 0 || kk > 0) ? 1u : 0u);
             }
           }
           if constexpr (CM > 1) tc::mma_commit_mc(&empty[s], kPeers);
@@ -543,8 +667,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int ta, tb;
       tile_of(sg.tile, ta, tb);
       const int tile = tb * tilesA + ta, sp = sg.slab;
-      const int buf = j & 1;
-      const uint32_t use = j >> 1;
+      const int buf = j % C::NBUF;
+      const uint32_t use = j / C::NBUF;
       // Whether to go on is decided by the four epilogue warps together (an
       // OR over the named barrier they share): a warp that left alone would
       // leave the others waiting at the barriers of the tile's finish.
@@ -574,12 +698,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       } else {
+#pragma unroll 1
+       for (int h = 0; h < MA; ++h) {
+        const int tr = ta * MA + h;                          // 128-row block of the item
+        const uint32_t tcol = (uint32_t)((buf * MA + h) * BN);   // its accumulator
         // lane = row m: transpose 32 x 32 blocks through shared memory, then
         // each warp store writes 4 rows x 128 contiguous bytes. A fused head
         // epilogue on an unsplit tile reduces the row straight from TMEM and
         // stores fp32 only if the caller asked for logits.
         float* stg = staging + (warp - 2) * 32 * C::STG_LD;
-        const int m0 = ta * 128 + quad * 32;
+        const int m0 = tr * 128 + quad * 32;
         const bool head = g.op == EPI_ARGMAX || g.op == EPI_CE;
         if (g.op == EPI_QKV) {
           // columns [q heads | k heads | v heads] of 128: q and k rotated by
@@ -617,8 +745,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll 1
             for (int j0 = 0; j0 < 64; j0 += 16) {
               uint32_t rl[16], rh[16];
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + hh * 128 + j0, rl);
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + hh * 128 + 64 + j0, rh);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + hh * 128 + j0, rl);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + hh * 128 + 64 + j0, rh);
               float c[16], sv[16];
               if (rot) {
 #pragma unroll
@@ -664,8 +792,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
             for (int h16 = 0; h16 < 32; h16 += 16) {
               uint32_t rg[16], ru[16];
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + h16, rg);
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + HALF + c0 + h16, ru);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + c0 + h16, rg);
+              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + HALF + c0 + h16, ru);
 #pragma unroll
               for (int c = 0; c < 16; ++c) {
                 const float gt = __uint_as_float(rg[c]);
@@ -711,10 +839,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t r[16];
           float v[32];
-          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0, r);
+          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + c0, r);
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(r[c]);
-          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + buf * BN + c0 + 16, r);
+          tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + c0 + 16, r);
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[16 + c] = __uint_as_float(r[c]);
           if (fuse) acc.add_chunk(v, tb * BN + c0, min(32, g.N - (tb * BN + c0)), lab, ce);
@@ -747,11 +875,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (fuse && my_m < g.M) acc.write(g, my_m, tb);
         }
+       }
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-      if (sg.nslab > 1) {
+      const bool coop = !SWAP && g.coop && sg.nslab > 1;
+      if (coop) {
+        // every K slice of every tile runs at once (one round of items): the
+        // tile's CTAs wait for all of its partial slabs, then each sums its
+        // own share of the tile's rows into slab 0 (in slab order) and runs
+        // the fused head / SwiGLU step on those rows. The counter goes to
+        // nslab (slabs written), then to 2 nslab (shares done); the last
+        // CTA re-arms it for the next launch.
+        __threadfence();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) {
+          atomicAdd(&g.sem[tile], 1);
+          const bool all_in = wait_count(&g.sem[tile], sg.nslab, g.wait_ns);
+          if (!all_in) set_status(g.status, PEAGLE_DEV_TIMEOUT);
+          *s_last = all_in ? 1 : 0;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (*s_last) {
+          __threadfence();
+          const int ew = warp - 2;
+          const int RT = 128 * MA;
+          const int mlo = ta * RT + RT * sp / sg.nslab;
+          const int mhi = min(g.M, ta * RT + RT * (sp + 1) / sg.nslab);
+          coop_sum_rows<BN>(g, mlo, mhi, tb * BN, sg.nslab, ew, lane);
+          if (g.op == EPI_SWIGLU || g.op == EPI_ARGMAX || g.op == EPI_CE) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (g.op == EPI_SWIGLU)
+              swiglu_finish_rows(g, mlo + ew, mhi, 4, tb * BN, BN / 2, tb * (BN / 2), lane);
+            else
+              head_finish_rows(g, mlo + ew, mhi, 4, tb * BN, min(BN, g.N - tb * BN), tb, lane);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (warp == 2 && lane == 0) {
+          __threadfence();
+          if (atomicAdd(&g.sem[tile], 1) == 2 * sg.nslab - 1) g.sem[tile] = 0;
+        }
+      }
+      if (sg.nslab > 1 && !coop) {
         // the last of the tile's CTAs to arrive sums every slab of the tile
         // into slab 0, in slab order (deterministic), and re-arms the tile's
         // counter for the next launch
@@ -831,11 +998,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // warp sums its 32 rows, four at a time; lanes take float4
             // columns lane*4 + 128j. Four rows of two slabs are in flight
             // per thread before any of their sums is stored.
-            constexpr int NV = BN >= 128 ? BN / 128 : 1;
+            constexpr int NV = (BN + 127) / 128;
             constexpr int RB = 4;
             const int n0 = tb * BN;
-            for (int r0 = 0; r0 < 32; r0 += RB) {
-              const int mb = ta * 128 + quad * 32 + r0;
+            const int ncol = min(g.N, n0 + BN);   // this tile's columns end here
+            for (int r0 = 0; r0 < 32 * MA; r0 += RB) {
+              const int mb = (ta * MA + r0 / 32) * 128 + quad * 32 + r0 % 32;
               if (mb >= g.M) break;
               float4 acc[RB][NV];
 #pragma unroll
@@ -851,7 +1019,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                     for (int jv = 0; jv < NV; ++jv) {
                       const int m = mb + i, n = n0 + jv * 128 + lane * 4;
-                      t[qi][i][jv] = (q0 + qi < sg.nslab && m < g.M && n < g.N)
+                      t[qi][i][jv] = (q0 + qi < sg.nslab && m < g.M && n < ncol)
                                          ? __ldcg(reinterpret_cast<const float4*>(
                                                g.out + (size_t)(q0 + qi) * g.split_stride + (size_t)m * g.ldo + n))
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -874,7 +1042,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int jv = 0; jv < NV; ++jv) {
                   const int m = mb + i, n = n0 + jv * 128 + lane * 4;
-                  if (m < g.M && n < g.N) *reinterpret_cast<float4*>(g.out + (size_t)m * g.ldo + n) = acc[i][jv];
+                  if (m < g.M && n < ncol) *reinterpret_cast<float4*>(g.out + (size_t)m * g.ldo + n) = acc[i][jv];
                 }
             }
           } else {
@@ -883,8 +1051,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // its stores, which could alias them.
             constexpr int NC = BN >= 32 ? BN / 32 : 1;
             const int n0 = tb * BN;
-            for (int rr = 0; rr < 32; ++rr) {
-              const int m = ta * 128 + quad * 32 + rr;
+            for (int rr = 0; rr < 32 * MA; ++rr) {
+              const int m = (ta * MA + rr / 32) * 128 + quad * 32 + rr % 32;
               if (m >= g.M) break;
               const size_t base = (size_t)m * g.ldo + n0 + lane;
               float acc[NC];
@@ -913,7 +1081,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (warp == 2 && lane == 0) g.sem[tile] = 0;
         }
       }
-      if (g.op == EPI_SWIGLU && (SWAP || sg.nslab > 1)) {
+      if (g.op == EPI_SWIGLU && (SWAP || sg.nslab > 1) && !coop) {
         // silu(gate) * up of a finished tile, from slab 0
         const bool fin = (sg.nslab == 1) || *s_last;
         if (fin) {
@@ -921,11 +1089,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (SWAP)
             swiglu_finish_rows(g, warp - 2, g.M, 4, ta * 128, 64, ta * 64, lane);
           else
-            swiglu_finish_rows(g, ta * 128 + quad * 32, min(g.M, ta * 128 + quad * 32 + 32), 1, tb * BN, BN / 2,
-                               tb * (BN / 2), lane);
+            for (int h = 0; h < MA; ++h) {
+              const int r0 = (ta * MA + h) * 128 + quad * 32;
+              swiglu_finish_rows(g, r0, min(g.M, r0 + 32), 1, tb * BN, BN / 2, tb * (BN / 2), lane);
+            }
         }
       }
-      if ((g.op == EPI_ARGMAX || g.op == EPI_CE) && (SWAP || sg.nslab > 1)) {
+      if ((g.op == EPI_ARGMAX || g.op == EPI_CE) && (SWAP || sg.nslab > 1) && !coop) {
         // head statistics of a finished tile, from slab 0: by the only CTA
         // of an unsplit tile, or by the CTA that summed the slabs
         const bool fin = (sg.nslab == 1) || *s_last;
@@ -934,8 +1104,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (SWAP)
             head_finish_rows(g, warp - 2, g.M, 4, ta * 128, min(128, g.N - ta * 128), ta, lane);
           else
-            head_finish_rows(g, ta * 128 + quad * 32, min(g.M, ta * 128 + quad * 32 + 32), 1, tb * BN,
-                             min(BN, g.N - tb * BN), tb, lane);
+            for (int h = 0; h < MA; ++h) {
+              const int r0 = (ta * MA + h) * 128 + quad * 32;
+              head_finish_rows(g, r0, min(g.M, r0 + 32), 1, tb * BN, min(BN, g.N - tb * BN), tb, lane);
+            }
         }
       }
     }
@@ -1055,6 +1227,7 @@ struct Plan {
   bool swap;
   int bn;
   int cm;       // CTAs per cluster sharing a weight tile (1 or 2)
+  int ma;       // 128-row blocks per work item (1 or 2)
   int splits;   // partial slabs per tile (the most any tile needs)
   int tiles;
   int ktiles;
@@ -1065,12 +1238,58 @@ struct Plan {
 static int sub_boxes(int bn) { return bn == 16 ? 4 : (bn <= 64 ? 2 : 1); }
 static int cluster_slots(int bn);
 
+// A few hundred rows (256 < M <= 1024, a batched decode step): the plan with
+// the least estimated time among 128-row items 128 or 256 wide (whole, or in
+// up to four K slices when every slice of every tile runs in the first round,
+// so the tile's CTAs share its sum) and, for M a multiple of 256, whole
+// 256-row items 224 or 256 wide. An item's K step costs what was measured on
+// GB300 for that shape with the whole GPU busy (the ring is latency-bound
+// there: 0.33 / 0.47 us per 128-row step 128 / 256 wide, 0.81 / 0.88 us per
+// 256-row step 224 / 256 wide); a sliced tile adds about 3 us for its sum.
+// Gated (SwiGLU) tiles keep 128-row items.
+static void plan_few_hundred_rows(Plan& p, int M, int N, int K, bool gated) {
+  const int sms = num_sms();
+  const int ktiles = (K + 63) / 64;
+  struct Shape {
+    int ma, bn, step_ns;
+  };
+  const Shape shapes[] = {{1, 128, 330}, {1, 256, 470}, {2, 224, 810}, {2, 256, 880}};
+  long long best = -1;
+  for (const Shape& sh : shapes) {
+    if (sh.ma == 2 && (gated || M % 256 != 0)) continue;
+    const int tiles = ((M + 128 * sh.ma - 1) / (128 * sh.ma)) * ((N + sh.bn - 1) / sh.bn);
+    const int smax = sh.ma == 2 ? 1 : std::min(4, ktiles);
+    for (int sp = 1; sp <= smax; ++sp) {
+      if (sp > 1 && ((long long)tiles * sp > sms || tiles > kGemmSemCount)) break;
+      const long long rounds = ((long long)tiles * sp + sms - 1) / sms;
+      const long long cost = rounds * (long long)((ktiles + sp - 1) / sp) * sh.step_ns + (sp > 1 ? 3000 : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        p.ma = sh.ma;
+        p.bn = sh.bn;
+        p.splits = sp;
+        p.tiles = tiles;
+      }
+    }
+  }
+  p.swap = false;
+  p.cm = 1;
+  p.streamk = 0;
+  p.ktiles = ktiles;
+  p.grid = (int)std::min<long long>((long long)p.tiles * p.splits, sms);
+}
+
 // Few activation rows (swap): stream-K over all (tile, k-tile) units, one
 // persistent CTA per SM. Wide tiles: items (tile, K slice), choosing the
 // slice count that best fills whole rounds of CTAs (fewer on ties).
-static Plan plan_gemm(int M, int N, int K) {
+static Plan plan_gemm(int M, int N, int K, bool gated = false) {
   Plan p;
+  p.ma = 1;
   p.swap = M <= 256;
+  if (!p.swap && M <= 1024) {
+    plan_few_hundred_rows(p, M, N, K, gated);
+    return p;
+  }
   p.bn = p.swap ? swap_bn(M) : 256;
   if (!p.swap && N <= 128 * 6) p.bn = 128;
   // too few 256-wide tiles to give every SM work: halve the tile width
@@ -1136,28 +1355,31 @@ int gemm_splits(int M, int N, int K) { return plan_gemm(M, N, K).splits; }
 bool gemm_qkv_fusable(int dtype, int M, int N, int K) {
   if (dtype != PEAGLE_BF16 || M <= 0 || N % 128 != 0) return false;
   const Plan p = plan_gemm(M, N, K);
-  return !p.swap && p.splits == 1;
+  return !p.swap && p.splits == 1 && p.bn % 128 == 0;
 }
 
 size_t gemm_out_floats(int dtype, int M, int N, int K) {
   if (dtype != PEAGLE_BF16) return (size_t)M * N;
-  return (size_t)plan_gemm(M, N, K).splits * M * N;
+  // a gated (SwiGLU) contraction may plan other K slices than a plain one
+  const int sp = std::max(plan_gemm(M, N, K).splits, plan_gemm(M, N, K, true).splits);
+  return (size_t)sp * M * N;
 }
 
-template <int BN, bool SWAP, int CM>
+template <int BN, bool SWAP, int CM, int MA = 1>
 static cudaError_t set_smem_attr() {
-  using C = TcCfg<BN, SWAP>;
+  using C = TcCfg<BN, SWAP, MA>;
   static std::atomic<unsigned long long> attr_done{0};
   return once_per_device(attr_done, [] {
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, SWAP, CM, MA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM);
   });
 }
 
-template <int BN, bool SWAP, int CM>
+template <int BN, bool SWAP, int CM, int MA = 1>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const TcArgs& args, int grid,
                              cudaStream_t s) {
-  using C = TcCfg<BN, SWAP>;
-  cudaError_t e0 = set_smem_attr<BN, SWAP, CM>();
+  using C = TcCfg<BN, SWAP, MA>;
+  cudaError_t e0 = set_smem_attr<BN, SWAP, CM, MA>();
   if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1173,7 +1395,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const T
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CM > 1 ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP, CM>, a, b, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, SWAP, CM, MA>, a, b, args);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1205,7 +1427,7 @@ static int cluster_slots_bn() {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, false, 2>, &cfg) != cudaSuccess) n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, false, 2, 1>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();   // a refused query leaves no sticky error
     slots[dev].store(n);
@@ -1244,11 +1466,14 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
     probe_stop(probe_op, s);
     return cudaGetLastError();
   }
-  const Plan p = plan_gemm(M, N, K);
+  const bool gated = epi && epi->op == GEMM_EPI_SWIGLU;
+  const Plan p = plan_gemm(M, N, K, gated);
   TcArgs args;
   args.K = K;
   args.splits = p.splits;
   args.streamk = p.streamk;
+  // every split item in the first round (the tile's CTAs then share its sum)
+  args.coop = (!p.swap && p.splits > 1 && (long long)(p.tiles / p.cm) * p.splits <= p.grid / p.cm) ? 1 : 0;
   args.out = out;
   args.ldo = N;
   args.split_stride = (size_t)M * N;
@@ -1261,7 +1486,7 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.op = EPI_STORE;
   args.gate_off = 0;
   if (epi && epi->op == GEMM_EPI_QKV) {
-    if (p.swap || p.splits != 1 || N % 128 != 0) {
+    if (p.swap || p.splits != 1 || N % 128 != 0 || p.bn % 128 != 0) {
       set_error("q/k/v epilogue needs wide unsplit tiles (M=%d N=%d K=%d)", M, N, K);
       return cudaErrorInvalidValue;
     }
@@ -1327,6 +1552,9 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
       case 128: e = launch_tc<128, true, 1>(ma, mb, args, items, s); break;
       default: e = launch_tc<256, true, 1>(ma, mb, args, items, s); break;
     }
+  } else if (p.ma == 2) {
+    e = (p.bn == 224) ? launch_tc<224, false, 1, 2>(ma, mb, args, items, s)
+                      : launch_tc<256, false, 1, 2>(ma, mb, args, items, s);
   } else if (p.cm == 2) {
     e = (p.bn == 128) ? launch_tc<128, false, 2>(ma, mb, args, items, s)
                       : launch_tc<256, false, 2>(ma, mb, args, items, s);

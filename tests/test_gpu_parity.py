@@ -50,10 +50,10 @@ GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17,
                (300, 40000, 320), (512, 32000, 512),
                # few wide tiles with a long K: 256-wide tiles in four K slices
                (300, 1024, 9000),
-               # pairs of row tiles sharing each weight tile (multicast): the
-               # batched-decode O and down projections (the latter in K slices)
-               # and a ragged width
-               (512, 4096, 4096), (512, 4096, 14336), (768, 1300, 600)]
+               # 256-row items (two 128-row blocks sharing each weight stage):
+               # the batched-decode O and down projections (K slices), a ragged
+               # width, four row pairs in K slices, a single K step
+               (512, 4096, 4096), (512, 4096, 14336), (768, 1300, 600), (1024, 640, 1000), (512, 200, 64)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -185,7 +185,10 @@ def test_decode_tiny_f32():
                                 dict(head_dim=128, num_q_heads=8, num_kv_heads=2, hidden=1024, batch=12, K=8,
                                      kv_len_range=(0, 4000), max_position=8192),
                                 dict(head_dim=128, num_q_heads=4, num_kv_heads=2, hidden=512, batch=9, K=3,
-                                     kv_len_range=(200, 2600), max_position=8192)])
+                                     kv_len_range=(200, 2600), max_position=8192),
+                                # 512 rows in 256-row items: fused SwiGLU (96 of 192 columns gate,
+                                # the last tile ragged) and the argmax head over a ragged vocab
+                                dict(batch=64, K=8, vocab=5000, intermediate=640)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
@@ -456,6 +459,24 @@ def test_train_bf16_unfused_swiglu_width():
     # 2I not a multiple of 256: the SwiGLU runs as its own kernel
     wl, inp = small_train(dtype="bf16", n=300, lens=(120, 180), K=3, intermediate=200)
     check_train(wl, inp, 3, 0.7, 0.2, 4, BF16_TOL)
+
+
+@pytest.mark.parametrize("n,lens,kw", [(512, (200, 312), dict(vocab=32000)), (768, (500, 268), {}),
+                                      (512, (300, 212), dict(head_dim=128)),
+                                      (512, (200, 312), dict(hidden=2048, intermediate=512))])
+def test_train_bf16_two_block_items(n, lens, kw):
+    # depth 0 only: every contraction of the forward has 512 or 768 rows, the
+    # plans of a batched decode step: 256-row items under the cross-entropy
+    # head (32000 columns), and with a long K (hidden 2048) K slices whose
+    # CTAs share the tile's sum before the cross-entropy / SwiGLU step
+    wl, inp = small_train(dtype="bf16", n=n, lens=lens, K=1, **kw)
+    check_train(wl, inp, 1, 0.7, 0.2, 17, BF16_TOL)
+
+
+def test_backward_bf16_two_block_items():
+    # 512 rows: the forward and backward contractions over them in 256-row items
+    wl, inp = small_train(dtype="bf16", n=512, lens=(200, 312), K=1)
+    check_backward(wl, inp, 1, 0.7, 0.2, 17, BF16_TOL)
 
 
 def test_train_bf16_multi_chunk_rows():
