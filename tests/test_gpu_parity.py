@@ -50,10 +50,12 @@ GEMM_SHAPES = [(1, 128, 64), (4, 256, 128), (3, 200, 520), (16, 384, 1024), (17,
                (300, 40000, 320), (512, 32000, 512),
                # few wide tiles with a long K: 256-wide tiles in four K slices
                (300, 1024, 9000),
-               # 256-row items (two 128-row blocks sharing each weight stage):
-               # the batched-decode O and down projections (K slices), a ragged
-               # width, four row pairs in K slices, a single K step
-               (512, 4096, 4096), (512, 4096, 14336), (768, 1300, 600), (1024, 640, 1000), (512, 200, 64)]
+               # a few hundred rows (a batched decode step): the O and down
+               # projections in K slices whose CTAs share the sum, a ragged
+               # width, 1024 rows in three K slices, a single K step, a ragged
+               # width in K slices; 256-row items under (512, 32000, 512) above
+               (512, 4096, 4096), (512, 4096, 14336), (768, 1300, 600), (1024, 640, 1000), (512, 200, 64),
+               (512, 3000, 4096)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -188,7 +190,10 @@ def test_decode_tiny_f32():
                                      kv_len_range=(200, 2600), max_position=8192),
                                 # 512 rows in 256-row items: fused SwiGLU (96 of 192 columns gate,
                                 # the last tile ragged) and the argmax head over a ragged vocab
-                                dict(batch=64, K=8, vocab=5000, intermediate=640)])
+                                dict(batch=64, K=8, vocab=5000, intermediate=640),
+                                # a wide gated SwiGLU over 512 rows (two rounds of 256-wide
+                                # tiles) and the down projection in K slices sharing their sum
+                                dict(batch=64, K=8, intermediate=6144)])
 def test_decode_bf16_small(kw):
     wl = small_bf16_decode(**kw)
     W = synth.make_weights(wl)
