@@ -39,12 +39,16 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 OP_IDS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6}
+# timed steps when --steps is not given: a timed region of seconds, not
+# minutes (the 32768-token training step takes about 0.2 s)
+DEFAULT_STEPS = {"train_n4096_k4": 1000, "train_n32768_k8": 100}
 
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 3000 for decode, fewer for the training workloads)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -57,7 +61,10 @@ def parse_args():
                     help="steps of each per-op timing pass (default: --steps, at least 300, at most 2000)")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the end-to-end pass (default: as --probe-steps)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(args.workload, 3000)
+    return args
 
 
 def pass_steps(args):
