@@ -95,6 +95,8 @@ _sig("peagle_next_context", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_voi
      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p)
 _sig("peagle_verify_accept", c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
      c_void_p)
+_sig("peagle_copy_to_device", c_int32, c_void_p, c_void_p, c_size_t, c_void_p)
+_sig("peagle_copy_to_host", c_int32, c_void_p, c_void_p, c_size_t, c_void_p)
 _sig("peagle_verify_sample", c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
      c_void_p, c_void_p, c_void_p, c_void_p)
 _sig("peagle_cod_counts", c_int32, c_int32, c_int32, c_double, c_double, ctypes.POINTER(c_int32))
@@ -248,6 +250,14 @@ def peagle_next_context(B, K, draft_tokens, accept_len, next_token, cur_offsets,
 def peagle_verify_accept(B, K, draft_tokens, target_tokens, accept_len, next_token, stream=None):
     _check(_lib.peagle_verify_accept(B, K, ptr(draft_tokens), ptr(target_tokens), ptr(accept_len),
                                      ptr(next_token), _stream(stream)), "peagle_verify_accept")
+
+
+def peagle_copy_to_device(dev, host, nbytes, stream=None):
+    _check(_lib.peagle_copy_to_device(ptr(dev), ptr(host), nbytes, _stream(stream)), "peagle_copy_to_device")
+
+
+def peagle_copy_to_host(host, dev, nbytes, stream=None):
+    _check(_lib.peagle_copy_to_host(ptr(host), ptr(dev), nbytes, _stream(stream)), "peagle_copy_to_host")
 
 
 def peagle_verify_sample(B, K, V, draft_tokens, draft_probs, target_probs, accept_u, draws, accept_len,

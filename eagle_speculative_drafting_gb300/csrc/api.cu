@@ -834,6 +834,36 @@ peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, in
   return PEAGLE_OK;
 }
 
+// The address through which the device reaches page-locked, mapped host
+// memory `p`, or NULL when `p` is not such memory (pageable, device or
+// unknown memory: the staging copies refuse it rather than launch).
+static const void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+peagle_status peagle_copy_to_device(void* dev, const void* host, size_t bytes, void* stream) {
+  if (bytes == 0) return PEAGLE_OK;
+  if (!dev || !host) FAIL(PEAGLE_ERR_INVALID_ARG, "copy_to_device: NULL pointer");
+  const void* src = mapped_host(host);
+  if (!src) FAIL(PEAGLE_ERR_INVALID_ARG, "copy_to_device: the host buffer is not mapped page-locked memory");
+  CUDA_TRY(launch_stage_copy(dev, src, (long long)bytes, true, static_cast<cudaStream_t>(stream)));
+  return PEAGLE_OK;
+}
+
+peagle_status peagle_copy_to_host(void* host, const void* dev, size_t bytes, void* stream) {
+  if (bytes == 0) return PEAGLE_OK;
+  if (!dev || !host) FAIL(PEAGLE_ERR_INVALID_ARG, "copy_to_host: NULL pointer");
+  void* dst = const_cast<void*>(mapped_host(host));
+  if (!dst) FAIL(PEAGLE_ERR_INVALID_ARG, "copy_to_host: the host buffer is not mapped page-locked memory");
+  CUDA_TRY(launch_stage_copy(dst, dev, (long long)bytes, false, static_cast<cudaStream_t>(stream)));
+  return PEAGLE_OK;
+}
+
 peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X, const void* W, float* D,
                           void* workspace, size_t workspace_bytes, void* stream) {
   if (M < 0 || N < 0 || K < 1 || (dtype != PEAGLE_F32 && dtype != PEAGLE_BF16))

@@ -771,6 +771,60 @@ __global__ void sum_splits_kernel(GemmOut in, int M, int N, float* D) {
   }
 }
 
+// ------------------------------------------------------ host staging
+// Copies between mapped page-locked host memory and device memory run as
+// kernels so they stay in the stream's chain of dependent launches. The
+// copy to the device loads its first batch (host memory, which no kernel
+// of the chain writes) before waiting for the previous kernel; only its
+// stores wait. 16-byte vectors, R per thread in flight.
+constexpr int kStageR = 4;
+__global__ void __launch_bounds__(256) copy_to_device_kernel(uint4* __restrict__ dst, const uint4* src,
+                                                             long long n16) {
+  pdl_trigger();
+  const long long stride = (long long)gridDim.x * blockDim.x * kStageR;
+  long long base = (long long)blockIdx.x * blockDim.x * kStageR + threadIdx.x;
+  uint4 v[kStageR];
+#pragma unroll
+  for (int r = 0; r < kStageR; ++r) {
+    const long long i = base + (long long)r * blockDim.x;
+    if (i < n16) v[r] = src[i];
+  }
+  pdl_wait();
+  for (;;) {
+#pragma unroll
+    for (int r = 0; r < kStageR; ++r) {
+      const long long i = base + (long long)r * blockDim.x;
+      if (i < n16) dst[i] = v[r];
+    }
+    base += stride;
+    if (base >= n16) break;
+#pragma unroll
+    for (int r = 0; r < kStageR; ++r) {
+      const long long i = base + (long long)r * blockDim.x;
+      if (i < n16) v[r] = src[i];
+    }
+  }
+}
+
+// The copy to the host reads device memory an earlier kernel may write, so
+// it waits first.
+__global__ void __launch_bounds__(256) copy_to_host_kernel(uint4* dst, const uint4* __restrict__ src,
+                                                           long long n16) {
+  pdl_trigger();
+  pdl_wait();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+// Byte copies for sizes or addresses off the 16-byte grid (either direction).
+__global__ void __launch_bounds__(256) copy_bytes_kernel(uint8_t* dst, const uint8_t* src, long long n) {
+  pdl_trigger();
+  pdl_wait();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 // =========================================================================
 // launchers
 // =========================================================================
@@ -992,6 +1046,29 @@ cudaError_t launch_sum_splits(const GemmOut& in, int M, int N, float* D, cudaStr
   const long long total = (long long)M * N;
   if (total <= 0) return cudaSuccess;
   launch_pdl(sum_splits_kernel, grid_for(total, 256), 256, 0, st, in, M, N, D);
+  PE_LAUNCH_END();
+}
+
+cudaError_t launch_stage_copy(void* dst, const void* src, long long bytes, bool to_device, cudaStream_t st) {
+  if (bytes <= 0) return cudaSuccess;
+  const bool vec = (bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+  if (!vec) {
+    launch_pdl(copy_bytes_kernel, grid_for(bytes, 256), 256, 0, st, static_cast<uint8_t*>(dst),
+               static_cast<const uint8_t*>(src), bytes);
+    PE_LAUNCH_END();
+  }
+  const long long n16 = bytes / 16;
+  if (to_device) {
+    const long long per_block = 256LL * kStageR;
+    const long long want = (n16 + per_block - 1) / per_block;
+    const int grid = (int)std::min<long long>(want, (long long)num_sms() * 8);
+    launch_pdl(copy_to_device_kernel, std::max(grid, 1), 256, 0, st, static_cast<uint4*>(dst),
+               static_cast<const uint4*>(src), n16);
+  } else {
+    launch_pdl(copy_to_host_kernel, grid_for(n16, 256), 256, 0, st, static_cast<uint4*>(dst),
+               static_cast<const uint4*>(src), n16);
+  }
   PE_LAUNCH_END();
 }
 

@@ -265,4 +265,8 @@ cudaError_t launch_train_attn(int dtype, const TrainAttnArgs& a, const TrainTile
 bool train_attn_tc_supported(int dtype, const TrainAttnArgs& a);
 cudaError_t launch_train_attn_tc(const TrainAttnArgs& a, const TrainTileArgs& tt, cudaStream_t st);
 
+// Copy between mapped page-locked host memory and device memory as a
+// kernel in the launch chain (dst / src: addresses the device can use).
+cudaError_t launch_stage_copy(void* dst, const void* src, long long bytes, bool to_device, cudaStream_t st);
+
 }  // namespace pe

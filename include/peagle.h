@@ -252,6 +252,26 @@ peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_to
                                    const int32_t* target_tokens, int32_t* accept_len,
                                    int32_t* next_token, void* stream);
 
+/* ---- host staging inside the launch chain ------------------------------ */
+/* Copies `bytes` between page-locked host memory and device memory with a
+ * kernel instead of a copy-engine transfer, so that the copy joins the
+ * stream's chain of programmatically dependent launches like the kernels of
+ * a step: the next kernel launches while the copy runs, and a copy to the
+ * device loads its source before it waits for the previous kernel (only its
+ * stores wait). On GB300 the device reads and writes host memory over
+ * NVLink-C2C. Serving plumbing; the pages have no counterpart for it.
+ *   host   page-locked host memory mapped into the device's address space
+ *          (cudaHostAlloc / cudaMallocHost, or a pinned torch tensor);
+ *          anything else returns PEAGLE_ERR_INVALID_ARG and launches nothing
+ *   dev    device memory
+ *   bytes  >= 0; a multiple of 16 with 16-byte aligned addresses moves in
+ *          16-byte vectors, anything else byte by byte
+ * Ordering is the stream's, as for cudaMemcpyAsync: do not rewrite `host`
+ * before a copy to the device that reads it has completed, and read a copy
+ * to the host only after synchronizing the stream. */
+peagle_status peagle_copy_to_device(void* dev, const void* host, size_t bytes, void* stream);
+peagle_status peagle_copy_to_host(void* host, const void* dev, size_t bytes, void* stream);
+
 /* ---- stochastic verification ------------------------------------------- */
 /* Rejection sampling of the drafts ("P_Eagle" README, How Speculative
  * Decoding Works: accepted tokens are used, rejected ones resampled, and the

@@ -388,6 +388,61 @@ def test_decode_step_replays_as_cuda_graph(kw):
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
+def test_staging_copies_through_mapped_host_memory():
+    # the copies in the launch chain: vector and byte paths, both directions,
+    # offsets off the 16-byte grid; memory the device cannot reach as host
+    # memory (pageable, or device memory) is refused before any launch
+    import torch
+    m = pe()
+    g = torch.Generator().manual_seed(3)
+    for nbytes, off in ((16, 0), (1576464, 0), (1000003, 0), (4104, 8), (77, 5)):
+        src = torch.randint(0, 256, (nbytes + off,), dtype=torch.uint8, generator=g).pin_memory()
+        dev = torch.zeros(nbytes + off, dtype=torch.uint8, device="cuda")
+        back = torch.zeros(nbytes + off, dtype=torch.uint8).pin_memory()
+        m.peagle_copy_to_device(dev.data_ptr() + off, src.data_ptr() + off, nbytes)
+        m.peagle_copy_to_host(back.data_ptr() + off, dev.data_ptr() + off, nbytes)
+        torch.cuda.synchronize()
+        assert torch.equal(dev.cpu()[off:], src[off:]) and torch.equal(back[off:], src[off:])
+        assert not dev.cpu()[:off].any() and not back[:off].any()
+    m.peagle_copy_to_device(dev, src, 0)
+    pageable = torch.zeros(64, dtype=torch.uint8)
+    d64 = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    for bad in (pageable, torch.zeros(64, dtype=torch.uint8, device="cuda")):
+        with pytest.raises(m.PeagleError):
+            m.peagle_copy_to_device(d64, bad, 64)
+        with pytest.raises(m.PeagleError):
+            m.peagle_copy_to_host(bad, d64, 64)
+    torch.cuda.synchronize()
+
+
+def test_draft_step_with_staged_inputs_and_outputs():
+    # inputs staged in from page-locked host memory, the step and greedy
+    # verify, the results staged out: the plain step's tokens, bit for bit
+    import torch
+    wl = small_bf16_decode(batch=12, K=4)
+    W = synth.make_weights(wl)
+    inp = synth.make_decode_inputs(wl)
+    model = H().make_model(wl, W)
+    d = H().upload_decode(wl, inp)
+    B, K = wl.batch, wl.K
+    cap, max_kv = int(inp["kv_capacity"]), int(np.max(inp["kv_lens"]))
+    want = H().run_decode(wl, model, inp, d=d)["draft_tokens"]
+    aux_h = d["aux"].cpu().pin_memory()
+    tok_h = d["anchor_tokens"].cpu().pin_memory()
+    aux_d, tok_d = torch.empty_like(d["aux"]), torch.empty_like(d["anchor_tokens"])
+    toks = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    toks_h = torch.full((B, K), -1, dtype=torch.int32).pin_memory()
+    m = pe()
+    m.peagle_copy_to_device(aux_d, aux_h, aux_h.numel() * aux_h.element_size())
+    m.peagle_copy_to_device(tok_d, tok_h, tok_h.numel() * 4)
+    model.draft_step(K, aux_d, tok_d, d["anchor_pos"], d["k_cache"], d["v_cache"], d["kv_offsets"],
+                     d["kv_lens"], cap, max_kv, False, draft_tokens=toks)
+    m.peagle_copy_to_host(toks_h, toks, B * K * 4)
+    torch.cuda.synchronize()
+    assert np.array_equal(toks_h.numpy(), want)
+    assert m.peagle_get_device_status(model.handle) == 0
+
+
 # -------------------------------------------------------------- training
 def small_train(dtype="f32", n=64, lens=(20, 1, 30, 13), K=4, **kw):
     wl = small_bf16_decode(dtype=dtype, kind="train", n_tokens=n, K=K, **kw)
