@@ -61,6 +61,8 @@ def parse_args():
                     help="steps of each per-op timing pass (default: --steps, at least 300, at most 2000)")
     ap.add_argument("--e2e-steps", type=int, default=None,
                     help="steps of the end-to-end pass (default: as --probe-steps)")
+    ap.add_argument("--no-aux-ops", action="store_true",
+                    help="decode workloads: skip the closed-loop / verification / COD latency pass")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = DEFAULT_STEPS.get(args.workload, 3000)
@@ -402,6 +404,100 @@ def workload_config(wl):
             "parallelism": "replicas (independent requests per GPU)"}
 
 
+# ---------------------------------------- the rows around the draft step
+LOOP_ROUNDS = 64
+
+
+def aux_ops(pe, synth, marshal, wl, model, d, inp, stream, rounds=LOOP_ROUNDS):
+    """Latency of the rows around the draft step, each timed with CUDA events
+    on its stream after the headline passes: the closed draft -> verify ->
+    next-context loop over the workload's requests (a synthetic target stands
+    in: aux states of the new rows, and targets agreeing with the drafts for
+    a truncated-geometric number of depths; it runs outside the timed
+    events), greedy and stochastic verification, and COD selection at the
+    two training shapes."""
+    import torch
+    from eagle_speculative_drafting_gb300.loop import DraftLoop
+    B, K, V = wl.batch, wl.K, wl.vocab
+    Vd = model.cfg.draft_vocab
+    dev = "cuda"
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    out = {}
+    # ---- closed loop
+    loop = DraftLoop(model, K, d["k_cache"], d["v_cache"], d["kv_offsets"], d["kv_lens"], int(inp["kv_capacity"]),
+                     stream)
+    loop.start(inp["anchor_tokens"], inp["anchor_pos"])
+    g = torch.Generator(device=dev).manual_seed(7)
+    aux_rows = torch.randn(B * (K + 1), wl.num_aux * wl.target_hidden, device=dev, generator=g).to(marshal.tdtype(wl))
+    ar = torch.arange(K + 1, device=dev)
+    zero_col = torch.zeros(B, 1, dtype=torch.int32, device=dev)
+    t_draft = t_rest = 0.0
+    kept = 0
+    torch.cuda.synchronize()
+    for r in range(rounds):
+        e0, e1, e2, e3 = ev(), ev(), ev(), ev()
+        e0.record(stream)
+        drafts = loop.draft(aux_rows[:loop.total_new])
+        e1.record(stream)
+        a = torch.from_numpy(synth.draw_accept_lengths(wl, B, K, salt=r + 1)).to(dev)
+        ext = torch.cat([drafts, zero_col], 1)
+        tgt = torch.where(ar[None] < a[:, None], ext, (ext + 1) % V).to(torch.int32).contiguous()
+        torch.cuda.synchronize()
+        e2.record(stream)
+        acc, _ = loop.verify_greedy(tgt)   # verify, next rows, and the host read that sizes the next round
+        e3.record(stream)
+        torch.cuda.synchronize()
+        t_draft += e0.elapsed_time(e1)
+        t_rest += e2.elapsed_time(e3)
+        kept += int(acc.sum().item()) + B
+    ms = (t_draft + t_rest) / rounds
+    out["closed_loop"] = {
+        "rounds": rounds, "requests": B, "K": K, "ms_per_round": ms, "draft_ms": t_draft / rounds,
+        "verify_next_context_ms": t_rest / rounds, "mean_accept": kept / (rounds * B) - 1.0,
+        "drafted_tokens_per_s": B * K / (ms / 1000.0), "kept_tokens_per_s": kept / ((t_draft + t_rest) / 1000.0),
+        "device_status": pe.peagle_get_device_status(model.handle)}
+
+    def per_call_us(fn, n):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1000.0 * e0.elapsed_time(e1) / n
+
+    # ---- greedy and stochastic verification of B x K drafts
+    dr = torch.randint(0, Vd, (B, K), dtype=torch.int32, device=dev, generator=g)
+    tg = torch.randint(0, Vd, (B, K + 1), dtype=torch.int32, device=dev, generator=g)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    out["verify_accept_us"] = per_call_us(lambda: pe.peagle_verify_accept(B, K, dr, tg, acc, nxt, stream), 1000)
+    logits = torch.randn(B, K + 1, Vd, device=dev, generator=g) * 3.0
+    p = torch.softmax(logits + 0.5 * torch.randn(B, K + 1, Vd, device=dev, generator=g), -1).contiguous()
+    q = torch.softmax(logits[:, :K], -1).contiguous()
+    dq = torch.multinomial(q.view(-1, Vd), 1, generator=g).view(B, K).to(torch.int32).contiguous()
+    u = torch.rand(B, K, device=dev, generator=g)
+    draws = torch.randint(0, 2 ** 31 - 1, (B,), dtype=torch.int32, device=dev, generator=g)
+    out["verify_sample_us"] = per_call_us(
+        lambda: pe.peagle_verify_sample(B, K, Vd, dq, q, p, u, draws, acc, nxt, stream), 200)
+    out["verify_sample_shape"] = f"B={B} K={K} V={Vd}"
+    # ---- COD selection at the training shapes (r = 0.7, r_min = 0.2)
+    cod = {}
+    for n, Kc in ((4096, 4), (32768, 8)):
+        R = sum(pe.peagle_cod_counts(n, Kc, 0.7, 0.2))
+        idx = torch.empty(R, dtype=torch.int32, device=dev)
+        row_of = torch.empty(Kc * n, dtype=torch.int32, device=dev)
+        wsb = pe.peagle_cod_select_workspace_size(n, Kc)
+        wsc = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        cod[f"n{n}_k{Kc}"] = per_call_us(
+            lambda: pe.peagle_cod_select(n, Kc, 0.7, 0.2, 0x5EED, idx, row_of, wsc, wsb, stream), 50)
+    out["cod_select_us"] = cod
+    out["timing"] = "CUDA events on the launching stream, after the headline passes"
+    return out
+
+
 # ------------------------------------------------------ training-shaped pass
 TRAIN_METRIC = "drafted depth-rows/s per P-EAGLE parallel forward"
 TRAIN_OPS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6, "ce": 9}
@@ -686,7 +782,8 @@ def main():
     from eagle_speculative_drafting_gb300 import marshal
 
     W = synth.make_weights(wl)
-    inp = synth.make_decode_inputs(wl)
+    # spare cache rows per request for the closed loop's appended rows
+    inp = synth.make_decode_inputs(wl, spare=wl.K + LOOP_ROUNDS * (wl.K + 1))
     model = marshal.make_model(wl, W)
     d = marshal.upload_decode(wl, inp)
     B, K = wl.batch, wl.K
@@ -873,6 +970,8 @@ def main():
         "device_status": status,
     }
     line["clocks"] = clk.summary()
+    if not args.no_aux_ops:
+        line["aux_ops"] = aux_ops(pe, synth, marshal, wl, model, d, inp, stream)
     if world == 1 and not args.no_cpu_baseline:
         v, steps, el, cores = oracle_leg(wl, W, inp, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",

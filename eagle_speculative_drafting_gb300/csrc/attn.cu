@@ -523,29 +523,38 @@ __global__ void __launch_bounds__(MmaAttnCfg<MT, HD, NW, NS>::THREADS) decode_sp
 // At the end the NW warps' (m, l, O) meet once in shared memory and the CTA
 // writes the chunk's partial as the block-synchronous kernel does, so the
 // combine is shared.
-template <int MT, int HD, int NW, int NS>
+// RG = 2 (multi-row steps, up to 32*MT*2 rows): warp w keeps the online
+// softmax of row group w % RG over key stream w / RG. The RG warps of a
+// stream share its ring: each issues 1/RG of a tile's copies, and once per
+// tile they meet on a named barrier (after each has waited for its own
+// copies, before either refills the stage the previous tile used). Each K/V
+// tile still leaves HBM once, and a warp holds O for 16*MT rows only.
+template <int MT, int HD, int NW, int NS, int RG = 1>
 struct WarpAttnCfg {
   static constexpr int THREADS = 32 * NW;
-  static constexpr int QR = 16 * MT, TK = 16, LDS = HD + 8;
+  static constexpr int NTS = NW / RG;                            // key streams
+  static constexpr int QR = 16 * MT, QT = RG * QR, TK = 16, LDS = HD + 8;
   static constexpr int STAGE = 2 * TK * HD * 2;                  // K and V of one 16-key tile, bytes
-  static constexpr int RING = NW * NS * STAGE;
+  static constexpr int RING = NTS * NS * STAGE;
   static constexpr int MERGE = NW * QR * (HD + 2) * 4;           // per-warp O, m, l at the end
-  static constexpr int SMEM = QR * LDS * 2 + (RING > MERGE ? RING : MERGE);
+  static constexpr int SMEM = QT * LDS * 2 + (RING > MERGE ? RING : MERGE);
+  static_assert(NW % RG == 0 && NTS <= 8, "warps per key stream");
 };
 
-template <int MT, int HD, int NW, int NS>
-__global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_warp_mma(DecodeAttnArgs a) {
+template <int MT, int HD, int NW, int NS, int RG = 1>
+__global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS, RG>::THREADS) decode_warp_mma(DecodeAttnArgs a) {
   pdl_trigger();
   pdl_wait();
-  using C = WarpAttnCfg<MT, HD, NW, NS>;
-  constexpr int QR = C::QR, TK = C::TK, LDS = C::LDS, NT = HD / 8;
+  using C = WarpAttnCfg<MT, HD, NW, NS, RG>;
+  constexpr int QR = C::QR, QT = C::QT, TK = C::TK, LDS = C::LDS, NT = HD / 8, NTS = C::NTS;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
-  uint8_t* ring = smem_raw + QR * LDS * 2;
+  uint8_t* ring = smem_raw + QT * LDS * 2;
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.nq / a.nkv;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int rg = w % RG, ts = w / RG;   // row group, key stream
   const long long off = a.kv_off[b];
   int L = a.kv_len[b];
   const bool ok = L >= 0 && L <= a.max_kv_len && off >= 0 && off + L <= a.kv_off[b + 1] && off + L <= a.kv_cap;
@@ -562,16 +571,16 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
   const bf16* vc = static_cast<const bf16*>(a.vcache);
   const bf16* Q = static_cast<const bf16*>(a.Q);
 
-  // this warp's tiles: i-th = chunk tile w + i * NW
-  const int my_tiles = ntiles > w ? (ntiles - w + NW - 1) / NW : 0;
-  uint8_t* wring = ring + (size_t)w * NS * C::STAGE;
+  // this stream's tiles: i-th = chunk tile ts + i * NTS
+  const int my_tiles = ntiles > ts ? (ntiles - ts + NTS - 1) / NTS : 0;
+  uint8_t* wring = ring + (size_t)ts * NS * C::STAGE;
   auto load_tile = [&](int i) {
-    const int t = w + i * NW;
+    const int t = ts + i * NTS;
     bf16* sk = reinterpret_cast<bf16*>(wring + (i % NS) * C::STAGE);
     bf16* sv = sk + TK * HD;
     const int base = k0 + t * TK;
 #pragma unroll
-    for (int e = lane; e < TK * (HD / 8); e += 32) {
+    for (int e = lane + 32 * rg; e < TK * (HD / 8); e += 32 * RG) {
       const int kr = e / (HD / 8), c8 = e % (HD / 8);
       const int key = base + kr;
       const bool in = key < k1;
@@ -586,7 +595,7 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
     if (i < my_tiles) load_tile(i);
     mm::cp_commit();
   }
-  for (int e = tid; e < QR * (HD / 8); e += C::THREADS) {
+  for (int e = tid; e < QT * (HD / 8); e += C::THREADS) {
     const int qi = e / (HD / 8), c8 = e % (HD / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
     if (qi < KG) {
@@ -609,11 +618,23 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
     for (int nt = 0; nt < NT; ++nt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
   }
 
+  // a row group past the request's rows only helps stream the tiles
+  const bool live = RG == 1 || rg * QR < KG;
   for (int i = 0; i < my_tiles; ++i) {
-    if (i + NS - 1 < my_tiles) load_tile(i + NS - 1);
-    mm::cp_commit();
-    mm::cp_wait<NS - 1>();
-    __syncwarp();
+    if constexpr (RG == 1) {
+      if (i + NS - 1 < my_tiles) load_tile(i + NS - 1);
+      mm::cp_commit();
+      mm::cp_wait<NS - 1>();
+      __syncwarp();
+    } else {
+      // this warp's share of tile i has landed; after the barrier so has the
+      // partner's, and both are done with tile i - 1, whose stage is refilled
+      mm::cp_wait<NS - 2>();
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + ts), "r"(32 * RG) : "memory");
+      if (i + NS - 1 < my_tiles) load_tile(i + NS - 1);
+      mm::cp_commit();
+    }
+    if (!live) continue;
     const bf16* tK = reinterpret_cast<const bf16*>(wring + (i % NS) * C::STAGE);
     const bf16* tV = tK + TK * HD;
     // ---- S = Q K^T over this tile's 16 keys
@@ -629,13 +650,13 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         uint32_t aq[4];
-        mm::ldsm4(aq, mm::sa(sQ + (mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
+        mm::ldsm4(aq, mm::sa(sQ + (rg * QR + mt * 16 + (lane & 15)) * LDS + ks * 16 + (lane >> 4) * 8));
         mm::mma16816(S[mt][0], aq, bk[0], bk[1]);
         mm::mma16816(S[mt][1], aq, bk[2], bk[3]);
       }
     }
     // ---- mask the tail, tile maxima per row (the quad of lanes holding it)
-    const int kbase = k0 + (w + i * NW) * TK + (lane & 3) * 2;
+    const int kbase = k0 + (ts + i * NTS) * TK + (lane & 3) * 2;
     bool raise_any = false;
     float tmax[MT][2];
 #pragma unroll
@@ -735,21 +756,23 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
   const size_t prow = ((size_t)(b * a.nkv + g) * a.nsplit + split) * KGmax;
   for (int e = tid; e < KG * (HD / 4); e += C::THREADS) {
     const int row = e / (HD / 4), c4 = (e % (HD / 4)) * 4;
+    const int rgr = RG == 1 ? 0 : row / QR, lr = RG == 1 ? row : row % QR;   // its row group, row there
     float M = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < NW; ++q) M = fmaxf(M, sM[q * QR + row]);
+    for (int q = 0; q < NTS; ++q) M = fmaxf(M, sM[(q * RG + rgr) * QR + lr]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
 #pragma unroll
-    for (int q = 0; q < NW; ++q) {
-      const float mq = sM[q * QR + row];
+    for (int q = 0; q < NTS; ++q) {
+      const int wq = q * RG + rgr;
+      const float mq = sM[wq * QR + lr];
       const float f = (mq == -INFINITY) ? 0.f : exp2f(mq - M);
-      const float4 o = *reinterpret_cast<const float4*>(sO + ((size_t)q * QR + row) * HD + c4);
+      const float4 o = *reinterpret_cast<const float4*>(sO + ((size_t)wq * QR + lr) * HD + c4);
       acc.x += o.x * f;
       acc.y += o.y * f;
       acc.z += o.z * f;
       acc.w += o.w * f;
-      l += sL[q * QR + row] * f;
+      l += sL[wq * QR + lr] * f;
     }
     *reinterpret_cast<float4*>(a.part_o + (prow + row) * HD + c4) = acc;
     if (c4 == 0) {
@@ -759,16 +782,16 @@ __global__ void __launch_bounds__(WarpAttnCfg<MT, HD, NW, NS>::THREADS) decode_w
   }
 }
 
-template <int MT, int HD, int NW, int NS>
+template <int MT, int HD, int NW, int NS, int RG = 1>
 static cudaError_t launch_warp_mma(const DecodeAttnArgs& a, cudaStream_t st) {
-  using C = WarpAttnCfg<MT, HD, NW, NS>;
+  using C = WarpAttnCfg<MT, HD, NW, NS, RG>;
   static std::atomic<unsigned long long> attr{0};
   cudaError_t e = once_per_device(attr, [] {
-    return cudaFuncSetAttribute(decode_warp_mma<MT, HD, NW, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(decode_warp_mma<MT, HD, NW, NS, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::SMEM);
   });
   if (e != cudaSuccess) return e;
-  launch_pdl(decode_warp_mma<MT, HD, NW, NS>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
+  launch_pdl(decode_warp_mma<MT, HD, NW, NS, RG>, dim3(a.nsplit, a.nkv, a.B), C::THREADS, C::SMEM, st, a);
   return cudaGetLastError();
 }
 
@@ -788,11 +811,12 @@ static cudaError_t launch_split_mma(const DecodeAttnArgs& a, cudaStream_t st) {
 template <int HD>
 static cudaError_t split_mma_hd(const DecodeAttnArgs& a, cudaStream_t st) {
   const int KG = a.rows_max * (a.nq / a.nkv);
-  // up to 32 query rows per KV head: warp-independent key slices; more rows
-  // (multi-row steps) share each K/V tile across the block
+  // up to 32 query rows per KV head: warp-independent key slices; up to 64
+  // (multi-row steps): two row groups whose warp pairs share each key tile;
+  // more rows share each K/V tile across the block
   if (KG <= 16) return launch_warp_mma<1, HD, 4, 3>(a, st);
   if (KG <= 32) return launch_warp_mma<2, HD, 4, 3>(a, st);
-  if (KG <= 64) return launch_split_mma<4, HD>(a, st);
+  if (KG <= 64) return launch_warp_mma<2, HD, 8, 3, 2>(a, st);
   return launch_split_mma<8, HD>(a, st);
 }
 

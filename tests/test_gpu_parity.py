@@ -708,6 +708,11 @@ def _ctx_rows(wl, inp, counts, seed):
 @pytest.mark.parametrize("dtype,tol,kw", [("f32", F32_TOL, dict()), ("bf16", BF16_TOL, dict()),
                                           ("bf16", BF16_TOL, dict(head_dim=128, num_q_heads=8, num_kv_heads=2,
                                                                   hidden=1024, batch=6, K=8,
+                                                                  kv_len_range=(0, 3000), max_position=8192)),
+                                          # 8 query heads per KV head: up to 64 query rows per KV
+                                          # head, two row groups sharing each key tile
+                                          ("bf16", BF16_TOL, dict(head_dim=64, num_q_heads=16, num_kv_heads=2,
+                                                                  hidden=1024, batch=6, K=4,
                                                                   kv_len_range=(0, 3000), max_position=8192))])
 def test_draft_step_over_new_context_rows(dtype, tol, kw):
     # ragged new rows per request (1..9): causal among themselves over the
