@@ -10,7 +10,7 @@
 //   warps 2-5 drain a finished accumulator with tcgen05.ld and store fp32
 //           partial sums while the next work item accumulates in the other.
 // The 128-row operand ("A role") is the activation tile, or -- for a few
-// activation rows (M <= 256) -- the weight tile ("swap": weights stream
+// activation rows (M <= 128) -- the weight tile ("swap": weights stream
 // through the 128-lane side, activations sit in the narrow N side). Work
 // items are (output tile, K slice); the K slices of a tile land in separate
 // partial slabs that the consumer kernel sums, so no item waits on another.
@@ -1238,7 +1238,7 @@ struct Plan {
 static int sub_boxes(int bn) { return bn == 16 ? 4 : (bn <= 64 ? 2 : 1); }
 static int cluster_slots(int bn);
 
-// A few hundred rows (256 < M <= 1024, a batched decode step): the plan with
+// A few hundred rows (128 < M <= 1024, a batched decode step): the plan with
 // the least estimated time among 128-row items 128 or 256 wide (whole, or in
 // up to four K slices when every slice of every tile runs in the first round,
 // so the tile's CTAs share its sum) and, for M a multiple of 256, whole
@@ -1285,7 +1285,10 @@ static void plan_few_hundred_rows(Plan& p, int M, int N, int K, bool gated) {
 static Plan plan_gemm(int M, int N, int K, bool gated = false) {
   Plan p;
   p.ma = 1;
-  p.swap = M <= 256;
+  // up to 128 rows the weights stream through the 128-lane side; from 129
+  // rows the wide plans below measured faster (205 rows x 4096 x 4096: 48 ->
+  // 29 us; x 12288 K: 59 -> 45 us)
+  p.swap = M <= 128;
   if (!p.swap && M <= 1024) {
     plan_few_hundred_rows(p, M, N, K, gated);
     return p;
@@ -1549,8 +1552,7 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
       case 16: e = launch_tc<16, true, 1>(ma, mb, args, items, s); break;
       case 32: e = launch_tc<32, true, 1>(ma, mb, args, items, s); break;
       case 64: e = launch_tc<64, true, 1>(ma, mb, args, items, s); break;
-      case 128: e = launch_tc<128, true, 1>(ma, mb, args, items, s); break;
-      default: e = launch_tc<256, true, 1>(ma, mb, args, items, s); break;
+      default: e = launch_tc<128, true, 1>(ma, mb, args, items, s); break;
     }
   } else if (p.ma == 2) {
     e = (p.bn == 224) ? launch_tc<224, false, 1, 2>(ma, mb, args, items, s)

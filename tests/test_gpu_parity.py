@@ -499,8 +499,15 @@ def test_train_bf16_small():
 
 
 def test_train_bf16_swapped_rows():
-    # at most 256 rows: every GEMM runs swapped, so the cross-entropy
+    # at most 128 rows: every GEMM runs swapped, so the cross-entropy
     # statistics come from the swapped epilogue
+    wl, inp = small_train(dtype="bf16", n=60, lens=(35, 25), K=2)
+    check_train(wl, inp, 2, 0.7, 0.2, 8, BF16_TOL)
+
+
+def test_train_bf16_rows_between_the_plans():
+    # 170 rows: wide tiles of the few-hundred-row planner under the
+    # cross-entropy head
     wl, inp = small_train(dtype="bf16", n=100, lens=(60, 40), K=2)
     check_train(wl, inp, 2, 0.7, 0.2, 8, BF16_TOL)
 
