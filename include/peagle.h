@@ -417,7 +417,12 @@ peagle_status peagle_gemm_workspace_size(int32_t dtype, int32_t M, int32_t N, in
  * (K % 8 == 0, 16-byte aligned X and W), fp32 on the CUDA cores.
  * Asynchronous: a bounded wait that runs out inside the kernel sets
  * PEAGLE_DEV_TIMEOUT in the library status word (peagle_get_library_status)
- * and leaves D undefined. */
+ * and leaves D undefined.
+ * Concurrency: a bf16 contraction of 129-1024 rows may cut K into slices
+ * whose CTAs (at most one per SM) wait for one another to share the sum of
+ * each tile. They all become resident unless other work holds SMs for the
+ * whole wait bound (1 s by default, peagle_set_wait_limit_ns); a kernel on
+ * another stream that does makes the call fail as above. */
 peagle_status peagle_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* X,
                           const void* W, float* D, void* workspace, size_t workspace_bytes,
                           void* stream);
