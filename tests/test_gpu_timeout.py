@@ -37,8 +37,11 @@ def _rel(D, ref):
 
 
 @pytest.mark.parametrize("noalloc", [False, True])
-def test_wait_that_runs_out_is_reported_and_the_device_recovers(pe, noalloc):
-    M, N, K = 4, 512, 256
+@pytest.mark.parametrize("M,N,K", [(4, 512, 256),
+                                   # 512 rows in four K slices whose CTAs wait for one
+                                   # another to share each tile's sum
+                                   (512, 1024, 4096)])
+def test_wait_that_runs_out_is_reported_and_the_device_recovers(pe, noalloc, M, N, K):
     X, W, ref = _case(M, N, K, seed=11)
     D = torch.empty((M, N), dtype=torch.float32, device="cuda")
     nb = pe.peagle_gemm_workspace_size(pe.PEAGLE_BF16, M, N, K)
