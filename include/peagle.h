@@ -268,7 +268,11 @@ peagle_status peagle_verify_accept(int32_t B, int32_t K, const int32_t* draft_to
  *          16-byte vectors, anything else byte by byte
  * Ordering is the stream's, as for cudaMemcpyAsync: do not rewrite `host`
  * before a copy to the device that reads it has completed, and read a copy
- * to the host only after synchronizing the stream. */
+ * to the host only after synchronizing the stream. One difference: a copy
+ * to the device reads `host` before the previous kernel has finished, so
+ * its source must not be written by an earlier kernel still in the launch
+ * chain (e.g. a copy to the host into the same buffer): use separate
+ * buffers for the two directions. */
 peagle_status peagle_copy_to_device(void* dev, const void* host, size_t bytes, void* stream);
 peagle_status peagle_copy_to_host(void* host, const void* dev, size_t bytes, void* stream);
 
