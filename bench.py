@@ -327,37 +327,61 @@ def oracle_leg(wl, W, inp, seconds, warm=1, max_steps=None):
     return wl.batch * wl.K * steps / el, steps, el, cores
 
 
-def run_reference_train(args, wl):
-    """Oracle timing of the training-shaped forward on whole sampled
-    conversations (exact on their own: conversations never attend to one
-    another), reported as rows of those conversations per second."""
-    import synth
+def oracle_train_leg(wl, W, inp, seconds, max_steps=None, backward=False):
+    """The oracle on the host cores over a bounded sample of a training
+    workload: the forward of its shortest conversation (exact on its own:
+    conversations never attend to one another), or, for the backward, the
+    float64 autograd gradients of every weight over the first <= 128 tokens
+    of that conversation as a packed sequence of their own. Returns
+    (rows/s, steps, seconds, cores, sample)."""
     from oracle import peagle_oracle as O
-    W = synth.make_weights(wl)
-    inp = synth.make_train_inputs(wl)
     model = O.DraftModel(O.model_config(wl), W)
     cu = inp["cu_seqlens"]
     conv = int(np.argmin(np.diff(cu)))
-    fwd = {k: inp[k] for k in ("aux", "input_ids", "position_ids", "cu_seqlens", "labels", "loss_mask")}
-    kw = dict(K=inp["K"], r=inp["r"], r_min=inp["r_min"], seed=inp["seed"], conversations=[conv],
-              keep_logits=False)
-    res = O.parallel_forward(model, **fwd, **kw)
-    rows = int(np.sum(res["row_argmax"] >= 0))
+    K, r, rmin, seed = inp["K"], inp["r"], inp["r_min"], inp["seed"]
+    if not backward:
+        fwd = {k: inp[k] for k in ("aux", "input_ids", "position_ids", "cu_seqlens", "labels", "loss_mask")}
+        kw = dict(K=K, r=r, r_min=rmin, seed=seed, conversations=[conv], keep_logits=False)
+        res = O.parallel_forward(model, **fwd, **kw)
+        rows = int(np.sum(res["row_argmax"] >= 0))
+        run = lambda: O.parallel_forward(model, **fwd, **kw)
+        what = f"oracle forwards of conversation {conv} ({int(cu[conv + 1] - cu[conv])} tokens, {rows} rows)"
+    else:
+        a = int(cu[conv])
+        b = min(int(cu[conv + 1]), a + 128)
+        sub = dict(aux=inp["aux"][a:b], input_ids=np.asarray(inp["input_ids"])[a:b],
+                   position_ids=np.asarray(inp["position_ids"])[a:b], cu_seqlens=np.array([0, b - a]),
+                   labels=np.asarray(inp["labels"])[a:b], loss_mask=None)
+        rows = int(sum(O.cod_counts(b - a, K, r, rmin)))
+        run = lambda: O.parallel_grads(model, **sub, K=K, r=r, r_min=rmin, seed=seed,
+                                       depth_decay=inp["depth_decay"])
+        what = (f"oracle backward passes (float64 autograd gradients of every weight) over the first {b - a} "
+                f"tokens of conversation {conv} as a packed sequence of their own ({rows} rows)")
     steps, t0 = 0, time.perf_counter()
     while True:
-        O.parallel_forward(model, **fwd, **kw)
+        run()
         steps += 1
         el = time.perf_counter() - t0
-        if el >= min(60.0, args.cpu_seconds * 2) or steps >= args.steps:
+        if el >= seconds or (max_steps and steps >= max_steps):
             break
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
         cores = os.cpu_count()
-    v = rows * steps / el
-    sample = (f"{steps} oracle forwards of conversation {conv} ({int(cu[conv + 1] - cu[conv])} tokens, "
-              f"{rows} rows) in {el:.1f} s")
-    line = {"impl": "reference", "metric": TRAIN_METRIC, "value": v, "unit": "rows/s",
+    return rows * steps / el, steps, el, cores, f"{steps} {what} in {el:.1f} s"
+
+
+def run_reference_train(args, wl):
+    """Oracle timing of the training-shaped forward on whole sampled
+    conversations (exact on their own: conversations never attend to one
+    another), reported as rows of those conversations per second."""
+    import synth
+    W = synth.make_weights(wl)
+    inp = synth.make_train_inputs(wl)
+    v, steps, el, cores, sample = oracle_train_leg(wl, W, inp, min(60.0, args.cpu_seconds * 2),
+                                                   max_steps=args.steps, backward=args.backward)
+    metric = "training rows/s per P-EAGLE forward + backward" if args.backward else TRAIN_METRIC
+    line = {"impl": "reference", "metric": metric, "value": v, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": steps, "warmup": 1, "ms_per_step": 1000.0 * el / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name},
@@ -501,6 +525,7 @@ def aux_ops(pe, synth, marshal, wl, model, d, inp, stream, rounds=LOOP_ROUNDS):
 # ------------------------------------------------------ training-shaped pass
 TRAIN_METRIC = "drafted depth-rows/s per P-EAGLE parallel forward"
 TRAIN_OPS = {"fc": 0, "qkv": 1, "attn": 2, "o_proj": 3, "gate_up": 4, "down": 5, "lm_head": 6, "ce": 9}
+BWD_GEMM_OP = 10   # every contraction of the parallel backward
 
 
 def train_flops(wl, n, R, pairs):
@@ -686,6 +711,9 @@ def run_train(args, wl):
         "device_status": status,
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_cpu_baseline:
+        v, _, _, cores, sample = oracle_train_leg(wl, W, inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     model.close()
     if dist:
@@ -741,16 +769,57 @@ def run_backward(args, wl):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    clk.__exit__(None, None, None)
+    launches = pe.peagle_kernel_launches() - launches0
     ms = e0.elapsed_time(e1) / args.steps
+    # the pass's contractions (the forward again, then dX and dW of each),
+    # timed with CUDA events around each launch in a pass of their own
+    probe_steps = max(1, min(args.steps, 5))
+    pe.peagle_probe_begin(BWD_GEMM_OP, 1 << 16)
+    for _ in range(probe_steps):
+        step()
+    torch.cuda.synchronize()
+    gemm_ms = float(np.sum(pe.peagle_probe_end(1 << 16))) / probe_steps
+    f = train_flops(wl, n, R, 0)
+    dense = sum(f[k] for k in ("fc", "qkv", "o_proj", "gate_up", "down", "lm_head"))
+    gemm_flops = 3.0 * dense - f["fc"]   # forward, dX and dW of each; fc has no dX (aux is an input)
+    _, _, peak, src = measured_peaks()
+    achieved = gemm_flops / (gemm_ms / 1000.0) / 1e12 if gemm_ms > 0 else None
+    # end to end: the step's inputs from pinned host memory, the loss back
+    keys = ("aux", "input_ids", "position_ids", "cu_seqlens", "labels")
+    h_in = {k: d[k].cpu().pin_memory() for k in keys}
+    h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    e_steps = max(1, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(e_steps):
+        for k in keys:
+            d[k].copy_(h_in[k], non_blocking=True)
+        step()
+        h_loss.copy_(loss, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
+    e2e_ms = e2.elapsed_time(e3) / e_steps
     line = {"metric": "training rows/s per P-EAGLE forward + backward", "value": R / (ms / 1000.0),
             "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic", "config": {"workload": wl.name, "n_tokens": n, "K": K, "rows": R,
                                             "pass": "forward + backward, gradients of every weight"},
-            "gpu_launches": int(pe.peagle_kernel_launches() - launches0), "loss": float(loss.item()),
+            "gpu_launches": int(launches), "loss": float(loss.item()),
+            "e2e": {"value": R / (e2e_ms / 1000.0), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": 4},
+            "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel (every contraction of the pass)",
+                         "achieved": achieved, "peak": peak, "peak_source": src + " (sustained)",
+                         "unit": "TFLOP/s", "frac": achieved / peak if achieved else None, "traffic": None,
+                         "algorithmic_flops_per_step": gemm_flops, "ms_per_step": gemm_ms,
+                         "timing": f"CUDA events around each launch on its stream, {probe_steps} steps"},
             "workspace_bytes": int(nbytes), "device_status": pe.peagle_get_device_status(model.handle),
             "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        v, _, _, cores, sample = oracle_train_leg(wl, W, inp, args.cpu_seconds, backward=True)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     model.close()
 

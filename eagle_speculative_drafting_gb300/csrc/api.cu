@@ -160,7 +160,7 @@ uint64_t peagle_kernel_launches(void) { return g_launches.load(); }
 
 const char* peagle_op_name(int32_t op) {
   static const char* names[] = {"fc", "qkv", "attn", "o_proj", "gate_up", "down", "lm_head",
-                                "verify", "cod", "ce"};
+                                "verify", "cod", "ce", "bwd_gemm"};
   return (op >= 0 && op < PEAGLE_OP_COUNT) ? names[op] : "unknown";
 }
 
@@ -1421,7 +1421,8 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   // its predecessor: the transposed copies of this pass are written by
   // kernels of the same launch chain.
   auto mm = [&](const void* X, int ldx, const void* W, int M, int N, int Kd, bool w_early = false) {
-    return gemm_launch(dt, X, ldx, W, M, N, Kd, ws.part, &go, ws.sem, m->status, -1, s, w_early);
+    return gemm_launch(dt, X, ldx, W, M, N, Kd, ws.part, &go, ws.sem, m->status, PEAGLE_OP_BWD_GEMM, s,
+                       w_early);
   };
   auto copy_out = [&](int M, int N, float* dst) { return launch_sum_splits(go, M, N, dst, s); };
   // D = X W^T into dst [M, N]: straight there when the contraction needs one
@@ -1430,7 +1431,8 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   auto mm_into = [&](float* dst, const void* X, int ldx, const void* W, int M, int N, int Kd,
                      bool w_early = false) -> cudaError_t {
     if (gemm_out_floats(dt, M, N, Kd) == (size_t)M * N)
-      return gemm_launch(dt, X, ldx, W, M, N, Kd, dst, &go, ws.sem, m->status, -1, s, w_early);
+      return gemm_launch(dt, X, ldx, W, M, N, Kd, dst, &go, ws.sem, m->status, PEAGLE_OP_BWD_GEMM, s,
+                         w_early);
     cudaError_t e = mm(X, ldx, W, M, N, Kd, w_early);
     return e == cudaSuccess ? copy_out(M, N, dst) : e;
   };
@@ -1465,7 +1467,8 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
 
   // ---- forward, keeping activations. fc over the n aux rows and the
   // mask_hidden row (source row n)
-  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, n, H, AHt, ws.U, &go, ws.sem, m->status, -1, s));
+  CUDA_TRY(gemm_launch(dt, aux, AHt, m->w.fc_w, n, H, AHt, ws.U, &go, ws.sem, m->status, PEAGLE_OP_BWD_GEMM,
+                       s));
   FcFinishArgs fa{};
   fa.u = go;
   fa.H = H;
@@ -1482,7 +1485,8 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
   fa.hid = ws.hidsrc;
   fa.status = m->status;
   CUDA_TRY(launch_fc_finish(dt, n, fa, s));
-  CUDA_TRY(gemm_launch(dt, m->w.mask_hidden, AHt, m->w.fc_w, 1, H, AHt, ws.Um, &go, ws.sem, m->status, -1, s));
+  CUDA_TRY(gemm_launch(dt, m->w.mask_hidden, AHt, m->w.fc_w, 1, H, AHt, ws.Um, &go, ws.sem, m->status,
+                       PEAGLE_OP_BWD_GEMM, s));
   fa.u = go;
   fa.tok = nullptr;
   fa.tok_const = c.ptd_token_id;
@@ -1512,7 +1516,7 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
       ep.q = ws.q[l];
       ep.k = ws.k[l];
       ep.v = ws.v[l];
-      CUDA_TRY(gemm_launch_epi(dt, ws.xin[l], in, W.qkv_w, R, QKV, in, ws.part, &go, ws.sem, m->status, -1, &ep, s,
+      CUDA_TRY(gemm_launch_epi(dt, ws.xin[l], in, W.qkv_w, R, QKV, in, ws.part, &go, ws.sem, m->status, PEAGLE_OP_BWD_GEMM, &ep, s,
                                true));
       if (l == 0)
         CUDA_TRY(cudaMemcpyAsync(hstream, ws.residfull, (size_t)R * H * 4, cudaMemcpyDeviceToDevice, s));

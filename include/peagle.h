@@ -513,7 +513,9 @@ peagle_status peagle_set_wait_limit_ns(uint64_t ns);
 typedef enum peagle_op {
   PEAGLE_OP_FC = 0, PEAGLE_OP_QKV = 1, PEAGLE_OP_ATTN = 2, PEAGLE_OP_O = 3,
   PEAGLE_OP_GATE_UP = 4, PEAGLE_OP_DOWN = 5, PEAGLE_OP_LM_HEAD = 6,
-  PEAGLE_OP_VERIFY = 7, PEAGLE_OP_COD = 8, PEAGLE_OP_CE = 9, PEAGLE_OP_COUNT = 10
+  PEAGLE_OP_VERIFY = 7, PEAGLE_OP_COD = 8, PEAGLE_OP_CE = 9,
+  PEAGLE_OP_BWD_GEMM = 10,   /* every contraction of peagle_parallel_backward */
+  PEAGLE_OP_COUNT = 11
 } peagle_op;
 const char* peagle_op_name(int32_t op);
 /* Starts recording a CUDA event pair around every launch of the main kernel
