@@ -388,6 +388,68 @@ def test_decode_step_replays_as_cuda_graph(kw):
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
+def test_closed_loop_with_stochastic_verification_matches_the_oracle():
+    # three rounds of draft -> rejection-sampling verify -> next context: the
+    # drafter is greedy, so its distribution q is one-hot at each draft; the
+    # target's p is a random softmax; uniforms and draws are seeded. GPU and
+    # oracle see the same inputs and must agree on every integer
+    from eagle_speculative_drafting_gb300.loop import DraftLoop
+    wl = small_bf16_decode(dtype="f32", batch=5, K=4, kv_len_range=(3, 40))
+    W = synth.make_weights(wl)
+    T = 3
+    inp = synth.make_decode_inputs(wl, spare=T * (wl.K + 1))
+    model = H().make_model(wl, W)
+    om = H().oracle_model(wl, W)
+    d = H().upload_decode(wl, inp)
+    B, K, V = wl.batch, wl.K, wl.vocab
+    loop = DraftLoop(model, K, d["k_cache"], d["v_cache"], d["kv_offsets"], d["kv_lens"], inp["kv_capacity"])
+    loop.start(inp["anchor_tokens"], inp["kv_lens"].copy())
+    kc = [k.copy() for k in inp["k_cache"]]
+    vc = [v.copy() for v in inp["v_cache"]]
+    lens = inp["kv_lens"].astype(np.int64).copy()
+    rtok = [[int(t)] for t in inp["anchor_tokens"]]
+    rpos = [[int(p)] for p in inp["kv_lens"]]
+    rng = np.random.default_rng(2024)
+    accepted = []
+    for t in range(T):
+        goff = loop.new_offsets.cpu().numpy()
+        aux_rows = np.stack([_target_aux(wl, b, p) for b in range(B) for p in rpos[b]])
+        drafts = loop.draft(H().dev(aux_rows)).cpu().numpy()
+        ref = O.draft_step_ctx(om, [aux_rows[goff[b]:goff[b + 1]] for b in range(B)], rtok, rpos, kc, vc,
+                               inp["kv_offsets"], lens, K)
+        assert np.array_equal(drafts, ref["draft_tokens"]), t
+        for b in range(B):
+            o = int(inp["kv_offsets"][b] + lens[b])
+            for l in range(wl.num_layers):
+                k, v = ref["appended"][l][b]
+                kc[l][o:o + len(k)] = k
+                vc[l][o:o + len(v)] = v
+        q = np.eye(V, dtype=np.float32)[drafts]
+        p = _softmax32(rng.standard_normal((B, K + 1, V)) * 2.0)
+        # make acceptance likely for some drafts: raise p at the draft token
+        for b in range(B):
+            for i in range(K):
+                if (b + i + t) % 3:
+                    p[b, i, drafts[b, i]] += 4.0
+        p /= p.sum(-1, keepdims=True)
+        u = rng.random((B, K)).astype(np.float32)
+        draws = rng.integers(0, 2 ** 32, B, dtype=np.uint64)
+        a, nx = run_verify_sample(drafts, q, p, u, draws)
+        ra, rn = O.verify_sample(drafts, q, p, u, draws)
+        assert np.array_equal(a, ra) and np.array_equal(nx, rn), t
+        accepted.append(a.copy())
+        loop.advance_after(torch.from_numpy(a).cuda(), torch.from_numpy(nx).cuda())
+        anchor = [pp[-1] for pp in rpos]
+        lens += np.array([len(pp) for pp in rpos])
+        rtok, rpos = O.next_context(ref["draft_tokens"], ra, rn, anchor)
+        assert np.array_equal(loop.kv_lens.cpu().numpy(), lens)
+        gtok = loop.new_tokens.cpu().numpy()
+        goff = loop.new_offsets.cpu().numpy()
+        assert [list(gtok[goff[b]:goff[b + 1]]) for b in range(B)] == rtok
+    assert np.concatenate(accepted).max() > 0   # some drafts were kept
+    assert pe().peagle_get_device_status(model.handle) == 0
+
+
 def test_staging_copies_through_mapped_host_memory():
     # the copies in the launch chain: vector and byte paths, both directions,
     # offsets off the 16-byte grid; memory the device cannot reach as host
