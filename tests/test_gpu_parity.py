@@ -450,6 +450,28 @@ def test_closed_loop_with_stochastic_verification_matches_the_oracle():
     assert pe().peagle_get_device_status(model.handle) == 0
 
 
+def test_empty_calls_succeed_and_launch_nothing():
+    # no requests, no rows, no bytes: each call returns PEAGLE_OK without a
+    # kernel launch (the library's launch counter does not move)
+    import torch
+    m = pe()
+    wl = synth.WORKLOADS["tiny_f32_decode"]
+    model = H().make_model(wl, synth.make_weights(wl))
+    cache = [torch.zeros((1, wl.num_kv_heads, wl.head_dim), device="cuda") for _ in range(wl.num_layers)]
+    torch.cuda.synchronize()
+    n0 = m.peagle_kernel_launches()
+    m.peagle_draft_step(model.handle, 0, wl.K, None, None, None, cache, cache, None, None, 1, 0, 0, None, None,
+                        None, 0)
+    m.peagle_verify_accept(0, wl.K, None, None, None, None)
+    D = torch.empty((0, 16), device="cuda")
+    m.peagle_gemm(m.PEAGLE_BF16, 0, 16, 64, D, D, D, None, 0)
+    m.peagle_copy_to_device(D, D, 0)
+    m.peagle_copy_to_host(D, D, 0)
+    torch.cuda.synchronize()
+    assert m.peagle_kernel_launches() == n0
+    assert m.peagle_get_device_status(model.handle) == 0
+
+
 def test_staging_copies_through_mapped_host_memory():
     # the copies in the launch chain: vector and byte paths, both directions,
     # offsets off the 16-byte grid; memory the device cannot reach as host
