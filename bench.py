@@ -519,6 +519,28 @@ def aux_ops(pe, synth, marshal, wl, model, d, inp, stream, rounds=LOOP_ROUNDS):
             lambda: pe.peagle_cod_select(n, Kc, 0.7, 0.2, 0x5EED, idx, row_of, wsc, wsb, stream), 50)
     out["cod_select_us"] = cod
     out["timing"] = "CUDA events on the launching stream, after the headline passes"
+    # ---- checkpoint I/O: the model's device weights saved in vLLM's layout
+    # (safetensors + config.json) to a temporary directory and loaded into
+    # fresh device buffers (host wall clock; the files sit in the page cache)
+    import shutil
+    import tempfile
+    from eagle_speculative_drafting_gb300.model import load_checkpoint
+    tmp = tempfile.mkdtemp(prefix="peagle_ckpt_")
+    try:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        model.save_checkpoint(tmp)
+        t1 = time.perf_counter()
+        m2 = load_checkpoint(tmp)
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        m2.close()
+        nbytes = sum(os.path.getsize(os.path.join(tmp, f)) for f in os.listdir(tmp))
+        out["checkpoint"] = {"bytes": nbytes, "save_s": t1 - t0, "load_s": t2 - t1,
+                             "save_gbs": nbytes / (t1 - t0) / 1e9, "load_gbs": nbytes / (t2 - t1) / 1e9,
+                             "timing": "host wall clock, device memory <-> files in a temporary directory"}
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
     return out
 
 
