@@ -1581,8 +1581,21 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     ra.eps = eps;
     ra.y = ws.y[l];
     CUDA_TRY(launch_resid_norm(dt, R, ra, s));   // hstream = h_mid
-    CUDA_TRY(mm_into(ws.gu[l], ws.y[l], H, W.gate_up_w, R, 2 * I, H, true));
-    CUDA_TRY(launch_swiglu(dt, GemmOut{ws.gu[l], 2 * I, 1, 0}, R, I, ws.act[l], s));
+    if (gemm_swiglu_keeps_gu(dt, R, 2 * I, H)) {
+      // one contraction: the activation for the down projection and the
+      // fp32 gate / up values the SwiGLU backward needs
+      GemmEpi ep{};
+      ep.op = GEMM_EPI_SWIGLU;
+      ep.act = ws.act[l];
+      ep.act_ld = I;
+      ep.gu = ws.gu[l];
+      ep.gu_ld = 2 * I;
+      CUDA_TRY(gemm_launch_epi(dt, ws.y[l], H, W.gate_up_w, R, 2 * I, H, ws.part, &go, ws.sem, m->status,
+                               PEAGLE_OP_BWD_GEMM, &ep, s, true));
+    } else {
+      CUDA_TRY(mm_into(ws.gu[l], ws.y[l], H, W.gate_up_w, R, 2 * I, H, true));
+      CUDA_TRY(launch_swiglu(dt, GemmOut{ws.gu[l], 2 * I, 1, 0}, R, I, ws.act[l], s));
+    }
     CUDA_TRY(mm(ws.act[l], I, W.down_w, R, H, I, true));
     // h_out = h_mid + down: into the next layer's input stream (or hL)
     float* hnext = (l + 1 < L) ? ws.hin[l + 1] : ws.hL;

@@ -161,7 +161,9 @@ cudaError_t gemm_launch(int dtype, const void* X, int ldx, const void* W, int M,
 // the label's logit (-inf when the label is in another tile).
 // GEMM_EPI_SWIGLU: W is a [2I, K] gate/up weight (gate rows first); the
 // result silu(gate) * up [M, I] is written as bf16 to act (row stride
-// act_ld). Needs 2I % 256 == 0.
+// act_ld). Needs 2I % 256 == 0. With gu set (wide unsplit tiles only, see
+// gemm_swiglu_keeps_gu), the fp32 gate and up values are written too, at
+// their own columns of gu [M, gu_ld] (gate j at j, up j at I + j).
 // GEMM_EPI_QKV: D's columns are [q heads | k heads | v heads], head dim
 // 128; q and k are rotated by the position of their row (pairs j, j + 64,
 // cos/sin tables [max_pos][64]) and q, k, v are written as bf16 to
@@ -172,6 +174,8 @@ struct GemmEpi {
   int op;
   void* act;
   int act_ld;
+  float* gu;            // GEMM_EPI_SWIGLU: optional fp32 gate / up values
+  int gu_ld;
   float* logits;        // optional fp32 copy of D [M, logits_ld]
   int logits_ld;
   float *p_max, *p_sum, *p_lab;   // [M, gemm_col_tiles]
@@ -186,6 +190,9 @@ struct GemmEpi {
 // Whether D = X W^T [M, N] (bf16) can take the q/k/v epilogue: unswapped
 // tiles, one partial slab, whole 128-column heads.
 bool gemm_qkv_fusable(int dtype, int M, int N, int K);
+// Whether the gated contraction (N = 2I) can also keep its fp32 gate / up
+// values in the SwiGLU epilogue: unswapped tiles, one partial slab.
+bool gemm_swiglu_keeps_gu(int dtype, int M, int N, int K);
 // 2-D bf16 tensor map over a [rows, cols] matrix (row stride ld elements),
 // box = 64 columns x box_rows rows, 128-byte swizzle. False if the driver
 // rejects it.

@@ -65,6 +65,8 @@ struct TcArgs {
   int gate_off;
   void* act;
   int act_ld;
+  float* gu;               // optional fp32 gate / up values [M, gu_ld] (unsplit wide tiles)
+  int gu_ld;
   // EPI_QKV: rotate q/k by position, write q/k/v as bf16 (head dim 128)
   int nq, nkv, max_pos, row_base;
   const float *rcos, *rsin;
@@ -787,18 +789,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           constexpr int HALF = BN / 2;
           bf16* act = static_cast<bf16*>(g.act);
           const int I = g.N / 2;
+          // the warp's staged 32 rows x 32 fp32 columns to gu from column col0
+          // (4 rows x 128 bytes per store); this half of gu ends at column lim
+          auto store_gu = [&](int col0, int lim) {
+            __syncwarp();
+            const int cc = (lane & 7) * 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + (lane >> 3);
+              const int m = m0 + rr;
+              const int n = col0 + cc;
+              if (m < g.M && n < lim) {
+                const float* srow = stg + rr * C::STG_LD + cc;
+                float* dst = g.gu + (size_t)m * g.gu_ld + n;
+                if (n + 4 <= lim) {
+                  *reinterpret_cast<float4*>(dst) = make_float4(srow[0], srow[1], srow[2], srow[3]);
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c)
+                    if (n + c < lim) dst[c] = srow[c];
+                }
+              }
+            }
+            __syncwarp();
+          };
 #pragma unroll 1
           for (int c0 = 0; c0 < HALF; c0 += 32) {
+            uint32_t rg[2][16], ru[2][16];   // gate / up columns c0 .. c0 + 31
+            const uint32_t tl = tbase + ((uint32_t)(quad * 32) << 16) + tcol;
+            tc::tmem_ld16(tl + c0, rg[0]);
+            tc::tmem_ld16(tl + c0 + 16, rg[1]);
+            tc::tmem_ld16(tl + HALF + c0, ru[0]);
+            tc::tmem_ld16(tl + HALF + c0 + 16, ru[1]);
+            if (g.gu) {
+              // the gate and up values themselves, kept for the SwiGLU backward
 #pragma unroll
-            for (int h16 = 0; h16 < 32; h16 += 16) {
-              uint32_t rg[16], ru[16];
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + c0 + h16, rg);
-              tc::tmem_ld16(tbase + ((uint32_t)(quad * 32) << 16) + tcol + HALF + c0 + h16, ru);
+              for (int c = 0; c < 32; ++c) stg[lane * C::STG_LD + c] = __uint_as_float(rg[c >> 4][c & 15]);
+              store_gu(tb * HALF + c0, I);
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float gt = __uint_as_float(rg[c]);
-                stg[lane * C::STG_LD + h16 + c] = gt / (1.f + __expf(-gt)) * __uint_as_float(ru[c]);
-              }
+              for (int c = 0; c < 32; ++c) stg[lane * C::STG_LD + c] = __uint_as_float(ru[c >> 4][c & 15]);
+              store_gu(I + tb * HALF + c0, 2 * I);
+            }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float gt = __uint_as_float(rg[c >> 4][c & 15]);
+              stg[lane * C::STG_LD + c] = gt / (1.f + __expf(-gt)) * __uint_as_float(ru[c >> 4][c & 15]);
             }
             __syncwarp();
             const int cc = (lane & 7) * 4;
@@ -1355,6 +1390,12 @@ static Plan plan_gemm(int M, int N, int K, bool gated = false) {
 
 int gemm_splits(int M, int N, int K) { return plan_gemm(M, N, K).splits; }
 
+bool gemm_swiglu_keeps_gu(int dtype, int M, int N, int K) {
+  if (dtype != PEAGLE_BF16 || M <= 0 || N % 256 != 0) return false;
+  const Plan p = plan_gemm(M, N, K, true);
+  return !p.swap && p.splits == 1;
+}
+
 bool gemm_qkv_fusable(int dtype, int M, int N, int K) {
   if (dtype != PEAGLE_BF16 || M <= 0 || N % 128 != 0) return false;
   const Plan p = plan_gemm(M, N, K);
@@ -1488,6 +1529,8 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
   args.w_early = w_early ? 1 : 0;
   args.op = EPI_STORE;
   args.gate_off = 0;
+  args.gu = nullptr;
+  args.gu_ld = 0;
   if (epi && epi->op == GEMM_EPI_QKV) {
     if (p.swap || p.splits != 1 || N % 128 != 0 || p.bn % 128 != 0) {
       set_error("q/k/v epilogue needs wide unsplit tiles (M=%d N=%d K=%d)", M, N, K);
@@ -1509,10 +1552,16 @@ cudaError_t gemm_launch_epi(int dtype, const void* X, int ldx, const void* W, in
       set_error("fused SwiGLU needs the gate/up width %d to be a multiple of 256", N);
       return cudaErrorInvalidValue;
     }
+    if (epi->gu && (p.swap || p.splits != 1)) {
+      set_error("keeping the gate/up values needs wide unsplit tiles (M=%d N=%d K=%d)", M, N, K);
+      return cudaErrorInvalidValue;
+    }
     args.op = EPI_SWIGLU;
     args.gate_off = N / 2;
     args.act = epi->act;
     args.act_ld = epi->act_ld;
+    args.gu = epi->gu;
+    args.gu_ld = epi->gu_ld;
   } else if (epi) {
     args.op = epi->op;
     args.part_ld = p.swap ? (N + 127) / 128 : (N + p.bn - 1) / p.bn;
