@@ -1234,6 +1234,8 @@ struct BwdWs {
   void* vt;   // V transposed [nkv*hd, Rp] for the tensor-core forward attention, or NULL
   float *U, *Um, *hidsrc, *residsrc, *hidfull, *residfull, *hL, *logits, *part, *rce;
   int* ram;
+  float *p_max, *p_sum, *p_lab;   // fused head partials [R, column tiles] (bf16 path)
+  int* p_idx;
   float *loss_d, *acc_d;
   int* valid_d;
   float *dh, *dh2, *dhid, *dbig, *dQ, *dK, *dV, *lse, *Dv, *rrow, *rrow2, *du, *dmask;
@@ -1311,6 +1313,13 @@ static void bwd_layout(const peagle_config& c, int n, int K, int R, Bump& bp, Bw
   ws.logits = bp.take<float>((size_t)R * V);
   ws.rce = bp.take<float>(R);
   ws.ram = bp.take<int>(R);
+  {
+    const size_t np = dt == PEAGLE_BF16 ? (size_t)R * gemm_col_tiles(R, V, H) : 0;
+    ws.p_max = bp.take<float>(np);
+    ws.p_sum = bp.take<float>(np);
+    ws.p_lab = bp.take<float>(np);
+    ws.p_idx = bp.take<int>(np);
+  }
   ws.loss_d = bp.take<float>(K);
   ws.acc_d = bp.take<float>(K);
   ws.valid_d = bp.take<int>(K);
@@ -1607,8 +1616,26 @@ peagle_status peagle_parallel_backward(const peagle_model* m, int32_t n, const v
     CUDA_TRY(launch_resid_norm(dt, R, ra, s));
   }
   // head: logits, per-row CE, the loss and its per-depth counts
-  CUDA_TRY(mm_into(ws.logits, ws.z, H, m->w.lm_head_w, R, V, H, true));
-  CUDA_TRY(launch_ce_rows(GemmOut{ws.logits, V, 1, 0}, R, V, 0, ws.label, nullptr, ws.rce, ws.ram, s));
+  if (dt == PEAGLE_BF16) {
+    // the logits (kept for the cross-entropy gradient) and each row's CE
+    // and argmax partials from the contraction's epilogue, merged per row
+    GemmEpi ep{};
+    ep.op = GEMM_EPI_CE;
+    ep.logits = ws.logits;
+    ep.logits_ld = V;
+    ep.p_max = ws.p_max;
+    ep.p_sum = ws.p_sum;
+    ep.p_lab = ws.p_lab;
+    ep.p_idx = ws.p_idx;
+    ep.labels = ws.label;
+    CUDA_TRY(gemm_launch_epi(dt, ws.z, H, m->w.lm_head_w, R, V, H, ws.part, &go, ws.sem, m->status,
+                             PEAGLE_OP_BWD_GEMM, &ep, s, true));
+    CUDA_TRY(launch_ce_merge(R, gemm_col_tiles(R, V, H), 0, ws.p_max, ws.p_sum, ws.p_lab, ws.p_idx, ws.label,
+                             ws.rce, ws.ram, s));
+  } else {
+    CUDA_TRY(mm_into(ws.logits, ws.z, H, m->w.lm_head_w, R, V, H, true));
+    CUDA_TRY(launch_ce_rows(GemmOut{ws.logits, V, 1, 0}, R, V, 0, ws.label, nullptr, ws.rce, ws.ram, s));
+  }
   CeReduceArgs cr{};
   cr.row_ce = ws.rce;
   cr.row_am = ws.ram;
